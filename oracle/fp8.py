@@ -1,0 +1,205 @@
+"""FP8 (E4M3) block quantisation and FP8 attention, written out plainly.
+
+Test infrastructure only. Sources (FlashAttention-3, zenmind.me summary):
+* §3.5 "block quantisation" (paper §3.3): one scale per Br x d block of Q and
+  per Bc x d block of K and V instead of one per tensor; the S block is
+  rescaled by the product of its Q and K scales.
+* §3.5 "incoherent processing" (paper §3.3): Q and K are multiplied by
+  M = diag(random signs) * Hadamard before quantisation, so (QM)(KM)^T = QK^T.
+* §3.2 Algorithm 1: the tiled online softmax that the FP8 forward follows.
+* m.xxqk.cn FA3 walkthrough §4.1-4.2: E4M3 operands, FP32 accumulation,
+  power-of-two scale factors.
+
+Readings (the pages leave these open):
+* E4M3 is the OCP "e4m3fn" format: bias 7, largest finite 448, no infinity,
+  NaN = S.1111.111. Encoding rounds to nearest even and saturates to +-448.
+* Block = 128 rows of one (batch, head); scale e = the largest integer with
+  amax * 2^e <= 448; the stored dequantisation factor is 2^-e (1 if amax = 0).
+* The rotation is y = fp32(FWHT_fp32(sigma o x) * fp32(1/sqrt(d))), with the
+  fast Walsh-Hadamard transform taken in the textbook radix-2 order (stride
+  1, 2, 4, ...), every add and subtract rounded to float32. Sylvester order.
+* The V factor of KV tile j, sv_j = 2^f_j, is folded into P~ before its
+  E4M3 rounding, relative to F, the running maximum of f over the tiles seen
+  so far: P~ enters the second product as e4m3(P~ * 2^(8 + f_j - F)), and
+  the accumulated O is multiplied by 2^(F_old - F_new) whenever F grows (the
+  same correction as for the running row max m). The running max m is exact
+  (O is rescaled whenever it grows), so P~ <= 1 and the rounded value lies in
+  (0, 256]. At the end O = O_acc * 2^(F - 8) / l; l sums the unrounded P~.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+E4M3_MAX = 448.0
+BLOCK = 128
+
+
+def e4m3_decode(codes):
+    """uint8 codes -> float64 values."""
+    c = np.asarray(codes).astype(np.int64)
+    sign = (c >> 7) & 1
+    e = (c >> 3) & 0xF
+    m = c & 7
+    mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return np.where(sign == 1, -mag, mag)
+
+
+def e4m3_encode(x):
+    """float values -> uint8 codes, round to nearest even, saturating at +-448."""
+    x = np.asarray(x, dtype=np.float64)
+    nan = np.isnan(x)
+    neg = np.signbit(x)
+    a = np.minimum(np.abs(np.where(nan, 0.0, x)), E4M3_MAX)
+    mant, ex = np.frexp(a)                     # a = mant * 2^ex, mant in [0.5, 1)
+    e = ex - 1                                  # a = (2 mant) * 2^e
+    q_norm = np.rint((2.0 * mant - 1.0) * 8.0)  # exact products, ties to even
+    carry = q_norm == 8
+    e = np.where(carry, e + 1, e)
+    q_norm = np.where(carry, 0, q_norm)
+    code_norm = ((e + 7) << 3) + q_norm.astype(np.int64)
+    q_sub = np.rint(a / 2.0 ** -9).astype(np.int64)   # subnormal step 2^-9
+    code = np.where(a < 2.0 ** -6, q_sub, code_norm)
+    code = code + np.where(neg, 128, 0)
+    code = np.where(nan, 0x7F, code)
+    return code.astype(np.uint8)
+
+
+def pow2_exponent(amax):
+    """Largest integer e with amax * 2^e <= 448 (0 where amax == 0)."""
+    amax = np.asarray(amax, dtype=np.float64)
+    safe = np.where(amax > 0, amax, 1.0)
+    e = np.floor(np.log2(E4M3_MAX / safe)).astype(np.int64)
+    # settle the floor exactly: scaling by a power of two is exact
+    e = np.where(safe * np.exp2(e + 1.0) <= E4M3_MAX, e + 1, e)
+    e = np.where(safe * np.exp2(e * 1.0) > E4M3_MAX, e - 1, e)
+    return np.where(amax > 0, e, 0)
+
+
+def hadamard(d):
+    """Sylvester Hadamard matrix of order d (a power of two), entries +-1."""
+    h = np.ones((1, 1))
+    while h.shape[0] < d:
+        h = np.block([[h, h], [h, -h]])
+    if h.shape[0] != d:
+        raise ValueError("d must be a power of two")
+    return h
+
+
+def fwht_fp32(x):
+    """x @ H along the last axis, radix-2 stages h = 1, 2, 4, ..., all in float32."""
+    y = np.array(x, dtype=np.float32, copy=True)
+    d = y.shape[-1]
+    h = 1
+    while h < d:
+        z = y.reshape(y.shape[:-1] + (d // (2 * h), 2, h))
+        a = z[..., 0, :].copy()
+        b = z[..., 1, :].copy()
+        z[..., 0, :] = a + b
+        z[..., 1, :] = a - b
+        y = z.reshape(y.shape)
+        h *= 2
+    return y
+
+
+def rotate_fp32(x, signs):
+    """Incoherent processing in float32: fp32(FWHT(sigma o x) * fp32(1/sqrt(d)))."""
+    x = np.asarray(x, dtype=np.float32)
+    d = x.shape[-1]
+    s = np.asarray(signs, dtype=np.float32)
+    c = np.float32(1.0 / np.sqrt(d))
+    return (fwht_fp32(x * s) * c).astype(np.float32)
+
+
+def rotate_f64(x, signs):
+    """The same rotation as a dense float64 product x diag(sigma) H / sqrt(d)."""
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    return (x * np.asarray(signs, dtype=np.float64)) @ hadamard(d) / np.sqrt(d)
+
+
+def quantize_blocks(x, signs=None, block=BLOCK):
+    """[B, H, N, d] -> (codes uint8 [B, H, N, d], factors float32 [B, H, ceil(N/block)]).
+
+    x is taken in float32 (as the GPU sees bf16/fp16 inputs); with ``signs``
+    the rotation is applied first. Each block of ``block`` rows of one
+    (batch, head) gets its own power-of-two factor.
+    """
+    if hasattr(x, "detach"):
+        x = x.detach().float().numpy()
+    x = np.asarray(x, dtype=np.float32)
+    if signs is not None:
+        x = rotate_fp32(x, signs)
+    b_, h_, n, d = x.shape
+    nb = (n + block - 1) // block
+    codes = np.empty(x.shape, dtype=np.uint8)
+    fac = np.empty((b_, h_, nb), dtype=np.float32)
+    for i in range(nb):
+        blk = x[:, :, i * block:(i + 1) * block, :].astype(np.float64)
+        e = pow2_exponent(np.abs(blk).max(axis=(2, 3)))
+        codes[:, :, i * block:(i + 1) * block, :] = e4m3_encode(blk * np.exp2(e * 1.0)[:, :, None, None])
+        fac[:, :, i] = np.exp2(-e * 1.0)
+    return codes, fac
+
+
+def quantize_tensor(x, signs=None, block=BLOCK):
+    """Per-tensor power-of-two scaling (the baseline): one factor for all of x.
+
+    Returns the factor broadcast to the block-scale shape so that the same
+    attention routine consumes either form.
+    """
+    if hasattr(x, "detach"):
+        x = x.detach().float().numpy()
+    x = np.asarray(x, dtype=np.float32)
+    if signs is not None:
+        x = rotate_fp32(x, signs)
+    b_, h_, n, d = x.shape
+    xd = x.astype(np.float64)
+    e = int(pow2_exponent(np.abs(xd).max()))
+    codes = e4m3_encode(xd * 2.0 ** e)
+    nb = (n + block - 1) // block
+    fac = np.full((b_, h_, nb), 2.0 ** -e, dtype=np.float32)
+    return codes, fac
+
+
+def attention_fp8(q8, k8, v8, sq, sk, sv, scale, causal=False, block=BLOCK, p_shift=8):
+    """FP8 forward following Algorithm 1 tile by tile (Bc = block keys per tile).
+
+    q8 [B, Hq, N, d], k8/v8 [B, Hkv, N, d] are E4M3 codes; sq/sk/sv are the
+    dequantisation factors per 128-row block. Arithmetic is float64 except the
+    E4M3 rounding of P~ before the second product. Returns (O, LSE).
+    """
+    qf, kf, vf = e4m3_decode(q8), e4m3_decode(k8), e4m3_decode(v8)
+    sq, sk, sv = (np.asarray(a, dtype=np.float64) for a in (sq, sk, sv))
+    b_, hq, n, d = qf.shape
+    g = hq // kf.shape[1]
+    o = np.empty(qf.shape)
+    lse = np.empty((b_, hq, n))
+    rows = np.arange(n)
+    q_fac = sq[:, :, rows // block]                       # [B, Hq, N]
+    for b in range(b_):
+        for h in range(hq):
+            kv = h // g
+            m = np.full(n, -np.inf)
+            l = np.zeros(n)
+            acc = np.zeros((n, d))
+            f_run = -np.inf
+            for j in range((n + block - 1) // block):
+                cols = np.arange(j * block, min(n, (j + 1) * block))
+                s = scale * q_fac[b, h][:, None] * sk[b, kv, j] * (qf[b, h] @ kf[b, kv, cols].T)
+                if causal:
+                    s = np.where(cols[None, :] > rows[:, None], -np.inf, s)
+                m_new = np.maximum(m, s.max(axis=1))
+                m_use = np.where(np.isfinite(m_new), m_new, 0.0)
+                corr = np.exp(m - m_use)
+                f_j = np.log2(sv[b, kv, j])
+                f_new = max(f_run, f_j)
+                v_corr = np.exp2(f_run - f_new)
+                pt = np.exp(s - m_use[:, None])
+                l = corr * l + pt.sum(axis=1)
+                p8 = e4m3_decode(e4m3_encode(pt * np.exp2(p_shift + f_j - f_new)))
+                acc = (corr * v_corr)[:, None] * acc + p8 @ vf[b, kv, cols]
+                m, f_run = m_new, f_new
+            o[b, h] = acc * np.exp2(f_run - p_shift) / l[:, None]
+            lse[b, h] = m + np.log(l)
+    return o, lse
