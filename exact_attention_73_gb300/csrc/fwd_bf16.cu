@@ -1,0 +1,17 @@
+// Forward instances with bf16 operands: d = 64 and 128 with two query tiles
+// per CTA, d = 256 with one (tensor memory holds S and O for 512 columns).
+#include "fwd_launch.cuh"
+
+namespace attn {
+
+cudaError_t launch_fwd_bf16(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                            const FwdArgs& a, int rows, int gy, int gz, cudaStream_t st) {
+  switch (d) {
+    case 64: return launch_fwd_inst<kBF16, 64, 2>(q, k, v, a, rows, gy, gz, st);
+    case 128: return launch_fwd_inst<kBF16, 128, 2>(q, k, v, a, rows, gy, gz, st);
+    case 256: return launch_fwd_inst<kBF16, 256, 1>(q, k, v, a, rows, gy, gz, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace attn

@@ -1,0 +1,380 @@
+// Forward attention kernel for sm_103a (BF16 / FP16 / E4M3 operands).
+//
+// Method: FlashAttention-3 (zenmind.me summary) §3.2 Algorithm 1 — a tiled
+// online softmax with running max m and running sum l; O is rescaled by
+// exp(m_old - m_new) and divided by l at the end, LSE = m + log l. S and P
+// stay on chip. §3.5 adds the FP8 variant (block scales folded into S).
+//
+// GB300 design (not the pages' Hopper layout):
+//   * one CTA owns QT query tiles of 128 rows of one (batch, head);
+//   * warp 0 issues TMA loads: Q once, then K_j and V_j into a ring of
+//     NSLOT shared-memory slots guarded by full/empty mbarriers;
+//   * warp 1 (one thread) issues tcgen05.mma: S_t = Q_t K_j^T into tensor
+//     memory, then O_t += P_t V_j with P_t read straight from tensor memory;
+//   * one warpgroup per query tile runs the softmax: it loads its S rows
+//     from tensor memory (thread = row), applies the mask, updates m and l,
+//     writes P (BF16/FP16/E4M3) back over S and rescales O in tensor memory
+//     when the max moved by more than kTau (log2 units); the last step
+//     normalises O and writes O and LSE.
+//   With QT = 2 the tensor core computes S for one tile while the other
+//   tile's softmax runs, the role the pages' ping-pong schedule plays.
+//   Completion of S_t(j) implies completion of every earlier MMA of the CTA,
+//   including O_t += P_t V_{j-1}, so O_t can be rescaled right then.
+#pragma once
+#include <cmath>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace attn {
+
+enum : int { kBF16 = 0, kFP16 = 1, kE4M3 = 2 };
+
+struct FwdArgs {
+  void* o;
+  float* lse;
+  long long o_sn, o_sh, o_sb;   // element strides of O: row, head, batch
+  long long l_sh, l_sb;         // element strides of LSE: head, batch (row stride 1)
+  int Hq, Hkv, group;           // group = Hq / Hkv
+  int N;                        // dense sequence length
+  const int* cu_seqlens;        // packed layout when non-null
+  float scale_log2;             // scale * log2(e)
+  int causal;
+  const float* sq;              // FP8 dequantisation factors per 128-row block
+  const float* sk;
+  const float* sv;
+  int nblk;                     // blocks per (batch, head) in sq/sk/sv
+  int* status;
+};
+
+template <int DT, int D, int QT>
+struct FwdCfg {
+  static constexpr bool kFp8 = DT == kE4M3;
+  static constexpr int ESZ = kFp8 ? 1 : 2;
+  static constexpr int ROW_B = D * ESZ;
+  static constexpr int BOX_B = ROW_B < 128 ? ROW_B : 128;   // inner extent of one TMA box
+  static constexpr int BOX_E = BOX_B / ESZ;
+  static constexpr int NBOX = D / BOX_E;
+  static constexpr int TILE_B = 128 * ROW_B;                // one 128-row tile
+  static constexpr int BOXT_B = 128 * BOX_B;                // one box of 128 rows
+  static constexpr uint32_t SWZ = BOX_B == 128 ? kSwizzle128 : kSwizzle64;
+  static constexpr int SBO = 8 * BOX_B;                     // 8-row core-matrix group
+  static constexpr int KSTEP_B = 32;                        // K bytes per MMA
+  static constexpr int KSTEP_E = KSTEP_B / ESZ;
+  static constexpr int Q_B = QT * TILE_B;
+  static constexpr int BUDGET = 200 * 1024;
+  static constexpr int NSLOT_RAW = (BUDGET - Q_B) / TILE_B;
+  static constexpr int NSLOT = NSLOT_RAW > 8 ? 8 : NSLOT_RAW;
+  static_assert(NSLOT >= 2, "shared memory too small for the K/V ring");
+  static constexpr int O_COL = QT * 128;                    // O_t at O_COL + t * D
+  static_assert(O_COL + QT * D <= 512, "tensor memory overflow");
+  static constexpr int NTHREADS = 128 + 128 * QT;
+  static constexpr int NBAR = 1 + 2 * NSLOT + 2 * QT + 1;
+  static constexpr int SMEM_BYTES = 1024 + Q_B + NSLOT * TILE_B + NBAR * 8 + 16;
+  static constexpr uint32_t FMT = DT == kBF16 ? 1u : 0u;    // BF16=1, F16=0, E4M3=0
+  static constexpr uint32_t IDESC_S = instr_desc(128, 128, FMT, FMT, 0, 0);
+  static constexpr uint32_t IDESC_O = instr_desc(128, D, FMT, FMT, 0, 1);
+  // Rescale threshold (log2 units): keep a stale max while exp2(x - m) <= 2^kTau.
+  static constexpr float kTau = kFp8 ? 0.0f : 8.0f;
+  // Power-of-two shift of P~ before its E4M3 rounding.
+  static constexpr int kPShift = 8;
+};
+
+__device__ __forceinline__ int pow2_exponent_of(float x) {   // x an exact power of two
+  return static_cast<int>((__float_as_uint(x) >> 23) & 0xFFu) - 127;
+}
+__device__ __forceinline__ float exp2i(int e) {               // exact 2^e, |e| < 127
+  return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+}
+
+template <int DT, int D, int QT>
+__global__ void __launch_bounds__(FwdCfg<DT, D, QT>::NTHREADS, 1)
+fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+           const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
+  using C = FwdCfg<DT, D, QT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sKV = smem + C::Q_B;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + C::NSLOT * C::TILE_B);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_empty = kv_full + C::NSLOT;
+  uint64_t* s_full = kv_empty + C::NSLOT;
+  uint64_t* p_ready = s_full + QT;
+  uint64_t* o_final = p_ready + QT;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(o_final + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.y;
+  const bool packed = a.cu_seqlens != nullptr;
+  int b, seq0, L;
+  if (packed) {
+    b = 0;
+    seq0 = a.cu_seqlens[blockIdx.z];
+    L = a.cu_seqlens[blockIdx.z + 1] - seq0;
+  } else {
+    b = blockIdx.z;
+    seq0 = 0;
+    L = a.N;
+  }
+  const int nqt = (L + 127) >> 7;
+  // Causal CTAs with the most KV tiles start first.
+  const int cblk = a.causal ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
+  const int qt0 = cblk * QT;
+  if (qt0 >= nqt) return;   // whole CTA leaves before any set-up
+  const int nkv = a.causal ? min(nqt, qt0 + QT) : nqt;
+  const int hkv = h / a.group;
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    mbar_init(q_full, 1);
+    for (int s = 0; s < C::NSLOT; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int t = 0; t < QT; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_ready[t], 128);
+    }
+    mbar_init(o_final, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, C::Q_B);
+      for (int t = 0; t < QT; ++t) {
+        const int row = seq0 + (qt0 + t) * 128;
+        for (int c = 0; c < C::NBOX; ++c) {
+          uint8_t* dst = sQ + t * C::TILE_B + c * C::BOXT_B;
+          if (packed) tma_load_4d(dst, &tmQ, q_full, c * C::BOX_E, h, row, 0);
+          else tma_load_4d(dst, &tmQ, q_full, c * C::BOX_E, row, h, b);
+        }
+      }
+      for (int it = 0; it < 2 * nkv; ++it) {
+        const int slot = it % C::NSLOT;
+        if (!mbar_wait(&kv_empty[slot], ((it / C::NSLOT) & 1) ^ 1, a.status)) break;
+        mbar_arrive_expect_tx(&kv_full[slot], C::TILE_B);
+        const CUtensorMap* m = (it & 1) ? &tmV : &tmK;
+        const int row = seq0 + (it >> 1) * 128;
+        for (int c = 0; c < C::NBOX; ++c) {
+          uint8_t* dst = sKV + slot * C::TILE_B + c * C::BOXT_B;
+          if (packed) tma_load_4d(dst, m, &kv_full[slot], c * C::BOX_E, hkv, row, 0);
+          else tma_load_4d(dst, m, &kv_full[slot], c * C::BOX_E, row, hkv, b);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t q_addr = smem_u32(sQ);
+      const uint32_t kv_addr = smem_u32(sKV);
+      bool ok = mbar_wait(q_full, 0, a.status);
+      for (int j = 0; j < nkv && ok; ++j) {
+        const int itk = 2 * j;
+        const int sk_ = itk % C::NSLOT;
+        if (!(ok = mbar_wait(&kv_full[sk_], (itk / C::NSLOT) & 1, a.status))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < QT; ++t) {
+#pragma unroll
+          for (int kk = 0; kk < D / C::KSTEP_E; ++kk) {
+            const uint32_t off = (kk * C::KSTEP_B / C::BOX_B) * C::BOXT_B + (kk * C::KSTEP_B) % C::BOX_B;
+            const uint64_t ad = smem_desc(q_addr + t * C::TILE_B + off, 16, C::SBO, C::SWZ);
+            const uint64_t bd = smem_desc(kv_addr + sk_ * C::TILE_B + off, 16, C::SBO, C::SWZ);
+            mma_ss<C::kFp8>(tbase + t * 128, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&s_full[t]);
+        }
+        mma_commit(&kv_empty[sk_]);
+        const int itv = 2 * j + 1;
+        const int sv_ = itv % C::NSLOT;
+        if (!(ok = mbar_wait(&kv_full[sv_], (itv / C::NSLOT) & 1, a.status))) break;
+#pragma unroll
+        for (int t = 0; t < QT; ++t) {
+          if (!(ok = mbar_wait(&p_ready[t], j & 1, a.status))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 128 / C::KSTEP_E; ++kk) {
+            const uint64_t bd = smem_desc(kv_addr + sv_ * C::TILE_B + kk * C::KSTEP_E * C::BOX_B,
+                                          C::BOXT_B, C::SBO, C::SWZ);
+            mma_ts<C::kFp8>(tbase + C::O_COL + t * D, tbase + t * 128 + kk * 8, bd, C::IDESC_O,
+                            (j > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        mma_commit(&kv_empty[sv_]);
+      }
+      mma_commit(o_final);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------- softmax
+    const int t = (warp - 4) >> 2;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const int qtile = qt0 + t;
+    const int qrow = qtile * 128 + row;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tbase + lane_off + t * 128;
+    const uint32_t tO = tbase + lane_off + C::O_COL + t * D;
+    float m = -INFINITY;     // running max of x = S * scale * log2(e)
+    float l = 0.f;           // running sum of exp2(x - m)
+    int f_run = -1000;       // FP8: running max exponent of the V factors
+    float q_fac = 1.f;
+    long long vs_base = 0;
+    if constexpr (C::kFp8) {
+      q_fac = a.sq[(static_cast<long long>(b) * a.Hq + h) * a.nblk + min(qtile, nqt - 1)];
+      vs_base = (static_cast<long long>(b) * a.Hkv + hkv) * a.nblk;
+    }
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, a.status));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+      const int kb = j * 128;
+      if (kb + 128 > L || (a.causal && kb + 127 > qtile * 128)) {
+        int lim = L - kb;
+        if (a.causal) lim = min(lim, qrow - kb + 1);
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+      float sl2 = a.scale_log2;
+      int f_j = 0, f_new = 0;
+      if constexpr (C::kFp8) {
+        sl2 *= q_fac * a.sk[vs_base + j];
+        f_j = pow2_exponent_of(a.sv[vs_base + j]);
+        f_new = max(f_run, f_j);
+      }
+      const float mxs = mx * sl2;
+      const float m_new = (mxs > m + C::kTau) ? mxs : m;
+      float corr = 1.f;
+      if (m_new != m) corr = ex2(m - m_new);   // m = -inf gives 0
+      float corr_o = corr;
+      if constexpr (C::kFp8) {
+        if (f_new != f_run) corr_o *= exp2i(max(f_run - f_new, -126));
+      }
+      l *= corr;
+      m = m_new;
+      if (j > 0 && warp_any(corr_o != 1.f)) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tO + 32 * c, r);
+          tmem_wait_ld();
+          reg_fence(r);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr_o);
+          tmem_st32(tO + 32 * c, r);
+        }
+      }
+      const float mu = (m == -INFINITY) ? 0.f : m;
+      float bias = -mu;
+      if constexpr (C::kFp8) bias += static_cast<float>(C::kPShift + f_j - f_new);
+      float rs = 0.f;
+      if constexpr (C::kFp8) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float p0 = ex2(fmaf(__uint_as_float(sr[32 * c + 4 * e + 0]), sl2, bias));
+            const float p1 = ex2(fmaf(__uint_as_float(sr[32 * c + 4 * e + 1]), sl2, bias));
+            const float p2 = ex2(fmaf(__uint_as_float(sr[32 * c + 4 * e + 2]), sl2, bias));
+            const float p3 = ex2(fmaf(__uint_as_float(sr[32 * c + 4 * e + 3]), sl2, bias));
+            rs += (p0 + p1) + (p2 + p3);
+            pk[e] = pack_e4m3x4(p0, p1, p2, p3);
+          }
+          tmem_st8(tS + 8 * c, pk);
+        }
+        l += rs * exp2i(-(C::kPShift + f_j - f_new));
+        f_run = f_new;
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = ex2(fmaf(__uint_as_float(sr[32 * c + 2 * e]), sl2, bias));
+            const float p1 = ex2(fmaf(__uint_as_float(sr[32 * c + 2 * e + 1]), sl2, bias));
+            rs += p0 + p1;
+            pk[e] = (DT == kBF16) ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
+          }
+          tmem_st16(tS + 16 * c, pk);
+        }
+        l += rs;
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&p_ready[t]);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_final, 0, a.status));
+    tc_fence_after();
+    if (ok) {
+      float inv = 1.f / l;
+      if constexpr (C::kFp8) inv *= exp2i(f_run - C::kPShift);
+      const bool valid = qrow < L;
+      const long long row_off = static_cast<long long>(b) * a.o_sb + static_cast<long long>(h) * a.o_sh +
+                                static_cast<long long>(seq0 + qrow) * a.o_sn;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tO + 32 * c, r);
+        tmem_wait_ld();
+        reg_fence(r);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float x0 = __uint_as_float(r[2 * e]) * inv;
+          const float x1 = __uint_as_float(r[2 * e + 1]) * inv;
+          pk[e] = (DT == kFP16) ? pack_f16x2(x0, x1) : pack_bf16x2(x0, x1);
+        }
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.o) + row_off + 32 * c);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+      }
+      if (valid) {
+        const float lse2 = (m == -INFINITY ? 0.f : m) + __log2f(l);
+        a.lse[static_cast<long long>(b) * a.l_sb + static_cast<long long>(h) * a.l_sh + seq0 + qrow] =
+            lse2 * 0.69314718055994530942f;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+}  // namespace attn

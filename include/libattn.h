@@ -1,0 +1,171 @@
+/*
+ * libattn — exact fused scaled-dot-product attention for one NVIDIA GB300
+ * (sm_103a). C ABI: plain device pointers, sizes and an opaque stream.
+ *
+ * What is computed (FlashAttention-3, zenmind.me summary of the paper):
+ *   §3.1  S = scale * Q K^T, P = softmax(S) with the row max subtracted,
+ *         O = P V; backward dV = P^T dO, dP = dO V^T, dS = P o (dP - D),
+ *         dQ = scale dS K, dK = scale dS^T Q.
+ *   §3.2  Algorithm 1: tiled online softmax with running max m and running
+ *         sum l, O rescaled by exp(m_old - m_new); epilogue O / l and
+ *         LSE = m + log(l). S and P never reach global memory.
+ *   §3.5  FP8 (E4M3) forward: per-block power-of-two scales, FP32
+ *         accumulation, optional random-sign Hadamard rotation of Q and K.
+ *   §4 step 5 (paper App. B.1): D = rowsum(dO o O) before the backward;
+ *         dQ partials are accumulated atomically in FP32.
+ *   §3.2 / paper p.6: grouped-query attention by index mapping, K/V are
+ *         not replicated in memory.
+ *   guijiagi.com "Flash Attention 3 explained", practical notes: packed
+ *         variable-length batches described by cu_seqlens.
+ *
+ * Conventions shared by every entry point
+ *   - Dense tensors are contiguous [B, H, N, d] (d fastest). Packed tensors
+ *     are contiguous [T, H, d] with cu_seqlens (int32, nseq + 1 entries,
+ *     device memory) holding the exclusive prefix sum of the lengths.
+ *   - d is 64, 128 or 256. Hq is a multiple of Hkv; query head h reads
+ *     key/value head h / (Hq / Hkv).
+ *   - causal: key j is visible to query i iff j <= i (positions counted
+ *     inside each sequence; queries and keys have the same length).
+ *   - LSE is float32, natural log: dense [B, Hq, N], packed [Hq, T].
+ *   - All pointers are device pointers owned by the caller; the library
+ *     never allocates or frees device memory and never synchronises.
+ *     Every pointer must be 16-byte aligned.
+ *   - stream is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Calls are asynchronous on it.
+ *   - Arguments are checked before anything is launched; a failed check
+ *     returns an error code and launches nothing. A CUDA error raised by a
+ *     launch is returned as ATTN_ERR_CUDA.
+ */
+#ifndef LIBATTN_H
+#define LIBATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_BF16 = 0,
+  ATTN_FP16 = 1,
+  ATTN_E4M3 = 2
+} attn_dtype;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_NULL = 1,       /* a required pointer is NULL */
+  ATTN_ERR_ALIGN = 2,      /* a pointer is not 16-byte aligned */
+  ATTN_ERR_SHAPE = 3,      /* B, H, N, T, nseq or max_seqlen out of range */
+  ATTN_ERR_HEADDIM = 4,    /* d not in {64, 128, 256} */
+  ATTN_ERR_GQA = 5,        /* Hq is not a positive multiple of Hkv */
+  ATTN_ERR_DTYPE = 6,      /* dtype not accepted by this entry point */
+  ATTN_ERR_WORKSPACE = 7,  /* workspace NULL or smaller than the size query */
+  ATTN_ERR_LAUNCH = 8,     /* kernel resources (shared memory) not granted */
+  ATTN_ERR_TIMEOUT = 9,    /* a device-side wait ran out (see status query) */
+  ATTN_ERR_CUDA = 10,      /* CUDA runtime/driver error */
+  ATTN_ERR_NODEVICE = 11   /* no sm_103 device is current */
+} attn_status;
+
+/* Human-readable name of a status code (static string). */
+ATTN_API const char* attn_status_string(attn_status s);
+
+/*
+ * Forward, dense. Algorithm 1 (§3.2) with scale = alpha (§3.1).
+ * q [B,Hq,N,d], k/v [B,Hkv,N,d] of `dtype` (ATTN_BF16 or ATTN_FP16);
+ * o [B,Hq,N,d] same dtype (written); lse [B,Hq,N] float32 (written).
+ */
+ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                     attn_dtype dtype, void* stream);
+
+/*
+ * Forward, packed variable length (guijiagi.com, practical notes).
+ * q [T,Hq,d], k/v [T,Hkv,d], o [T,Hq,d], lse [Hq,T]; cu_seqlens int32 [nseq+1]
+ * on the device; max_seqlen is the largest length (host value, >= 1; used to
+ * size the grid). Every sequence must have length >= 1.
+ */
+ATTN_API attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int* cu_seqlens, int nseq, int T, int max_seqlen,
+                            int Hq, int Hkv, int d, float scale, int causal,
+                            attn_dtype dtype, void* stream);
+
+/*
+ * Block quantisation to E4M3 (§3.5 block quantisation and incoherent
+ * processing; m.xxqk.cn walkthrough §4.2 power-of-two scales).
+ * x [B,H,N,d] of in_dtype (BF16/FP16) -> x8 [B,H,N,d] E4M3 codes (uint8) and
+ * scales [B,H,ceil(N/128)] float32: for each 128-row block of one (b,h),
+ * e = the largest integer with amax * 2^e <= 448, x8 = e4m3_rn_satfinite(x * 2^e),
+ * scales = 2^-e (1 when the block is all zero).
+ * hadamard_signs: NULL = no rotation; else int8 [d] of +-1 on the device, and
+ * each row is first replaced by fp32(FWHT(signs o x) * fp32(1/sqrt(d))).
+ */
+ATTN_API attn_status attn_quantize_fp8(const void* x, attn_dtype in_dtype, void* x8, float* scales,
+                              int B, int H, int N, int d, const int8_t* hadamard_signs,
+                              void* stream);
+
+/*
+ * FP8 forward, dense (§3.5). q8 [B,Hq,N,d], k8/v8 [B,Hkv,N,d] E4M3 codes;
+ * sq [B,Hq,ceil(N/128)], sk/sv [B,Hkv,ceil(N/128)] float32 power-of-two
+ * dequantisation factors from attn_quantize_fp8. o [B,Hq,N,d] BF16,
+ * lse [B,Hq,N] float32. Both products accumulate in FP32; P~ is rounded to
+ * E4M3 as e4m3(P~ * 2^(8 + f_j - F)) with sv_j = 2^f_j and F the running
+ * maximum of f over the KV tiles seen (O rescaled when F grows).
+ */
+ATTN_API attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8,
+                         const float* sq, const float* sk, const float* sv,
+                         void* o, float* lse,
+                         int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                         void* stream);
+
+/* Bytes of device workspace attn_bwd needs: FP32 dQ accumulator [B,Hq,N,d]
+ * plus D = rowsum(dO o O) [B,Hq,N], each rounded up to 256 bytes. */
+ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d);
+
+/*
+ * Backward, dense (§3.1 backward chain; §4 step 5). Inputs q, k, v, o, dout of
+ * `dtype` with the forward's shapes and lse from attn_fwd; outputs dq
+ * [B,Hq,N,d], dk/dv [B,Hkv,N,d] of `dtype` (dk/dv sum over the query heads
+ * of each group). P is recomputed from lse. workspace: device memory of at
+ * least attn_bwd_workspace_size bytes, contents need not be initialised.
+ * lse is treated as a non-differentiable output.
+ */
+ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const void* dout,
+                     void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                     int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                     attn_dtype dtype, void* stream);
+
+/* Workspace for attn_bwd_varlen: FP32 dQ [T,Hq,d] plus D [Hq,T]. */
+ATTN_API size_t attn_bwd_varlen_workspace_size(int T, int Hq, int Hkv, int d);
+
+/* Backward, packed variable length; layouts as attn_fwd_varlen. */
+ATTN_API attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                            const float* lse, const void* dout,
+                            void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                            const int* cu_seqlens, int nseq, int T, int max_seqlen,
+                            int Hq, int Hkv, int d, float scale, int causal,
+                            attn_dtype dtype, void* stream);
+
+/*
+ * Device status of the library's kernels on the current device: every wait
+ * inside a kernel is bounded; one that runs out records ATTN_ERR_TIMEOUT in a
+ * device word and the kernel returns early. This call synchronises `stream`,
+ * reads the word, clears it and returns it (ATTN_OK when nothing happened).
+ */
+ATTN_API attn_status attn_get_device_status(void* stream);
+
+/* Library version, e.g. "libattn 0.1 sm_103a". */
+ATTN_API const char* attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBATTN_H */

@@ -162,31 +162,34 @@ def quantize_tensor(x, signs=None, block=BLOCK):
     return codes, fac
 
 
-def attention_fp8(q8, k8, v8, sq, sk, sv, scale, causal=False, block=BLOCK, p_shift=8):
+def attention_fp8(q8, k8, v8, sq, sk, sv, scale, causal=False, block=BLOCK, p_shift=8, heads=None, rows=None):
     """FP8 forward following Algorithm 1 tile by tile (Bc = block keys per tile).
 
     q8 [B, Hq, N, d], k8/v8 [B, Hkv, N, d] are E4M3 codes; sq/sk/sv are the
     dequantisation factors per 128-row block. Arithmetic is float64 except the
     E4M3 rounding of P~ before the second product. Returns (O, LSE).
+    ``heads`` (list of (b, h)) and ``rows`` restrict the work to those query
+    heads and rows (rows are independent); other entries are left as NaN.
     """
     qf, kf, vf = e4m3_decode(q8), e4m3_decode(k8), e4m3_decode(v8)
     sq, sk, sv = (np.asarray(a, dtype=np.float64) for a in (sq, sk, sv))
     b_, hq, n, d = qf.shape
     g = hq // kf.shape[1]
-    o = np.empty(qf.shape)
-    lse = np.empty((b_, hq, n))
-    rows = np.arange(n)
-    q_fac = sq[:, :, rows // block]                       # [B, Hq, N]
-    for b in range(b_):
-        for h in range(hq):
+    o = np.full(qf.shape, np.nan)
+    lse = np.full((b_, hq, n), np.nan)
+    rows = np.arange(n) if rows is None else np.asarray(rows)
+    heads = [(b, h) for b in range(b_) for h in range(hq)] if heads is None else heads
+    for b, h in heads:
             kv = h // g
-            m = np.full(n, -np.inf)
-            l = np.zeros(n)
-            acc = np.zeros((n, d))
+            q_fac = sq[b, h, rows // block]
+            qrows = qf[b, h, rows]
+            m = np.full(len(rows), -np.inf)
+            l = np.zeros(len(rows))
+            acc = np.zeros((len(rows), d))
             f_run = -np.inf
             for j in range((n + block - 1) // block):
                 cols = np.arange(j * block, min(n, (j + 1) * block))
-                s = scale * q_fac[b, h][:, None] * sk[b, kv, j] * (qf[b, h] @ kf[b, kv, cols].T)
+                s = scale * q_fac[:, None] * sk[b, kv, j] * (qrows @ kf[b, kv, cols].T)
                 if causal:
                     s = np.where(cols[None, :] > rows[:, None], -np.inf, s)
                 m_new = np.maximum(m, s.max(axis=1))
@@ -200,6 +203,6 @@ def attention_fp8(q8, k8, v8, sq, sk, sv, scale, causal=False, block=BLOCK, p_sh
                 p8 = e4m3_decode(e4m3_encode(pt * np.exp2(p_shift + f_j - f_new)))
                 acc = (corr * v_corr)[:, None] * acc + p8 @ vf[b, kv, cols]
                 m, f_run = m_new, f_new
-            o[b, h] = acc * np.exp2(f_run - p_shift) / l[:, None]
-            lse[b, h] = m + np.log(l)
+            o[b, h, rows] = acc * np.exp2(f_run - p_shift) / l[:, None]
+            lse[b, h, rows] = m + np.log(l)
     return o, lse

@@ -1,0 +1,75 @@
+"""The C-ABI library builds, loads and exports what include/libattn.h declares.
+
+Runs without a GPU: only argument checks that return before any device work
+are exercised, plus the loud failure when no sm_103 device is present.
+"""
+import ctypes as C
+import os
+import re
+
+import pytest
+import torch
+
+from exact_attention_73_gb300 import binding
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "libattn.h")
+
+
+def declared():
+    txt = open(HEADER).read()
+    return re.findall(r"ATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", txt)
+
+
+def test_header_declares_the_binding_exports():
+    assert sorted(declared()) == sorted(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert binding.attn_version().startswith("libattn")
+    for code, name in binding.STATUS.items():
+        assert binding.attn_status_string(code).startswith(name)
+
+
+def _fwd(lib, q=16, k=16, v=16, o=16, lse=16, B=1, Hq=2, Hkv=1, N=8, d=64, dt=0):
+    P = lambda x: C.c_void_p(x) if x else None
+    return lib.attn_fwd(P(q), P(k), P(v), P(o), P(lse), B, Hq, Hkv, N, d, 0.125, 0, dt, None)
+
+
+def test_argument_checks_before_any_device_work(lib):
+    assert _fwd(lib, q=0) == 1                      # NULL
+    assert _fwd(lib, k=0x1008) == 2                 # not 16-byte aligned
+    assert _fwd(lib, N=0) == 3                      # shape
+    assert _fwd(lib, B=0) == 3
+    assert _fwd(lib, d=96) == 4                     # head dim
+    assert _fwd(lib, Hq=3, Hkv=2) == 5              # GQA
+    assert _fwd(lib, dt=2) == 6                     # E4M3 goes through attn_fwd_fp8
+    P = C.c_void_p
+    # varlen: nseq, T and max_seqlen are checked
+    assert lib.attn_fwd_varlen(P(16), P(16), P(16), P(16), P(16), P(16), 0, 10, 5, 2, 1, 64, 0.1, 0, 0, None) == 3
+    assert lib.attn_fwd_varlen(P(16), P(16), P(16), P(16), P(16), P(16), 2, 10, 11, 2, 1, 64, 0.1, 0, 0, None) == 3
+    assert lib.attn_fwd_varlen(P(16), P(16), P(16), P(16), P(16), None, 2, 10, 5, 2, 1, 64, 0.1, 0, 0, None) == 1
+    # quantiser: head dim and dtype
+    assert lib.attn_quantize_fp8(P(16), 0, P(16), P(16), 1, 1, 8, 32, None, None) == 4
+    assert lib.attn_quantize_fp8(P(16), 2, P(16), P(16), 1, 1, 8, 64, None, None) == 6
+    # backward: workspace must be present and large enough
+    ws = binding.attn_bwd_workspace_size(1, 2, 1, 8, 64)
+    args = [P(16)] * 9
+    assert lib.attn_bwd(*args, None, ws, 1, 2, 1, 8, 64, 0.1, 0, 0, None) == 1
+    assert lib.attn_bwd(*args, P(16), ws - 1, 1, 2, 1, 8, 64, 0.1, 0, 0, None) == 7
+
+
+def test_workspace_size_arithmetic():
+    up = lambda x: (x + 255) // 256 * 256
+    B, Hq, N, d = 2, 32, 8192, 128
+    assert binding.attn_bwd_workspace_size(B, Hq, 8, N, d) == up(B * Hq * N * d * 4) + up(B * Hq * N * 4)
+    assert binding.attn_bwd_varlen_workspace_size(1000, 4, 2, 64) == up(1000 * 4 * 64 * 4) + up(1000 * 4 * 4)
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_valid_call_without_gpu_fails_loudly(lib):
+    assert _fwd(lib) == 11                          # ATTN_ERR_NODEVICE, nothing launched

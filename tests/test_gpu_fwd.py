@@ -1,0 +1,230 @@
+"""Forward parity: the CUDA library against the float64 oracle (GPU only).
+
+Tolerances (on N(0,1) inputs, O of the input dtype, LSE float32):
+max |O - O_ref| <= 1e-2, RMS(O - O_ref) <= 2e-3, max |LSE - LSE_ref| <= 1e-3.
+The oracle sees exactly the rounded bf16/fp16 values the GPU sees.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_73_gb300 import binding as L
+from exact_attention_73_gb300 import inputs
+from oracle import attention as A
+from oracle import fp8 as F
+
+pytestmark = pytest.mark.gpu
+
+DT = {"bf16": torch.bfloat16, "fp16": torch.float16}
+
+
+def check_o_lse(o, lse, o_ref, lse_ref, tag=""):
+    o = o.double().cpu().numpy() if hasattr(o, "cpu") else o
+    lse = lse.double().cpu().numpy() if hasattr(lse, "cpu") else lse
+    err = np.abs(o - o_ref)
+    assert np.isfinite(o).all(), tag
+    assert err.max() <= 1e-2, (tag, err.max())
+    assert math.sqrt((err ** 2).mean()) <= 2e-3, (tag, math.sqrt((err ** 2).mean()))
+    assert np.abs(lse - lse_ref).max() <= 1e-3, (tag, np.abs(lse - lse_ref).max())
+
+
+def run_fwd(q, k, v, causal, scale=None):
+    qd, kd, vd = (x.cuda() for x in (q, k, v))
+    B, Hq, N, d = q.shape
+    o = torch.full_like(qd, float("nan"))
+    lse = torch.full((B, Hq, N), float("nan"), device="cuda")
+    L.attn_fwd(qd, kd, vd, o, lse, scale=scale, causal=causal)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def test_tiny_config_bf16_copy_of_fp32_inputs(lib):
+    # B=1, H=2, N=256, d=64, i.i.d. N(0,1) fp32 and its bf16-rounded copy
+    q32, k32, v32 = inputs.normal(0, [(1, 2, 256, 64)] * 3, dtype="fp32")
+    q, k, v = (x.to(torch.bfloat16) for x in (q32, k32, v32))
+    o, lse = run_fwd(q, k, v, False)
+    o_ref, lse_ref = A.forward(q, k, v, 1 / 8, False)
+    check_o_lse(o, lse, o_ref, lse_ref, "tiny")
+    # against the unrounded fp32 inputs the bf16 input rounding dominates
+    o32, _ = A.forward(q32, k32, v32, 1 / 8, False)
+    assert np.abs(o.double().cpu().numpy() - o32).max() < 3e-2
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("n", [1, 129, 640, 1000])
+def test_dense_gqa_ragged(dtype, d, causal, n):
+    q, k, v = inputs.normal(100 + d + n, [(2, 4, n, d), (2, 2, n, d), (2, 2, n, d)], dtype=dtype)
+    o, lse = run_fwd(q, k, v, causal)
+    o_ref, lse_ref = A.forward(q, k, v, d ** -0.5, causal)
+    check_o_lse(o, lse, o_ref, lse_ref, f"{dtype} d{d} n{n} c{causal}")
+
+
+def test_scale_argument_is_used(lib):
+    q, k, v = inputs.normal(7, [(1, 2, 300, 128)] * 3)
+    o, lse = run_fwd(q, k, v, True, scale=0.2)
+    o_ref, lse_ref = A.forward(q, k, v, 0.2, True)
+    check_o_lse(o, lse, o_ref, lse_ref, "scale")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_varlen_small(causal, d):
+    lens = [1, 127, 128, 300, 1000, 5]
+    cu = inputs.cu_seqlens(lens)
+    T = int(cu[-1])
+    q, k, v = inputs.normal(11, [(T, 4, d), (T, 2, d), (T, 2, d)])
+    o = torch.full((T, 4, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((4, T), float("nan"), device="cuda")
+    L.attn_fwd_varlen(q.cuda(), k.cuda(), v.cuda(), o, lse, cu.cuda(), max(lens), causal=causal)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = A.forward_varlen(q, k, v, cu.numpy(), d ** -0.5, causal)
+    check_o_lse(o, lse, o_ref, lse_ref, "varlen")
+
+
+def sampled_rows(n, count, seed):
+    r = np.random.default_rng(seed).choice(n, size=min(n, count), replace=False)
+    return np.unique(np.concatenate([r, [0, n - 1, min(n - 1, 127), min(n - 1, 128)]]))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("d,H,n", [(128, 16, 8192), (128, 16, 16384), (64, 32, 16384), (256, 8, 16384),
+                                   (128, 16, 512)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_sweep_full_size_sampled(d, H, n, causal):
+    B = 16384 // n
+    q, k, v = inputs.normal(1, [(B, H, n, d)] * 3)
+    o, lse = run_fwd(q, k, v, causal)
+    o, lse = o.cpu(), lse.cpu()
+    for (b, h) in [(0, 0), (B - 1, H - 1), (B // 2, H // 2)]:
+        rows = sampled_rows(n, 48, b * 100 + h)
+        o_ref, lse_ref = A.forward_rows(q[b, h], k[b, h], v[b, h], rows, d ** -0.5, causal)
+        check_o_lse(o[b, h, rows], lse[b, h, rows], o_ref, lse_ref, f"sweep d{d} n{n} b{b} h{h}")
+
+
+@pytest.mark.slow
+def test_gqa_config_forward_sampled():
+    q, k, v = inputs.normal(2, [(2, 32, 8192, 128), (2, 8, 8192, 128), (2, 8, 8192, 128)])
+    o, lse = run_fwd(q, k, v, True)
+    o, lse = o.cpu(), lse.cpu()
+    for (b, h) in [(0, 0), (0, 5), (1, 31)]:
+        rows = sampled_rows(8192, 48, h)
+        o_ref, lse_ref = A.forward_rows(q[b, h], k[b, h // 4], v[b, h // 4], rows, 128 ** -0.5, True)
+        check_o_lse(o[b, h, rows], lse[b, h, rows], o_ref, lse_ref, f"gqa b{b} h{h}")
+
+
+@pytest.mark.slow
+def test_varlen_config_forward_sampled():
+    lens = inputs.varlen_lengths()
+    cu = inputs.cu_seqlens(lens)
+    T = int(cu[-1])
+    q, k, v = inputs.normal(5, [(T, 32, 128), (T, 8, 128), (T, 8, 128)])
+    o = torch.empty((T, 32, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((32, T), device="cuda")
+    L.attn_fwd_varlen(q.cuda(), k.cuda(), v.cuda(), o, lse, cu.cuda(), max(lens), causal=True)
+    o, lse = o.cpu(), lse.cpu()
+    for s in (0, 3, 7):
+        a, e = int(cu[s]), int(cu[s + 1])
+        for h in (0, 17):
+            rows = sampled_rows(e - a, 24, s * 10 + h)
+            o_ref, lse_ref = A.forward_rows(q[a:e, h], k[a:e, h // 4], v[a:e, h // 4], rows, 128 ** -0.5, True)
+            check_o_lse(o[a:e, h][rows], lse[h, a:e][rows], o_ref, lse_ref, f"varlen s{s} h{h}")
+
+
+# ------------------------------------------------------------------- FP8
+
+def quantize_gpu(x, signs=None):
+    B, H, N, d = x.shape
+    xd = x.cuda()
+    x8 = torch.empty(x.shape, dtype=torch.uint8, device="cuda")
+    sc = torch.empty((B, H, (N + 127) // 128), dtype=torch.float32, device="cuda")
+    L.attn_quantize_fp8(xd, x8, sc, None if signs is None else signs.cuda())
+    torch.cuda.synchronize()
+    return x8, sc
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("rotate", [False, True])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_quantizer_bit_exact(d, rotate, dtype):
+    (x,) = inputs.outliers(3, [(2, 3, 300, d)], dtype=dtype)
+    signs = inputs.random_signs(4, d) if rotate else None
+    x8, sc = quantize_gpu(x, signs)
+    codes, fac = F.quantize_blocks(x, None if signs is None else signs.numpy())
+    np.testing.assert_array_equal(sc.cpu().numpy(), fac)
+    np.testing.assert_array_equal(x8.cpu().numpy(), codes)
+
+
+def test_quantizer_zero_block_gets_unit_scale():
+    x = torch.zeros(1, 1, 256, 64, dtype=torch.bfloat16)
+    x[0, 0, 200] = 3.0
+    x8, sc = quantize_gpu(x)
+    assert sc.cpu().tolist() == [[[1.0, 2.0 ** -7]]]
+    assert int(x8[0, 0, :128].sum()) == 0
+
+
+def run_fp8(q, k, v, causal, signs=None):
+    q8, sq = quantize_gpu(q, signs)
+    k8, sk = quantize_gpu(k, signs)
+    v8, sv = quantize_gpu(v)
+    B, Hq, N, d = q.shape
+    o = torch.full((B, Hq, N, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, Hq, N), float("nan"), device="cuda")
+    L.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, o, lse, causal=causal)
+    torch.cuda.synchronize()
+    return o.cpu(), lse.cpu(), (q8.cpu().numpy(), k8.cpu().numpy(), v8.cpu().numpy(),
+                                sq.cpu().numpy(), sk.cpu().numpy(), sv.cpu().numpy())
+
+
+# The emulation rounds P~ to E4M3 from float64 values, the kernel from float32
+# values: a value that lands within float32 noise of a rounding midpoint may
+# round the other way (one E4M3 step, 2^-3 relative at most). The bound below
+# allows a few such flips per row on top of bf16 output rounding.
+FP8_EMU_MAX, FP8_EMU_RMS = 2e-2, 2e-3
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_forward_matches_emulation(d, causal):
+    q, k, v = inputs.outliers(3, [(1, 4, 700, d), (1, 2, 700, d), (1, 2, 700, d)])
+    o, lse, (q8, k8, v8, sq, sk, sv) = run_fp8(q, k, v, causal)
+    o_ref, lse_ref = F.attention_fp8(q8, k8, v8, sq, sk, sv, d ** -0.5, causal)
+    err = np.abs(o.double().numpy() - o_ref)
+    assert err.max() <= FP8_EMU_MAX and math.sqrt((err ** 2).mean()) <= FP8_EMU_RMS, (err.max(), (err ** 2).mean() ** 0.5)
+    assert np.abs(lse.double().numpy() - lse_ref).max() <= 1e-3
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_config_accuracy_sampled(d, causal):
+    """B=4, H=16, N=8192 on the outlier distribution, with the rotation: RMS
+    against float64 attention on the unquantised inputs <= 1.5e-2 and no worse
+    than the per-tensor-scaled emulation; sampled heads and rows."""
+    B, H, N = 4, 16, 8192
+    q, k, v = inputs.outliers(3, [(B, H, N, d)] * 3)
+    signs = inputs.random_signs(4, d)
+    o, lse, (q8, k8, v8, sq, sk, sv) = run_fp8(q, k, v, causal, signs)
+    heads = [(0, 0), (3, 15)]
+    rows = sampled_rows(N, 64, d)
+    qt, sqt = F.quantize_tensor(q, signs.numpy())
+    kt, skt = F.quantize_tensor(k, signs.numpy())
+    vt, svt = F.quantize_tensor(v)
+    o_ten, _ = F.attention_fp8(qt, kt, vt, sqt, skt, svt, d ** -0.5, causal, heads=heads, rows=rows)
+    o_emu, _ = F.attention_fp8(q8, k8, v8, sq, sk, sv, d ** -0.5, causal, heads=heads, rows=rows)
+    gpu, ten, emu, ref = [], [], [], []
+    for (b, h) in heads:
+        r, _ = A.forward_rows(q[b, h], k[b, h], v[b, h], rows, d ** -0.5, causal)
+        ref.append(r)
+        gpu.append(o[b, h, rows].double().numpy())
+        ten.append(o_ten[b, h, rows])
+        emu.append(o_emu[b, h, rows])
+    ref, gpu, ten, emu = (np.concatenate(x) for x in (ref, gpu, ten, emu))
+    rms = lambda x: math.sqrt(((x - ref) ** 2).mean())
+    assert rms(gpu) <= 1.5e-2, rms(gpu)
+    assert rms(gpu) <= rms(ten) * 1.02 + 1e-4, (rms(gpu), rms(ten))
+    err = np.abs(gpu - emu)
+    assert math.sqrt((err ** 2).mean()) <= FP8_EMU_RMS
