@@ -1,0 +1,340 @@
+#!/usr/bin/env python
+"""Throughput of the exact-attention hot path on GB300; prints one JSON line.
+
+One step = the whole hot path over one batch of synthetic input:
+  attn_fwd (BF16) -> attn_bwd (D pre-kernel, main kernel, dQ convert)
+  -> attn_quantize_fp8 of Q, K (random-sign Hadamard) and V -> attn_fwd_fp8.
+FLOPs per step follow the paper's metric (FlashAttention-3, zenmind.me summary
+§7.1): forward 4 B H N^2 d (halved when causal), backward 2.5x forward, so a
+step counts 4.5x the forward FLOPs (the quantiser adds no FLOPs).
+
+Default workload: the BF16 sweep point d=128, H=16, N=8192, B=2 (B*N = 16384
+tokens), non-causal, Q/K/V/dO i.i.d. N(0,1). Every kernel's inputs exceed the
+129 MB L2, so no flush is needed between steps.
+
+--impl reference times the float64 CPU oracle on a bounded sample of the same
+workload (one head per step) in the same units.
+Under torchrun every rank runs the same workload on its own GPU (replicas, no
+collective on the data path); value = all ranks' FLOPs / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOADS = {
+    # name: (B, Hq, Hkv, N, d, causal)
+    "bf16_sweep_d128_n8192": (2, 16, 16, 8192, 128, False),
+    "bf16_sweep_d128_n8192_causal": (2, 16, 16, 8192, 128, True),
+    "gqa_b2_hq32_hkv8_n8192_causal": (2, 32, 8, 8192, 128, True),
+}
+DEFAULT = "bf16_sweep_d128_n8192"
+LAUNCHES_PER_STEP = 8   # fwd 1, bwd 3, quantise 3, fp8 fwd 1
+
+
+def fwd_flops(B, Hq, N, d, causal):
+    f = 4.0 * B * Hq * N * N * d
+    return f / 2 if causal else f
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        m = json.load(open(p))
+        return {"bf16_burst": m["bf16_tflops"], "bf16_sustained": m.get("bf16_tflops_sustained"),
+                "hbm_gbs": m["hbm_gbs"], "source": "measured"}
+    return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [r.split(",") for r in open(self.path).read().strip().splitlines() if r.strip()]
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if "Active" in v and "Not" not in v})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def make_inputs(wl, device):
+    import torch
+    from exact_attention_73_gb300 import inputs
+    B, Hq, Hkv, N, d, causal = wl
+    q, k, v, do = inputs.normal(1, [(B, Hq, N, d), (B, Hkv, N, d), (B, Hkv, N, d), (B, Hq, N, d)])
+    signs = inputs.random_signs(4, d)
+    return [x.to(device) for x in (q, k, v, do)] + [signs.to(device)]
+
+
+def bench_ours(args, wl, rank, world):
+    import torch
+    from exact_attention_73_gb300 import binding as L
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    L.load(build_if_missing=True)
+    B, Hq, Hkv, N, d, causal = wl
+    nb = (N + 127) // 128
+    q, k, v, do, signs = make_inputs(wl, dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty((L.attn_bwd_workspace_size(B, Hq, Hkv, N, d),), dtype=torch.uint8, device=dev)
+    q8 = torch.empty(q.shape, dtype=torch.uint8, device=dev)
+    k8 = torch.empty(k.shape, dtype=torch.uint8, device=dev)
+    v8 = torch.empty(v.shape, dtype=torch.uint8, device=dev)
+    sq = torch.empty((B, Hq, nb), device=dev)
+    sk = torch.empty((B, Hkv, nb), device=dev)
+    sv = torch.empty((B, Hkv, nb), device=dev)
+    o8 = torch.empty_like(q)
+    lse8 = torch.empty_like(lse)
+    stream = torch.cuda.current_stream(dev)
+    ev = None
+
+    def step(marks=None):
+        if marks is not None:
+            marks[0].record(stream)
+        L.attn_fwd(q, k, v, o, lse, causal=causal)
+        if marks is not None:
+            marks[1].record(stream)
+        L.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, ws, causal=causal)
+        if marks is not None:
+            marks[2].record(stream)
+        L.attn_quantize_fp8(q, q8, sq, signs)
+        L.attn_quantize_fp8(k, k8, sk, signs)
+        L.attn_quantize_fp8(v, v8, sv)
+        if marks is not None:
+            marks[3].record(stream)
+        L.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, o8, lse8, causal=causal)
+        if marks is not None:
+            marks[4].record(stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    status = L.attn_get_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {L.attn_status_string(status)} after warm-up")
+
+    # ---------------------------------------------------------- device-timed
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    clocks = Clocks(dev.index)
+    barrier()
+    clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s in range(args.steps):
+        step(marks[s])
+    t1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms_total = t0.elapsed_time(t1)
+    stage = {n: sum(m[i].elapsed_time(m[i + 1]) for m in marks) / args.steps
+             for i, n in enumerate(("fwd", "bwd", "quant", "fwd_fp8"))}
+    if L.attn_get_device_status() != 0:
+        raise RuntimeError("device-side wait timed out during the timed region")
+
+    # --------------------------------------------------------------- e2e
+    pin = [x.cpu().pin_memory() for x in (q, k, v, do)]
+    outs = [o, lse, dq, dk, dv, o8, lse8]
+    host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs]
+    h2d = sum(x.numel() * x.element_size() for x in pin)
+    d2h = sum(x.numel() * x.element_size() for x in host_out)
+
+    def e2e_step():
+        for dst, src in zip((q, k, v, do), pin):
+            dst.copy_(src, non_blocking=True)
+        step()
+        for dst, src in zip(host_out, outs):
+            dst.copy_(src, non_blocking=True)
+
+    e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    ms_e2e = e0.elapsed_time(e1)
+
+    times = torch.tensor([ms_total, ms_e2e], dtype=torch.float64)
+    if world > 1:
+        import torch.distributed as dist
+        t = times.to(dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        times = t.cpu()
+    return {"ms_total": float(times[0]), "ms_e2e": float(times[1]), "stage_ms": stage, "clocks": clk,
+            "h2d": h2d, "d2h": d2h}
+
+
+def cpu_sample(wl, steps=1):
+    """The oracle, as it stands, on one head of the workload: forward, backward
+    and the FP8 emulation (block quantisation with the rotation). Returns
+    (FLOPs processed, seconds)."""
+    import numpy as np
+    from oracle import attention as A
+    from oracle import fp8 as F
+    from exact_attention_73_gb300 import inputs
+    B, Hq, Hkv, N, d, causal = wl
+    q, k, v, do = inputs.normal(1, [(1, 1, N, d)] * 4)
+    signs = inputs.random_signs(4, d).numpy()
+    sc = d ** -0.5
+    t = time.perf_counter()
+    for _ in range(steps):
+        A.forward(q, k, v, sc, causal)
+        A.backward(q, k, v, do, sc, causal)
+        q8, sq = F.quantize_blocks(q, signs)
+        k8, sk = F.quantize_blocks(k, signs)
+        v8, sv = F.quantize_blocks(v)
+        F.attention_fp8(q8, k8, v8, sq, sk, sv, sc, causal)
+    dt = time.perf_counter() - t
+    return 4.5 * fwd_flops(1, 1, N, d, causal) * steps, dt
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT)
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle timing")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    wl = WORKLOADS[args.workload]
+    B, Hq, Hkv, N, d, causal = wl
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    config = {"workload": args.workload, "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d, "causal": causal,
+              "step": "fwd bf16 + bwd bf16 + fp8 quantise (Q,K rotated) + fwd fp8",
+              "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"}
+    metric = "attention fwd+bwd (BF16) + FP8 fwd TFLOP/s on GB300"
+    step_flops = 4.5 * fwd_flops(B, Hq, N, d, causal)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        # the oracle keeps no state between steps, so warm-up steps are not run
+        fl, sec = cpu_sample(wl, steps=args.steps)
+        val = fl / sec / 1e12
+        line = {"impl": "reference", "metric": metric, "value": val, "unit": "TFLOP/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": config,
+                "cpu_baseline": {"kind": "oracle", "value": val, "unit": "TFLOP/s", "cores": cpu_cores(),
+                                 "sample": f"one head (b=0,h=0) of the workload per step: fwd + bwd + FP8 emulation"},
+                "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    r = bench_ours(args, wl, rank, world)
+    pk = peaks()
+    ms_step = r["ms_total"] / args.steps
+    value = world * step_flops * args.steps / (r["ms_total"] * 1e-3) / 1e12
+    e2e_val = world * step_flops * args.steps / (r["ms_e2e"] * 1e-3) / 1e12
+    st = r["stage_ms"]
+    f = fwd_flops(B, Hq, N, d, causal)
+    stages = {
+        "fwd_bf16": {"ms": st["fwd"], "tflops": f / st["fwd"] / 1e9, "frac_of_bf16_peak": f / st["fwd"] / 1e9 / pk["bf16_burst"]},
+        "bwd_bf16": {"ms": st["bwd"], "tflops": 2.5 * f / st["bwd"] / 1e9,
+                     "frac_of_bf16_peak": 2.5 * f / st["bwd"] / 1e9 / pk["bf16_burst"]},
+        "quant_fp8": {"ms": st["quant"], "gbs": ((Hq + 2 * Hkv) * B * N * d * 3) / st["quant"] / 1e6},
+        "fwd_fp8": {"ms": st["fwd_fp8"], "tflops": f / st["fwd_fp8"] / 1e9,
+                    "frac_of_fp8_peak": f / st["fwd_fp8"] / 1e9 / (2 * pk["bf16_burst"])},
+    }
+    # dominant kernel: the stage with the longest time (the backward call
+    # holds its main kernel plus two HBM-bound helpers of a few percent)
+    dom = max(("fwd", "bwd", "fwd_fp8"), key=lambda n: st[n])
+    dom_flops = {"fwd": f, "bwd": 2.5 * f, "fwd_fp8": f}[dom]
+    dom_peak = pk["bf16_burst"] * (2 if dom == "fwd_fp8" else 1)
+    achieved = dom_flops / st[dom] / 1e9
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tp):
+        traffic = json.load(open(tp)).get(f"{args.workload}:{dom}")
+    line = {
+        "metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16+e4m3", "data": "synthetic", "config": config,
+        "stages": stages,
+        "roofline": {"bound": "tensor", "kernel": {"fwd": "attn_fwd", "bwd": "attn_bwd (main + 2 helpers)",
+                                                    "fwd_fp8": "attn_fwd_fp8"}[dom],
+                     "achieved": achieved, "peak": dom_peak, "unit": "TFLOP/s", "frac": achieved / dom_peak,
+                     "peak_source": pk["source"] + (" bf16 burst x2 (fp8 nominal ratio)" if dom == "fwd_fp8" else " bf16 burst"),
+                     "traffic": traffic},
+        "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "clocks": r["clocks"],
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        fl, sec = cpu_sample(wl)
+        line["cpu_baseline"] = {"value": fl / sec / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                                "sample": f"one head of the workload (N={N}, d={d}): fwd + bwd + FP8 emulation, "
+                                          f"{sec:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -86,25 +86,6 @@ CUtensorMapDataType tma_type(int dt) {
   }
 }
 
-// Map over dense [B, H, N, d] or packed [T, H, d] operands, 128-row boxes.
-bool operand_map(CUtensorMap* m, const void* base, int dt, int d, bool packed, int B, int H, long long rows) {
-  const uint64_t esz = dt == kE4M3 ? 1 : 2;
-  const uint32_t box_e = static_cast<uint32_t>(fwd_box_elems(dt, d));
-  const CUtensorMapSwizzle sw = box_e * esz == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-  if (packed) {   // dims (d, H, T, 1)
-    const uint64_t dims[4] = {static_cast<uint64_t>(d), static_cast<uint64_t>(H), static_cast<uint64_t>(rows), 1};
-    const uint64_t str[3] = {d * esz, static_cast<uint64_t>(H) * d * esz, static_cast<uint64_t>(rows) * H * d * esz};
-    const uint32_t box[4] = {box_e, 1, 128, 1};
-    return encode_map(m, base, tma_type(dt), dims, str, box, sw);
-  }
-  // dims (d, N, H, B)
-  const uint64_t dims[4] = {static_cast<uint64_t>(d), static_cast<uint64_t>(rows), static_cast<uint64_t>(H),
-                            static_cast<uint64_t>(B)};
-  const uint64_t str[3] = {d * esz, static_cast<uint64_t>(rows) * d * esz, static_cast<uint64_t>(H) * rows * d * esz};
-  const uint32_t box[4] = {box_e, 128, 1, 1};
-  return encode_map(m, base, tma_type(dt), dims, str, box, sw);
-}
-
 attn_status from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return ATTN_OK;
   if (e == cudaErrorInvalidValue) return ATTN_ERR_LAUNCH;
@@ -135,6 +116,28 @@ constexpr float kLog2e = 1.4426950408889634f;
 attn_status device_context(int** status) {
   int dev;
   return current_device(&dev, status);
+}
+
+// Map over dense [B, H, N, d] or packed [T, H, d] operands with boxes of
+// `box_rows` rows and the widest swizzled inner extent (64 or 128 bytes).
+bool operand_map(CUtensorMap* m, const void* base, int dt, int d, bool packed, int B, int H, long long rows,
+                 int box_rows) {
+  const uint64_t esz = dt == kE4M3 ? 1 : 2;
+  const uint32_t box_e = static_cast<uint32_t>(fwd_box_elems(dt, d));
+  const uint32_t br = static_cast<uint32_t>(box_rows);
+  const CUtensorMapSwizzle sw = box_e * esz == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  if (packed) {   // dims (d, H, T, 1)
+    const uint64_t dims[4] = {static_cast<uint64_t>(d), static_cast<uint64_t>(H), static_cast<uint64_t>(rows), 1};
+    const uint64_t str[3] = {d * esz, static_cast<uint64_t>(H) * d * esz, static_cast<uint64_t>(rows) * H * d * esz};
+    const uint32_t box[4] = {box_e, 1, br, 1};
+    return encode_map(m, base, tma_type(dt), dims, str, box, sw);
+  }
+  // dims (d, N, H, B)
+  const uint64_t dims[4] = {static_cast<uint64_t>(d), static_cast<uint64_t>(rows), static_cast<uint64_t>(H),
+                            static_cast<uint64_t>(B)};
+  const uint64_t str[3] = {d * esz, static_cast<uint64_t>(rows) * d * esz, static_cast<uint64_t>(H) * rows * d * esz};
+  const uint32_t box[4] = {box_e, br, 1, 1};
+  return encode_map(m, base, tma_type(dt), dims, str, box, sw);
 }
 
 }  // namespace attn
@@ -175,8 +178,8 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   int* status;
   if ((s = device_context(&status)) != ATTN_OK) return s;
   CUtensorMap tq, tk, tv;
-  if (!operand_map(&tq, q, dtype, d, false, B, Hq, N) || !operand_map(&tk, k, dtype, d, false, B, Hkv, N) ||
-      !operand_map(&tv, v, dtype, d, false, B, Hkv, N))
+  if (!operand_map(&tq, q, dtype, d, false, B, Hq, N, 128) || !operand_map(&tk, k, dtype, d, false, B, Hkv, N, 128) ||
+      !operand_map(&tv, v, dtype, d, false, B, Hkv, N, 128))
     return ATTN_ERR_CUDA;
   FwdArgs a{};
   a.o = o;
@@ -212,8 +215,8 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
   int* status;
   if ((s = device_context(&status)) != ATTN_OK) return s;
   CUtensorMap tq, tk, tv;
-  if (!operand_map(&tq, q, dtype, d, true, 1, Hq, T) || !operand_map(&tk, k, dtype, d, true, 1, Hkv, T) ||
-      !operand_map(&tv, v, dtype, d, true, 1, Hkv, T))
+  if (!operand_map(&tq, q, dtype, d, true, 1, Hq, T, 128) || !operand_map(&tk, k, dtype, d, true, 1, Hkv, T, 128) ||
+      !operand_map(&tv, v, dtype, d, true, 1, Hkv, T, 128))
     return ATTN_ERR_CUDA;
   FwdArgs a{};
   a.o = o;
@@ -249,8 +252,8 @@ attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8,
   int* status;
   if ((s = device_context(&status)) != ATTN_OK) return s;
   CUtensorMap tq, tk, tv;
-  if (!operand_map(&tq, q8, kE4M3, d, false, B, Hq, N) || !operand_map(&tk, k8, kE4M3, d, false, B, Hkv, N) ||
-      !operand_map(&tv, v8, kE4M3, d, false, B, Hkv, N))
+  if (!operand_map(&tq, q8, kE4M3, d, false, B, Hq, N, 128) || !operand_map(&tk, k8, kE4M3, d, false, B, Hkv, N, 128) ||
+      !operand_map(&tv, v8, kE4M3, d, false, B, Hkv, N, 128))
     return ATTN_ERR_CUDA;
   FwdArgs a{};
   a.o = o;

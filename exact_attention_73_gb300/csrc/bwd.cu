@@ -1,0 +1,109 @@
+// Backward launchers: D = rowsum(dO o O) with the dQ accumulator cleared,
+// the tcgen05 main kernel, and the FP32 -> BF16/FP16 dQ conversion.
+//
+// The two helper kernels are HBM-bound streams: one warp per row of d
+// elements (pre) and four elements per thread (convert), coalesced.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "bwd_kernel.cuh"
+#include "ops.h"
+
+namespace attn {
+
+namespace {
+
+template <typename T>
+__device__ __forceinline__ float to_f(T x);
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <>
+__device__ __forceinline__ float to_f<__half>(__half x) { return __half2float(x); }
+
+// rows = B*Hq*N (dense, row r = (b*Hq + h)*N + n) or T*Hq (packed, r = t*Hq + h).
+template <typename T, int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ o, const T* __restrict__ dout,
+                                                      float* __restrict__ dvec, float* __restrict__ dq_acc,
+                                                      long long rows, int Hq, int T_tokens, int packed) {
+  constexpr int c = D / 32;
+  const long long r = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const T* po = o + r * D + lane * c;
+  const T* pd = dout + r * D + lane * c;
+  float acc = 0.f;
+#pragma unroll
+  for (int e = 0; e < c; ++e) acc = fmaf(to_f(po[e]), to_f(pd[e]), acc);
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+  float4* z = reinterpret_cast<float4*>(dq_acc + r * D + lane * c);
+#pragma unroll
+  for (int e = 0; e < c / 4; ++e) z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (lane == 0) {
+    long long idx = r;
+    if (packed) idx = static_cast<long long>(r % Hq) * T_tokens + r / Hq;
+    dvec[idx] = acc;
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc, T* __restrict__ dq,
+                                                         long long n4, float scale) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n4) return;
+  const float4 x = reinterpret_cast<const float4*>(acc)[i];
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(x.x * scale, x.y * scale);
+    __nv_bfloat162 b = __floats2bfloat162_rn(x.z * scale, x.w * scale);
+    reinterpret_cast<uint2*>(dq)[i] = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+  } else {
+    __half2 a = __floats2half2_rn(x.x * scale, x.y * scale);
+    __half2 b = __floats2half2_rn(x.z * scale, x.w * scale);
+    reinterpret_cast<uint2*>(dq)[i] = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+  }
+}
+
+template <int DT>
+cudaError_t launch_main(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q, const CUtensorMap& d,
+                        const BwdArgs& a, int max_len, int nz, cudaStream_t st) {
+  using C = BwdCfg<DT, 128>;
+  auto kern = bwd_kernel<DT, 128>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((max_len + C::BC - 1) / C::BC, a.Hkv, nz);
+  kern<<<grid, C::NTHREADS, C::SMEM_BYTES, st>>>(k, v, q, d, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_pre(int dt, int d, const void* o, const void* dout, float* dvec, float* dq_acc, long long rows,
+                           int Hq, int T_tokens, int packed, cudaStream_t st) {
+  const dim3 grid(static_cast<unsigned>((rows + 7) / 8));
+  if (d != 128) return cudaErrorInvalidValue;
+  if (dt == kBF16)
+    bwd_pre_kernel<__nv_bfloat16, 128><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(o),
+        static_cast<const __nv_bfloat16*>(dout), dvec, dq_acc, rows, Hq, T_tokens, packed);
+  else
+    bwd_pre_kernel<__half, 128><<<grid, 256, 0, st>>>(static_cast<const __half*>(o), static_cast<const __half*>(dout),
+        dvec, dq_acc, rows, Hq, T_tokens, packed);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_main(int dt, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
+                            const CUtensorMap& dout, const BwdArgs& a, int max_len, int nz, cudaStream_t st) {
+  return dt == kBF16 ? launch_main<kBF16>(k, v, q, dout, a, max_len, nz, st)
+                     : launch_main<kFP16>(k, v, q, dout, a, max_len, nz, st);
+}
+
+cudaError_t launch_dq_convert(int dt, const float* acc, void* dq, long long n, float scale, cudaStream_t st) {
+  const long long n4 = n / 4;
+  const dim3 grid(static_cast<unsigned>((n4 + 255) / 256));
+  if (dt == kBF16)
+    dq_convert_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(acc, static_cast<__nv_bfloat16*>(dq), n4, scale);
+  else
+    dq_convert_kernel<__half><<<grid, 256, 0, st>>>(acc, static_cast<__half*>(dq), n4, scale);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

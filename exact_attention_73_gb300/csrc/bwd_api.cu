@@ -2,6 +2,7 @@
 #include <cstdint>
 
 #include "../../include/libattn.h"
+#include "bwd_kernel.cuh"
 #include "ops.h"
 
 namespace {
@@ -17,11 +18,69 @@ attn_status check_common(const void* q, const void* k, const void* v, const void
   for (const void* p : ptrs)
     if (!aligned16(p)) return ATTN_ERR_ALIGN;
   if (Hq < 1 || Hkv < 1 || Hq > 65535) return ATTN_ERR_SHAPE;
-  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_HEADDIM;
+  if (d != 128) return ATTN_ERR_HEADDIM;   // the backward kernel is built for d = 128
   if (Hq % Hkv) return ATTN_ERR_GQA;
   if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_DTYPE;
   if (ws_bytes < ws_need) return ATTN_ERR_WORKSPACE;
   return ATTN_OK;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+attn_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return ATTN_OK;
+  if (e == cudaErrorInvalidValue) return ATTN_ERR_LAUNCH;
+  return ATTN_ERR_CUDA;
+}
+
+// Dense when cu_seqlens is null (nz = B, rows per head = N = max_len);
+// packed otherwise (nz = nseq, T tokens, longest sequence max_len).
+attn_status run_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                    void* dq, void* dk, void* dv, void* ws, const int* cu_seqlens, int nz, int rows_or_T,
+                    int max_len, int Hq, int Hkv, int d, float scale, int causal, attn_dtype dtype, int* status,
+                    void* stream) {
+  using namespace attn;
+  const bool packed = cu_seqlens != nullptr;
+  const int B = packed ? 1 : nz;
+  const long long rows = static_cast<long long>(B) * Hq * rows_or_T;
+  float* dq_acc = static_cast<float*>(ws);
+  float* dvec = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + round256(static_cast<size_t>(rows) * d * 4));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  CUtensorMap tk, tv, tq, tdo;
+  if (!operand_map(&tk, k, dtype, d, packed, B, Hkv, rows_or_T, 128) ||
+      !operand_map(&tv, v, dtype, d, packed, B, Hkv, rows_or_T, 128) ||
+      !operand_map(&tq, q, dtype, d, packed, B, Hq, rows_or_T, 64) ||
+      !operand_map(&tdo, dout, dtype, d, packed, B, Hq, rows_or_T, 64))
+    return ATTN_ERR_CUDA;
+  BwdArgs a{};
+  a.lse = lse;
+  a.dvec = dvec;
+  a.dq_acc = dq_acc;
+  a.dk = dk;
+  a.dv = dv;
+  if (packed) {
+    a.q_sn = static_cast<long long>(Hq) * d; a.q_sh = d; a.q_sb = 0;
+    a.k_sn = static_cast<long long>(Hkv) * d; a.k_sh = d; a.k_sb = 0;
+    a.l_sh = rows_or_T; a.l_sb = 0;
+    a.N = 0;
+  } else {
+    a.q_sn = d; a.q_sh = static_cast<long long>(rows_or_T) * d; a.q_sb = static_cast<long long>(Hq) * rows_or_T * d;
+    a.k_sn = d; a.k_sh = static_cast<long long>(rows_or_T) * d; a.k_sb = static_cast<long long>(Hkv) * rows_or_T * d;
+    a.l_sh = rows_or_T; a.l_sb = static_cast<long long>(Hq) * rows_or_T;
+    a.N = rows_or_T;
+  }
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.group = Hq / Hkv;
+  a.cu_seqlens = cu_seqlens;
+  a.scale = scale;
+  a.scale_log2 = scale * kLog2e;
+  a.causal = causal ? 1 : 0;
+  a.status = status;
+  cudaError_t e = launch_bwd_pre(dtype, d, o, dout, dvec, dq_acc, rows, Hq, rows_or_T, packed ? 1 : 0, st);
+  if (e == cudaSuccess) e = launch_bwd_main(dtype, tk, tv, tq, tdo, a, max_len, nz, st);
+  if (e == cudaSuccess) e = launch_dq_convert(dtype, dq_acc, dq, rows * d, scale, st);
+  return from_cuda(e);
 }
 
 }  // namespace
@@ -49,8 +108,8 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   if (s != ATTN_OK) return s;
   int* status;
   if ((s = attn::device_context(&status)) != ATTN_OK) return s;
-  (void)scale; (void)causal; (void)stream;
-  return ATTN_ERR_LAUNCH;
+  return run_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, nullptr, B, N, N, Hq, Hkv, d, scale, causal, dtype,
+                 status, stream);
 }
 
 attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -65,8 +124,8 @@ attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const v
   if (s != ATTN_OK) return s;
   int* status;
   if ((s = attn::device_context(&status)) != ATTN_OK) return s;
-  (void)scale; (void)causal; (void)stream;
-  return ATTN_ERR_LAUNCH;
+  return run_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, cu_seqlens, nseq, T, max_seqlen, Hq, Hkv, d, scale,
+                 causal, dtype, status, stream);
 }
 
 }  // extern "C"

@@ -1,0 +1,391 @@
+// Backward attention kernels for sm_103a (BF16 / FP16, head dim 128).
+//
+// Method: FlashAttention-3 (zenmind.me summary) §3.1 backward chain with P
+// recomputed from the forward's log-sum-exp, and §4 step 5 (paper App. B.1):
+// a pre-kernel computes D = rowsum(dO o O); dQ partials of every KV block are
+// added atomically into an FP32 accumulator, then converted.
+//   P   = exp(scale * Q K^T - LSE)
+//   dV += P^T dO,  dP = dO V^T,  dS = P o (dP - D)
+//   dK += scale * dS^T Q,  dQ += scale * dS K
+//
+// GB300 design. One CTA owns one tile of 128 keys of one (batch, KV head) and
+// loops over every query head of the group and every 64-row query tile that
+// can see those keys, so dK and dV of the group accumulate in tensor memory
+// and are written once (no atomics on dK/dV). Tensor memory (512 columns):
+//   S^T  [128 keys x 64 queries]  cols   0..63   (P^T in BF16 over it)
+//   dP^T [128 keys x 64 queries]  cols  64..127  (dS^T in BF16 over it)
+//   dQ^T [128 dims x 64 queries]  cols 128..191
+//   dV   [128 keys x 128 dims]    cols 256..383
+//   dK   [128 keys x 128 dims]    cols 384..511
+// Warp roles: warp 0 loads (TMA for K, V, Q_i, dO_i; plain loads for LSE and
+// D), warp 1 issues tcgen05.mma, warps 4-7 turn S^T/dP^T into P^T/dS^T (one
+// key per thread) and also store dS^T to shared memory for dQ, warps 8-11
+// drain dQ^T (one head-dim index per thread) with coalesced FP32 atomic adds.
+#pragma once
+#include <cmath>
+#include <cstdint>
+#include <cuda.h>
+
+#include "fwd_kernel.cuh"
+#include "ptx.cuh"
+
+namespace attn {
+
+struct BwdArgs {
+  const float* lse;         // natural-log LSE, strides l_sh, l_sb, row stride 1
+  const float* dvec;        // D = rowsum(dO o O), same layout as lse
+  float* dq_acc;            // FP32, layout of q (strides q_sn, q_sh, q_sb)
+  void* dk;                 // layout of k (strides k_sn, k_sh, k_sb)
+  void* dv;
+  long long q_sn, q_sh, q_sb;
+  long long k_sn, k_sh, k_sb;
+  long long l_sh, l_sb;
+  int Hq, Hkv, group, N;
+  const int* cu_seqlens;
+  float scale;
+  float scale_log2;
+  int causal;
+  int* status;
+};
+
+template <int DT, int D>
+struct BwdCfg {
+  static_assert(D == 128, "backward kernel is written for head dim 128");
+  static constexpr int BR = 64;                     // query rows per iteration
+  static constexpr int BC = 128;                    // keys per CTA
+  static constexpr int NBOX = D / 64;               // 64-element (128-byte) boxes per row
+  static constexpr int KV_B = BC * D * 2;           // K or V tile
+  static constexpr int KV_BOX_B = BC * 128;
+  static constexpr int Q_B = BR * D * 2;            // Q_i or dO_i tile
+  static constexpr int Q_BOX_B = BR * 128;
+  static constexpr int DS_B = BC * BR * 2;          // dS^T tile [keys][queries]
+  static constexpr int NQ = 3;                      // stages of the Q/dO ring
+  static constexpr int LD_B = 2 * BR * 4;           // LSE*log2e and D for one tile
+  static constexpr int SMEM_BYTES = 1024 + 2 * KV_B + DS_B + NQ * (2 * Q_B) + NQ * LD_B + 16 * 8 + 16;
+  static constexpr int NTHREADS = 384;
+  static constexpr uint32_t FMT = DT == kBF16 ? 1u : 0u;
+  static constexpr uint32_t IDESC_SP = instr_desc(128, BR, FMT, FMT, 0, 0);
+  static constexpr uint32_t IDESC_KV = instr_desc(128, D, FMT, FMT, 0, 1);
+  static constexpr uint32_t IDESC_DQ = instr_desc(D, BR, FMT, FMT, 1, 1);
+  static constexpr uint32_t COL_S = 0, COL_DP = 64, COL_DQ = 128, COL_DV = 256, COL_DK = 384;
+};
+
+template <int DT, int D>
+__global__ void __launch_bounds__(384, 1)
+bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+           const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO, const BwdArgs a) {
+  using C = BwdCfg<DT, D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = sK + C::KV_B;
+  uint8_t* sDS = sV + C::KV_B;
+  uint8_t* sQ = sDS + C::DS_B;                      // [NQ][Q_B]
+  uint8_t* sdO = sQ + C::NQ * C::Q_B;               // [NQ][Q_B]
+  float* sLD = reinterpret_cast<float*>(sdO + C::NQ * C::Q_B);   // [NQ][2*BR]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sLD) + C::NQ * C::LD_B);
+  uint64_t* kv_full = bars;
+  uint64_t* q_full = bars + 1;
+  uint64_t* q_empty = q_full + C::NQ;
+  uint64_t* sp_full = q_empty + C::NQ;
+  uint64_t* ds_ready = sp_full + 1;
+  uint64_t* dq_full = ds_ready + 1;
+  uint64_t* dq_empty = dq_full + 1;
+  uint64_t* done = dq_empty + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int hkv = blockIdx.y;
+  const bool packed = a.cu_seqlens != nullptr;
+  int b, seq0, L;
+  if (packed) {
+    b = 0;
+    seq0 = a.cu_seqlens[blockIdx.z];
+    L = a.cu_seqlens[blockIdx.z + 1] - seq0;
+  } else {
+    b = blockIdx.z;
+    seq0 = 0;
+    L = a.N;
+  }
+  const int j = blockIdx.x;                 // key tile; with causal masking tile 0 has the most work
+  if (j * C::BC >= L) return;
+  const int nq = (L + C::BR - 1) / C::BR;
+  const int i0 = a.causal ? (j * C::BC) / C::BR : 0;
+  const int per_head = nq - i0;
+  const int niter = a.group * per_head;
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmdO);
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < C::NQ; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+    }
+    mbar_init(sp_full, 1);
+    mbar_init(ds_ready, 128);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, 128);
+    mbar_init(done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_holder;
+  const float kLog2e = 1.4426950408889634f;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ loads
+    const int krow = seq0 + j * C::BC;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(kv_full, 2 * C::KV_B);
+      for (int c = 0; c < C::NBOX; ++c) {
+        if (packed) {
+          tma_load_4d(sK + c * C::KV_BOX_B, &tmK, kv_full, c * 64, hkv, krow, 0);
+          tma_load_4d(sV + c * C::KV_BOX_B, &tmV, kv_full, c * 64, hkv, krow, 0);
+        } else {
+          tma_load_4d(sK + c * C::KV_BOX_B, &tmK, kv_full, c * 64, krow, hkv, b);
+          tma_load_4d(sV + c * C::KV_BOX_B, &tmV, kv_full, c * 64, krow, hkv, b);
+        }
+      }
+    }
+    for (int it = 0; it < niter; ++it) {
+      const int st = it % C::NQ;
+      if (!__all_sync(0xffffffffu, mbar_wait(&q_empty[st], ((it / C::NQ) & 1) ^ 1, a.status))) break;
+      const int h = hkv * a.group + it / per_head;
+      const int q0 = (i0 + it % per_head) * C::BR;
+      float* ld = sLD + st * 2 * C::BR;
+      const long long lrow = static_cast<long long>(b) * a.l_sb + static_cast<long long>(h) * a.l_sh + seq0;
+#pragma unroll
+      for (int r = lane; r < C::BR; r += 32) {
+        const int q = q0 + r;
+        const bool ok = q < L;
+        ld[r] = ok ? a.lse[lrow + q] * kLog2e : INFINITY;
+        ld[C::BR + r] = ok ? a.dvec[lrow + q] : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&q_full[st], 2 * C::Q_B);
+        for (int c = 0; c < C::NBOX; ++c) {
+          uint8_t* dq = sQ + st * C::Q_B + c * C::Q_BOX_B;
+          uint8_t* dd = sdO + st * C::Q_B + c * C::Q_BOX_B;
+          if (packed) {
+            tma_load_4d(dq, &tmQ, &q_full[st], c * 64, h, seq0 + q0, 0);
+            tma_load_4d(dd, &tmdO, &q_full[st], c * 64, h, seq0 + q0, 0);
+          } else {
+            tma_load_4d(dq, &tmQ, &q_full[st], c * 64, q0, h, b);
+            tma_load_4d(dd, &tmdO, &q_full[st], c * 64, q0, h, b);
+          }
+        }
+      }
+      __syncwarp();
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA
+    if (lane == 0) {
+      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), ds_addr = smem_u32(sDS);
+      bool ok = mbar_wait(kv_full, 0, a.status);
+      for (int it = 0; it < niter && ok; ++it) {
+        const int st = it % C::NQ;
+        if (!(ok = mbar_wait(&q_full[st], (it / C::NQ) & 1, a.status))) break;
+        tc_fence_after();
+        const uint32_t q_addr = smem_u32(sQ + st * C::Q_B);
+        const uint32_t do_addr = smem_u32(sdO + st * C::Q_B);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {   // S^T = K Q_i^T, K-major operands
+          const uint32_t offk = (kk / 4) * C::KV_BOX_B + (kk % 4) * 32;
+          const uint32_t offq = (kk / 4) * C::Q_BOX_B + (kk % 4) * 32;
+          mma_ss<false>(tbase + C::COL_S, smem_desc(k_addr + offk, 16, 1024, kSwizzle128),
+                        smem_desc(q_addr + offq, 16, 1024, kSwizzle128), C::IDESC_SP, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {   // dP^T = V dO_i^T
+          const uint32_t offk = (kk / 4) * C::KV_BOX_B + (kk % 4) * 32;
+          const uint32_t offq = (kk / 4) * C::Q_BOX_B + (kk % 4) * 32;
+          mma_ss<false>(tbase + C::COL_DP, smem_desc(v_addr + offk, 16, 1024, kSwizzle128),
+                        smem_desc(do_addr + offq, 16, 1024, kSwizzle128), C::IDESC_SP, kk > 0);
+        }
+        mma_commit(sp_full);
+        if (!(ok = mbar_wait(ds_ready, it & 1, a.status))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < C::BR / 16; ++kk) {   // dV += P^T dO_i, dK += dS^T Q_i
+          mma_ts<false>(tbase + C::COL_DV, tbase + C::COL_S + kk * 8,
+                        smem_desc(do_addr + kk * 2048, C::Q_BOX_B, 1024, kSwizzle128), C::IDESC_KV,
+                        (it > 0 || kk > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < C::BR / 16; ++kk) {
+          mma_ts<false>(tbase + C::COL_DK, tbase + C::COL_DP + kk * 8,
+                        smem_desc(q_addr + kk * 2048, C::Q_BOX_B, 1024, kSwizzle128), C::IDESC_KV,
+                        (it > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (!(ok = mbar_wait(dq_empty, (it & 1) ^ 1, a.status))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < C::BC / 16; ++kk) {   // dQ_i^T = K^T dS^T, both MN-major
+          mma_ss<false>(tbase + C::COL_DQ, smem_desc(k_addr + kk * 2048, C::KV_BOX_B, 1024, kSwizzle128),
+                        smem_desc(ds_addr + kk * 2048, C::DS_B, 1024, kSwizzle128), C::IDESC_DQ, kk > 0);
+        }
+        mma_commit(dq_full);
+        mma_commit(&q_empty[st]);
+      }
+      mma_commit(done);
+    }
+    __syncwarp();
+  } else if (warp >= 4 && warp < 8) {
+    // -------------------------------------------------- P^T and dS^T
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;              // key row of the tile
+    const int kloc = j * C::BC + r;                 // key position in the sequence
+    const bool kvalid = kloc < L;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tbase + lane_off + C::COL_S;
+    const uint32_t tdP = tbase + lane_off + C::COL_DP;
+    uint8_t* ds_row = sDS + r * 128;
+    bool ok = true;
+    for (int it = 0; it < niter; ++it) {
+      ok = __all_sync(0xffffffffu, mbar_wait(sp_full, it & 1, a.status));
+      if (!ok) break;
+      tc_fence_after();
+      const int st = it % C::NQ;
+      // LSE and D of this stage were written by the load warp before it
+      // arrived on q_full[st]; acquire them (the phase is already complete).
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&q_full[st], (it / C::NQ) & 1, a.status)))) break;
+      const int q0 = (i0 + it % per_head) * C::BR;
+      const float* ld = sLD + st * 2 * C::BR;
+      const bool diag = a.causal && (q0 < j * C::BC + C::BC - 1);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t s[32], dp[32];
+        tmem_ld32(tS + 32 * half, s);
+        tmem_ld32(tdP + 32 * half, dp);
+        tmem_wait_ld();
+        reg_fence(s);
+        reg_fence(dp);
+        uint32_t pp[16], dd[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float p[2], g[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int c = 32 * half + 2 * e + u;
+            float pv = ex2(fmaf(__uint_as_float(s[2 * e + u]), a.scale_log2, -ld[c]));
+            if (!kvalid || (diag && kloc > q0 + c)) pv = 0.f;
+            p[u] = pv;
+            g[u] = pv * (__uint_as_float(dp[2 * e + u]) - ld[C::BR + c]);
+          }
+          pp[e] = (DT == kBF16) ? pack_bf16x2(p[0], p[1]) : pack_f16x2(p[0], p[1]);
+          dd[e] = (DT == kBF16) ? pack_bf16x2(g[0], g[1]) : pack_f16x2(g[0], g[1]);
+        }
+        tmem_st16(tS + 16 * half, pp);
+        tmem_st16(tdP + 16 * half, dd);
+        // dS^T row r, queries 32*half .. +31: four 16-byte chunks, 128-byte swizzle
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const int chunk = (4 * half + c4) ^ (r & 7);
+          *reinterpret_cast<uint4*>(ds_row + chunk * 16) =
+              make_uint4(dd[4 * c4], dd[4 * c4 + 1], dd[4 * c4 + 2], dd[4 * c4 + 3]);
+        }
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(ds_ready);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(done, 0, a.status));
+    tc_fence_after();
+    if (ok) {   // dV rows
+      const long long off = static_cast<long long>(b) * a.k_sb + static_cast<long long>(hkv) * a.k_sh +
+                            static_cast<long long>(seq0 + kloc) * a.k_sn;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tbase + lane_off + C::COL_DV + 32 * c, v);
+        tmem_wait_ld();
+        reg_fence(v);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = (DT == kBF16) ? pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]))
+                                : pack_f16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+        if (kvalid) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dv) + off + 32 * c);
+#pragma unroll
+          for (int w = 0; w < 4; ++w) dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+        }
+      }
+    }
+  } else if (warp >= 8) {
+    // ---------------------------------------------------- dQ^T drain
+    const int quarter = warp & 3;
+    const int dim = quarter * 32 + lane;            // head-dim index = tensor-memory lane
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    bool ok = true;
+    for (int it = 0; it < niter; ++it) {
+      ok = __all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, a.status));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t x0[32], x1[32];
+      tmem_ld32(tbase + lane_off + C::COL_DQ, x0);
+      tmem_ld32(tbase + lane_off + C::COL_DQ + 32, x1);
+      tmem_wait_ld();
+      reg_fence(x0);
+      reg_fence(x1);
+      tc_fence_before();
+      mbar_arrive(dq_empty);
+      const int h = hkv * a.group + it / per_head;
+      const int q0 = (i0 + it % per_head) * C::BR;
+      float* base = a.dq_acc + static_cast<long long>(b) * a.q_sb + static_cast<long long>(h) * a.q_sh +
+                    static_cast<long long>(seq0) * a.q_sn + dim;
+      const int nvalid = min(C::BR, L - q0);
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        if (e < nvalid) atomicAdd(base + static_cast<long long>(q0 + e) * a.q_sn, __uint_as_float(x0[e]));
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        if (32 + e < nvalid) atomicAdd(base + static_cast<long long>(q0 + 32 + e) * a.q_sn, __uint_as_float(x1[e]));
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(done, 0, a.status));
+    tc_fence_after();
+    if (ok) {   // dK rows, times scale
+      const int kloc = j * C::BC + dim;             // here the lane indexes keys
+      const long long off = static_cast<long long>(b) * a.k_sb + static_cast<long long>(hkv) * a.k_sh +
+                            static_cast<long long>(seq0 + kloc) * a.k_sn;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tbase + lane_off + C::COL_DK + 32 * c, v);
+        tmem_wait_ld();
+        reg_fence(v);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float x0 = __uint_as_float(v[2 * e]) * a.scale, x1 = __uint_as_float(v[2 * e + 1]) * a.scale;
+          pk[e] = (DT == kBF16) ? pack_bf16x2(x0, x1) : pack_f16x2(x0, x1);
+        }
+        if (kloc < L) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dk) + off + 32 * c);
+#pragma unroll
+          for (int w = 0; w < 4; ++w) dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+}  // namespace attn

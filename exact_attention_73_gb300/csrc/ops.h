@@ -1,6 +1,7 @@
 // Launchers of the non-attention kernels (quantiser, backward helpers).
 #pragma once
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/libattn.h"
@@ -8,6 +9,15 @@
 namespace attn {
 
 attn_status device_context(int** status);
+
+struct BwdArgs;
+bool operand_map(CUtensorMap* m, const void* base, int dt, int d, bool packed, int B, int H, long long rows,
+                 int box_rows);
+cudaError_t launch_bwd_pre(int dt, int d, const void* o, const void* dout, float* dvec, float* dq_acc,
+                           long long rows, int Hq, int T_tokens, int packed, cudaStream_t st);
+cudaError_t launch_bwd_main(int dt, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
+                            const CUtensorMap& dout, const BwdArgs& a, int max_len, int nz, cudaStream_t st);
+cudaError_t launch_dq_convert(int dt, const float* acc, void* dq, long long n, float scale, cudaStream_t st);
 
 // Block quantisation to E4M3 (see attn_quantize_fp8).
 cudaError_t launch_quant_fp8(const void* x, int in_dt, uint8_t* x8, float* scales, int B, int H, int N, int d,

@@ -134,7 +134,9 @@ ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d);
  * [B,Hq,N,d], dk/dv [B,Hkv,N,d] of `dtype` (dk/dv sum over the query heads
  * of each group). P is recomputed from lse. workspace: device memory of at
  * least attn_bwd_workspace_size bytes, contents need not be initialised.
- * lse is treated as a non-differentiable output.
+ * lse is treated as a non-differentiable output. Head dim d must be 128
+ * (other values return ATTN_ERR_HEADDIM). Kernels: D = rowsum(dO o O) with
+ * the FP32 dQ accumulator cleared, the main kernel, the dQ conversion.
  */
 ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
                      const float* lse, const void* dout,

@@ -57,10 +57,11 @@ def test_argument_checks_before_any_device_work(lib):
     assert lib.attn_quantize_fp8(P(16), 0, P(16), P(16), 1, 1, 8, 32, None, None) == 4
     assert lib.attn_quantize_fp8(P(16), 2, P(16), P(16), 1, 1, 8, 64, None, None) == 6
     # backward: workspace must be present and large enough
-    ws = binding.attn_bwd_workspace_size(1, 2, 1, 8, 64)
+    ws = binding.attn_bwd_workspace_size(1, 2, 1, 8, 128)
     args = [P(16)] * 9
-    assert lib.attn_bwd(*args, None, ws, 1, 2, 1, 8, 64, 0.1, 0, 0, None) == 1
-    assert lib.attn_bwd(*args, P(16), ws - 1, 1, 2, 1, 8, 64, 0.1, 0, 0, None) == 7
+    assert lib.attn_bwd(*args, None, ws, 1, 2, 1, 8, 128, 0.1, 0, 0, None) == 1
+    assert lib.attn_bwd(*args, P(16), ws - 1, 1, 2, 1, 8, 128, 0.1, 0, 0, None) == 7
+    assert lib.attn_bwd(*args, P(16), ws, 1, 2, 1, 8, 64, 0.1, 0, 0, None) == 4   # backward: d = 128 only
 
 
 def test_workspace_size_arithmetic():

@@ -1,0 +1,119 @@
+"""Backward parity: CUDA library against the float64 oracle (GPU only).
+
+Tolerance: relative RMS = ||x - ref||_2 / ||ref||_2 <= 1e-2 for dQ, dK and dV.
+The GPU backward consumes the GPU forward's O and LSE, as a user would.
+"""
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_73_gb300 import binding as L
+from exact_attention_73_gb300 import inputs
+from oracle import attention as A
+
+pytestmark = pytest.mark.gpu
+
+
+def rel_rms(x, ref):
+    x = x.double().cpu().numpy() if hasattr(x, "cpu") else x
+    assert np.isfinite(x).all()
+    return float(np.linalg.norm(x - ref) / np.linalg.norm(ref))
+
+
+def run_dense(q, k, v, do, causal):
+    qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
+    B, Hq, N, d = q.shape
+    o = torch.empty_like(qd)
+    lse = torch.empty((B, Hq, N), device="cuda")
+    L.attn_fwd(qd, kd, vd, o, lse, causal=causal)
+    dq = torch.full_like(qd, float("nan"))
+    dk = torch.full_like(kd, float("nan"))
+    dv = torch.full_like(vd, float("nan"))
+    ws = torch.full((L.attn_bwd_workspace_size(B, Hq, k.shape[1], N, d),), 255, dtype=torch.uint8, device="cuda")
+    L.attn_bwd(qd, kd, vd, o, lse, dod, dq, dk, dv, ws, causal=causal)
+    torch.cuda.synchronize()
+    assert L.attn_get_device_status() == 0
+    return dq.cpu(), dk.cpu(), dv.cpu()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("n", [1, 64, 200, 640, 1000])
+def test_dense_gqa_ragged(dtype, causal, n):
+    q, k, v, do = inputs.normal(200 + n, [(2, 4, n, 128), (2, 2, n, 128), (2, 2, n, 128), (2, 4, n, 128)],
+                                dtype=dtype)
+    got = run_dense(q, k, v, do, causal)
+    ref = A.backward(q, k, v, do, 128 ** -0.5, causal)
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        assert rel_rms(g, r) <= 1e-2, (name, rel_rms(g, r))
+
+
+def test_two_calls_reuse_workspace():
+    q, k, v, do = inputs.normal(9, [(1, 2, 300, 128)] * 4)
+    a = run_dense(q, k, v, do, True)
+    b = run_dense(q, k, v, do, True)
+    ref = A.backward(q, k, v, do, 128 ** -0.5, True)
+    for x, y, r in zip(a, b, ref):
+        assert rel_rms(x, r) <= 1e-2 and rel_rms(y, r) <= 1e-2
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_small(causal):
+    lens = [1, 127, 128, 300, 1000, 5]
+    cu = inputs.cu_seqlens(lens)
+    T = int(cu[-1])
+    q, k, v, do = inputs.normal(12, [(T, 4, 128), (T, 2, 128), (T, 2, 128), (T, 4, 128)])
+    qd, kd, vd, dod, cud = (x.cuda() for x in (q, k, v, do, cu))
+    o = torch.empty_like(qd)
+    lse = torch.empty((4, T), device="cuda")
+    L.attn_fwd_varlen(qd, kd, vd, o, lse, cud, max(lens), causal=causal)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws = torch.empty((L.attn_bwd_varlen_workspace_size(T, 4, 2, 128),), dtype=torch.uint8, device="cuda")
+    L.attn_bwd_varlen(qd, kd, vd, o, lse, dod, dq, dk, dv, ws, cud, max(lens), causal=causal)
+    torch.cuda.synchronize()
+    ref = A.backward_varlen(q, k, v, do, cu.numpy(), 128 ** -0.5, causal)
+    for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        assert rel_rms(g, r) <= 1e-2, (name, rel_rms(g, r))
+
+
+@pytest.mark.slow
+def test_gqa_config_backward_sampled_heads():
+    """B=2, Hq=32, Hkv=8, N=8192, d=128, causal: full GPU run, oracle on two KV
+    groups (each with its four query heads)."""
+    q, k, v, do = inputs.normal(2, [(2, 32, 8192, 128), (2, 8, 8192, 128), (2, 8, 8192, 128),
+                                    (2, 32, 8192, 128)])
+    dq, dk, dv = run_dense(q, k, v, do, True)
+    for (b, g) in [(0, 0), (1, 7)]:
+        hs = slice(4 * g, 4 * g + 4)
+        ref = A.backward(q[b:b + 1, hs], k[b:b + 1, g:g + 1], v[b:b + 1, g:g + 1], do[b:b + 1, hs],
+                         128 ** -0.5, True)
+        for name, got, r in zip(("dQ", "dK", "dV"), (dq[b:b + 1, hs], dk[b:b + 1, g:g + 1], dv[b:b + 1, g:g + 1]),
+                                ref):
+            assert rel_rms(got, r) <= 1e-2, (name, b, g, rel_rms(got, r))
+
+
+@pytest.mark.slow
+def test_varlen_config_backward_sampled():
+    """Eight packed sequences (T = 129511), Hq=32, Hkv=8, causal: oracle on the
+    two shortest sequences for one KV group."""
+    lens = inputs.varlen_lengths()
+    cu = inputs.cu_seqlens(lens)
+    T = int(cu[-1])
+    q, k, v, do = inputs.normal(5, [(T, 32, 128), (T, 8, 128), (T, 8, 128), (T, 32, 128)])
+    qd, kd, vd, dod, cud = (x.cuda() for x in (q, k, v, do, cu))
+    o = torch.empty_like(qd)
+    lse = torch.empty((32, T), device="cuda")
+    L.attn_fwd_varlen(qd, kd, vd, o, lse, cud, max(lens), causal=True)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws = torch.empty((L.attn_bwd_varlen_workspace_size(T, 32, 8, 128),), dtype=torch.uint8, device="cuda")
+    L.attn_bwd_varlen(qd, kd, vd, o, lse, dod, dq, dk, dv, ws, cud, max(lens), causal=True)
+    torch.cuda.synchronize()
+    dq, dk, dv = dq.cpu(), dk.cpu(), dv.cpu()
+    for s in np.argsort(lens)[:2]:
+        a, e = int(cu[s]), int(cu[s + 1])
+        g = 3
+        hs = slice(4 * g, 4 * g + 4)
+        tr = lambda x: x[a:e].transpose(0, 1)[None]
+        ref = A.backward(tr(q[:, hs]), tr(k[:, g:g + 1]), tr(v[:, g:g + 1]), tr(do[:, hs]), 128 ** -0.5, True)
+        for name, got, r in zip(("dQ", "dK", "dV"), (tr(dq[:, hs]), tr(dk[:, g:g + 1]), tr(dv[:, g:g + 1])), ref):
+            assert rel_rms(got, r) <= 1e-2, (name, int(s), rel_rms(got, r))

@@ -20,12 +20,12 @@ pytestmark = pytest.mark.gpu
 DT = {"bf16": torch.bfloat16, "fp16": torch.float16}
 
 
-def check_o_lse(o, lse, o_ref, lse_ref, tag=""):
+def check_o_lse(o, lse, o_ref, lse_ref, tag="", rtol=0.0):
     o = o.double().cpu().numpy() if hasattr(o, "cpu") else o
     lse = lse.double().cpu().numpy() if hasattr(lse, "cpu") else lse
     err = np.abs(o - o_ref)
     assert np.isfinite(o).all(), tag
-    assert err.max() <= 1e-2, (tag, err.max())
+    assert (err - rtol * np.abs(o_ref)).max() <= 1e-2, (tag, err.max())
     assert math.sqrt((err ** 2).mean()) <= 2e-3, (tag, math.sqrt((err ** 2).mean()))
     assert np.abs(lse - lse_ref).max() <= 1e-3, (tag, np.abs(lse - lse_ref).max())
 
@@ -64,10 +64,15 @@ def test_dense_gqa_ragged(dtype, d, causal, n):
 
 
 def test_scale_argument_is_used(lib):
+    # A larger scale sharpens the softmax and |O| grows towards |V| (up to ~4),
+    # so bf16 output rounding (2^-9 relative) needs a relative term here.
     q, k, v = inputs.normal(7, [(1, 2, 300, 128)] * 3)
     o, lse = run_fwd(q, k, v, True, scale=0.2)
     o_ref, lse_ref = A.forward(q, k, v, 0.2, True)
-    check_o_lse(o, lse, o_ref, lse_ref, "scale")
+    check_o_lse(o, lse, o_ref, lse_ref, "scale", rtol=2.0 ** -8)
+    o, lse = run_fwd(q, k, v, False, scale=0.02)
+    o_ref, lse_ref = A.forward(q, k, v, 0.02, False)
+    check_o_lse(o, lse, o_ref, lse_ref, "scale small")
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -179,11 +184,22 @@ def run_fp8(q, k, v, causal, signs=None):
                                 sq.cpu().numpy(), sk.cpu().numpy(), sv.cpu().numpy())
 
 
-# The emulation rounds P~ to E4M3 from float64 values, the kernel from float32
-# values: a value that lands within float32 noise of a rounding midpoint may
-# round the other way (one E4M3 step, 2^-3 relative at most). The bound below
-# allows a few such flips per row on top of bf16 output rounding.
-FP8_EMU_MAX, FP8_EMU_RMS = 2e-2, 2e-3
+# The emulation rounds P~ to E4M3 from float64 scores, the kernel from
+# float32 tensor-core scores and ex2.approx: a value that lands within float32
+# noise of a rounding midpoint rounds the other way (one E4M3 step, up to 2^-3
+# of that entry). Such flips are rare but, next to an outlier V value (|V| up
+# to ~40 here), move one output by up to ~1e-1; bf16 output rounding adds
+# 2^-9 |O|. So the bulk is bounded tightly (RMS and the 99.99th percentile)
+# and the worst element loosely.
+FP8_EMU_RMS, FP8_EMU_Q9999, FP8_EMU_MAX = 2e-3, 1e-2, 1e-1
+
+
+def check_fp8_vs_emulation(o, o_ref):
+    err = np.abs(np.asarray(o, dtype=np.float64) - o_ref)
+    err = err[np.isfinite(o_ref)]
+    assert math.sqrt((err ** 2).mean()) <= FP8_EMU_RMS, math.sqrt((err ** 2).mean())
+    assert np.quantile(err, 0.9999) <= FP8_EMU_Q9999, np.quantile(err, 0.9999)
+    assert err.max() <= FP8_EMU_MAX, err.max()
 
 
 @pytest.mark.parametrize("d", [64, 128, 256])
@@ -192,8 +208,7 @@ def test_fp8_forward_matches_emulation(d, causal):
     q, k, v = inputs.outliers(3, [(1, 4, 700, d), (1, 2, 700, d), (1, 2, 700, d)])
     o, lse, (q8, k8, v8, sq, sk, sv) = run_fp8(q, k, v, causal)
     o_ref, lse_ref = F.attention_fp8(q8, k8, v8, sq, sk, sv, d ** -0.5, causal)
-    err = np.abs(o.double().numpy() - o_ref)
-    assert err.max() <= FP8_EMU_MAX and math.sqrt((err ** 2).mean()) <= FP8_EMU_RMS, (err.max(), (err ** 2).mean() ** 0.5)
+    check_fp8_vs_emulation(o.double().numpy(), o_ref)
     assert np.abs(lse.double().numpy() - lse_ref).max() <= 1e-3
 
 
@@ -226,5 +241,4 @@ def test_fp8_config_accuracy_sampled(d, causal):
     rms = lambda x: math.sqrt(((x - ref) ** 2).mean())
     assert rms(gpu) <= 1.5e-2, rms(gpu)
     assert rms(gpu) <= rms(ten) * 1.02 + 1e-4, (rms(gpu), rms(ten))
-    err = np.abs(gpu - emu)
-    assert math.sqrt((err ** 2).mean()) <= FP8_EMU_RMS
+    check_fp8_vs_emulation(gpu, emu)
