@@ -24,7 +24,7 @@ STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_NULL", 2: "ATTN_ERR_ALIGN", 3: "ATTN_ERR_SH
           9: "ATTN_ERR_TIMEOUT", 10: "ATTN_ERR_CUDA", 11: "ATTN_ERR_NODEVICE"}
 EXPORTS = ("attn_status_string", "attn_version", "attn_fwd", "attn_fwd_varlen", "attn_quantize_fp8",
            "attn_fwd_fp8", "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_varlen_workspace_size",
-           "attn_bwd_varlen", "attn_get_device_status")
+           "attn_bwd_varlen", "attn_get_device_status", "attn_bwd_noalloc")
 
 
 class AttnError(RuntimeError):
@@ -46,6 +46,7 @@ _SIGS = {
     "attn_bwd_varlen_workspace_size": ([_I, _I, _I, _I], _Z),
     "attn_bwd_varlen": ([_P] * 9 + [_P, _Z, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P], _I),
     "attn_get_device_status": ([_P], _I),
+    "attn_bwd_noalloc": ([_P] * 9 + [_I, _I, _I, _I, _I, _F, _I, _I, _P], _I),
 }
 
 
@@ -138,6 +139,20 @@ def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, scale=None, causal=Fa
     _check(load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
                            _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(),
                            B, Hq, Hkv, N, d, scale, int(bool(causal)), _dtype(q), _stream(stream)), "attn_bwd")
+
+
+def attn_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, scale=None, causal=False, stream=None):
+    """Dense backward with the library's own fixed device workspace (no allocation).
+
+    For callers that cannot allocate device memory; see include/libattn.h.
+    Calls that overlap on the GPU share that workspace and must not be issued.
+    """
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    _check(load().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                                   _ptr(dv), B, Hq, Hkv, N, d, scale, int(bool(causal)), _dtype(q),
+                                   _stream(stream)), "attn_bwd_noalloc")
 
 
 def attn_bwd_varlen_workspace_size(T, Hq, Hkv, d):

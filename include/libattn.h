@@ -144,6 +144,29 @@ ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const
                      int B, int Hq, int Hkv, int N, int d, float scale, int causal,
                      attn_dtype dtype, void* stream);
 
+/* Size in bytes of the device array attn_bwd_noalloc uses as its workspace. */
+#define ATTN_BWD_NOALLOC_MAX_BYTES (32u * 1024u * 1024u)
+
+/*
+ * Dense backward for callers that cannot allocate device memory. The pages
+ * have no counterpart; it exists for callers such as a process whose device
+ * memory is already reserved by another allocator (a framework's caching
+ * pool), or a serving loop that must not allocate while running because
+ * cudaMalloc/cudaFree can synchronise the device. Arguments and results are
+ * those of attn_bwd without the workspace: the workspace is a library-owned
+ * device array of ATTN_BWD_NOALLOC_MAX_BYTES, which every GPU that loads it
+ * keeps until the process exits. A problem whose attn_bwd_workspace_size
+ * exceeds that returns ATTN_ERR_WORKSPACE before any device work. The first
+ * call on a device looks up the array's device address (do it before any
+ * stream capture). All calls share the array: calls that overlap on the GPU
+ * race and must not be issued. Nothing is allocated or freed.
+ */
+ATTN_API attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                                      const float* lse, const void* dout,
+                                      void* dq, void* dk, void* dv,
+                                      int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                                      attn_dtype dtype, void* stream);
+
 /* Workspace for attn_bwd_varlen: FP32 dQ [T,Hq,d] plus D [Hq,T]. */
 ATTN_API size_t attn_bwd_varlen_workspace_size(int T, int Hq, int Hkv, int d);
 
