@@ -36,6 +36,8 @@ WORKLOADS = {
     "bf16_sweep_d128_n8192": (2, 16, 16, 8192, 128, False),
     "bf16_sweep_d128_n8192_causal": (2, 16, 16, 8192, 128, True),
     "gqa_b2_hq32_hkv8_n8192_causal": (2, 32, 8, 8192, 128, True),
+    # same token count as the default, shorter rows: the size used for ncu --set full captures
+    "bf16_b4_h16_n4096": (4, 16, 16, 4096, 128, False),
 }
 DEFAULT = "bf16_sweep_d128_n8192"
 LAUNCHES_PER_STEP = 8   # fwd 1, bwd 3, quantise 3, fp8 fwd 1

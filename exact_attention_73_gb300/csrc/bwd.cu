@@ -65,13 +65,13 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
 
 template <int DT>
 cudaError_t launch_main(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q, const CUtensorMap& d,
-                        const BwdArgs& a, int max_len, int nz, cudaStream_t st) {
+                        const CUtensorMap& dq, const BwdArgs& a, int max_len, int nz, cudaStream_t st) {
   using C = BwdCfg<DT, 128>;
   auto kern = bwd_kernel<DT, 128>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const dim3 grid((max_len + C::BC - 1) / C::BC, a.Hkv, nz);
-  kern<<<grid, C::NTHREADS, C::SMEM_BYTES, st>>>(k, v, q, d, a);
+  kern<<<grid, C::NTHREADS, C::SMEM_BYTES, st>>>(k, v, q, d, dq, a);
   return cudaGetLastError();
 }
 
@@ -91,9 +91,10 @@ cudaError_t launch_bwd_pre(int dt, int d, const void* o, const void* dout, float
 }
 
 cudaError_t launch_bwd_main(int dt, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
-                            const CUtensorMap& dout, const BwdArgs& a, int max_len, int nz, cudaStream_t st) {
-  return dt == kBF16 ? launch_main<kBF16>(k, v, q, dout, a, max_len, nz, st)
-                     : launch_main<kFP16>(k, v, q, dout, a, max_len, nz, st);
+                            const CUtensorMap& dout, const CUtensorMap& dq_acc, const BwdArgs& a, int max_len, int nz,
+                            cudaStream_t st) {
+  return dt == kBF16 ? launch_main<kBF16>(k, v, q, dout, dq_acc, a, max_len, nz, st)
+                     : launch_main<kFP16>(k, v, q, dout, dq_acc, a, max_len, nz, st);
 }
 
 cudaError_t launch_dq_convert(int dt, const float* acc, void* dq, long long n, float scale, cudaStream_t st) {

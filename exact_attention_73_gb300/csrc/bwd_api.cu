@@ -46,11 +46,12 @@ attn_status run_bwd(const void* q, const void* k, const void* v, const void* o, 
   float* dq_acc = static_cast<float*>(ws);
   float* dvec = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + round256(static_cast<size_t>(rows) * d * 4));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  CUtensorMap tk, tv, tq, tdo;
+  CUtensorMap tk, tv, tq, tdo, tdq;
   if (!operand_map(&tk, k, dtype, d, packed, B, Hkv, rows_or_T, 128) ||
       !operand_map(&tv, v, dtype, d, packed, B, Hkv, rows_or_T, 128) ||
       !operand_map(&tq, q, dtype, d, packed, B, Hq, rows_or_T, 64) ||
-      !operand_map(&tdo, dout, dtype, d, packed, B, Hq, rows_or_T, 64))
+      !operand_map(&tdo, dout, dtype, d, packed, B, Hq, rows_or_T, 64) ||
+      !accum_map(&tdq, dq_acc, d, packed, B, Hq, rows_or_T, 64))
     return ATTN_ERR_CUDA;
   BwdArgs a{};
   a.lse = lse;
@@ -78,7 +79,7 @@ attn_status run_bwd(const void* q, const void* k, const void* v, const void* o, 
   a.causal = causal ? 1 : 0;
   a.status = status;
   cudaError_t e = launch_bwd_pre(dtype, d, o, dout, dvec, dq_acc, rows, Hq, rows_or_T, packed ? 1 : 0, st);
-  if (e == cudaSuccess) e = launch_bwd_main(dtype, tk, tv, tq, tdo, a, max_len, nz, st);
+  if (e == cudaSuccess) e = launch_bwd_main(dtype, tk, tv, tq, tdo, tdq, a, max_len, nz, st);
   if (e == cudaSuccess) e = launch_dq_convert(dtype, dq_acc, dq, rows * d, scale, st);
   return from_cuda(e);
 }

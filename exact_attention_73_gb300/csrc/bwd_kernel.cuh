@@ -21,10 +21,13 @@
 //     +96..127 dQ^T for queries 32..63
 //   dV [128 keys x 128 dims] cols 256..383, dK cols 384..511.
 // Warp roles: warp 0 loads (TMA for K, V, Q_i, dO_i; plain loads for LSE and
-// D), warp 1 issues tcgen05.mma, warps 4-7 turn S^T/dP^T into P^T/dS^T (one
-// key per thread) and also store dS^T to shared memory (double-buffered) for
-// the dQ product, warps 8-11 drain dQ^T (one head-dim index per thread) with
-// coalesced FP32 atomic adds.
+// D), warp 1 issues tcgen05.mma, warps 4-7 and 12-15 turn S^T/dP^T into
+// P^T/dS^T (one key per thread; the first group takes queries 0..31 of the
+// tile, the second 32..63) and also store dS^T to shared memory
+// (double-buffered) for the dQ product, warps 8-11 drain dQ^T (one head-dim
+// index per thread) into
+// a [64 queries][128 dims] FP32 tile in shared memory, which one thread adds
+// into the global dQ accumulator with a single TMA reduce-add.
 #pragma once
 #include <cmath>
 #include <cstdint>
@@ -66,8 +69,11 @@ struct BwdCfg {
   static constexpr int DS_HALF_B = DS_B / 2;
   static constexpr int NQ = 3;                      // stages of the Q/dO ring
   static constexpr int LD_B = 2 * BR * 4;           // LSE*log2e and D for one tile
-  static constexpr int SMEM_BYTES = 1024 + 2 * KV_B + 2 * DS_B + NQ * (2 * Q_B) + NQ * LD_B + 16 * 8 + 16;
-  static constexpr int NTHREADS = 384;
+  static constexpr int DQ_STAGE_B = BR * D * 4;     // FP32 dQ tile for the reduce-add
+  static constexpr int SMEM_BYTES =
+      1024 + 2 * KV_B + 2 * DS_B + NQ * (2 * Q_B) + DQ_STAGE_B + NQ * LD_B + 16 * 8 + 16;
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeded");
+  static constexpr int NTHREADS = 512;
   static constexpr uint32_t FMT = DT == kBF16 ? 1u : 0u;
   static constexpr uint32_t IDESC_SP = instr_desc(128, BR, FMT, FMT, 0, 0);
   static constexpr uint32_t IDESC_KV = instr_desc(128, D, FMT, FMT, 0, 1);
@@ -77,9 +83,10 @@ struct BwdCfg {
 };
 
 template <int DT, int D>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-           const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO, const BwdArgs a) {
+           const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+           const __grid_constant__ CUtensorMap tmdQ, const BwdArgs a) {
   using C = BwdCfg<DT, D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -88,7 +95,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
   uint8_t* sDS = sV + C::KV_B;                      // [2][DS_B], halves of 32 queries, 64-byte swizzle
   uint8_t* sQ = sDS + 2 * C::DS_B;                  // [NQ][Q_B]
   uint8_t* sdO = sQ + C::NQ * C::Q_B;               // [NQ][Q_B]
-  float* sLD = reinterpret_cast<float*>(sdO + C::NQ * C::Q_B);   // [NQ][2*BR]
+  float* sDQ = reinterpret_cast<float*>(sdO + C::NQ * C::Q_B);   // [BR][D] FP32
+  float* sLD = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(sDQ) + C::DQ_STAGE_B);   // [NQ][2*BR]
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sLD) + C::NQ * C::LD_B);
   uint64_t* kv_full = bars;
   uint64_t* q_full = bars + 1;
@@ -126,6 +134,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmdO);
+    tma_prefetch_desc(&tmdQ);
     mbar_init(kv_full, 1);
     for (int s = 0; s < C::NQ; ++s) {
       mbar_init(&q_full[s], 1);
@@ -133,7 +142,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     }
     mbar_init(&sp_full[0], 1);
     mbar_init(&sp_full[1], 1);
-    mbar_init(ds_ready, 128);
+    mbar_init(ds_ready, 256);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 128);
     mbar_init(done, 1);
@@ -175,8 +184,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       for (int r = lane; r < C::BR; r += 32) {
         const int q = q0 + r;
         const bool ok = q < L;
-        ld[r] = ok ? a.lse[lrow + q] * kLog2e : INFINITY;
-        ld[C::BR + r] = ok ? a.dvec[lrow + q] : 0.f;
+        ld[r] = ok ? -a.lse[lrow + q] * kLog2e : -INFINITY;    // -LSE in log2 units
+        ld[C::BR + r] = ok ? -a.dvec[lrow + q] : 0.f;           // -D
       }
       __syncwarp();
       if (lane == 0) {
@@ -271,13 +280,15 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       mma_commit(done);
     }
     __syncwarp();
-  } else if (warp >= 4 && warp < 8) {
+  } else if ((warp >= 4 && warp < 8) || warp >= 12) {
     // -------------------------------------------------- P^T and dS^T
+    const int half = warp >= 12 ? 1 : 0;            // queries 32*half .. +31 of each tile
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;              // key row of the tile
     const int kloc = j * C::BC + r;                 // key position in the sequence
     const bool kvalid = kloc < L;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const float2 sl2v = make_float2(a.scale_log2, a.scale_log2);
     bool ok = true;
     for (int it = 0; it < niter; ++it) {
       ok = __all_sync(0xffffffffu, mbar_wait(&sp_full[it & 1], (it >> 1) & 1, a.status));
@@ -285,47 +296,63 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       tc_fence_after();
       const uint32_t tS = tbase + lane_off + 128u * (it & 1) + C::COL_S;
       const uint32_t tdP = tbase + lane_off + 128u * (it & 1) + C::COL_DP;
-      uint8_t* ds_row = sDS + (it & 1) * C::DS_B + r * 64;
+      uint8_t* ds_row = sDS + (it & 1) * C::DS_B + half * C::DS_HALF_B + r * 64;
       const int st = it % C::NQ;
       // LSE and D of this stage were written by the load warp before it
       // arrived on q_full[st]; acquire them (the phase is already complete).
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(&q_full[st], (it / C::NQ) & 1, a.status)))) break;
-      const int q0 = (i0 + it % per_head) * C::BR;
-      const float* ld = sLD + st * 2 * C::BR;
+      const int q0 = (i0 + it % per_head) * C::BR + 32 * half;
+      const float* nlse = sLD + st * 2 * C::BR + 32 * half;       // -LSE * log2(e)
+      const float* nd = nlse + C::BR;                             // -D
       const bool diag = a.causal && (q0 < j * C::BC + C::BC - 1);
+      uint32_t sv[32], dp[32];
+      tmem_ld32(tS + 32 * half, sv);
+      tmem_ld32(tdP + 32 * half, dp);
+      tmem_wait_ld();
+      reg_fence(sv);
+      reg_fence(dp);
+      uint32_t pp[16], dd[16];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t s[32], dp[32];
-        tmem_ld32(tS + 32 * half, s);
-        tmem_ld32(tdP + 32 * half, dp);
-        tmem_wait_ld();
-        reg_fence(s);
-        reg_fence(dp);
-        uint32_t pp[16], dd[16];
+      for (int e4 = 0; e4 < 8; ++e4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(nlse + 4 * e4);
+        const float4 d4 = *reinterpret_cast<const float4*>(nd + 4 * e4);
+        float2 x01 = ffma2(make_float2(__uint_as_float(sv[4 * e4]), __uint_as_float(sv[4 * e4 + 1])), sl2v,
+                           make_float2(l4.x, l4.y));
+        float2 x23 = ffma2(make_float2(__uint_as_float(sv[4 * e4 + 2]), __uint_as_float(sv[4 * e4 + 3])), sl2v,
+                           make_float2(l4.z, l4.w));
+        float p[4] = {ex2(x01.x), ex2(x01.y), ex2(x23.x), ex2(x23.y)};
+        if (!kvalid || diag) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float p[2], g[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int c = 32 * half + 2 * e + u;
-            float pv = ex2(fmaf(__uint_as_float(s[2 * e + u]), a.scale_log2, -ld[c]));
-            if (!kvalid || (diag && kloc > q0 + c)) pv = 0.f;
-            p[u] = pv;
-            g[u] = pv * (__uint_as_float(dp[2 * e + u]) - ld[C::BR + c]);
-          }
-          pp[e] = (DT == kBF16) ? pack_bf16x2(p[0], p[1]) : pack_f16x2(p[0], p[1]);
-          dd[e] = (DT == kBF16) ? pack_bf16x2(g[0], g[1]) : pack_f16x2(g[0], g[1]);
+          for (int u = 0; u < 4; ++u)
+            if (!kvalid || kloc > q0 + 4 * e4 + u) p[u] = 0.f;
         }
-        tmem_st16(tS + 16 * half, pp);
-        tmem_st16(tdP + 16 * half, dd);
-        // dS^T row r, queries 32*half .. +31 into half `half`: four 16-byte
-        // chunks of a 64-byte row, 64-byte swizzle (chunk ^= (row / 2) % 4)
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          const int chunk = c4 ^ ((r >> 1) & 3);
-          *reinterpret_cast<uint4*>(ds_row + half * C::DS_HALF_B + chunk * 16) =
-              make_uint4(dd[4 * c4], dd[4 * c4 + 1], dd[4 * c4 + 2], dd[4 * c4 + 3]);
+        const float2 t01 = fadd2(make_float2(__uint_as_float(dp[4 * e4]), __uint_as_float(dp[4 * e4 + 1])),
+                                 make_float2(d4.x, d4.y));
+        const float2 t23 = fadd2(make_float2(__uint_as_float(dp[4 * e4 + 2]), __uint_as_float(dp[4 * e4 + 3])),
+                                 make_float2(d4.z, d4.w));
+        const float2 g01 = fmul2(make_float2(p[0], p[1]), t01);
+        const float2 g23 = fmul2(make_float2(p[2], p[3]), t23);
+        if constexpr (DT == kBF16) {
+          pp[2 * e4] = pack_bf16x2(p[0], p[1]);
+          pp[2 * e4 + 1] = pack_bf16x2(p[2], p[3]);
+          dd[2 * e4] = pack_bf16x2(g01.x, g01.y);
+          dd[2 * e4 + 1] = pack_bf16x2(g23.x, g23.y);
+        } else {
+          pp[2 * e4] = pack_f16x2(p[0], p[1]);
+          pp[2 * e4 + 1] = pack_f16x2(p[2], p[3]);
+          dd[2 * e4] = pack_f16x2(g01.x, g01.y);
+          dd[2 * e4 + 1] = pack_f16x2(g23.x, g23.y);
         }
+      }
+      tmem_st16(tS + 16 * half, pp);
+      tmem_st16(tdP + 16 * half, dd);
+      // dS^T row r of this half: four 16-byte chunks of a 64-byte row,
+      // 64-byte swizzle (chunk ^= (row / 2) % 4)
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const int chunk = c4 ^ ((r >> 1) & 3);
+        *reinterpret_cast<uint4*>(ds_row + chunk * 16) =
+            make_uint4(dd[4 * c4], dd[4 * c4 + 1], dd[4 * c4 + 2], dd[4 * c4 + 3]);
       }
       tmem_wait_st();
       fence_proxy_async_smem();
@@ -334,11 +361,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(done, 0, a.status));
     tc_fence_after();
-    if (ok) {   // dV rows
+    if (ok) {   // dV rows, columns 64*half .. +63
       const long long off = static_cast<long long>(b) * a.k_sb + static_cast<long long>(hkv) * a.k_sh +
                             static_cast<long long>(seq0 + kloc) * a.k_sn;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 2 * half; c < 2 * half + 2; ++c) {
         uint32_t v[32];
         tmem_ld32(tbase + lane_off + C::COL_DV + 32 * c, v);
         tmem_wait_ld();
@@ -355,14 +382,16 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         }
       }
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 8 && warp < 12) {
     // ---------------------------------------------------- dQ^T drain
     const int quarter = warp & 3;
     const int dim = quarter * 32 + lane;            // head-dim index = tensor-memory lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     bool ok = true;
     for (int it = 0; it < niter; ++it) {
-      ok = __all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, a.status));
+      // one decision for all four drain warps, so none is left alone at the
+      // named barriers below
+      ok = named_bar_and(1, 128, __all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, a.status)));
       if (!ok) break;
       tc_fence_after();
       uint32_t x0[32], x1[32];
@@ -375,16 +404,25 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       mbar_arrive(dq_empty);
       const int h = hkv * a.group + it / per_head;
       const int q0 = (i0 + it % per_head) * C::BR;
-      float* base = a.dq_acc + static_cast<long long>(b) * a.q_sb + static_cast<long long>(h) * a.q_sh +
-                    static_cast<long long>(seq0) * a.q_sn + dim;
-      const int nvalid = min(C::BR, L - q0);
+      // the previous reduce-add must have finished reading the staging tile
+      if (threadIdx.x == 256) bulk_wait_read_all();
+      named_bar_sync(1, 128);
 #pragma unroll
-      for (int e = 0; e < 32; ++e)
-        if (e < nvalid) atomicAdd(base + static_cast<long long>(q0 + e) * a.q_sn, __uint_as_float(x0[e]));
+      for (int e = 0; e < 32; ++e) sDQ[e * D + dim] = __uint_as_float(x0[e]);
 #pragma unroll
-      for (int e = 0; e < 32; ++e)
-        if (32 + e < nvalid) atomicAdd(base + static_cast<long long>(q0 + 32 + e) * a.q_sn, __uint_as_float(x1[e]));
+      for (int e = 0; e < 32; ++e) sDQ[(32 + e) * D + dim] = __uint_as_float(x1[e]);
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      // Rows past the sequence hold exact zeros (P = 0 there): for the dense
+      // layout the map clips them, for the packed layout they add 0 to the
+      // next sequence's rows.
+      if (threadIdx.x == 256) {
+        if (packed) tma_reduce_add_4d(&tmdQ, sDQ, 0, h, seq0 + q0, 0);
+        else tma_reduce_add_4d(&tmdQ, sDQ, 0, q0, h, b);
+        bulk_commit();
+      }
     }
+    if (threadIdx.x == 256) bulk_wait_all();
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(done, 0, a.status));
     tc_fence_after();
     if (ok) {   // dK rows, times scale

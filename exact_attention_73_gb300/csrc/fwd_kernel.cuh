@@ -69,10 +69,13 @@ struct FwdCfg {
   static constexpr int NSLOT_RAW = (BUDGET - Q_B) / TILE_B;
   static constexpr int NSLOT = NSLOT_RAW > 8 ? 8 : NSLOT_RAW;
   static_assert(NSLOT >= 2, "shared memory too small for the K/V ring");
-  static constexpr int O_COL = QT * 128;                    // O_t at O_COL + t * D
+  // Score buffers in tensor memory: one per query tile, or two alternating
+  // buffers when the CTA has a single query tile.
+  static constexpr int NSB = QT == 1 ? 2 : QT;
+  static constexpr int O_COL = NSB * 128;                   // O_t at O_COL + t * D
   static_assert(O_COL + QT * D <= 512, "tensor memory overflow");
   static constexpr int NTHREADS = 128 + 128 * QT;
-  static constexpr int NBAR = 1 + 2 * NSLOT + 2 * QT + 1;
+  static constexpr int NBAR = 1 + 2 * NSLOT + 2 * NSB + 2;
   static constexpr int SMEM_BYTES = 1024 + Q_B + NSLOT * TILE_B + NBAR * 8 + 16;
   static constexpr uint32_t FMT = DT == kBF16 ? 1u : 0u;    // BF16=1, F16=0, E4M3=0
   static constexpr uint32_t IDESC_S = instr_desc(128, 128, FMT, FMT, 0, 0);
@@ -90,6 +93,28 @@ __device__ __forceinline__ float exp2i(int e) {               // exact 2^e, |e| 
   return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
 }
 
+// Order of the K/V tiles through the shared-memory ring. Two-tile CTAs load
+// K0 V0 K1 V1 ...; single-tile CTAs (two score buffers) consume K0 K1 V0 K2
+// V1 K3 ... V(n-1) and load in that order, so K(j+2) never waits behind V(j+1).
+__device__ __forceinline__ void kv_item(int qt, int it, int nkv, bool& is_v, int& j) {
+  if (qt != 1) {
+    is_v = it & 1;
+    j = it >> 1;
+    return;
+  }
+  if (nkv == 1) { is_v = it == 1; j = 0; return; }
+  if (it < 2) { is_v = false; j = it; return; }
+  if (it == 2 * nkv - 1) { is_v = true; j = nkv - 1; return; }
+  const int r = it - 2;
+  is_v = (r & 1) == 0;
+  j = is_v ? (r >> 1) : (r >> 1) + 2;
+}
+__device__ __forceinline__ int kv_index_k(int qt, int j) { return qt != 1 ? 2 * j : (j < 2 ? j : 2 * j - 1); }
+__device__ __forceinline__ int kv_index_v(int qt, int j, int nkv) {
+  if (qt != 1) return 2 * j + 1;
+  return nkv == 1 ? 1 : (j == nkv - 1 ? 2 * nkv - 1 : 2 + 2 * j);
+}
+
 template <int DT, int D, int QT>
 __global__ void __launch_bounds__(FwdCfg<DT, D, QT>::NTHREADS, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -103,10 +128,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = kv_full + C::NSLOT;
-  uint64_t* s_full = kv_empty + C::NSLOT;
-  uint64_t* p_ready = s_full + QT;
-  uint64_t* o_final = p_ready + QT;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(o_final + 1);
+  uint64_t* s_full = kv_empty + C::NSLOT;          // [NSB]
+  uint64_t* p_ready = s_full + C::NSB;             // [NSB]
+  uint64_t* o_final = p_ready + C::NSB;
+  uint64_t* o_done = o_final + 1;                  // one phase per O += P V (single-tile CTAs)
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(o_done + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -139,11 +165,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int t = 0; t < QT; ++t) {
+    for (int t = 0; t < C::NSB; ++t) {
       mbar_init(&s_full[t], 1);
       mbar_init(&p_ready[t], 128);
     }
     mbar_init(o_final, 1);
+    mbar_init(o_done, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -171,8 +198,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         const int slot = it % C::NSLOT;
         if (!mbar_wait(&kv_empty[slot], ((it / C::NSLOT) & 1) ^ 1, a.status)) break;
         mbar_arrive_expect_tx(&kv_full[slot], C::TILE_B);
-        const CUtensorMap* m = (it & 1) ? &tmV : &tmK;
-        const int row = seq0 + (it >> 1) * 128;
+        bool is_v;
+        int jt;
+        kv_item(QT, it, nkv, is_v, jt);
+        const CUtensorMap* m = is_v ? &tmV : &tmK;
+        const int row = seq0 + jt * 128;
         for (int c = 0; c < C::NBOX; ++c) {
           uint8_t* dst = sKV + slot * C::TILE_B + c * C::BOXT_B;
           if (packed) tma_load_4d(dst, m, &kv_full[slot], c * C::BOX_E, hkv, row, 0);
@@ -190,45 +220,90 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       //   PV_0(j), S_0(j+1), PV_1(j), S_1(j+1)
       // so the softmax of tile t for step j+1 overlaps the other tile's PV(j)
       // and S(j+1) (two GEMMs of slack).
-      auto issue_s = [&](int t, int slot) {
+      // S_t = Q_t K^T into score buffer sb
+      auto issue_s = [&](int t, int sb, int slot) {
 #pragma unroll
         for (int kk = 0; kk < D / C::KSTEP_E; ++kk) {
           const uint32_t off = (kk * C::KSTEP_B / C::BOX_B) * C::BOXT_B + (kk * C::KSTEP_B) % C::BOX_B;
           const uint64_t ad = smem_desc(q_addr + t * C::TILE_B + off, 16, C::SBO, C::SWZ);
           const uint64_t bd = smem_desc(kv_addr + slot * C::TILE_B + off, 16, C::SBO, C::SWZ);
-          mma_ss<C::kFp8>(tbase + t * 128, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
+          mma_ss<C::kFp8>(tbase + sb * 128, ad, bd, C::IDESC_S, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&s_full[t]);
+        mma_commit(&s_full[sb]);
       };
-      auto issue_pv = [&](int t, int slot, int j) {
+      // O_t += P V with P in score buffer sb
+      auto issue_pv = [&](int t, int sb, int slot, int j) {
 #pragma unroll
         for (int kk = 0; kk < 128 / C::KSTEP_E; ++kk) {
           const uint64_t bd = smem_desc(kv_addr + slot * C::TILE_B + kk * C::KSTEP_E * C::BOX_B,
                                         C::BOXT_B, C::SBO, C::SWZ);
-          mma_ts<C::kFp8>(tbase + C::O_COL + t * D, tbase + t * 128 + kk * 8, bd, C::IDESC_O,
+          mma_ts<C::kFp8>(tbase + C::O_COL + t * D, tbase + sb * 128 + kk * 8, bd, C::IDESC_O,
                           (j > 0 || kk > 0) ? 1u : 0u);
         }
       };
+      auto kv_wait = [&](int it) {
+        return mbar_wait(&kv_full[it % C::NSLOT], (it / C::NSLOT) & 1, a.status);
+      };
       bool ok = mbar_wait(q_full, 0, a.status) && mbar_wait(&kv_full[0], 0, a.status);
+      if constexpr (QT == 1) {
+        // One query tile, two score buffers: S(j+2) is issued right after
+        // PV(j), so the softmax of step j+1 overlaps PV(j) and S(j+2).
+        if (ok) {
+          tc_fence_after();
+          issue_s(0, 0, 0);
+          mma_commit(&kv_empty[0]);
+        }
+        if (ok && nkv > 1) {
+          const int itk1 = kv_index_k(1, 1);
+          if ((ok = kv_wait(itk1))) {
+            tc_fence_after();
+            issue_s(0, 1, itk1 % C::NSLOT);
+            mma_commit(&kv_empty[itk1 % C::NSLOT]);
+          }
+        }
+        for (int j = 0; j < nkv && ok; ++j) {
+          const int itv = kv_index_v(1, j, nkv), itk = j + 2 < nkv ? kv_index_k(1, j + 2) : 0;
+          if (!(ok = kv_wait(itv))) break;
+          if (!(ok = mbar_wait(&p_ready[j & 1], (j >> 1) & 1, a.status))) break;
+          tc_fence_after();
+          issue_pv(0, j & 1, itv % C::NSLOT, j);
+          mma_commit(o_done);
+          mma_commit(&kv_empty[itv % C::NSLOT]);
+          if (j + 2 < nkv) {
+            if (!(ok = kv_wait(itk))) break;
+            tc_fence_after();
+            issue_s(0, j & 1, itk % C::NSLOT);
+            mma_commit(&kv_empty[itk % C::NSLOT]);
+          }
+        }
+        ok = false;   // the two-tile schedule below is not used
+      }
       if (ok) {
         tc_fence_after();
-        for (int t = 0; t < QT; ++t) issue_s(t, 0);
+        for (int t = 0; t < QT; ++t) issue_s(t, t, 0);
         mma_commit(&kv_empty[0]);
       }
       for (int j = 0; j < nkv && ok; ++j) {
         const int itv = 2 * j + 1, sv_ = itv % C::NSLOT;
         const int itk = 2 * j + 2, sk_ = itk % C::NSLOT;
         const bool next = j + 1 < nkv;
-        if (!(ok = mbar_wait(&kv_full[sv_], (itv / C::NSLOT) & 1, a.status))) break;
-        if (next && !(ok = mbar_wait(&kv_full[sk_], (itk / C::NSLOT) & 1, a.status))) break;
+        if (!(ok = kv_wait(itv))) break;
+        bool k_ready = false;
         for (int t = 0; t < QT && ok; ++t) {
           if (!(ok = mbar_wait(&p_ready[t], j & 1, a.status))) break;
           tc_fence_after();
-          issue_pv(t, sv_, j);
-          if (next) issue_s(t, sk_);
+          issue_pv(t, t, sv_, j);
+          if (next) {
+            if (!k_ready) {                 // K(j+1) is needed only now
+              if (!(ok = kv_wait(itk))) break;
+              tc_fence_after();
+              k_ready = true;
+            }
+            issue_s(t, t, sk_);
+          }
         }
         mma_commit(&kv_empty[sv_]);
-        if (next) mma_commit(&kv_empty[sk_]);
+        if (next && k_ready) mma_commit(&kv_empty[sk_]);
       }
       mma_commit(o_final);
     }
@@ -241,7 +316,6 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     const int qtile = qt0 + t;
     const int qrow = qtile * 128 + row;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tbase + lane_off + t * 128;
     const uint32_t tO = tbase + lane_off + C::O_COL + t * D;
     float m = -INFINITY;     // running max of x = S * scale * log2(e)
     float l = 0.f;           // running sum of exp2(x - m)
@@ -254,7 +328,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     }
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, a.status));
+      const int sb = QT == 1 ? (j & 1) : t;              // score buffer of this step
+      const uint32_t sphase = QT == 1 ? ((j >> 1) & 1) : (j & 1);
+      const uint32_t tS = tbase + lane_off + sb * 128;
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], sphase, a.status));
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[128];
@@ -291,6 +368,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       l *= corr;
       m = m_new;
       if (j > 0 && warp_any(corr_o != 1.f)) {
+        if constexpr (QT == 1) {   // PV(j-1) may still be running with two score buffers
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, a.status)))) break;
+          tc_fence_after();
+        }
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
@@ -351,7 +432,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_ready[t]);
+      mbar_arrive(&p_ready[sb]);
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_final, 0, a.status));
     tc_fence_after();

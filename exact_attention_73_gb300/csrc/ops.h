@@ -16,7 +16,10 @@ bool operand_map(CUtensorMap* m, const void* base, int dt, int d, bool packed, i
 cudaError_t launch_bwd_pre(int dt, int d, const void* o, const void* dout, float* dvec, float* dq_acc,
                            long long rows, int Hq, int T_tokens, int packed, cudaStream_t st);
 cudaError_t launch_bwd_main(int dt, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
-                            const CUtensorMap& dout, const BwdArgs& a, int max_len, int nz, cudaStream_t st);
+                            const CUtensorMap& dout, const CUtensorMap& dq_acc, const BwdArgs& a, int max_len, int nz,
+                            cudaStream_t st);
+// FP32 accumulator map (layout of the operands, no swizzle), boxes of d x box_rows.
+bool accum_map(CUtensorMap* m, const float* base, int d, bool packed, int B, int H, long long rows, int box_rows);
 cudaError_t launch_dq_convert(int dt, const float* acc, void* dq, long long n, float scale, cudaStream_t st);
 
 // Block quantisation to E4M3 (see attn_quantize_fp8).
