@@ -48,6 +48,24 @@ def fwd_flops(B, Hq, N, d, causal):
     return f / 2 if causal else f
 
 
+def max_over_ranks(values, world, device="cpu"):
+    """Elementwise maximum of a list of floats over all ranks (the job's time)."""
+    import torch
+    t = torch.tensor(values, dtype=torch.float64)
+    if world > 1:
+        import torch.distributed as dist
+        t = t.to(device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t = t.cpu()
+    return [float(x) for x in t]
+
+
+def job_tflops(step_flops, steps, world, ms):
+    """Whole-job throughput: every rank ran `steps` steps of `step_flops`; the
+    job took the slowest rank's `ms`."""
+    return world * step_flops * steps / (ms * 1e-3) / 1e12
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -73,7 +91,7 @@ class Clocks:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -206,13 +224,8 @@ def bench_ours(args, wl, rank, world):
     barrier()
     ms_e2e = e0.elapsed_time(e1)
 
-    times = torch.tensor([ms_total, ms_e2e], dtype=torch.float64)
-    if world > 1:
-        import torch.distributed as dist
-        t = times.to(dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        times = t.cpu()
-    return {"ms_total": float(times[0]), "ms_e2e": float(times[1]), "stage_ms": stage, "clocks": clk,
+    ms_total, ms_e2e = max_over_ranks([ms_total, ms_e2e], world, dev)
+    return {"ms_total": ms_total, "ms_e2e": ms_e2e, "stage_ms": stage, "clocks": clk,
             "h2d": h2d, "d2h": d2h}
 
 
@@ -250,7 +263,7 @@ def cpu_cores():
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT)
@@ -290,8 +303,8 @@ def main():
     r = bench_ours(args, wl, rank, world)
     pk = peaks()
     ms_step = r["ms_total"] / args.steps
-    value = world * step_flops * args.steps / (r["ms_total"] * 1e-3) / 1e12
-    e2e_val = world * step_flops * args.steps / (r["ms_e2e"] * 1e-3) / 1e12
+    value = job_tflops(step_flops, args.steps, world, r["ms_total"])
+    e2e_val = job_tflops(step_flops, args.steps, world, r["ms_e2e"])
     st = r["stage_ms"]
     f = fwd_flops(B, Hq, N, d, causal)
     stages = {

@@ -207,7 +207,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA
     // Order: SdP(0); per iteration it: SdP(it+1) into the other buffer, then
-    // (after P^T/dS^T of it are ready) dV, dK and the two dQ^T halves of it.
+    // (after P^T/dS^T of it are ready) the two dQ^T halves, dV and dK of it.
     if (lane == 0) {
       const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), ds_addr = smem_u32(sDS);
       auto issue_sdp = [&](int it) {   // S^T = K Q^T and dP^T = V dO^T into buffer it % 2
@@ -251,18 +251,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         tc_fence_after();
         const uint32_t q_addr = smem_u32(sQ + st * C::Q_B);
         const uint32_t do_addr = smem_u32(sdO + st * C::Q_B);
-#pragma unroll
-        for (int kk = 0; kk < C::BR / 16; ++kk) {   // dV += P^T dO_i
-          mma_ts<false>(tbase + C::COL_DV, xb + C::COL_S + kk * 8,
-                        smem_desc(do_addr + kk * 2048, C::Q_BOX_B, 1024, kSwizzle128), C::IDESC_KV,
-                        (it > 0 || kk > 0) ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < C::BR / 16; ++kk) {   // dK += dS^T Q_i
-          mma_ts<false>(tbase + C::COL_DK, xb + C::COL_DP + kk * 8,
-                        smem_desc(q_addr + kk * 2048, C::Q_BOX_B, 1024, kSwizzle128), C::IDESC_KV,
-                        (it > 0 || kk > 0) ? 1u : 0u);
-        }
+        // dQ^T first, so the drain warps can read it while dV and dK run and
+        // the next S^T/dP^T never waits for an empty tensor pipe
         const uint32_t dsb = ds_addr + (it & 1) * C::DS_B;
 #pragma unroll
         for (int hq = 0; hq < 2; ++hq) {            // dQ^T (32 queries) = K^T dS^T, both MN-major
@@ -275,6 +265,18 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
           }
         }
         mma_commit(dq_full);
+#pragma unroll
+        for (int kk = 0; kk < C::BR / 16; ++kk) {   // dV += P^T dO_i
+          mma_ts<false>(tbase + C::COL_DV, xb + C::COL_S + kk * 8,
+                        smem_desc(do_addr + kk * 2048, C::Q_BOX_B, 1024, kSwizzle128), C::IDESC_KV,
+                        (it > 0 || kk > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < C::BR / 16; ++kk) {   // dK += dS^T Q_i
+          mma_ts<false>(tbase + C::COL_DK, xb + C::COL_DP + kk * 8,
+                        smem_desc(q_addr + kk * 2048, C::Q_BOX_B, 1024, kSwizzle128), C::IDESC_KV,
+                        (it > 0 || kk > 0) ? 1u : 0u);
+        }
         mma_commit(&q_empty[st]);
       }
       mma_commit(done);
