@@ -14,18 +14,19 @@
 // and are written once (no atomics on dK/dV). Tensor memory (512 columns),
 // with the score buffers doubled so that S^T/dP^T of the next query tile are
 // computed while the current one is being turned into P^T/dS^T:
-//   buffer X (X = 0, 1) at cols 128X:
-//     +0..31   P^T  (BF16, written over S^T [128 keys x 64 queries] at +0..63)
-//     +32..63  dQ^T for queries 0..31  (after S^T has been consumed)
-//     +64..95  dS^T (BF16, written over dP^T at +64..127)
-//     +96..127 dQ^T for queries 32..63
+//   buffer X (X = 0, 1) at cols 128X: S^T [128 keys x 64 queries] at +0..63
+//   and dP^T at +64..127; once both are in registers they are replaced by
+//     +0..31   P^T  (BF16 pairs)
+//     +32..95  dQ^T [128 dims x 64 queries] (FP32, one N = 64 product)
+//     +96..127 dS^T (BF16 pairs)
 //   dV [128 keys x 128 dims] cols 256..383, dK cols 384..511.
 // Warp roles: warp 0 loads (TMA for K, V, Q_i, dO_i; plain loads for LSE and
 // D), warp 1 issues tcgen05.mma, warps 4-7 and 12-15 turn S^T/dP^T into
 // P^T/dS^T (one key per thread; the first group takes queries 0..31 of the
-// tile, the second 32..63) and also store dS^T to shared memory
-// (double-buffered) for the dQ product, warps 8-11 drain dQ^T (one head-dim
-// index per thread) into
+// tile, the second 32..63; the two meet at a barrier between loading S^T/dP^T
+// and writing P^T/dS^T over them) and also store dS^T to shared memory
+// (double-buffered, 128-byte swizzle) for the dQ product, warps 8-11 drain
+// dQ^T (one head-dim index per thread) into
 // a [64 queries][128 dims] FP32 tile in shared memory, which one thread adds
 // into the global dQ accumulator with a single TMA reduce-add.
 #pragma once
@@ -65,8 +66,7 @@ struct BwdCfg {
   static constexpr int KV_BOX_B = BC * 128;
   static constexpr int Q_B = BR * D * 2;            // Q_i or dO_i tile
   static constexpr int Q_BOX_B = BR * 128;
-  static constexpr int DS_B = BC * BR * 2;          // dS^T tile: two [128 keys][32 queries] halves
-  static constexpr int DS_HALF_B = DS_B / 2;
+  static constexpr int DS_B = BC * BR * 2;          // dS^T tile [128 keys][64 queries]
   static constexpr int NQ = 3;                      // stages of the Q/dO ring
   static constexpr int LD_B = 2 * BR * 4;           // LSE*log2e and D for one tile
   static constexpr int DQ_STAGE_B = BR * D * 4;     // FP32 dQ tile for the reduce-add
@@ -77,9 +77,10 @@ struct BwdCfg {
   static constexpr uint32_t FMT = DT == kBF16 ? 1u : 0u;
   static constexpr uint32_t IDESC_SP = instr_desc(128, BR, FMT, FMT, 0, 0);
   static constexpr uint32_t IDESC_KV = instr_desc(128, D, FMT, FMT, 0, 1);
-  static constexpr uint32_t IDESC_DQ = instr_desc(D, 32, FMT, FMT, 1, 1);
-  // within score buffer X (base 128X): S^T/P^T, dQ^T low half, dP^T/dS^T, dQ^T high half
-  static constexpr uint32_t COL_S = 0, COL_DQ0 = 32, COL_DP = 64, COL_DQ1 = 96, COL_DV = 256, COL_DK = 384;
+  static constexpr uint32_t IDESC_DQ = instr_desc(D, BR, FMT, FMT, 1, 1);
+  // within score buffer X (base 128X)
+  static constexpr uint32_t COL_S = 0, COL_DP = 64, COL_P = 0, COL_DQ = 32, COL_DS = 96;
+  static constexpr uint32_t COL_DV = 256, COL_DK = 384;
 };
 
 template <int DT, int D>
@@ -92,7 +93,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem;
   uint8_t* sV = sK + C::KV_B;
-  uint8_t* sDS = sV + C::KV_B;                      // [2][DS_B], halves of 32 queries, 64-byte swizzle
+  uint8_t* sDS = sV + C::KV_B;                      // [2][DS_B], 128-byte swizzle
   uint8_t* sQ = sDS + 2 * C::DS_B;                  // [NQ][Q_B]
   uint8_t* sdO = sQ + C::NQ * C::Q_B;               // [NQ][Q_B]
   float* sDQ = reinterpret_cast<float*>(sdO + C::NQ * C::Q_B);   // [BR][D] FP32
@@ -209,25 +210,31 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     // Order: SdP(0); per iteration it: SdP(it+1) into the other buffer, then
     // (after P^T/dS^T of it are ready) the two dQ^T halves, dV and dK of it.
     if (lane == 0) {
-      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), ds_addr = smem_u32(sDS);
+      // Descriptors are built once; a byte offset is added to the
+      // start-address field (16-byte units) for each K step and stage.
+      const uint64_t dK_kmaj = smem_desc(smem_u32(sK), 16, 1024, kSwizzle128);
+      const uint64_t dV_kmaj = smem_desc(smem_u32(sV), 16, 1024, kSwizzle128);
+      const uint64_t dK_mn = smem_desc(smem_u32(sK), C::KV_BOX_B, 1024, kSwizzle128);
+      const uint64_t dQ0_kmaj = smem_desc(smem_u32(sQ), 16, 1024, kSwizzle128);
+      const uint64_t ddO0_kmaj = smem_desc(smem_u32(sdO), 16, 1024, kSwizzle128);
+      const uint64_t dQ0_mn = smem_desc(smem_u32(sQ), C::Q_BOX_B, 1024, kSwizzle128);
+      const uint64_t ddO0_mn = smem_desc(smem_u32(sdO), C::Q_BOX_B, 1024, kSwizzle128);
+      const uint64_t dDS0_mn = smem_desc(smem_u32(sDS), C::DS_B, 1024, kSwizzle128);
+      auto dadd = [](uint64_t d, uint32_t bytes) { return d + (bytes >> 4); };
       auto issue_sdp = [&](int it) {   // S^T = K Q^T and dP^T = V dO^T into buffer it % 2
-        const int st = it % C::NQ;
-        const uint32_t q_addr = smem_u32(sQ + st * C::Q_B);
-        const uint32_t do_addr = smem_u32(sdO + st * C::Q_B);
+        const uint32_t so = (it % C::NQ) * C::Q_B;
         const uint32_t xb = tbase + 128u * (it & 1);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t offk = (kk / 4) * C::KV_BOX_B + (kk % 4) * 32;
-          const uint32_t offq = (kk / 4) * C::Q_BOX_B + (kk % 4) * 32;
-          mma_ss<false>(xb + C::COL_S, smem_desc(k_addr + offk, 16, 1024, kSwizzle128),
-                        smem_desc(q_addr + offq, 16, 1024, kSwizzle128), C::IDESC_SP, kk > 0);
+          const uint32_t offq = so + (kk / 4) * C::Q_BOX_B + (kk % 4) * 32;
+          mma_ss<false>(xb + C::COL_S, dadd(dK_kmaj, offk), dadd(dQ0_kmaj, offq), C::IDESC_SP, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t offk = (kk / 4) * C::KV_BOX_B + (kk % 4) * 32;
-          const uint32_t offq = (kk / 4) * C::Q_BOX_B + (kk % 4) * 32;
-          mma_ss<false>(xb + C::COL_DP, smem_desc(v_addr + offk, 16, 1024, kSwizzle128),
-                        smem_desc(do_addr + offq, 16, 1024, kSwizzle128), C::IDESC_SP, kk > 0);
+          const uint32_t offq = so + (kk / 4) * C::Q_BOX_B + (kk % 4) * 32;
+          mma_ss<false>(xb + C::COL_DP, dadd(dV_kmaj, offk), dadd(ddO0_kmaj, offq), C::IDESC_SP, kk > 0);
         }
         mma_commit(&sp_full[it & 1]);
       };
@@ -249,32 +256,23 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         }
         if (!(ok = mbar_wait(ds_ready, it & 1, a.status))) break;
         tc_fence_after();
-        const uint32_t q_addr = smem_u32(sQ + st * C::Q_B);
-        const uint32_t do_addr = smem_u32(sdO + st * C::Q_B);
+        const uint32_t so = st * C::Q_B;
         // dQ^T first, so the drain warps can read it while dV and dK run and
         // the next S^T/dP^T never waits for an empty tensor pipe
-        const uint32_t dsb = ds_addr + (it & 1) * C::DS_B;
 #pragma unroll
-        for (int hq = 0; hq < 2; ++hq) {            // dQ^T (32 queries) = K^T dS^T, both MN-major
-#pragma unroll
-          for (int kk = 0; kk < C::BC / 16; ++kk) {
-            mma_ss<false>(xb + (hq ? C::COL_DQ1 : C::COL_DQ0),
-                          smem_desc(k_addr + kk * 2048, C::KV_BOX_B, 1024, kSwizzle128),
-                          smem_desc(dsb + hq * C::DS_HALF_B + kk * 1024, C::DS_HALF_B, 512, kSwizzle64),
-                          C::IDESC_DQ, kk > 0);
-          }
+        for (int kk = 0; kk < C::BC / 16; ++kk) {   // dQ^T = K^T dS^T, both MN-major
+          mma_ss<false>(xb + C::COL_DQ, dadd(dK_mn, kk * 2048), dadd(dDS0_mn, (it & 1) * C::DS_B + kk * 2048),
+                        C::IDESC_DQ, kk > 0);
         }
         mma_commit(dq_full);
 #pragma unroll
         for (int kk = 0; kk < C::BR / 16; ++kk) {   // dV += P^T dO_i
-          mma_ts<false>(tbase + C::COL_DV, xb + C::COL_S + kk * 8,
-                        smem_desc(do_addr + kk * 2048, C::Q_BOX_B, 1024, kSwizzle128), C::IDESC_KV,
+          mma_ts<false>(tbase + C::COL_DV, xb + C::COL_P + kk * 8, dadd(ddO0_mn, so + kk * 2048), C::IDESC_KV,
                         (it > 0 || kk > 0) ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < C::BR / 16; ++kk) {   // dK += dS^T Q_i
-          mma_ts<false>(tbase + C::COL_DK, xb + C::COL_DP + kk * 8,
-                        smem_desc(q_addr + kk * 2048, C::Q_BOX_B, 1024, kSwizzle128), C::IDESC_KV,
+          mma_ts<false>(tbase + C::COL_DK, xb + C::COL_DS + kk * 8, dadd(dQ0_mn, so + kk * 2048), C::IDESC_KV,
                         (it > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&q_empty[st]);
@@ -293,26 +291,30 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     const float2 sl2v = make_float2(a.scale_log2, a.scale_log2);
     bool ok = true;
     for (int it = 0; it < niter; ++it) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&sp_full[it & 1], (it >> 1) & 1, a.status));
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t tS = tbase + lane_off + 128u * (it & 1) + C::COL_S;
-      const uint32_t tdP = tbase + lane_off + 128u * (it & 1) + C::COL_DP;
-      uint8_t* ds_row = sDS + (it & 1) * C::DS_B + half * C::DS_HALF_B + r * 64;
+      const uint32_t xb = tbase + lane_off + 128u * (it & 1);
+      uint8_t* ds_row = sDS + (it & 1) * C::DS_B + r * 128;
       const int st = it % C::NQ;
-      // LSE and D of this stage were written by the load warp before it
-      // arrived on q_full[st]; acquire them (the phase is already complete).
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&q_full[st], (it / C::NQ) & 1, a.status)))) break;
+      // S^T/dP^T of this tile, then LSE and D of this stage (written by the
+      // load warp before it arrived on q_full[st]; that phase is complete)
+      bool got = __all_sync(0xffffffffu, mbar_wait(&sp_full[it & 1], (it >> 1) & 1, a.status));
+      if (got) got = __all_sync(0xffffffffu, mbar_wait(&q_full[st], (it / C::NQ) & 1, a.status));
+      uint32_t sv[32], dp[32];
+      if (got) {
+        tc_fence_after();
+        tmem_ld32(xb + C::COL_S + 32 * half, sv);
+        tmem_ld32(xb + C::COL_DP + 32 * half, dp);
+        tmem_wait_ld();
+        reg_fence(sv);
+        reg_fence(dp);
+      }
+      // Both groups have their scores in registers before either overwrites
+      // columns the other reads; one decision for both groups.
+      ok = named_bar_and(2, 256, got);
+      if (!ok) break;
       const int q0 = (i0 + it % per_head) * C::BR + 32 * half;
       const float* nlse = sLD + st * 2 * C::BR + 32 * half;       // -LSE * log2(e)
       const float* nd = nlse + C::BR;                             // -D
       const bool diag = a.causal && (q0 < j * C::BC + C::BC - 1);
-      uint32_t sv[32], dp[32];
-      tmem_ld32(tS + 32 * half, sv);
-      tmem_ld32(tdP + 32 * half, dp);
-      tmem_wait_ld();
-      reg_fence(sv);
-      reg_fence(dp);
       uint32_t pp[16], dd[16];
 #pragma unroll
       for (int e4 = 0; e4 < 8; ++e4) {
@@ -346,13 +348,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
           dd[2 * e4 + 1] = pack_f16x2(g23.x, g23.y);
         }
       }
-      tmem_st16(tS + 16 * half, pp);
-      tmem_st16(tdP + 16 * half, dd);
-      // dS^T row r of this half: four 16-byte chunks of a 64-byte row,
-      // 64-byte swizzle (chunk ^= (row / 2) % 4)
+      tmem_st16(xb + C::COL_P + 16 * half, pp);
+      tmem_st16(xb + C::COL_DS + 16 * half, dd);
+      // dS^T row r, queries 32*half .. +31: 16-byte chunks 4*half .. +3 of a
+      // 128-byte row, 128-byte swizzle (chunk ^= row % 8)
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
-        const int chunk = c4 ^ ((r >> 1) & 3);
+        const int chunk = (4 * half + c4) ^ (r & 7);
         *reinterpret_cast<uint4*>(ds_row + chunk * 16) =
             make_uint4(dd[4 * c4], dd[4 * c4 + 1], dd[4 * c4 + 2], dd[4 * c4 + 3]);
       }
@@ -397,8 +399,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       if (!ok) break;
       tc_fence_after();
       uint32_t x0[32], x1[32];
-      tmem_ld32(tbase + lane_off + 128u * (it & 1) + C::COL_DQ0, x0);
-      tmem_ld32(tbase + lane_off + 128u * (it & 1) + C::COL_DQ1, x1);
+      tmem_ld32(tbase + lane_off + 128u * (it & 1) + C::COL_DQ, x0);
+      tmem_ld32(tbase + lane_off + 128u * (it & 1) + C::COL_DQ + 32, x1);
       tmem_wait_ld();
       reg_fence(x0);
       reg_fence(x1);

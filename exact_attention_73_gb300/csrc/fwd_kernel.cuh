@@ -81,9 +81,9 @@ struct FwdCfg {
   static constexpr uint32_t IDESC_S = instr_desc(128, 128, FMT, FMT, 0, 0);
   static constexpr uint32_t IDESC_O = instr_desc(128, D, FMT, FMT, 0, 1);
   // Rescale threshold (log2 units): keep a stale max while exp2(x - m) <= 2^kTau.
-  static constexpr float kTau = kFp8 ? 0.0f : 8.0f;
+  static constexpr float kTau = kFp8 ? 4.0f : 8.0f;
   // Power-of-two shift of P~ before its E4M3 rounding.
-  static constexpr int kPShift = 8;
+  static constexpr int kPShift = 4;   // P~ <= 2^kTau, so P~ * 2^kPShift <= 256 < 448
 };
 
 __device__ __forceinline__ int pow2_exponent_of(float x) {   // x an exact power of two

@@ -114,9 +114,11 @@ ATTN_API attn_status attn_quantize_fp8(const void* x, attn_dtype in_dtype, void*
  * FP8 forward, dense (§3.5). q8 [B,Hq,N,d], k8/v8 [B,Hkv,N,d] E4M3 codes;
  * sq [B,Hq,ceil(N/128)], sk/sv [B,Hkv,ceil(N/128)] float32 power-of-two
  * dequantisation factors from attn_quantize_fp8. o [B,Hq,N,d] BF16,
- * lse [B,Hq,N] float32. Both products accumulate in FP32; P~ is rounded to
- * E4M3 as e4m3(P~ * 2^(8 + f_j - F)) with sv_j = 2^f_j and F the running
- * maximum of f over the KV tiles seen (O rescaled when F grows).
+ * lse [B,Hq,N] float32. Both products accumulate in FP32. The running row
+ * max is raised only when a tile's max exceeds it by more than 4 (log2
+ * units), so P~ = exp2(x - m) <= 16; P~ is rounded to E4M3 as
+ * e4m3(P~ * 2^(4 + f_j - F)) with sv_j = 2^f_j and F the running maximum of
+ * f over the KV tiles seen (O rescaled when F grows).
  */
 ATTN_API attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8,
                          const float* sq, const float* sk, const float* sv,

@@ -18,13 +18,16 @@ Readings (the pages leave these open):
 * The rotation is y = fp32(FWHT_fp32(sigma o x) * fp32(1/sqrt(d))), with the
   fast Walsh-Hadamard transform taken in the textbook radix-2 order (stride
   1, 2, 4, ...), every add and subtract rounded to float32. Sylvester order.
+* The running max m of Algorithm 1 is raised only when a KV tile's row max
+  exceeds it by more than tau = 4 (log2 units, i.e. S units of 4 ln 2); then
+  P~ = exp(S - m) <= 2^4, O and l are rescaled as in Algorithm 1, and the
+  result is unchanged in exact arithmetic.
 * The V factor of KV tile j, sv_j = 2^f_j, is folded into P~ before its
   E4M3 rounding, relative to F, the running maximum of f over the tiles seen
-  so far: P~ enters the second product as e4m3(P~ * 2^(8 + f_j - F)), and
+  so far: P~ enters the second product as e4m3(P~ * 2^(4 + f_j - F)), and
   the accumulated O is multiplied by 2^(F_old - F_new) whenever F grows (the
-  same correction as for the running row max m). The running max m is exact
-  (O is rescaled whenever it grows), so P~ <= 1 and the rounded value lies in
-  (0, 256]. At the end O = O_acc * 2^(F - 8) / l; l sums the unrounded P~.
+  same correction as for the running row max m). The rounded value lies in
+  (0, 256]. At the end O = O_acc * 2^(F - 4) / l; l sums the unrounded P~.
 """
 from __future__ import annotations
 
@@ -162,7 +165,8 @@ def quantize_tensor(x, signs=None, block=BLOCK):
     return codes, fac
 
 
-def attention_fp8(q8, k8, v8, sq, sk, sv, scale, causal=False, block=BLOCK, p_shift=8, heads=None, rows=None):
+def attention_fp8(q8, k8, v8, sq, sk, sv, scale, causal=False, block=BLOCK, p_shift=4, tau=4.0, heads=None,
+                  rows=None):
     """FP8 forward following Algorithm 1 tile by tile (Bc = block keys per tile).
 
     q8 [B, Hq, N, d], k8/v8 [B, Hkv, N, d] are E4M3 codes; sq/sk/sv are the
@@ -192,7 +196,8 @@ def attention_fp8(q8, k8, v8, sq, sk, sv, scale, causal=False, block=BLOCK, p_sh
                 s = scale * q_fac[:, None] * sk[b, kv, j] * (qrows @ kf[b, kv, cols].T)
                 if causal:
                     s = np.where(cols[None, :] > rows[:, None], -np.inf, s)
-                m_new = np.maximum(m, s.max(axis=1))
+                mx = s.max(axis=1)
+                m_new = np.where(mx > m + tau * np.log(2.0), mx, m)   # stale max within 2^tau
                 m_use = np.where(np.isfinite(m_new), m_new, 0.0)
                 corr = np.exp(m - m_use)
                 f_j = np.log2(sv[b, kv, j])
