@@ -69,9 +69,10 @@ struct BwdCfg {
   static constexpr int DS_B = BC * BR * 2;          // dS^T tile [128 keys][64 queries]
   static constexpr int NQ = 3;                      // stages of the Q/dO ring
   static constexpr int LD_B = 2 * BR * 4;           // LSE*log2e and D for one tile
-  static constexpr int DQ_STAGE_B = BR * D * 4;     // FP32 dQ tile for the reduce-add
+  static constexpr int DQ_ROWS = BR;                // rows of dQ per reduce-add (one per tile)
+  static constexpr int DQ_STAGE_B = DQ_ROWS * D * 4;  // FP32 staging for one reduce-add
   static constexpr int SMEM_BYTES =
-      1024 + 2 * KV_B + 2 * DS_B + NQ * (2 * Q_B) + DQ_STAGE_B + NQ * LD_B + 16 * 8 + 16;
+      1024 + 2 * KV_B + DS_B + NQ * (2 * Q_B) + DQ_STAGE_B + NQ * LD_B + 18 * 8 + 16;
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeded");
   static constexpr int NTHREADS = 512;
   static constexpr uint32_t FMT = DT == kBF16 ? 1u : 0u;
@@ -93,10 +94,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem;
   uint8_t* sV = sK + C::KV_B;
-  uint8_t* sDS = sV + C::KV_B;                      // [2][DS_B], 128-byte swizzle
-  uint8_t* sQ = sDS + 2 * C::DS_B;                  // [NQ][Q_B]
+  uint8_t* sDS = sV + C::KV_B;                      // [DS_B], 128-byte swizzle
+  uint8_t* sQ = sDS + C::DS_B;                      // [NQ][Q_B]
   uint8_t* sdO = sQ + C::NQ * C::Q_B;               // [NQ][Q_B]
-  float* sDQ = reinterpret_cast<float*>(sdO + C::NQ * C::Q_B);   // [BR][D] FP32
+  float* sDQ = reinterpret_cast<float*>(sdO + C::NQ * C::Q_B);   // [DQ_ROWS][D] FP32
   float* sLD = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(sDQ) + C::DQ_STAGE_B);   // [NQ][2*BR]
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sLD) + C::NQ * C::LD_B);
   uint64_t* kv_full = bars;
@@ -129,6 +130,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
   const int i0 = a.causal ? (j * C::BC) / C::BR : 0;
   const int per_head = nq - i0;
   const int niter = a.group * per_head;
+  // Query tile of iteration it. Each key tile starts its walk at a different
+  // query tile, so the CTAs of one head neither load the same Q/dO tile nor
+  // add into the same dQ rows at the same moment.
+  const int rot = j % per_head;
+  auto q_tile = [&](int it) {
+    const int r = it % per_head + rot;
+    return i0 + (r >= per_head ? r - per_head : r);
+  };
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmK);
@@ -138,7 +147,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     tma_prefetch_desc(&tmdQ);
     mbar_init(kv_full, 1);
     for (int s = 0; s < C::NQ; ++s) {
-      mbar_init(&q_full[s], 1);
+      mbar_init(&q_full[s], 2);   // TMA transaction + the LSE/D stores
       mbar_init(&q_empty[s], 1);
     }
     mbar_init(&sp_full[0], 1);
@@ -178,17 +187,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       const int st = it % C::NQ;
       if (!__all_sync(0xffffffffu, mbar_wait(&q_empty[st], ((it / C::NQ) & 1) ^ 1, a.status))) break;
       const int h = hkv * a.group + it / per_head;
-      const int q0 = (i0 + it % per_head) * C::BR;
-      float* ld = sLD + st * 2 * C::BR;
-      const long long lrow = static_cast<long long>(b) * a.l_sb + static_cast<long long>(h) * a.l_sh + seq0;
-#pragma unroll
-      for (int r = lane; r < C::BR; r += 32) {
-        const int q = q0 + r;
-        const bool ok = q < L;
-        ld[r] = ok ? -a.lse[lrow + q] * kLog2e : -INFINITY;    // -LSE in log2 units
-        ld[C::BR + r] = ok ? -a.dvec[lrow + q] : 0.f;           // -D
-      }
-      __syncwarp();
+      const int q0 = q_tile(it) * C::BR;
+      // the tile loads go first; LSE and D follow with plain loads and a
+      // second arrival on the same barrier
       if (lane == 0) {
         mbar_arrive_expect_tx(&q_full[st], 2 * C::Q_B);
         for (int c = 0; c < C::NBOX; ++c) {
@@ -203,6 +204,17 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
           }
         }
       }
+      float* ld = sLD + st * 2 * C::BR;
+      const long long lrow = static_cast<long long>(b) * a.l_sb + static_cast<long long>(h) * a.l_sh + seq0;
+#pragma unroll
+      for (int r = lane; r < C::BR; r += 32) {
+        const int q = q0 + r;
+        const bool ok = q < L;
+        ld[r] = ok ? -a.lse[lrow + q] * kLog2e : -INFINITY;    // -LSE in log2 units
+        ld[C::BR + r] = ok ? -a.dvec[lrow + q] : 0.f;           // -D
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_full[st]);
       __syncwarp();
     }
   } else if (warp == 1) {
@@ -261,7 +273,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         // the next S^T/dP^T never waits for an empty tensor pipe
 #pragma unroll
         for (int kk = 0; kk < C::BC / 16; ++kk) {   // dQ^T = K^T dS^T, both MN-major
-          mma_ss<false>(xb + C::COL_DQ, dadd(dK_mn, kk * 2048), dadd(dDS0_mn, (it & 1) * C::DS_B + kk * 2048),
+          mma_ss<false>(xb + C::COL_DQ, dadd(dK_mn, kk * 2048), dadd(dDS0_mn, kk * 2048),
                         C::IDESC_DQ, kk > 0);
         }
         mma_commit(dq_full);
@@ -292,12 +304,15 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     bool ok = true;
     for (int it = 0; it < niter; ++it) {
       const uint32_t xb = tbase + lane_off + 128u * (it & 1);
-      uint8_t* ds_row = sDS + (it & 1) * C::DS_B + r * 128;
+      uint8_t* ds_row = sDS + r * 128;
       const int st = it % C::NQ;
       // S^T/dP^T of this tile, then LSE and D of this stage (written by the
       // load warp before it arrived on q_full[st]; that phase is complete)
       bool got = __all_sync(0xffffffffu, mbar_wait(&sp_full[it & 1], (it >> 1) & 1, a.status));
       if (got) got = __all_sync(0xffffffffu, mbar_wait(&q_full[st], (it / C::NQ) & 1, a.status));
+      // the single dS^T tile in shared memory is read by dQ^T of the previous
+      // tile; it must be complete before this tile's dS^T is stored
+      if (got && it > 0) got = __all_sync(0xffffffffu, mbar_wait(dq_full, (it - 1) & 1, a.status));
       uint32_t sv[32], dp[32];
       if (got) {
         tc_fence_after();
@@ -311,7 +326,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       // columns the other reads; one decision for both groups.
       ok = named_bar_and(2, 256, got);
       if (!ok) break;
-      const int q0 = (i0 + it % per_head) * C::BR + 32 * half;
+      const int q0 = q_tile(it) * C::BR + 32 * half;
       const float* nlse = sLD + st * 2 * C::BR + 32 * half;       // -LSE * log2(e)
       const float* nd = nlse + C::BR;                             // -D
       const bool diag = a.causal && (q0 < j * C::BC + C::BC - 1);
@@ -351,7 +366,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       tmem_st16(xb + C::COL_P + 16 * half, pp);
       tmem_st16(xb + C::COL_DS + 16 * half, dd);
       // dS^T row r, queries 32*half .. +31: 16-byte chunks 4*half .. +3 of a
-      // 128-byte row, 128-byte swizzle (chunk ^= row % 8)
+      // 128-byte row, 128-byte swizzle (chunk ^= row % 8). The tile is free:
+      // dQ^T of the previous tile (its only reader) completed before the
+      // barrier above.
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
         const int chunk = (4 * half + c4) ^ (r & 7);
@@ -407,9 +424,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       tc_fence_before();
       mbar_arrive(dq_empty);
       const int h = hkv * a.group + it / per_head;
-      const int q0 = (i0 + it % per_head) * C::BR;
-      // the previous reduce-add must have finished reading the staging tile
-      if (threadIdx.x == 256) bulk_wait_read_all();
+      const int q0 = q_tile(it) * C::BR;
+      // one reduce-add of the whole [64 x 128] FP32 tile; rows past the
+      // sequence hold exact zeros (P = 0 there): for the dense layout the map
+      // clips them, for the packed layout they add 0 to the next sequence's rows
+      if (threadIdx.x == 256) bulk_wait_read_all();   // previous reduce-add has read the buffer
       named_bar_sync(1, 128);
 #pragma unroll
       for (int e = 0; e < 32; ++e) sDQ[e * D + dim] = __uint_as_float(x0[e]);
@@ -417,9 +436,6 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       for (int e = 0; e < 32; ++e) sDQ[(32 + e) * D + dim] = __uint_as_float(x1[e]);
       fence_proxy_async_smem();
       named_bar_sync(1, 128);
-      // Rows past the sequence hold exact zeros (P = 0 there): for the dense
-      // layout the map clips them, for the packed layout they add 0 to the
-      // next sequence's rows.
       if (threadIdx.x == 256) {
         if (packed) tma_reduce_add_4d(&tmdQ, sDQ, 0, h, seq0 + q0, 0);
         else tma_reduce_add_4d(&tmdQ, sDQ, 0, q0, h, b);
