@@ -185,11 +185,20 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     }
     for (int it = 0; it < niter; ++it) {
       const int st = it % C::NQ;
-      if (!__all_sync(0xffffffffu, mbar_wait(&q_empty[st], ((it / C::NQ) & 1) ^ 1, a.status))) break;
       const int h = hkv * a.group + it / per_head;
       const int q0 = q_tile(it) * C::BR;
-      // the tile loads go first; LSE and D follow with plain loads and a
-      // second arrival on the same barrier
+      // LSE and D of this tile are fetched before waiting for the stage (they
+      // do not depend on it), so their latency hides behind that wait
+      const long long lrow = static_cast<long long>(b) * a.l_sb + static_cast<long long>(h) * a.l_sh + seq0;
+      float nl[C::BR / 32], nd[C::BR / 32];
+#pragma unroll
+      for (int u = 0; u < C::BR / 32; ++u) {
+        const int q = q0 + lane + 32 * u;
+        const bool in = q < L;
+        nl[u] = in ? -a.lse[lrow + q] * kLog2e : -INFINITY;    // -LSE in log2 units
+        nd[u] = in ? -a.dvec[lrow + q] : 0.f;                  // -D
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait(&q_empty[st], ((it / C::NQ) & 1) ^ 1, a.status))) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(&q_full[st], 2 * C::Q_B);
         for (int c = 0; c < C::NBOX; ++c) {
@@ -205,13 +214,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         }
       }
       float* ld = sLD + st * 2 * C::BR;
-      const long long lrow = static_cast<long long>(b) * a.l_sb + static_cast<long long>(h) * a.l_sh + seq0;
 #pragma unroll
-      for (int r = lane; r < C::BR; r += 32) {
-        const int q = q0 + r;
-        const bool ok = q < L;
-        ld[r] = ok ? -a.lse[lrow + q] * kLog2e : -INFINITY;    // -LSE in log2 units
-        ld[C::BR + r] = ok ? -a.dvec[lrow + q] : 0.f;           // -D
+      for (int u = 0; u < C::BR / 32; ++u) {
+        ld[lane + 32 * u] = nl[u];
+        ld[C::BR + lane + 32 * u] = nd[u];
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&q_full[st]);
