@@ -51,7 +51,7 @@ attn_status run_bwd(const void* q, const void* k, const void* v, const void* o, 
       !operand_map(&tv, v, dtype, d, packed, B, Hkv, rows_or_T, 128) ||
       !operand_map(&tq, q, dtype, d, packed, B, Hq, rows_or_T, 64) ||
       !operand_map(&tdo, dout, dtype, d, packed, B, Hq, rows_or_T, 64) ||
-      !accum_map(&tdq, dq_acc, d, packed, B, Hq, rows_or_T, 64))
+      !accum_map(&tdq, dq_acc, d, packed, B, Hq, rows_or_T, 32))
     return ATTN_ERR_CUDA;
   BwdArgs a{};
   a.lse = lse;

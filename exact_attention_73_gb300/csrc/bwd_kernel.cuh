@@ -67,12 +67,12 @@ struct BwdCfg {
   static constexpr int Q_B = BR * D * 2;            // Q_i or dO_i tile
   static constexpr int Q_BOX_B = BR * 128;
   static constexpr int DS_B = BC * BR * 2;          // dS^T tile [128 keys][64 queries]
-  static constexpr int NQ = 3;                      // stages of the Q/dO ring
+  static constexpr int NQ = 4;                      // stages of the Q/dO ring
   static constexpr int LD_B = 2 * BR * 4;           // LSE*log2e and D for one tile
-  static constexpr int DQ_ROWS = BR;                // rows of dQ per reduce-add (one per tile)
+  static constexpr int DQ_ROWS = BR / 2;            // rows of dQ per reduce-add (two per tile)
   static constexpr int DQ_STAGE_B = DQ_ROWS * D * 4;  // FP32 staging for one reduce-add
   static constexpr int SMEM_BYTES =
-      1024 + 2 * KV_B + DS_B + NQ * (2 * Q_B) + DQ_STAGE_B + NQ * LD_B + 18 * 8 + 16;
+      2 * KV_B + DS_B + NQ * (2 * Q_B) + DQ_STAGE_B + NQ * LD_B + 18 * 8 + 16;   // base is 1024-aligned
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeded");
   static constexpr int NTHREADS = 512;
   static constexpr uint32_t FMT = DT == kBF16 ? 1u : 0u;
@@ -90,8 +90,15 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
            const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
            const __grid_constant__ CUtensorMap tmdQ, const BwdArgs a) {
   using C = BwdCfg<DT, D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // The layout uses all the shared memory it asks for, with no room to align
+  // the base by hand: a base that is not 1024-byte aligned (needed by the
+  // swizzled tiles) is reported and the CTA leaves before touching it.
+  extern __shared__ __align__(1024) uint8_t bwd_smem[];
+  if (smem_u32(bwd_smem) & 1023u) {
+    if (threadIdx.x == 0 && a.status) atomicExch(a.status, kDevBadSmemAlign);
+    return;
+  }
+  uint8_t* smem = bwd_smem;
   uint8_t* sK = smem;
   uint8_t* sV = sK + C::KV_B;
   uint8_t* sDS = sV + C::KV_B;                      // [DS_B], 128-byte swizzle
@@ -273,6 +280,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
           issue_sdp(it + 1);
         }
         if (!(ok = mbar_wait(ds_ready, it & 1, a.status))) break;
+        // The drain warps wait on dq_full by parity. On the last tile there is
+        // no S^T/dP^T issue (and no dq_empty wait) above, so wait here for the
+        // drain of it-1: dq_full then never runs two phases ahead of them.
+        if (it + 1 >= niter && it > 0 && !(ok = mbar_wait(dq_empty, (it & 1) ^ 1, a.status))) break;
         tc_fence_after();
         const uint32_t so = st * C::Q_B;
         // dQ^T first, so the drain warps can read it while dV and dK run and
@@ -431,21 +442,23 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       mbar_arrive(dq_empty);
       const int h = hkv * a.group + it / per_head;
       const int q0 = q_tile(it) * C::BR;
-      // one reduce-add of the whole [64 x 128] FP32 tile; rows past the
-      // sequence hold exact zeros (P = 0 there): for the dense layout the map
-      // clips them, for the packed layout they add 0 to the next sequence's rows
-      if (threadIdx.x == 256) bulk_wait_read_all();   // previous reduce-add has read the buffer
-      named_bar_sync(1, 128);
+      // two reduce-adds of 32 rows through one FP32 staging buffer; rows past
+      // the sequence hold exact zeros (P = 0 there): for the dense layout the
+      // map clips them, for the packed layout they add 0 to the next
+      // sequence's rows
 #pragma unroll
-      for (int e = 0; e < 32; ++e) sDQ[e * D + dim] = __uint_as_float(x0[e]);
+      for (int part = 0; part < 2; ++part) {
+        if (threadIdx.x == 256) bulk_wait_read_all();   // previous reduce-add has read the buffer
+        named_bar_sync(1, 128);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) sDQ[(32 + e) * D + dim] = __uint_as_float(x1[e]);
-      fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (threadIdx.x == 256) {
-        if (packed) tma_reduce_add_4d(&tmdQ, sDQ, 0, h, seq0 + q0, 0);
-        else tma_reduce_add_4d(&tmdQ, sDQ, 0, q0, h, b);
-        bulk_commit();
+        for (int e = 0; e < 32; ++e) sDQ[e * D + dim] = __uint_as_float(part == 0 ? x0[e] : x1[e]);
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (threadIdx.x == 256) {
+          if (packed) tma_reduce_add_4d(&tmdQ, sDQ, 0, h, seq0 + q0 + 32 * part, 0);
+          else tma_reduce_add_4d(&tmdQ, sDQ, 0, q0 + 32 * part, h, b);
+          bulk_commit();
+        }
       }
     }
     if (threadIdx.x == 256) bulk_wait_all();

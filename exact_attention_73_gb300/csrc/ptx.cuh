@@ -10,7 +10,7 @@ namespace attn {
 
 // ----------------------------------------------------------------- status
 // Written by a kernel whose bounded wait ran out; read by the host.
-enum : int { kDevOk = 0, kDevTimeout = 9 };
+enum : int { kDevOk = 0, kDevTimeout = 9, kDevBadSmemAlign = 10 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
