@@ -24,7 +24,7 @@ STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_NULL", 2: "ATTN_ERR_ALIGN", 3: "ATTN_ERR_SH
           9: "ATTN_ERR_TIMEOUT", 10: "ATTN_ERR_CUDA", 11: "ATTN_ERR_NODEVICE"}
 EXPORTS = ("attn_status_string", "attn_version", "attn_fwd", "attn_fwd_varlen", "attn_quantize_fp8",
            "attn_fwd_fp8", "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_varlen_workspace_size",
-           "attn_bwd_varlen", "attn_get_device_status", "attn_bwd_noalloc")
+           "attn_bwd_varlen", "attn_get_device_status", "attn_bwd_noalloc", "attn_selftest_wait_timeout")
 
 
 class AttnError(RuntimeError):
@@ -46,6 +46,7 @@ _SIGS = {
     "attn_bwd_varlen_workspace_size": ([_I, _I, _I, _I], _Z),
     "attn_bwd_varlen": ([_P] * 9 + [_P, _Z, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P], _I),
     "attn_get_device_status": ([_P], _I),
+    "attn_selftest_wait_timeout": ([C.c_uint, _P], _I),
     "attn_bwd_noalloc": ([_P] * 9 + [_I, _I, _I, _I, _I, _F, _I, _I, _P], _I),
 }
 
@@ -172,6 +173,11 @@ def attn_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, workspace, cu_seqlens, ma
 
 def attn_get_device_status(stream=None):
     return int(load().attn_get_device_status(_stream(stream)))
+
+
+def attn_selftest_wait_timeout(limit_ms, stream=None):
+    """Launch a warp whose bounded wait runs out after limit_ms (failure-path check)."""
+    _check(load().attn_selftest_wait_timeout(int(limit_ms), _stream(stream)), "attn_selftest_wait_timeout")
 
 
 def attn_status_string(code):

@@ -188,6 +188,16 @@ ATTN_API attn_status attn_bwd_varlen(const void* q, const void* k, const void* v
  */
 ATTN_API attn_status attn_get_device_status(void* stream);
 
+/*
+ * Diagnostic of the failure path; the pages have no counterpart. Launches one
+ * warp that waits, with the kernels' own bounded wait and a limit of limit_ms
+ * milliseconds (1..10000), on a barrier that nothing completes. The wait ends
+ * on its own, records ATTN_ERR_TIMEOUT in the device status word and the
+ * kernel returns: attn_get_device_status then reports ATTN_ERR_TIMEOUT once,
+ * and the context stays usable. Asynchronous on `stream`.
+ */
+ATTN_API attn_status attn_selftest_wait_timeout(unsigned int limit_ms, void* stream);
+
 /* Library version, e.g. "libattn 0.1 sm_103a". */
 ATTN_API const char* attn_version(void);
 
