@@ -326,8 +326,22 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       q_fac = a.sq[(static_cast<long long>(b) * a.Hq + h) * a.nblk + min(qtile, nqt - 1)];
       vs_base = (static_cast<long long>(b) * a.Hkv + hkv) * a.nblk;
     }
+    // FP8: the K and V block factors are fetched one KV step ahead, so their
+    // global-load latency overlaps the wait for the next score tile.
+    float sk_next = 1.f, sv_next = 1.f;
+    if constexpr (C::kFp8) {
+      sk_next = a.sk[vs_base];
+      sv_next = a.sv[vs_base];
+    }
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
+      const float sk_j = sk_next, sv_j = sv_next;
+      if constexpr (C::kFp8) {
+        if (j + 1 < nkv) {
+          sk_next = a.sk[vs_base + j + 1];
+          sv_next = a.sv[vs_base + j + 1];
+        }
+      }
       const int sb = QT == 1 ? (j & 1) : t;              // score buffer of this step
       const uint32_t sphase = QT == 1 ? ((j >> 1) & 1) : (j & 1);
       const uint32_t tS = tbase + lane_off + sb * 128;
@@ -349,12 +363,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         for (int c = 0; c < 128; ++c)
           if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
       }
-      const float mx = rowmax128(sr);
+      const float mx = rowmax(sr);
       float sl2 = a.scale_log2;
       int f_j = 0, f_new = 0;
       if constexpr (C::kFp8) {
-        sl2 *= q_fac * a.sk[vs_base + j];
-        f_j = pow2_exponent_of(a.sv[vs_base + j]);
+        sl2 *= q_fac * sk_j;
+        f_j = pow2_exponent_of(sv_j);
         f_new = max(f_run, f_j);
       }
       const float mxs = mx * sl2;

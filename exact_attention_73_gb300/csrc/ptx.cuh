@@ -50,11 +50,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a waiting thread sleeps until the phase
+// completes (or the hint runs out) instead of spinning, so idle warps leave
+// the issue slots of their scheduler to the warps that have work.
+constexpr uint32_t kWaitHintNs = 20000;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(bar), "r"(parity), "n"(kWaitHintNs) : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete. Returns false
-// (and records kDevTimeout) once both `limit_ns` of wall time and 2^20 polls
+// (and records kDevTimeout) once both `limit_ns` of wall time and 2^16 polls
 // have passed without completion: the poll count keeps a kernel that is
 // suspended from the outside (a profiler replaying it) from timing out while
-// the global timer runs on.
+// the global timer runs on. Each poll sleeps for at most kWaitHintNs, so a
+// wait that never completes ends after max(limit_ns, 2^16 * kWaitHintNs).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
                                           uint64_t limit_ns = 4000000000ull) {
   const uint32_t a = smem_u32(bar);
@@ -62,8 +77,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
   const uint64_t t0 = globaltimer();
   uint32_t n = 0;
   while (true) {
-    if (mbar_try_wait(a, parity)) return true;
-    if ((++n & 63u) == 0u && n > (1u << 20)) {
+    if (mbar_try_wait_sleep(a, parity)) return true;
+    if ((++n & 15u) == 0u && n > (1u << 16)) {
       if (globaltimer() - t0 > limit_ns) {
         if (status) atomicExch(status, kDevTimeout);
         return false;
@@ -334,12 +349,14 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
   return r;
 }
 
-// Maximum of 128 values held as raw 32-bit words, in four independent
+// Maximum of N float values held as raw 32-bit words, in four independent
 // chains of three-input max (short dependency chains).
-__device__ __forceinline__ float rowmax128(const uint32_t (&v)[128]) {
+template <int N>
+__device__ __forceinline__ float rowmax(const uint32_t (&v)[N]) {
+  static_assert(N % 8 == 0, "row chunk must be a multiple of 8");
   float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
 #pragma unroll
-  for (int c = 0; c < 128; c += 8) {
+  for (int c = 0; c < N; c += 8) {
     m0 = fmax3(m0, __uint_as_float(v[c + 0]), __uint_as_float(v[c + 1]));
     m1 = fmax3(m1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
     m2 = fmax3(m2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
