@@ -20,6 +20,8 @@
 //     +32..95  dQ^T [128 dims x 64 queries] (FP32, one N = 64 product)
 //     +96..127 dS^T (BF16 pairs)
 //   dV [128 keys x 128 dims] cols 256..383, dK cols 384..511.
+// Registers are split per warpgroup (setmaxnreg): load/MMA 88, dQ drain 88,
+// each P^T/dS^T warpgroup 168 (launch: 128 for all 512 threads).
 // Warp roles: warp 0 loads (TMA for K, V, Q_i, dO_i; plain loads for LSE and
 // D), warp 1 issues tcgen05.mma, warps 4-7 and 12-15 turn S^T/dP^T into
 // P^T/dS^T (one key per thread; the first group takes queries 0..31 of the
@@ -75,6 +77,12 @@ struct BwdCfg {
       2 * KV_B + DS_B + NQ * (2 * Q_B) + DQ_STAGE_B + NQ * LD_B + 18 * 8 + 16;   // base is 1024-aligned
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeded");
   static constexpr int NTHREADS = 512;
+  // Registers: the launch gives 128 per thread (the whole register file);
+  // the load/MMA warpgroup and the dQ drain warpgroup return part of theirs
+  // so the two P^T/dS^T warpgroups, whose per-key work is a set of
+  // independent exp2 chains, can keep all of them in flight.
+  static constexpr uint32_t kRegsCtl = 88, kRegsDrain = 88, kRegsMath = 168;
+  static_assert(128 * (kRegsCtl + kRegsDrain + 2 * kRegsMath) <= NTHREADS * 128, "register split");
   static constexpr uint32_t FMT = DT == kBF16 ? 1u : 0u;
   static constexpr uint32_t IDESC_SP = instr_desc(128, BR, FMT, FMT, 0, 0);
   static constexpr uint32_t IDESC_KV = instr_desc(128, D, FMT, FMT, 0, 1);
@@ -175,6 +183,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
   const uint32_t tbase = *tmem_holder;
   const float kLog2e = 1.4426950408889634f;
 
+  // Each role changes its register budget inside its own branch, so the
+  // compiler sizes every role's code for the budget it runs with.
+  if (warp < 4) {
+  regs_dec<C::kRegsCtl>();
   if (warp == 0) {
     // ------------------------------------------------------------ loads
     const int krow = seq0 + j * C::BC;
@@ -309,7 +321,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       mma_commit(done);
     }
     __syncwarp();
+  }
   } else if ((warp >= 4 && warp < 8) || warp >= 12) {
+    regs_inc<C::kRegsMath>();
     // -------------------------------------------------- P^T and dS^T
     const int half = warp >= 12 ? 1 : 0;            // queries 32*half .. +31 of each tile
     const int quarter = warp & 3;
@@ -323,10 +337,21 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       const uint32_t xb = tbase + lane_off + 128u * (it & 1);
       uint8_t* ds_row = sDS + r * 128;
       const int st = it % C::NQ;
-      // S^T/dP^T of this tile, then LSE and D of this stage (written by the
-      // load warp before it arrived on q_full[st]; that phase is complete)
-      bool got = __all_sync(0xffffffffu, mbar_wait(&sp_full[it & 1], (it >> 1) & 1, a.status));
-      if (got) got = __all_sync(0xffffffffu, mbar_wait(&q_full[st], (it / C::NQ) & 1, a.status));
+      // LSE and D of this stage (written by the load warp before it arrived
+      // on q_full[st]) go to registers first: these shared-memory reads then
+      // overlap the wait for S^T/dP^T instead of heading every exp2 chain
+      // while the tensor core's operand reads keep shared memory busy.
+      bool got = __all_sync(0xffffffffu, mbar_wait(&q_full[st], (it / C::NQ) & 1, a.status));
+      float4 l4r[8], d4r[8];
+      if (got) {
+        const float* nlse = sLD + st * 2 * C::BR + 32 * half;     // -LSE * log2(e)
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+          l4r[e4] = *reinterpret_cast<const float4*>(nlse + 4 * e4);
+          d4r[e4] = *reinterpret_cast<const float4*>(nlse + C::BR + 4 * e4);   // -D
+        }
+      }
+      if (got) got = __all_sync(0xffffffffu, mbar_wait(&sp_full[it & 1], (it >> 1) & 1, a.status));
       // the single dS^T tile in shared memory is read by dQ^T of the previous
       // tile; it must be complete before this tile's dS^T is stored
       if (got && it > 0) got = __all_sync(0xffffffffu, mbar_wait(dq_full, (it - 1) & 1, a.status));
@@ -344,14 +369,12 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       ok = named_bar_and(2, 256, got);
       if (!ok) break;
       const int q0 = q_tile(it) * C::BR + 32 * half;
-      const float* nlse = sLD + st * 2 * C::BR + 32 * half;       // -LSE * log2(e)
-      const float* nd = nlse + C::BR;                             // -D
       const bool diag = a.causal && (q0 < j * C::BC + C::BC - 1);
       uint32_t pp[16], dd[16];
 #pragma unroll
       for (int e4 = 0; e4 < 8; ++e4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(nlse + 4 * e4);
-        const float4 d4 = *reinterpret_cast<const float4*>(nd + 4 * e4);
+        const float4 l4 = l4r[e4];
+        const float4 d4 = d4r[e4];
         float2 x01 = ffma2(make_float2(__uint_as_float(sv[4 * e4]), __uint_as_float(sv[4 * e4 + 1])), sl2v,
                            make_float2(l4.x, l4.y));
         float2 x23 = ffma2(make_float2(__uint_as_float(sv[4 * e4 + 2]), __uint_as_float(sv[4 * e4 + 3])), sl2v,
@@ -420,7 +443,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         }
       }
     }
-  } else if (warp >= 8 && warp < 12) {
+  } else {
+    regs_dec<C::kRegsDrain>();
     // ---------------------------------------------------- dQ^T drain
     const int quarter = warp & 3;
     const int dim = quarter * 32 + lane;            // head-dim index = tensor-memory lane
