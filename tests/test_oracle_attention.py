@@ -256,3 +256,127 @@ def test_pins_catch_planted_mistakes():
         return scale * ds @ k, scale * ds.T @ q, p.T @ do
     dq, dk, dv = dropped_d(q, k, v, rnd(103, 24, 8), 0.3, False)
     assert abs(dk.sum(axis=0)).max() > 1e-6
+
+
+# ------------------------------------------------------------ sliding window
+
+WINDOWS = [(3, 0), (2, 5), (0, 4), (7, -1), (-1, 2), (0, 0), (1, 1)]
+
+
+def _mask_loops(n, left, right):
+    """Visibility written as explicit loops (independent of the oracle's)."""
+    m = np.zeros((n, n), dtype=bool)
+    for i in range(n):
+        for j in range(n):
+            ok = True
+            if right >= 0 and j > i + right:
+                ok = False
+            if left >= 0 and j < i - left:
+                ok = False
+            m[i, j] = ok
+    return m
+
+
+def test_window_zero_selects_own_value():
+    """Window (0, 0): every query sees only its own key, so O = V, LSE = s_ii."""
+    q, k, v = rnd(110, 1, 2, 19, 6), rnd(111, 1, 2, 19, 6), rnd(112, 1, 2, 19, 6)
+    o, lse = A.forward(q, k, v, 0.4, False, (0, 0))
+    np.testing.assert_allclose(o, v, atol=1e-14, rtol=0)
+    np.testing.assert_allclose(lse, 0.4 * (q * k).sum(-1), atol=1e-14, rtol=0)
+
+
+def test_window_brute_force_rows():
+    n, d, scale = 11, 3, 0.7
+    q, k, v = rnd(113, n, d), rnd(114, n, d), rnd(115, n, d)
+    for left, right in WINDOWS:
+        o, lse, _ = A.head_forward(q, k, v, scale, False, (left, right))
+        for i in range(n):
+            keys = [j for j in range(n) if (right < 0 or j <= i + right) and (left < 0 or j >= i - left)]
+            s = [scale * sum(q[i, t] * k[j, t] for t in range(d)) for j in keys]
+            mx = max(s)
+            e = [math.exp(x - mx) for x in s]
+            tot = sum(e)
+            ref = [sum(e[a] * v[j, t] for a, j in enumerate(keys)) / tot for t in range(d)]
+            np.testing.assert_allclose(o[i], ref, atol=1e-13, rtol=0)
+            assert abs(lse[i] - (mx + math.log(tot))) < 1e-13
+
+
+@pytest.mark.parametrize("window", WINDOWS)
+def test_window_matches_torch_sdpa_masked(window):
+    n = 23
+    q, k, v, do = (torch.from_numpy(rnd(s, 1, 4, n, 5)) for s in (116, 117, 118, 119))
+    k, v = k[:, :2].clone(), v[:, :2].clone()
+    mask = torch.from_numpy(_mask_loops(n, *window))
+    qt, kt, vt = (x.clone().requires_grad_(True) for x in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        qt, kt.repeat_interleave(2, 1), vt.repeat_interleave(2, 1), attn_mask=mask, scale=0.55)
+    ref.backward(do)
+    o, _ = A.forward(q, k, v, 0.55, False, window)
+    np.testing.assert_allclose(o, ref.detach().numpy(), atol=1e-12, rtol=0)
+    dq, dk, dv = A.backward(q, k, v, do, 0.55, False, window)
+    for got, g in ((dq, qt.grad), (dk, kt.grad), (dv, vt.grad)):
+        np.testing.assert_allclose(got, g.numpy(), atol=1e-12, rtol=0)
+
+
+def test_window_limits():
+    """A window wider than the sequence is full attention; (n, 0) is causal;
+    causal given with a window caps the window's right bound at 0."""
+    q, k, v = rnd(120, 1, 1, 17, 4), rnd(121, 1, 1, 17, 4), rnd(122, 1, 1, 17, 4)
+    full = A.forward(q, k, v, 0.3, False)
+    causal = A.forward(q, k, v, 0.3, True)
+    for got, ref in ((A.forward(q, k, v, 0.3, False, (17, 17)), full),
+                     (A.forward(q, k, v, 0.3, False, (40, 0)), causal),
+                     (A.forward(q, k, v, 0.3, True, (-1, 5)), causal)):
+        np.testing.assert_array_equal(got[0], ref[0])
+        np.testing.assert_array_equal(got[1], ref[1])
+    with pytest.raises(ValueError):
+        A.forward(q, k, v, 0.3, False, (-2, 0))
+
+
+def test_window_backward_central_differences():
+    n, d, scale, h = 9, 4, 0.6, 1e-6
+    q, k, v, do = rnd(123, n, d), rnd(124, n, d), rnd(125, n, d), rnd(126, n, d)
+    window = (2, 1)
+    dq, dk, dv = A.head_backward(q, k, v, do, scale, False, window)
+
+    def loss(qq, kk, vv):
+        return (A.head_forward(qq, kk, vv, scale, False, window)[0] * do).sum()
+
+    for which, grad in ((0, dq), (1, dk), (2, dv)):
+        num = np.zeros_like(grad)
+        for idx in np.ndindex(grad.shape):
+            args = [q.copy(), k.copy(), v.copy()]
+            args[which][idx] += h
+            up = loss(*args)
+            args[which][idx] -= 2 * h
+            num[idx] = (up - loss(*args)) / (2 * h)
+        assert np.linalg.norm(num - grad) / np.linalg.norm(grad) < 1e-6, which
+
+
+def test_window_forward_rows_matches_full():
+    q, k, v = rnd(127, 40, 6), rnd(128, 40, 6), rnd(129, 40, 6)
+    for window in WINDOWS:
+        o, lse, _ = A.head_forward(q, k, v, 0.25, False, window)
+        rows = [0, 1, 13, 38, 39]
+        o2, l2 = A.forward_rows(q, k, v, rows, 0.25, False, window)
+        np.testing.assert_allclose(o2, o[rows], atol=1e-14)
+        np.testing.assert_allclose(l2, lse[rows], atol=1e-14)
+
+
+def test_window_pins_catch_off_by_one():
+    """Plant an off-by-one in the window's left bound (on the CPU): the
+    brute-force rows must disagree."""
+    good = A.visible
+
+    def shifted(nq, nk, causal, window=None):
+        left, right = A.window_bounds(causal, window)
+        return good(nq, nk, causal, (left + 1 if left >= 0 else left, right))
+
+    q, k, v = rnd(130, 10, 3), rnd(131, 10, 3), rnd(132, 10, 3)
+    ref, _, _ = A.head_forward(q, k, v, 0.5, False, (2, 0))
+    A.visible = shifted
+    try:
+        bad, _, _ = A.head_forward(q, k, v, 0.5, False, (2, 0))
+    finally:
+        A.visible = good
+    assert not np.allclose(bad, ref, atol=1e-12)
