@@ -12,6 +12,10 @@ Default workload: the BF16 sweep point d=128, H=16, N=8192, B=2 (B*N = 16384
 tokens), non-causal, Q/K/V/dO i.i.d. N(0,1). Every kernel's inputs exceed the
 129 MB L2, so no flush is needed between steps.
 
+Sliding-window workloads (name starting "window_") time a step of
+attn_fwd_window + attn_bwd_window (BF16) instead; their FLOPs count only the
+visible (query, key) pairs: 4 B H d * pairs forward, 2.5x that backward.
+
 --impl reference times the float64 CPU oracle on a bounded sample of the same
 workload (one head per step) in the same units.
 Under torchrun every rank runs the same workload on its own GPU (replicas, no
@@ -32,18 +36,32 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOADS = {
-    # name: (B, Hq, Hkv, N, d, causal)
-    "bf16_sweep_d128_n8192": (2, 16, 16, 8192, 128, False),
-    "bf16_sweep_d128_n8192_causal": (2, 16, 16, 8192, 128, True),
-    "gqa_b2_hq32_hkv8_n8192_causal": (2, 32, 8, 8192, 128, True),
+    # name: (B, Hq, Hkv, N, d, causal, window)
+    "bf16_sweep_d128_n8192": (2, 16, 16, 8192, 128, False, None),
+    "bf16_sweep_d128_n8192_causal": (2, 16, 16, 8192, 128, True, None),
+    "gqa_b2_hq32_hkv8_n8192_causal": (2, 32, 8, 8192, 128, True, None),
     # same token count as the default, shorter rows: the size used for ncu --set full captures
-    "bf16_b4_h16_n4096": (4, 16, 16, 4096, 128, False),
+    "bf16_b4_h16_n4096": (4, 16, 16, 4096, 128, False, None),
+    # sliding window: each query sees itself and the 1024 keys before it
+    "window_b1_h16_n16384_w1024": (1, 16, 16, 16384, 128, False, (1024, 0)),
 }
 DEFAULT = "bf16_sweep_d128_n8192"
 LAUNCHES_PER_STEP = 8   # fwd 1, bwd 3, quantise 3, fp8 fwd 1
 
 
-def fwd_flops(B, Hq, N, d, causal):
+def visible_pairs(N, left, right):
+    """Number of (query i, key j) pairs with i - left <= j <= i + right (-1: no bound)."""
+    total = 0
+    for i in range(N):
+        lo = 0 if left < 0 else max(0, i - left)
+        hi = N - 1 if right < 0 else min(N - 1, i + right)
+        total += hi - lo + 1
+    return total
+
+
+def fwd_flops(B, Hq, N, d, causal, window=None):
+    if window is not None:
+        return 4.0 * B * Hq * d * visible_pairs(N, *window)
     f = 4.0 * B * Hq * N * N * d
     return f / 2 if causal else f
 
@@ -119,7 +137,7 @@ class Clocks:
 def make_inputs(wl, device):
     import torch
     from exact_attention_73_gb300 import inputs
-    B, Hq, Hkv, N, d, causal = wl
+    B, Hq, Hkv, N, d, causal, window = wl
     q, k, v, do = inputs.normal(1, [(B, Hq, N, d), (B, Hkv, N, d), (B, Hkv, N, d), (B, Hq, N, d)])
     signs = inputs.random_signs(4, d)
     return [x.to(device) for x in (q, k, v, do)] + [signs.to(device)]
@@ -132,7 +150,7 @@ def bench_ours(args, wl, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     L.load(build_if_missing=True)
-    B, Hq, Hkv, N, d, causal = wl
+    B, Hq, Hkv, N, d, causal, window = wl
     nb = (N + 127) // 128
     q, k, v, do, signs = make_inputs(wl, dev)
     o = torch.empty_like(q)
@@ -158,12 +176,23 @@ def bench_ours(args, wl, rank, world):
         o_, lse_, dq_, dk_, dv_, o8_, lse8_ = bs["out"]
         if marks is not None:
             marks[0].record(stream)
-        L.attn_fwd(q_, k_, v_, o_, lse_, causal=causal)
+        if window is not None:
+            L.attn_fwd_window(q_, k_, v_, o_, lse_, window)
+        else:
+            L.attn_fwd(q_, k_, v_, o_, lse_, causal=causal)
         if marks is not None:
             marks[1].record(stream)
-        L.attn_bwd(q_, k_, v_, o_, lse_, do_, dq_, dk_, dv_, ws, causal=causal)
+        if window is not None:
+            L.attn_bwd_window(q_, k_, v_, o_, lse_, do_, dq_, dk_, dv_, ws, window)
+        else:
+            L.attn_bwd(q_, k_, v_, o_, lse_, do_, dq_, dk_, dv_, ws, causal=causal)
         if marks is not None:
             marks[2].record(stream)
+        if window is not None:      # the FP8 path has no window: BF16 forward + backward only
+            if marks is not None:
+                marks[3].record(stream)
+                marks[4].record(stream)
+            return
         L.attn_quantize_fp8(q_, q8, sq, signs)
         L.attn_quantize_fp8(k_, k8, sk, signs)
         L.attn_quantize_fp8(v_, v8, sv)
@@ -215,7 +244,8 @@ def bench_ours(args, wl, rank, world):
     sets = [set0, {"in": [torch.empty_like(x) for x in set0["in"]],
                    "out": [torch.empty_like(x) for x in set0["out"]]}]
     pin = [x.cpu().pin_memory() for x in set0["in"]]
-    host_out = [[torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in bs["out"]] for bs in sets]
+    n_out = 5 if window is not None else 7            # a window step produces no FP8 results
+    host_out = [[torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in bs["out"][:n_out]] for bs in sets]
     h2d = sum(x.numel() * x.element_size() for x in pin)
     d2h = sum(x.numel() * x.element_size() for x in host_out[0])
     s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -274,20 +304,23 @@ def cpu_sample(wl, steps=1):
     from oracle import attention as A
     from oracle import fp8 as F
     from exact_attention_73_gb300 import inputs
-    B, Hq, Hkv, N, d, causal = wl
+    B, Hq, Hkv, N, d, causal, window = wl
     q, k, v, do = inputs.normal(1, [(1, 1, N, d)] * 4)
     signs = inputs.random_signs(4, d).numpy()
     sc = d ** -0.5
     t = time.perf_counter()
     for _ in range(steps):
-        A.forward(q, k, v, sc, causal)
-        A.backward(q, k, v, do, sc, causal)
+        A.forward(q, k, v, sc, causal, window)
+        A.backward(q, k, v, do, sc, causal, window)
+        if window is not None:
+            continue
         q8, sq = F.quantize_blocks(q, signs)
         k8, sk = F.quantize_blocks(k, signs)
         v8, sv = F.quantize_blocks(v)
         F.attention_fp8(q8, k8, v8, sq, sk, sv, sc, causal)
     dt = time.perf_counter() - t
-    return 4.5 * fwd_flops(1, 1, N, d, causal) * steps, dt
+    per_step = (3.5 if window is not None else 4.5) * fwd_flops(1, 1, N, d, causal, window)
+    return per_step * steps, dt
 
 
 def cpu_cores():
@@ -309,7 +342,7 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     wl = WORKLOADS[args.workload]
-    B, Hq, Hkv, N, d, causal = wl
+    B, Hq, Hkv, N, d, causal, window = wl
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     config = {"workload": args.workload, "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d, "causal": causal,
@@ -317,6 +350,11 @@ def main():
               "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"}
     metric = "attention fwd+bwd (BF16) + FP8 fwd TFLOP/s on GB300"
     step_flops = 4.5 * fwd_flops(B, Hq, N, d, causal)
+    if window is not None:
+        config["window"] = list(window)
+        config["step"] = "fwd bf16 + bwd bf16, sliding window (FLOPs of visible pairs only)"
+        metric = "attention fwd+bwd (BF16, sliding window) TFLOP/s on GB300"
+        step_flops = 3.5 * fwd_flops(B, Hq, N, d, causal, window)
 
     if args.impl == "reference":
         if rank != 0:
@@ -343,7 +381,7 @@ def main():
     value = job_tflops(step_flops, args.steps, world, r["ms_total"])
     e2e_val = job_tflops(step_flops, args.steps, world, r["ms_e2e"])
     st = r["stage_ms"]
-    f = fwd_flops(B, Hq, N, d, causal)
+    f = fwd_flops(B, Hq, N, d, causal, window)
     stages = {
         "fwd_bf16": {"ms": st["fwd"], "tflops": f / st["fwd"] / 1e9, "frac_of_bf16_peak": f / st["fwd"] / 1e9 / pk["bf16_burst"]},
         "bwd_bf16": {"ms": st["bwd"], "tflops": 2.5 * f / st["bwd"] / 1e9,
@@ -354,6 +392,8 @@ def main():
     }
     # dominant kernel: the stage with the longest time (the backward call
     # holds its main kernel plus two HBM-bound helpers of a few percent)
+    if window is not None:
+        del stages["quant_fp8"], stages["fwd_fp8"]
     dom = max(("fwd", "bwd", "fwd_fp8"), key=lambda n: st[n])
     dom_flops = {"fwd": f, "bwd": 2.5 * f, "fwd_fp8": f}[dom]
     dom_peak = pk["bf16_burst"] * (2 if dom == "fwd_fp8" else 1)
@@ -365,15 +405,15 @@ def main():
     line = {
         "metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16+e4m3", "data": "synthetic", "config": config,
-        "stages": stages,
+        "vs_baseline": None, "dtype": "bf16" if window is not None else "bf16+e4m3", "data": "synthetic",
+        "config": config, "stages": stages,
         "roofline": {"bound": "tensor", "kernel": {"fwd": "attn_fwd", "bwd": "attn_bwd (main + 2 helpers)",
                                                     "fwd_fp8": "attn_fwd_fp8"}[dom],
                      "achieved": achieved, "peak": dom_peak, "unit": "TFLOP/s", "frac": achieved / dom_peak,
                      "peak_source": pk["source"] + (" bf16 burst x2 (fp8 nominal ratio)" if dom == "fwd_fp8" else " bf16 burst"),
                      "traffic": traffic},
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": (4 if window is not None else LAUNCHES_PER_STEP) * args.steps,
         "clocks": r["clocks"],
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -24,7 +24,8 @@ STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_NULL", 2: "ATTN_ERR_ALIGN", 3: "ATTN_ERR_SH
           9: "ATTN_ERR_TIMEOUT", 10: "ATTN_ERR_CUDA", 11: "ATTN_ERR_NODEVICE"}
 EXPORTS = ("attn_status_string", "attn_version", "attn_fwd", "attn_fwd_varlen", "attn_quantize_fp8",
            "attn_fwd_fp8", "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_varlen_workspace_size",
-           "attn_bwd_varlen", "attn_get_device_status", "attn_bwd_noalloc", "attn_selftest_wait_timeout")
+           "attn_bwd_varlen", "attn_get_device_status", "attn_bwd_noalloc", "attn_selftest_wait_timeout",
+           "attn_fwd_window", "attn_bwd_window")
 
 
 class AttnError(RuntimeError):
@@ -48,6 +49,8 @@ _SIGS = {
     "attn_get_device_status": ([_P], _I),
     "attn_selftest_wait_timeout": ([C.c_uint, _P], _I),
     "attn_bwd_noalloc": ([_P] * 9 + [_I, _I, _I, _I, _I, _F, _I, _I, _P], _I),
+    "attn_fwd_window": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P], _I),
+    "attn_bwd_window": ([_P] * 9 + [_P, _Z, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P], _I),
 }
 
 
@@ -102,6 +105,17 @@ def attn_fwd(q, k, v, o, lse, scale=None, causal=False, stream=None):
                            int(bool(causal)), _dtype(q), _stream(stream)), "attn_fwd")
 
 
+def attn_fwd_window(q, k, v, o, lse, window, scale=None, stream=None):
+    """Dense forward with a key window (left, right): key j is visible to
+    query i iff i - left <= j <= i + right; -1 means no bound on that side."""
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    left, right = (int(w) for w in window)
+    _check(load().attn_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d, scale,
+                                  left, right, _dtype(q), _stream(stream)), "attn_fwd_window")
+
+
 def attn_fwd_varlen(q, k, v, o, lse, cu_seqlens, max_seqlen, scale=None, causal=False, stream=None):
     """Packed forward: q [T,Hq,d], k/v [T,Hkv,d], o like q, lse [Hq,T]; cu_seqlens int32 on the device."""
     T, Hq, d = q.shape
@@ -140,6 +154,18 @@ def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, scale=None, causal=Fa
     _check(load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
                            _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(),
                            B, Hq, Hkv, N, d, scale, int(bool(causal)), _dtype(q), _stream(stream)), "attn_bwd")
+
+
+def attn_bwd_window(q, k, v, o, lse, dout, dq, dk, dv, workspace, window, scale=None, stream=None):
+    """Dense backward with the key window of attn_fwd_window."""
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    left, right = (int(w) for w in window)
+    _check(load().attn_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                                  _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  B, Hq, Hkv, N, d, scale, left, right, _dtype(q), _stream(stream)),
+           "attn_bwd_window")
 
 
 def attn_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, scale=None, causal=False, stream=None):

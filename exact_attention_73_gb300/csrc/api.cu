@@ -160,34 +160,13 @@ bool operand_map(CUtensorMap* m, const void* base, int dt, int d, bool packed, i
 
 using namespace attn;
 
-extern "C" {
-
-const char* attn_status_string(attn_status s) {
-  switch (s) {
-    case ATTN_OK: return "ATTN_OK";
-    case ATTN_ERR_NULL: return "ATTN_ERR_NULL: a required pointer is NULL";
-    case ATTN_ERR_ALIGN: return "ATTN_ERR_ALIGN: a pointer is not 16-byte aligned";
-    case ATTN_ERR_SHAPE: return "ATTN_ERR_SHAPE: a size is out of range";
-    case ATTN_ERR_HEADDIM: return "ATTN_ERR_HEADDIM: d must be 64, 128 or 256";
-    case ATTN_ERR_GQA: return "ATTN_ERR_GQA: Hq must be a positive multiple of Hkv";
-    case ATTN_ERR_DTYPE: return "ATTN_ERR_DTYPE: dtype not accepted here";
-    case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE: workspace missing or too small";
-    case ATTN_ERR_LAUNCH: return "ATTN_ERR_LAUNCH: kernel resources not granted";
-    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT: a device-side wait ran out";
-    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: CUDA error";
-    case ATTN_ERR_NODEVICE: return "ATTN_ERR_NODEVICE: no sm_103 device is current";
-  }
-  return "unknown attn_status";
-}
-
-const char* attn_version(void) { return "libattn 0.1 sm_103a"; }
-
-attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                     int B, int Hq, int Hkv, int N, int d, float scale, int causal,
-                     attn_dtype dtype, void* stream) {
+namespace {
+// Dense forward with a key window (left, right); -1 means no bound.
+attn_status fwd_dense(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                      int N, int d, float scale, int win_left, int win_right, attn_dtype dtype, void* stream) {
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_ALIGN;
-  if (B < 1 || B > 65535 || N < 1) return ATTN_ERR_SHAPE;
+  if (B < 1 || B > 65535 || N < 1 || win_left < -1 || win_right < -1) return ATTN_ERR_SHAPE;
   attn_status s = check_heads(Hq, Hkv, d);
   if (s != ATTN_OK) return s;
   if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_DTYPE;
@@ -211,9 +190,47 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   a.N = N;
   a.cu_seqlens = nullptr;
   a.scale_log2 = scale * kLog2e;
-  a.causal = causal ? 1 : 0;
+  a.win_left = win_left;
+  a.win_right = win_right;
+  a.causal = (win_left < 0 && win_right == 0) ? 1 : 0;
   a.status = status;
   return from_cuda(launch_fwd(dtype, d, tq, tk, tv, a, N, Hq, B, static_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+extern "C" {
+
+const char* attn_status_string(attn_status s) {
+  switch (s) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_NULL: return "ATTN_ERR_NULL: a required pointer is NULL";
+    case ATTN_ERR_ALIGN: return "ATTN_ERR_ALIGN: a pointer is not 16-byte aligned";
+    case ATTN_ERR_SHAPE: return "ATTN_ERR_SHAPE: a size is out of range";
+    case ATTN_ERR_HEADDIM: return "ATTN_ERR_HEADDIM: d must be 64, 128 or 256";
+    case ATTN_ERR_GQA: return "ATTN_ERR_GQA: Hq must be a positive multiple of Hkv";
+    case ATTN_ERR_DTYPE: return "ATTN_ERR_DTYPE: dtype not accepted here";
+    case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE: workspace missing or too small";
+    case ATTN_ERR_LAUNCH: return "ATTN_ERR_LAUNCH: kernel resources not granted";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT: a device-side wait ran out";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: CUDA error";
+    case ATTN_ERR_NODEVICE: return "ATTN_ERR_NODEVICE: no sm_103 device is current";
+  }
+  return "unknown attn_status";
+}
+
+const char* attn_version(void) { return "libattn 0.1 sm_103a"; }
+
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                     attn_dtype dtype, void* stream) {
+  return fwd_dense(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, -1, causal ? 0 : -1, dtype, stream);
+}
+
+attn_status attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int Hq, int Hkv, int N, int d, float scale, int window_left,
+                            int window_right, attn_dtype dtype, void* stream) {
+  return fwd_dense(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, window_left, window_right, dtype, stream);
 }
 
 attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -249,6 +266,8 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
   a.cu_seqlens = cu_seqlens;
   a.scale_log2 = scale * kLog2e;
   a.causal = causal ? 1 : 0;
+  a.win_left = -1;
+  a.win_right = causal ? 0 : -1;
   a.status = status;
   return from_cuda(launch_fwd(dtype, d, tq, tk, tv, a, max_seqlen, Hq, nseq, static_cast<cudaStream_t>(stream)));
 }
@@ -286,6 +305,8 @@ attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8,
   a.cu_seqlens = nullptr;
   a.scale_log2 = scale * kLog2e;
   a.causal = causal ? 1 : 0;
+  a.win_left = -1;
+  a.win_right = causal ? 0 : -1;
   a.sq = sq;
   a.sk = sk;
   a.sv = sv;

@@ -37,8 +37,8 @@ attn_status from_cuda(cudaError_t e) {
 // packed otherwise (nz = nseq, T tokens, longest sequence max_len).
 attn_status run_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                     void* dq, void* dk, void* dv, void* ws, const int* cu_seqlens, int nz, int rows_or_T,
-                    int max_len, int Hq, int Hkv, int d, float scale, int causal, attn_dtype dtype, int* status,
-                    void* stream) {
+                    int max_len, int Hq, int Hkv, int d, float scale, int win_left, int win_right,
+                    attn_dtype dtype, int* status, void* stream) {
   using namespace attn;
   const bool packed = cu_seqlens != nullptr;
   const int B = packed ? 1 : nz;
@@ -76,7 +76,9 @@ attn_status run_bwd(const void* q, const void* k, const void* v, const void* o, 
   a.cu_seqlens = cu_seqlens;
   a.scale = scale;
   a.scale_log2 = scale * kLog2e;
-  a.causal = causal ? 1 : 0;
+  a.win_left = win_left;
+  a.win_right = win_right;
+  a.causal = (win_left < 0 && win_right == 0) ? 1 : 0;
   a.status = status;
   cudaError_t e = launch_bwd_pre(dtype, d, o, dout, dvec, dq_acc, rows, Hq, rows_or_T, packed ? 1 : 0, st);
   if (e == cudaSuccess) e = launch_bwd_main(dtype, tk, tv, tq, tdo, tdq, a, max_len, nz, st);
@@ -109,8 +111,22 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   if (s != ATTN_OK) return s;
   int* status;
   if ((s = attn::device_context(&status)) != ATTN_OK) return s;
-  return run_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, nullptr, B, N, N, Hq, Hkv, d, scale, causal, dtype,
-                 status, stream);
+  return run_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, nullptr, B, N, N, Hq, Hkv, d, scale, -1,
+                 causal ? 0 : -1, dtype, status, stream);
+}
+
+attn_status attn_bwd_window(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                            const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                            int B, int Hq, int Hkv, int N, int d, float scale, int window_left, int window_right,
+                            attn_dtype dtype, void* stream) {
+  if (B < 1 || B > 65535 || N < 1 || window_left < -1 || window_right < -1) return ATTN_ERR_SHAPE;
+  attn_status s = check_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, ws_bytes,
+                               attn_bwd_workspace_size(B, Hq, Hkv, N, d), Hq, Hkv, d, dtype);
+  if (s != ATTN_OK) return s;
+  int* status;
+  if ((s = attn::device_context(&status)) != ATTN_OK) return s;
+  return run_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, nullptr, B, N, N, Hq, Hkv, d, scale, window_left,
+                 window_right, dtype, status, stream);
 }
 
 attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -126,7 +142,7 @@ attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const v
   int* status;
   if ((s = attn::device_context(&status)) != ATTN_OK) return s;
   return run_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, cu_seqlens, nseq, T, max_seqlen, Hq, Hkv, d, scale,
-                 causal, dtype, status, stream);
+                 -1, causal ? 0 : -1, dtype, status, stream);
 }
 
 }  // extern "C"

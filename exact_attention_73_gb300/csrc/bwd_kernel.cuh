@@ -54,7 +54,8 @@ struct BwdArgs {
   const int* cu_seqlens;
   float scale;
   float scale_log2;
-  int causal;
+  int causal;               // scheduling hint: window (-1, 0)
+  int win_left, win_right;  // key j visible to query i iff i - left <= j <= i + right (-1: no bound)
   int* status;
 };
 
@@ -141,9 +142,12 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
   }
   const int j = blockIdx.x;                 // key tile; with causal masking tile 0 has the most work
   if (j * C::BC >= L) return;
-  const int nq = (L + C::BR - 1) / C::BR;
-  const int i0 = a.causal ? (j * C::BC) / C::BR : 0;
-  const int per_head = nq - i0;
+  // query tiles holding a query that sees a key of this tile
+  const int klast = min(j * C::BC + C::BC, L) - 1;
+  const int qlo = a.win_right < 0 ? 0 : max(0, j * C::BC - a.win_right);
+  const int qhi = a.win_left < 0 ? L - 1 : min(L - 1, klast + a.win_left);
+  const int i0 = qlo / C::BR;
+  const int per_head = qhi / C::BR + 1 - i0;
   const int niter = a.group * per_head;
   // Query tile of iteration it. Each key tile starts its walk at a different
   // query tile, so the CTAs of one head neither load the same Q/dO tile nor
@@ -369,7 +373,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       ok = named_bar_and(2, 256, got);
       if (!ok) break;
       const int q0 = q_tile(it) * C::BR + 32 * half;
-      const bool diag = a.causal && (q0 < j * C::BC + C::BC - 1);
+      // this key against queries q0 .. q0 + 31: outside the sequence or the window?
+      const bool edge = !kvalid || (a.win_right >= 0 && kloc > q0 + a.win_right) ||
+                        (a.win_left >= 0 && kloc < q0 + 31 - a.win_left);
       uint32_t pp[16], dd[16];
 #pragma unroll
       for (int e4 = 0; e4 < 8; ++e4) {
@@ -380,10 +386,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         float2 x23 = ffma2(make_float2(__uint_as_float(sv[4 * e4 + 2]), __uint_as_float(sv[4 * e4 + 3])), sl2v,
                            make_float2(l4.z, l4.w));
         float p[4] = {ex2(x01.x), ex2(x01.y), ex2(x23.x), ex2(x23.y)};
-        if (!kvalid || diag) {
+        if (edge) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            if (!kvalid || kloc > q0 + 4 * e4 + u) p[u] = 0.f;
+          for (int u = 0; u < 4; ++u) {
+            const int q = q0 + 4 * e4 + u;
+            if (!kvalid || (a.win_right >= 0 && kloc > q + a.win_right) || (a.win_left >= 0 && kloc < q - a.win_left))
+              p[u] = 0.f;
+          }
         }
         const float2 t01 = fadd2(make_float2(__uint_as_float(dp[4 * e4]), __uint_as_float(dp[4 * e4 + 1])),
                                  make_float2(d4.x, d4.y));

@@ -42,7 +42,8 @@ struct FwdArgs {
   int N;                        // dense sequence length
   const int* cu_seqlens;        // packed layout when non-null
   float scale_log2;             // scale * log2(e)
-  int causal;
+  int causal;                   // scheduling hint: window (-1, 0)
+  int win_left, win_right;      // key j visible to query i iff i - left <= j <= i + right (-1: no bound)
   const float* sq;              // FP8 dequantisation factors per 128-row block
   const float* sk;
   const float* sv;
@@ -153,7 +154,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
   const int cblk = a.causal ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
   const int qt0 = cblk * QT;
   if (qt0 >= nqt) return;   // whole CTA leaves before any set-up
-  const int nkv = a.causal ? min(nqt, qt0 + QT) : nqt;
+  // KV tiles that hold a key visible to some query row of this CTA
+  const int r0 = qt0 * 128, r1 = min((qt0 + QT) * 128, L);
+  const int klo = a.win_left < 0 ? 0 : max(0, r0 - a.win_left);
+  const int khi = a.win_right < 0 ? L : min(L, r1 + a.win_right);   // exclusive
+  const int kv0 = klo >> 7;
+  const int nkv = ((khi + 127) >> 7) - kv0;
   const int hkv = h / a.group;
 
   if (threadIdx.x == 0) {
@@ -202,7 +208,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         int jt;
         kv_item(QT, it, nkv, is_v, jt);
         const CUtensorMap* m = is_v ? &tmV : &tmK;
-        const int row = seq0 + jt * 128;
+        const int row = seq0 + (kv0 + jt) * 128;
         for (int c = 0; c < C::NBOX; ++c) {
           uint8_t* dst = sKV + slot * C::TILE_B + c * C::BOXT_B;
           if (packed) tma_load_4d(dst, m, &kv_full[slot], c * C::BOX_E, hkv, row, 0);
@@ -324,7 +330,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     long long vs_base = 0;
     if constexpr (C::kFp8) {
       q_fac = a.sq[(static_cast<long long>(b) * a.Hq + h) * a.nblk + min(qtile, nqt - 1)];
-      vs_base = (static_cast<long long>(b) * a.Hkv + hkv) * a.nblk;
+      vs_base = (static_cast<long long>(b) * a.Hkv + hkv) * a.nblk + kv0;
     }
     // FP8: the K and V block factors are fetched one KV step ahead, so their
     // global-load latency overlaps the wait for the next score tile.
@@ -355,13 +361,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       tmem_wait_ld();
 #pragma unroll
       for (int c = 0; c < 4; ++c) reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
-      const int kb = j * 128;
-      if (kb + 128 > L || (a.causal && kb + 127 > qtile * 128)) {
-        int lim = L - kb;
-        if (a.causal) lim = min(lim, qrow - kb + 1);
+      const int kb = (kv0 + j) * 128;
+      // mask keys past the sequence and outside the window [qrow - left, qrow + right]
+      if (kb + 128 > L || (a.win_right >= 0 && kb + 127 > qtile * 128 + a.win_right) ||
+          (a.win_left >= 0 && kb < qtile * 128 + 127 - a.win_left)) {
+        int hi = L - kb;                                             // visible: lo <= c < hi
+        if (a.win_right >= 0) hi = min(hi, qrow + a.win_right - kb + 1);
+        const int lo = a.win_left >= 0 ? qrow - a.win_left - kb : 0;
 #pragma unroll
         for (int c = 0; c < 128; ++c)
-          if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
+          if (c >= hi || c < lo) sr[c] = __float_as_uint(-INFINITY);
       }
       const float mx = rowmax(sr);
       float sl2 = a.scale_log2;

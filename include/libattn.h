@@ -86,6 +86,19 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
                      attn_dtype dtype, void* stream);
 
 /*
+ * Forward, dense, sliding-window (local) attention (guijiagi.com, practical
+ * notes: sliding-window attention). Arguments as attn_fwd, with the mask
+ * given by a key window: key j is visible to query i iff
+ * i - window_left <= j <= i + window_right; -1 means no bound on that side
+ * (window (-1, 0) is causal, (-1, -1) full attention). Other negative values
+ * return ATTN_ERR_SHAPE. Every window contains the diagonal, so each row sees
+ * at least one key. KV tiles with no visible key are skipped.
+ */
+ATTN_API attn_status attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse,
+                                     int B, int Hq, int Hkv, int N, int d, float scale, int window_left,
+                                     int window_right, attn_dtype dtype, void* stream);
+
+/*
  * Forward, packed variable length (guijiagi.com, practical notes).
  * q [T,Hq,d], k/v [T,Hkv,d], o [T,Hq,d], lse [Hq,T]; cu_seqlens int32 [nseq+1]
  * on the device; max_seqlen is the largest length (host value, >= 1; used to
@@ -145,6 +158,16 @@ ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const
                      void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
                      int B, int Hq, int Hkv, int N, int d, float scale, int causal,
                      attn_dtype dtype, void* stream);
+
+/*
+ * Backward, dense, sliding window: arguments as attn_bwd with the key window
+ * of attn_fwd_window (lse from attn_fwd_window with the same window).
+ */
+ATTN_API attn_status attn_bwd_window(const void* q, const void* k, const void* v, const void* o,
+                                     const float* lse, const void* dout,
+                                     void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                                     int B, int Hq, int Hkv, int N, int d, float scale, int window_left,
+                                     int window_right, attn_dtype dtype, void* stream);
 
 /* Size in bytes of the device array attn_bwd_noalloc uses as its workspace. */
 #define ATTN_BWD_NOALLOC_MAX_BYTES (32u * 1024u * 1024u)

@@ -62,6 +62,12 @@ def test_argument_checks_before_any_device_work(lib):
     assert lib.attn_bwd(*args, None, ws, 1, 2, 1, 8, 128, 0.1, 0, 0, None) == 1
     assert lib.attn_bwd(*args, P(16), ws - 1, 1, 2, 1, 8, 128, 0.1, 0, 0, None) == 7
     assert lib.attn_bwd(*args, P(16), ws, 1, 2, 1, 8, 64, 0.1, 0, 0, None) == 4   # backward: d = 128 only
+    # sliding window: bounds are -1 (unbounded) or >= 0
+    assert lib.attn_fwd_window(P(16), P(16), P(16), P(16), P(16), 1, 2, 1, 8, 64, 0.1, -2, 0, 0, None) == 3
+    assert lib.attn_fwd_window(P(16), P(16), P(16), P(16), P(16), 1, 2, 1, 8, 64, 0.1, 4, -3, 0, None) == 3
+    assert lib.attn_fwd_window(None, P(16), P(16), P(16), P(16), 1, 2, 1, 8, 64, 0.1, 4, 0, 0, None) == 1
+    assert lib.attn_bwd_window(*args, P(16), ws, 1, 2, 1, 8, 128, 0.1, -5, 0, 0, None) == 3
+    assert lib.attn_bwd_window(*args, P(16), ws - 1, 1, 2, 1, 8, 128, 0.1, 3, 0, 0, None) == 7
 
 
 def test_workspace_size_arithmetic():

@@ -1,0 +1,129 @@
+"""Sliding-window (local) attention: the CUDA library against the float64
+oracle (GPU only).
+
+Key j is visible to query i iff i - left <= j <= i + right (-1: no bound).
+Tolerances are those of the dense forward and backward tests: RMS <= 2e-3,
+max |dLSE| <= 1e-3, relative RMS <= 1e-2 for dQ, dK, dV, and
+max (|dO| - 2^-8 |O_ref|) <= 1e-2. The relative term matters here: a narrow
+window averages few values, so |O| reaches 2-3, where rounding O to bf16
+(2^-9 relative) and P to bf16 (2^-9 relative per term) exceed 1e-2 absolute.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_73_gb300 import binding as L
+from exact_attention_73_gb300 import inputs
+from oracle import attention as A
+
+pytestmark = pytest.mark.gpu
+
+DT = {"bf16": torch.bfloat16, "fp16": torch.float16}
+
+# windows around the 128-wide tiles: inside one tile, exactly one tile, just
+# past a tile boundary, one-sided, two-sided, and wider than the sequence
+WINDOWS = [(0, 0), (3, 0), (127, 0), (128, 0), (130, 5), (-1, 40), (64, 64), (300, -1), (5000, 5000)]
+
+
+def check_o_lse(o, lse, o_ref, lse_ref, tag):
+    o = o.double().cpu().numpy() if hasattr(o, "cpu") else o
+    lse = lse.double().cpu().numpy() if hasattr(lse, "cpu") else lse
+    err = np.abs(o - o_ref)
+    assert np.isfinite(o).all(), tag
+    assert (err - 2.0 ** -8 * np.abs(o_ref)).max() <= 1e-2, (tag, err.max())
+    assert math.sqrt((err ** 2).mean()) <= 2e-3, (tag, math.sqrt((err ** 2).mean()))
+    assert np.abs(lse - lse_ref).max() <= 1e-3, (tag, np.abs(lse - lse_ref).max())
+
+
+def rel_rms(x, ref):
+    x = x.double().cpu().numpy() if hasattr(x, "cpu") else x
+    assert np.isfinite(x).all()
+    denom = max(float(np.linalg.norm(ref)), 1e-3 * np.sqrt(ref.size))
+    return float(np.linalg.norm(x - ref) / denom)
+
+
+def run_fwd(q, k, v, window):
+    qd, kd, vd = (x.cuda() for x in (q, k, v))
+    B, Hq, N, d = q.shape
+    o = torch.full_like(qd, float("nan"))
+    lse = torch.full((B, Hq, N), float("nan"), device="cuda")
+    L.attn_fwd_window(qd, kd, vd, o, lse, window)
+    torch.cuda.synchronize()
+    assert L.attn_get_device_status() == 0
+    return o, lse
+
+
+@pytest.mark.parametrize("window", WINDOWS)
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("n", [200, 1000])
+def test_forward_window(window, d, n):
+    q, k, v = inputs.normal(300 + d + n, [(2, 4, n, d), (2, 2, n, d), (2, 2, n, d)])
+    o, lse = run_fwd(q, k, v, window)
+    o_ref, lse_ref = A.forward(q, k, v, d ** -0.5, False, window)
+    check_o_lse(o, lse, o_ref, lse_ref, f"d{d} n{n} w{window}")
+
+
+def test_forward_window_fp16():
+    q, k, v = inputs.normal(310, [(1, 2, 700, 128)] * 3, dtype="fp16")
+    o, lse = run_fwd(q, k, v, (90, 10))
+    o_ref, lse_ref = A.forward(q, k, v, 128 ** -0.5, False, (90, 10))
+    check_o_lse(o, lse, o_ref, lse_ref, "fp16")
+
+
+def test_causal_window_equals_causal_entry_point():
+    q, k, v = inputs.normal(311, [(1, 4, 777, 128), (1, 2, 777, 128), (1, 2, 777, 128)])
+    o1, l1 = run_fwd(q, k, v, (-1, 0))
+    o2 = torch.empty_like(o1)
+    l2 = torch.empty_like(l1)
+    L.attn_fwd(q.cuda(), k.cuda(), v.cuda(), o2, l2, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def run_bwd(q, k, v, do, window):
+    qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
+    B, Hq, N, d = q.shape
+    o, lse = run_fwd(q, k, v, window)
+    dq = torch.full_like(qd, float("nan"))
+    dk = torch.full_like(kd, float("nan"))
+    dv = torch.full_like(vd, float("nan"))
+    ws = torch.full((L.attn_bwd_workspace_size(B, Hq, k.shape[1], N, d),), 255, dtype=torch.uint8, device="cuda")
+    L.attn_bwd_window(qd, kd, vd, o, lse, dod, dq, dk, dv, ws, window)
+    torch.cuda.synchronize()
+    assert L.attn_get_device_status() == 0
+    return dq.cpu(), dk.cpu(), dv.cpu()
+
+
+@pytest.mark.parametrize("window", WINDOWS)
+@pytest.mark.parametrize("n", [200, 700])
+def test_backward_window(window, n):
+    q, k, v, do = inputs.normal(320 + n, [(2, 4, n, 128), (2, 2, n, 128), (2, 2, n, 128), (2, 4, n, 128)])
+    got = run_bwd(q, k, v, do, window)
+    ref = A.backward(q, k, v, do, 128 ** -0.5, False, window)
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        assert rel_rms(g, r) <= 1e-2, (name, window, rel_rms(g, r))
+
+
+@pytest.mark.slow
+def test_window_config_sampled():
+    """B=1, H=16, N=16384, d=128, window (1024, 0): sampled rows of three heads
+    against the oracle's per-row forward; the backward on one head of a
+    2048-token slice of the same data against the full oracle backward."""
+    n, window = 16384, (1024, 0)
+    q, k, v = inputs.normal(6, [(1, 16, n, 128)] * 3)
+    o, lse = run_fwd(q, k, v, window)
+    o, lse = o.cpu(), lse.cpu()
+    rng = np.random.default_rng(61)
+    for h in (0, 7, 15):
+        rows = np.unique(np.concatenate([rng.choice(n, 40, replace=False), [0, 1023, 1024, 1025, n - 1]]))
+        o_ref, lse_ref = A.forward_rows(q[0, h], k[0, h], v[0, h], rows, 128 ** -0.5, False, window)
+        check_o_lse(o[0, h, rows], lse[0, h, rows], o_ref, lse_ref, f"h{h}")
+    m = 2048
+    qs, ks, vs = (x[:, :2, :m].contiguous() for x in (q, k, v))
+    do = inputs.normal(62, [(1, 2, m, 128)])[0]
+    got = run_bwd(qs, ks, vs, do, window)
+    ref = A.backward(qs, ks, vs, do, 128 ** -0.5, False, window)
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        assert rel_rms(g, r) <= 1e-2, (name, rel_rms(g, r))
