@@ -25,7 +25,8 @@ STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_NULL", 2: "ATTN_ERR_ALIGN", 3: "ATTN_ERR_SH
 EXPORTS = ("attn_status_string", "attn_version", "attn_fwd", "attn_fwd_varlen", "attn_quantize_fp8",
            "attn_fwd_fp8", "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_varlen_workspace_size",
            "attn_bwd_varlen", "attn_get_device_status", "attn_bwd_noalloc", "attn_selftest_wait_timeout",
-           "attn_fwd_window", "attn_bwd_window")
+           "attn_fwd_window", "attn_bwd_window", "attn_bwd_deterministic_workspace_size",
+           "attn_bwd_deterministic")
 
 
 class AttnError(RuntimeError):
@@ -51,6 +52,8 @@ _SIGS = {
     "attn_bwd_noalloc": ([_P] * 9 + [_I, _I, _I, _I, _I, _F, _I, _I, _P], _I),
     "attn_fwd_window": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P], _I),
     "attn_bwd_window": ([_P] * 9 + [_P, _Z, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P], _I),
+    "attn_bwd_deterministic_workspace_size": ([_I, _I, _I, _I, _I], _Z),
+    "attn_bwd_deterministic": ([_P] * 9 + [_P, _Z, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P], _I),
 }
 
 
@@ -166,6 +169,28 @@ def attn_bwd_window(q, k, v, o, lse, dout, dq, dk, dv, workspace, window, scale=
                                   _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                   B, Hq, Hkv, N, d, scale, left, right, _dtype(q), _stream(stream)),
            "attn_bwd_window")
+
+
+def attn_bwd_deterministic_workspace_size(B, Hq, Hkv, N, d):
+    return load().attn_bwd_deterministic_workspace_size(B, Hq, Hkv, N, d)
+
+
+def attn_bwd_deterministic(q, k, v, o, lse, dout, dq, dk, dv, workspace, window=(-1, -1), causal=False,
+                           scale=None, stream=None):
+    """Dense backward with one writer and one summation order per output
+    element (identical bits on every call); window as attn_fwd_window, and
+    causal=True means the window (-1, 0)."""
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    left, right = (int(w) for w in window)
+    if causal:
+        right = 0 if right < 0 else min(right, 0)
+    _check(load().attn_bwd_deterministic(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                                         _ptr(dk), _ptr(dv), _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(),
+                                         B, Hq, Hkv, N, d, scale, left, right, _dtype(q), _stream(stream)),
+           "attn_bwd_deterministic")
 
 
 def attn_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, scale=None, causal=False, stream=None):

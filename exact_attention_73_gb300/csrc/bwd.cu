@@ -36,9 +36,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ o, c
   for (int e = 0; e < c; ++e) acc = fmaf(to_f(po[e]), to_f(pd[e]), acc);
 #pragma unroll
   for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  float4* z = reinterpret_cast<float4*>(dq_acc + r * D + lane * c);
+  if (dq_acc) {   // absent for the deterministic backward (dQ written directly)
+    float4* z = reinterpret_cast<float4*>(dq_acc + r * D + lane * c);
 #pragma unroll
-  for (int e = 0; e < c / 4; ++e) z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int e = 0; e < c / 4; ++e) z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   if (lane == 0) {
     long long idx = r;
     if (packed) idx = static_cast<long long>(r % Hq) * T_tokens + r / Hq;
@@ -63,11 +65,11 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
   }
 }
 
-template <int DT>
+template <int DT, bool kDQ>
 cudaError_t launch_main(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q, const CUtensorMap& d,
                         const CUtensorMap& dq, const BwdArgs& a, int max_len, int nz, cudaStream_t st) {
   using C = BwdCfg<DT, 128>;
-  auto kern = bwd_kernel<DT, 128>;
+  auto kern = bwd_kernel<DT, 128, kDQ>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const dim3 grid((max_len + C::BC - 1) / C::BC, a.Hkv, nz);
@@ -93,8 +95,15 @@ cudaError_t launch_bwd_pre(int dt, int d, const void* o, const void* dout, float
 cudaError_t launch_bwd_main(int dt, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
                             const CUtensorMap& dout, const CUtensorMap& dq_acc, const BwdArgs& a, int max_len, int nz,
                             cudaStream_t st) {
-  return dt == kBF16 ? launch_main<kBF16>(k, v, q, dout, dq_acc, a, max_len, nz, st)
-                     : launch_main<kFP16>(k, v, q, dout, dq_acc, a, max_len, nz, st);
+  return dt == kBF16 ? launch_main<kBF16, true>(k, v, q, dout, dq_acc, a, max_len, nz, st)
+                     : launch_main<kFP16, true>(k, v, q, dout, dq_acc, a, max_len, nz, st);
+}
+
+cudaError_t launch_bwd_dkdv(int dt, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
+                            const CUtensorMap& dout, const BwdArgs& a, int max_len, int nz, cudaStream_t st) {
+  // the dQ map is never read without the dQ product; K's map stands in for it
+  return dt == kBF16 ? launch_main<kBF16, false>(k, v, q, dout, k, a, max_len, nz, st)
+                     : launch_main<kFP16, false>(k, v, q, dout, k, a, max_len, nz, st);
 }
 
 cudaError_t launch_dq_convert(int dt, const float* acc, void* dq, long long n, float scale, cudaStream_t st) {

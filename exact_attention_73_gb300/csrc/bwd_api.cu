@@ -86,9 +86,73 @@ attn_status run_bwd(const void* q, const void* k, const void* v, const void* o, 
   return from_cuda(e);
 }
 
+// Deterministic backward, dense: D (no dQ accumulator), the key-stationary
+// kernel for dK/dV without its dQ product, then the query-stationary dQ kernel.
+attn_status run_bwd_det(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                        const void* dout, void* dq, void* dk, void* dv, void* ws, int B, int N, int Hq, int Hkv,
+                        int d, float scale, int win_left, int win_right, attn_dtype dtype, int* status,
+                        void* stream) {
+  using namespace attn;
+  const long long rows = static_cast<long long>(B) * Hq * N;
+  float* dvec = static_cast<float*>(ws);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  CUtensorMap tk, tv, tq, tdo, tq128, tdo128;
+  if (!operand_map(&tk, k, dtype, d, false, B, Hkv, N, 128) || !operand_map(&tv, v, dtype, d, false, B, Hkv, N, 128) ||
+      !operand_map(&tq, q, dtype, d, false, B, Hq, N, 64) || !operand_map(&tdo, dout, dtype, d, false, B, Hq, N, 64) ||
+      !operand_map(&tq128, q, dtype, d, false, B, Hq, N, 128) ||
+      !operand_map(&tdo128, dout, dtype, d, false, B, Hq, N, 128))
+    return ATTN_ERR_CUDA;
+  BwdArgs a{};
+  a.lse = lse;
+  a.dvec = dvec;
+  a.dq_acc = nullptr;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.q_sn = d; a.q_sh = static_cast<long long>(N) * d; a.q_sb = static_cast<long long>(Hq) * N * d;
+  a.k_sn = d; a.k_sh = static_cast<long long>(N) * d; a.k_sb = static_cast<long long>(Hkv) * N * d;
+  a.l_sh = N; a.l_sb = static_cast<long long>(Hq) * N;
+  a.N = N;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.group = Hq / Hkv;
+  a.cu_seqlens = nullptr;
+  a.scale = scale;
+  a.scale_log2 = scale * kLog2e;
+  a.win_left = win_left;
+  a.win_right = win_right;
+  a.causal = (win_left < 0 && win_right == 0) ? 1 : 0;
+  a.status = status;
+  cudaError_t e = launch_bwd_pre(dtype, d, o, dout, dvec, nullptr, rows, Hq, N, 0, st);
+  if (e == cudaSuccess) e = launch_bwd_dkdv(dtype, tk, tv, tq, tdo, a, N, B, st);
+  if (e == cudaSuccess) e = launch_bwd_dq(dtype, tq128, tdo128, tk, tv, a, N, B, st);
+  return from_cuda(e);
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t attn_bwd_deterministic_workspace_size(int B, int Hq, int Hkv, int N, int d) {
+  (void)Hkv;
+  (void)d;
+  if (B < 1 || Hq < 1 || N < 1) return 0;
+  return round256(static_cast<size_t>(B) * Hq * N * 4);
+}
+
+attn_status attn_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                   const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                                   size_t ws_bytes, int B, int Hq, int Hkv, int N, int d, float scale,
+                                   int window_left, int window_right, attn_dtype dtype, void* stream) {
+  if (B < 1 || B > 65535 || N < 1 || window_left < -1 || window_right < -1) return ATTN_ERR_SHAPE;
+  attn_status s = check_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, ws_bytes,
+                               attn_bwd_deterministic_workspace_size(B, Hq, Hkv, N, d), Hq, Hkv, d, dtype);
+  if (s != ATTN_OK) return s;
+  int* status;
+  if ((s = attn::device_context(&status)) != ATTN_OK) return s;
+  return run_bwd_det(q, k, v, o, lse, dout, dq, dk, dv, workspace, B, N, Hq, Hkv, d, scale, window_left,
+                     window_right, dtype, status, stream);
+}
 
 size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d) {
   (void)Hkv;

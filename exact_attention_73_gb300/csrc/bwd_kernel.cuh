@@ -45,6 +45,7 @@ struct BwdArgs {
   const float* lse;         // natural-log LSE, strides l_sh, l_sb, row stride 1
   const float* dvec;        // D = rowsum(dO o O), same layout as lse
   float* dq_acc;            // FP32, layout of q (strides q_sn, q_sh, q_sb)
+  void* dq;                 // dQ written directly (deterministic backward), layout of q
   void* dk;                 // layout of k (strides k_sn, k_sh, k_sb)
   void* dv;
   long long q_sn, q_sh, q_sb;
@@ -93,7 +94,10 @@ struct BwdCfg {
   static constexpr uint32_t COL_DV = 256, COL_DK = 384;
 };
 
-template <int DT, int D>
+// kDQ = false: dK and dV only (the deterministic backward computes dQ in a
+// separate query-stationary kernel); the dQ^T product, its drain and the
+// reduce-adds are left out.
+template <int DT, int D, bool kDQ = true>
 __global__ void __launch_bounds__(512, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
            const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
@@ -291,7 +295,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
           // buffer (it+1)%2 was last used by it-1: its dQ^T halves must be drained
           const int sn = (it + 1) % C::NQ;
           if (!(ok = mbar_wait(&q_full[sn], ((it + 1) / C::NQ) & 1, a.status))) break;
-          if (!(ok = mbar_wait(dq_empty, (it & 1) ^ 1, a.status))) break;
+          if (kDQ && !(ok = mbar_wait(dq_empty, (it & 1) ^ 1, a.status))) break;
           tc_fence_after();
           issue_sdp(it + 1);
         }
@@ -299,17 +303,19 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         // The drain warps wait on dq_full by parity. On the last tile there is
         // no S^T/dP^T issue (and no dq_empty wait) above, so wait here for the
         // drain of it-1: dq_full then never runs two phases ahead of them.
-        if (it + 1 >= niter && it > 0 && !(ok = mbar_wait(dq_empty, (it & 1) ^ 1, a.status))) break;
+        if (kDQ && it + 1 >= niter && it > 0 && !(ok = mbar_wait(dq_empty, (it & 1) ^ 1, a.status))) break;
         tc_fence_after();
         const uint32_t so = st * C::Q_B;
         // dQ^T first, so the drain warps can read it while dV and dK run and
         // the next S^T/dP^T never waits for an empty tensor pipe
+        if constexpr (kDQ) {
 #pragma unroll
-        for (int kk = 0; kk < C::BC / 16; ++kk) {   // dQ^T = K^T dS^T, both MN-major
-          mma_ss<false>(xb + C::COL_DQ, dadd(dK_mn, kk * 2048), dadd(dDS0_mn, kk * 2048),
-                        C::IDESC_DQ, kk > 0);
+          for (int kk = 0; kk < C::BC / 16; ++kk) {   // dQ^T = K^T dS^T, both MN-major
+            mma_ss<false>(xb + C::COL_DQ, dadd(dK_mn, kk * 2048), dadd(dDS0_mn, kk * 2048),
+                          C::IDESC_DQ, kk > 0);
+          }
+          mma_commit(dq_full);
         }
-        mma_commit(dq_full);
 #pragma unroll
         for (int kk = 0; kk < C::BR / 16; ++kk) {   // dV += P^T dO_i
           mma_ts<false>(tbase + C::COL_DV, xb + C::COL_P + kk * 8, dadd(ddO0_mn, so + kk * 2048), C::IDESC_KV,
@@ -358,7 +364,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       if (got) got = __all_sync(0xffffffffu, mbar_wait(&sp_full[it & 1], (it >> 1) & 1, a.status));
       // the single dS^T tile in shared memory is read by dQ^T of the previous
       // tile; it must be complete before this tile's dS^T is stored
-      if (got && it > 0) got = __all_sync(0xffffffffu, mbar_wait(dq_full, (it - 1) & 1, a.status));
+      if (kDQ && got && it > 0) got = __all_sync(0xffffffffu, mbar_wait(dq_full, (it - 1) & 1, a.status));
       uint32_t sv[32], dp[32];
       if (got) {
         tc_fence_after();
@@ -418,14 +424,16 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       // 128-byte row, 128-byte swizzle (chunk ^= row % 8). The tile is free:
       // dQ^T of the previous tile (its only reader) completed before the
       // barrier above.
+      if constexpr (kDQ) {
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        const int chunk = (4 * half + c4) ^ (r & 7);
-        *reinterpret_cast<uint4*>(ds_row + chunk * 16) =
-            make_uint4(dd[4 * c4], dd[4 * c4 + 1], dd[4 * c4 + 2], dd[4 * c4 + 3]);
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const int chunk = (4 * half + c4) ^ (r & 7);
+          *reinterpret_cast<uint4*>(ds_row + chunk * 16) =
+              make_uint4(dd[4 * c4], dd[4 * c4 + 1], dd[4 * c4 + 2], dd[4 * c4 + 3]);
+        }
       }
       tmem_wait_st();
-      fence_proxy_async_smem();
+      if constexpr (kDQ) fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(ds_ready);
     }
@@ -459,7 +467,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     const int dim = quarter * 32 + lane;            // head-dim index = tensor-memory lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     bool ok = true;
-    for (int it = 0; it < niter; ++it) {
+    for (int it = 0; it < (kDQ ? niter : 0); ++it) {
       // one decision for all four drain warps, so none is left alone at the
       // named barriers below
       ok = named_bar_and(1, 128, __all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, a.status)));

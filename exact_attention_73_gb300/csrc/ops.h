@@ -20,6 +20,10 @@ cudaError_t launch_bwd_main(int dt, const CUtensorMap& k, const CUtensorMap& v, 
                             cudaStream_t st);
 // FP32 accumulator map (layout of the operands, no swizzle), boxes of d x box_rows.
 bool accum_map(CUtensorMap* m, const float* base, int d, bool packed, int B, int H, long long rows, int box_rows);
+cudaError_t launch_bwd_dkdv(int dt, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
+                            const CUtensorMap& dout, const BwdArgs& a, int max_len, int nz, cudaStream_t st);
+cudaError_t launch_bwd_dq(int dt, const CUtensorMap& q, const CUtensorMap& dout, const CUtensorMap& k,
+                          const CUtensorMap& v, const BwdArgs& a, int max_len, int nz, cudaStream_t st);
 cudaError_t launch_dq_convert(int dt, const float* acc, void* dq, long long n, float scale, cudaStream_t st);
 
 // Block quantisation to E4M3 (see attn_quantize_fp8).

@@ -169,6 +169,28 @@ ATTN_API attn_status attn_bwd_window(const void* q, const void* k, const void* v
                                      int B, int Hq, int Hkv, int N, int d, float scale, int window_left,
                                      int window_right, attn_dtype dtype, void* stream);
 
+/* Bytes of device workspace attn_bwd_deterministic needs: D = rowsum(dO o O)
+ * [B, Hq, N] float32, rounded up to 256 bytes (0 for sizes below 1). */
+ATTN_API size_t attn_bwd_deterministic_workspace_size(int B, int Hq, int Hkv, int N, int d);
+
+/*
+ * Deterministic backward, dense (§3.1 backward chain; §4 step 5 computes
+ * D first). Arguments as attn_bwd_window (window (-1, 0) = causal, (-1, -1)
+ * = full), workspace of attn_bwd_deterministic_workspace_size bytes. The
+ * pages accumulate dQ with atomic adds, whose order varies between runs; here
+ * dK and dV come from the key-stationary kernel (its dQ product left out) and
+ * dQ from a query-stationary kernel that recomputes S and dP per KV tile and
+ * sums dS K over the KV tiles in increasing order inside one CTA. Every output
+ * element has one writer and one summation order, so repeated calls with the
+ * same inputs return identical bits. Costs three more GEMMs per tile pair
+ * than attn_bwd (S and dP are computed twice). d must be 128.
+ */
+ATTN_API attn_status attn_bwd_deterministic(const void* q, const void* k, const void* v, const void* o,
+                                            const float* lse, const void* dout,
+                                            void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                                            int B, int Hq, int Hkv, int N, int d, float scale, int window_left,
+                                            int window_right, attn_dtype dtype, void* stream);
+
 /* Size in bytes of the device array attn_bwd_noalloc uses as its workspace. */
 #define ATTN_BWD_NOALLOC_MAX_BYTES (32u * 1024u * 1024u)
 
