@@ -9,6 +9,8 @@ Test infrastructure only. Sources (FlashAttention-3, zenmind.me summary):
 * §3.2 Algorithm 1: the tiled online softmax that the FP8 forward follows.
 * m.xxqk.cn FA3 walkthrough §4.1-4.2: E4M3 operands, FP32 accumulation,
   power-of-two scale factors.
+* §3.5 / guijiagi.com practical notes: quantisation is fused into the rotary
+  position embedding (RoPE) step that produces Q and K.
 
 Readings (the pages leave these open):
 * E4M3 is the OCP "e4m3fn" format: bias 7, largest finite 448, no infinity,
@@ -28,6 +30,12 @@ Readings (the pages leave these open):
   the accumulated O is multiplied by 2^(F_old - F_new) whenever F grows (the
   same correction as for the running row max m). The rounded value lies in
   (0, 256]. At the end O = O_acc * 2^(F - 4) / l; l sums the unrounded P~.
+* RoPE uses the rotate-half pairing (i, i + d/2), i < d/2: for the row at
+  position n, with c = cos[n, i] and s = sin[n, i] from caller-supplied float32
+  tables [N, d/2], y_i = x_i c - x_{i+d/2} s and y_{i+d/2} = x_{i+d/2} c + x_i s,
+  each product and the sum rounded to float32 separately (no fused multiply-
+  add). The producer order is RoPE, then the optional rotation, then the block
+  quantisation; V is not rotated.
 """
 from __future__ import annotations
 
@@ -121,16 +129,50 @@ def rotate_f64(x, signs):
     return (x * np.asarray(signs, dtype=np.float64)) @ hadamard(d) / np.sqrt(d)
 
 
-def quantize_blocks(x, signs=None, block=BLOCK):
+def rope_tables(n, d, base=10000.0):
+    """cos/sin tables [n, d/2] float32 of n * base^(-2i/d), computed in float64."""
+    i = np.arange(d // 2, dtype=np.float64)
+    ang = np.arange(n, dtype=np.float64)[:, None] * base ** (-2.0 * i / d)[None, :]
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+
+
+def rope_fp32(x, cos, sin):
+    """Rotate-half RoPE along the last axis of x [..., N, d] in float32, every
+    product and sum rounded separately; cos/sin [N, d/2] float32."""
+    x = np.asarray(x, dtype=np.float32)
+    c = np.asarray(cos, dtype=np.float32)
+    s = np.asarray(sin, dtype=np.float32)
+    h = x.shape[-1] // 2
+    a, b = x[..., :h], x[..., h:]
+    y = np.empty_like(x)
+    y[..., :h] = (a * c).astype(np.float32) - (b * s).astype(np.float32)
+    y[..., h:] = (b * c).astype(np.float32) + (a * s).astype(np.float32)
+    return y.astype(np.float32)
+
+
+def rope_f64(x, cos, sin):
+    """The same rotation in float64 (the definition, for pins)."""
+    x = np.asarray(x, dtype=np.float64)
+    c = np.asarray(cos, dtype=np.float64)
+    s = np.asarray(sin, dtype=np.float64)
+    h = x.shape[-1] // 2
+    a, b = x[..., :h], x[..., h:]
+    return np.concatenate([a * c - b * s, b * c + a * s], axis=-1)
+
+
+def quantize_blocks(x, signs=None, block=BLOCK, rope=None):
     """[B, H, N, d] -> (codes uint8 [B, H, N, d], factors float32 [B, H, ceil(N/block)]).
 
-    x is taken in float32 (as the GPU sees bf16/fp16 inputs); with ``signs``
-    the rotation is applied first. Each block of ``block`` rows of one
-    (batch, head) gets its own power-of-two factor.
+    x is taken in float32 (as the GPU sees bf16/fp16 inputs); with ``rope``
+    = (cos, sin) RoPE is applied first, then with ``signs`` the rotation. Each
+    block of ``block`` rows of one (batch, head) gets its own power-of-two
+    factor.
     """
     if hasattr(x, "detach"):
         x = x.detach().float().numpy()
     x = np.asarray(x, dtype=np.float32)
+    if rope is not None:
+        x = rope_fp32(x, *rope)
     if signs is not None:
         x = rotate_fp32(x, signs)
     b_, h_, n, d = x.shape

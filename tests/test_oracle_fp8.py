@@ -1,5 +1,6 @@
 """Pins for the FP8 part of the oracle: codec, scales, rotation, FP8 attention."""
 import json
+import math
 import os
 
 import numpy as np
@@ -191,3 +192,80 @@ def test_fp8_block_scales_beat_tensor_scale_when_one_block_is_large():
     blk = _emulated_rms(q, k, v, None, F.quantize_blocks, True, slice(0, 384))
     ten = _emulated_rms(q, k, v, None, F.quantize_tensor, True, slice(0, 384))
     assert blk < 0.75 * ten
+
+
+# ---------------------------------------------------------------------- RoPE
+
+def test_rope_equals_complex_rotation():
+    """Pairs (x_i, x_{i+d/2}) as complex numbers z: RoPE is z * exp(i theta)."""
+    rng = np.random.default_rng(60)
+    n, d = 37, 16
+    x = rng.standard_normal((2, 3, n, d))
+    c, s = F.rope_tables(n, d)
+    theta = np.arctan2(s.astype(np.float64), c.astype(np.float64))
+    radius = np.hypot(c.astype(np.float64), s.astype(np.float64))
+    z = (x[..., :d // 2] + 1j * x[..., d // 2:]) * radius * np.exp(1j * theta)
+    y = F.rope_f64(x, c, s)
+    np.testing.assert_allclose(y[..., :d // 2], z.real, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(y[..., d // 2:], z.imag, atol=1e-12, rtol=0)
+
+
+def test_rope_position_zero_is_identity_and_norms_are_kept():
+    rng = np.random.default_rng(61)
+    x = rng.standard_normal((1, 1, 50, 64)).astype(np.float32)
+    c, s = F.rope_tables(50, 64)
+    assert np.array_equal(F.rope_fp32(x, c, s)[..., 0, :], x[..., 0, :])
+    y = F.rope_f64(x, c, s)
+    pair = lambda t: np.hypot(t[..., :32], t[..., 32:])
+    np.testing.assert_allclose(pair(y), pair(x.astype(np.float64)) * np.hypot(c.astype(np.float64), s.astype(np.float64)), rtol=1e-12)
+
+
+def test_rope_scores_depend_on_relative_position_only():
+    """<R_m q, R_n k> = <R_(m+t) q, R_(n+t) k>: the defining property of RoPE."""
+    rng = np.random.default_rng(62)
+    d, n = 32, 64
+    q, k = rng.standard_normal(d), rng.standard_normal(d)
+    c, s = F.rope_tables(n, d)
+    # the float64 tables avoid float32 table rounding in this identity
+    i = np.arange(d // 2)
+    ang = np.arange(n)[:, None] * 10000.0 ** (-2.0 * i / d)[None, :]
+    c64, s64 = np.cos(ang), np.sin(ang)
+    rq = F.rope_f64(np.tile(q, (n, 1)), c64, s64)
+    rk = F.rope_f64(np.tile(k, (n, 1)), c64, s64)
+    for m, nn, t in ((5, 2, 7), (30, 30, 11), (0, 40, 3)):
+        np.testing.assert_allclose(rq[m] @ rk[nn], rq[m + t] @ rk[nn + t], atol=1e-10)
+    assert abs(rq[5] @ rk[2] - rq[5] @ rk[3]) > 1e-6     # and it does depend on m - n
+    # the float32 tables are the float64 ones rounded
+    np.testing.assert_array_equal(c, c64.astype(np.float32))
+
+
+def test_rope_fp32_is_the_f64_rotation_rounded():
+    rng = np.random.default_rng(63)
+    x = rng.standard_normal((1, 2, 40, 128)).astype(np.float32)
+    c, s = F.rope_tables(40, 128)
+    y32 = F.rope_fp32(x, c, s).astype(np.float64)
+    y64 = F.rope_f64(x, c, s)
+    # three float32 roundings of magnitudes <= |x| (|c|, |s| <= 1)
+    bound = 3 * 2.0 ** -24 * (np.abs(x) + np.abs(np.concatenate([x[..., 64:], x[..., :64]], -1))).astype(np.float64)
+    assert np.all(np.abs(y32 - y64) <= bound + 1e-45)
+
+
+def test_rope_worked_example():
+    """d = 4, position 1, base 10000: angles (1, 0.01)."""
+    c, s = F.rope_tables(2, 4)
+    x = np.array([[[[0.0, 0.0, 0.0, 0.0], [1.0, 2.0, 3.0, 4.0]]]], dtype=np.float32)
+    y = F.rope_f64(x, c, s)[0, 0, 1]
+    a0, a1 = 1.0, 0.01
+    ref = [1 * math.cos(a0) - 3 * math.sin(a0), 2 * math.cos(a1) - 4 * math.sin(a1),
+           3 * math.cos(a0) + 1 * math.sin(a0), 4 * math.cos(a1) + 2 * math.sin(a1)]
+    np.testing.assert_allclose(y, ref, rtol=1e-6)
+
+
+def test_quantize_with_rope_applies_rope_first():
+    rng = np.random.default_rng(64)
+    x = rng.standard_normal((1, 2, 130, 64)).astype(np.float32)
+    c, s = F.rope_tables(130, 64)
+    signs = np.where(rng.random(64) < 0.5, -1, 1)
+    a = F.quantize_blocks(x, signs, rope=(c, s))
+    b = F.quantize_blocks(F.rope_fp32(x, c, s), signs)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
