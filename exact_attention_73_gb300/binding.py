@@ -26,7 +26,7 @@ EXPORTS = ("attn_status_string", "attn_version", "attn_fwd", "attn_fwd_varlen", 
            "attn_fwd_fp8", "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_varlen_workspace_size",
            "attn_bwd_varlen", "attn_get_device_status", "attn_bwd_noalloc", "attn_selftest_wait_timeout",
            "attn_fwd_window", "attn_bwd_window", "attn_bwd_deterministic_workspace_size",
-           "attn_bwd_deterministic")
+           "attn_bwd_deterministic", "attn_quantize_fp8_rope")
 
 
 class AttnError(RuntimeError):
@@ -53,6 +53,7 @@ _SIGS = {
     "attn_fwd_window": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P], _I),
     "attn_bwd_window": ([_P] * 9 + [_P, _Z, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P], _I),
     "attn_bwd_deterministic_workspace_size": ([_I, _I, _I, _I, _I], _Z),
+    "attn_quantize_fp8_rope": ([_P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
     "attn_bwd_deterministic": ([_P] * 9 + [_P, _Z, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P], _I),
 }
 
@@ -134,6 +135,15 @@ def attn_quantize_fp8(x, x8, scales, hadamard_signs=None, stream=None):
     B, H, N, d = x.shape
     _check(load().attn_quantize_fp8(_ptr(x), _dtype(x), _ptr(x8), _ptr(scales), B, H, N, d,
                                     _ptr(hadamard_signs), _stream(stream)), "attn_quantize_fp8")
+
+
+def attn_quantize_fp8_rope(x, x8, scales, rope_cos, rope_sin, hadamard_signs=None, stream=None):
+    """RoPE (rotate-half, float32 cos/sin tables [N, d/2] on the device), then
+    the optional rotation and block quantisation, in one pass."""
+    B, H, N, d = x.shape
+    _check(load().attn_quantize_fp8_rope(_ptr(x), _dtype(x), _ptr(x8), _ptr(scales), B, H, N, d, _ptr(rope_cos),
+                                         _ptr(rope_sin), _ptr(hadamard_signs), _stream(stream)),
+           "attn_quantize_fp8_rope")
 
 
 def attn_fwd_fp8(q8, k8, v8, sq, sk, sv, o, lse, scale=None, causal=False, stream=None):

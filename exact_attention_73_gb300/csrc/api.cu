@@ -334,11 +334,12 @@ attn_status attn_get_device_status(void* stream) {
 
 }  // extern "C"
 
-extern "C" attn_status attn_quantize_fp8(const void* x, attn_dtype in_dtype, void* x8, float* scales,
-                                         int B, int H, int N, int d, const int8_t* hadamard_signs,
-                                         void* stream) {
+namespace {
+attn_status quantize(const void* x, attn_dtype in_dtype, void* x8, float* scales, int B, int H, int N, int d,
+                     const float* rope_cos, const float* rope_sin, const int8_t* hadamard_signs, void* stream) {
   if (!x || !x8 || !scales) return ATTN_ERR_NULL;
-  if (!aligned16(x) || !aligned16(x8) || !aligned16(scales) || (hadamard_signs && !aligned16(hadamard_signs)))
+  if (!aligned16(x) || !aligned16(x8) || !aligned16(scales) || (hadamard_signs && !aligned16(hadamard_signs)) ||
+      (rope_cos && !aligned16(rope_cos)) || (rope_sin && !aligned16(rope_sin)))
     return ATTN_ERR_ALIGN;
   if (B < 1 || B > 65535 || H < 1 || H > 65535 || N < 1) return ATTN_ERR_SHAPE;
   if (d != 64 && d != 128 && d != 256) return ATTN_ERR_HEADDIM;
@@ -348,5 +349,19 @@ extern "C" attn_status attn_quantize_fp8(const void* x, attn_dtype in_dtype, voi
   if (s != ATTN_OK) return s;
   const float inv_sqrt_d = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
   return from_cuda(launch_quant_fp8(x, in_dtype, static_cast<uint8_t*>(x8), scales, B, H, N, d, hadamard_signs,
-                                    inv_sqrt_d, static_cast<cudaStream_t>(stream)));
+                                    inv_sqrt_d, rope_cos, rope_sin, static_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+extern "C" attn_status attn_quantize_fp8(const void* x, attn_dtype in_dtype, void* x8, float* scales,
+                                         int B, int H, int N, int d, const int8_t* hadamard_signs,
+                                         void* stream) {
+  return quantize(x, in_dtype, x8, scales, B, H, N, d, nullptr, nullptr, hadamard_signs, stream);
+}
+
+extern "C" attn_status attn_quantize_fp8_rope(const void* x, attn_dtype in_dtype, void* x8, float* scales,
+                                              int B, int H, int N, int d, const float* rope_cos,
+                                              const float* rope_sin, const int8_t* hadamard_signs, void* stream) {
+  if (!rope_cos || !rope_sin) return ATTN_ERR_NULL;
+  return quantize(x, in_dtype, x8, scales, B, H, N, d, rope_cos, rope_sin, hadamard_signs, stream);
 }

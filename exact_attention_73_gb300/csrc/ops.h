@@ -28,6 +28,7 @@ cudaError_t launch_dq_convert(int dt, const float* acc, void* dq, long long n, f
 
 // Block quantisation to E4M3 (see attn_quantize_fp8).
 cudaError_t launch_quant_fp8(const void* x, int in_dt, uint8_t* x8, float* scales, int B, int H, int N, int d,
-                             const int8_t* signs, float inv_sqrt_d, cudaStream_t st);
+                             const int8_t* signs, float inv_sqrt_d, const float* rope_cos, const float* rope_sin,
+                             cudaStream_t st);
 
 }  // namespace attn

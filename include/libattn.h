@@ -124,6 +124,22 @@ ATTN_API attn_status attn_quantize_fp8(const void* x, attn_dtype in_dtype, void*
                               void* stream);
 
 /*
+ * Fused producer: rotary position embedding, optional rotation and block
+ * quantisation in one pass (§3.5: the paper fuses quantisation into the RoPE
+ * step that produces Q and K). Arguments as
+ * attn_quantize_fp8, plus rope_cos, rope_sin: float32 [N, d/2] device tables
+ * (16-byte aligned; the caller chooses the frequencies, row n = position n).
+ * Each row x at position n becomes, for i < d/2 with c = cos[n,i],
+ * s = sin[n,i]: y_i = x_i c - x_{i+d/2} s, y_{i+d/2} = x_{i+d/2} c + x_i s
+ * (rotate-half pairing; each product and sum rounded to float32 on its own),
+ * then the optional sign + Hadamard rotation and the per-block E4M3
+ * quantisation of attn_quantize_fp8. NULL tables return ATTN_ERR_NULL.
+ */
+ATTN_API attn_status attn_quantize_fp8_rope(const void* x, attn_dtype in_dtype, void* x8, float* scales,
+                                            int B, int H, int N, int d, const float* rope_cos,
+                                            const float* rope_sin, const int8_t* hadamard_signs, void* stream);
+
+/*
  * FP8 forward, dense (§3.5). q8 [B,Hq,N,d], k8/v8 [B,Hkv,N,d] E4M3 codes;
  * sq [B,Hq,ceil(N/128)], sk/sv [B,Hkv,ceil(N/128)] float32 power-of-two
  * dequantisation factors from attn_quantize_fp8. o [B,Hq,N,d] BF16,

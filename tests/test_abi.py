@@ -53,6 +53,10 @@ def test_argument_checks_before_any_device_work(lib):
     assert lib.attn_fwd_varlen(P(16), P(16), P(16), P(16), P(16), P(16), 0, 10, 5, 2, 1, 64, 0.1, 0, 0, None) == 3
     assert lib.attn_fwd_varlen(P(16), P(16), P(16), P(16), P(16), P(16), 2, 10, 11, 2, 1, 64, 0.1, 0, 0, None) == 3
     assert lib.attn_fwd_varlen(P(16), P(16), P(16), P(16), P(16), None, 2, 10, 5, 2, 1, 64, 0.1, 0, 0, None) == 1
+    # fused RoPE producer: the tables are required and aligned
+    assert lib.attn_quantize_fp8_rope(P(16), 0, P(16), P(16), 1, 1, 8, 64, None, P(16), None, None) == 1
+    assert lib.attn_quantize_fp8_rope(P(16), 0, P(16), P(16), 1, 1, 8, 64, P(16), P(20), None, None) == 2
+    assert lib.attn_quantize_fp8_rope(P(16), 0, P(16), P(16), 1, 1, 8, 96, P(16), P(16), None, None) == 4
     # quantiser: head dim and dtype
     assert lib.attn_quantize_fp8(P(16), 0, P(16), P(16), 1, 1, 8, 32, None, None) == 4
     assert lib.attn_quantize_fp8(P(16), 2, P(16), P(16), 1, 1, 8, 64, None, None) == 6

@@ -242,3 +242,52 @@ def test_fp8_config_accuracy_sampled(d, causal):
     assert rms(gpu) <= 1.5e-2, rms(gpu)
     assert rms(gpu) <= rms(ten) * 1.02 + 1e-4, (rms(gpu), rms(ten))
     check_fp8_vs_emulation(gpu, emu)
+
+
+# ---------------------------------------------------- fused RoPE producer
+
+def quantize_rope_gpu(x, cos, sin, signs=None):
+    B, H, N, d = x.shape
+    x8 = torch.empty(x.shape, dtype=torch.uint8, device="cuda")
+    sc = torch.empty((B, H, (N + 127) // 128), device="cuda")
+    L.attn_quantize_fp8_rope(x.cuda(), x8, sc, torch.from_numpy(cos).cuda(), torch.from_numpy(sin).cuda(),
+                             None if signs is None else signs.cuda())
+    torch.cuda.synchronize()
+    return x8, sc
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("rotate", [False, True])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("n", [1, 300])
+def test_rope_quantizer_bit_exact(d, rotate, dtype, n):
+    """RoPE (rotate-half, float32 tables), rotation and block quantisation in
+    one pass: codes and factors equal the oracle's bit for bit."""
+    (x,) = inputs.outliers(5, [(2, 3, n, d)], dtype=dtype)
+    cos, sin = F.rope_tables(n, d)
+    signs = inputs.random_signs(4, d) if rotate else None
+    x8, sc = quantize_rope_gpu(x, cos, sin, signs)
+    codes, fac = F.quantize_blocks(x, None if signs is None else signs.numpy(), rope=(cos, sin))
+    np.testing.assert_array_equal(sc.cpu().numpy(), fac)
+    np.testing.assert_array_equal(x8.cpu().numpy(), codes)
+
+
+def test_rope_producer_feeds_fp8_attention():
+    """Q, K through the fused producer, V through the plain quantiser: the FP8
+    forward against the float64 attention of the RoPE-rotated inputs."""
+    n, d = 700, 128
+    q, k, v = inputs.normal(12, [(1, 2, n, d)] * 3)
+    cos, sin = F.rope_tables(n, d)
+    signs = inputs.random_signs(4, d)
+    q8, sq = quantize_rope_gpu(q, cos, sin, signs)
+    k8, sk = quantize_rope_gpu(k, cos, sin, signs)
+    v8, sv = quantize_gpu(v)
+    o = torch.empty((1, 2, n, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((1, 2, n), device="cuda")
+    L.attn_fwd_fp8(q8, k8, v8, sq.cuda(), sk.cuda(), sv.cuda(), o, lse)
+    torch.cuda.synchronize()
+    qr = F.rope_f64(q.double().numpy(), cos, sin)
+    kr = F.rope_f64(k.double().numpy(), cos, sin)
+    o_ref, _ = A.forward(qr, kr, v, d ** -0.5, False)
+    err = o.double().cpu().numpy() - o_ref
+    assert math.sqrt((err ** 2).mean()) <= 1.5e-2
