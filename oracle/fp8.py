@@ -30,6 +30,11 @@ Readings (the pages leave these open):
   the accumulated O is multiplied by 2^(F_old - F_new) whenever F grows (the
   same correction as for the running row max m). The rounded value lies in
   (0, 256]. At the end O = O_acc * 2^(F - 4) / l; l sums the unrounded P~.
+* Decode over a KV cache: the g query heads of one KV group at the decoded
+  position are one block of g query rows with one factor; the cache keys are
+  split into runs of whole 128-key tiles, each run is processed as Algorithm 1
+  from a fresh state (m = -inf, l = 0, F = -inf), and the runs are combined
+  exactly by their log-sum-exp weights (the split-KV form of the forward).
 * RoPE uses the rotate-half pairing (i, i + d/2), i < d/2: for the row at
   position n, with c = cos[n, i] and s = sin[n, i] from caller-supplied float32
   tables [N, d/2], y_i = x_i c - x_{i+d/2} s and y_{i+d/2} = x_{i+d/2} c + x_i s,
@@ -207,6 +212,37 @@ def quantize_tensor(x, signs=None, block=BLOCK):
     return codes, fac
 
 
+def _fp8_rows(qrows, q_fac, kf, vf, sk, sv, tiles, n, scale, causal=False, rows=None, block=BLOCK, p_shift=4,
+              tau=4.0):
+    """Algorithm 1 in its FP8 form for query rows ``qrows`` [R, d] (decoded,
+    with per-row factors q_fac) over the key tiles ``tiles`` (in order) of one
+    KV head: kf/vf [N, d] decoded, sk/sv per-tile factors. Starts from m = -inf,
+    l = 0, O = 0. Returns (O [R, d], LSE [R])."""
+    d = qrows.shape[1]
+    m = np.full(len(qrows), -np.inf)
+    l = np.zeros(len(qrows))
+    acc = np.zeros((len(qrows), d))
+    f_run = -np.inf
+    for j in tiles:
+        cols = np.arange(j * block, min(n, (j + 1) * block))
+        s = scale * q_fac[:, None] * sk[j] * (qrows @ kf[cols].T)
+        if causal:
+            s = np.where(cols[None, :] > rows[:, None], -np.inf, s)
+        mx = s.max(axis=1)
+        m_new = np.where(mx > m + tau * np.log(2.0), mx, m)   # stale max within 2^tau
+        m_use = np.where(np.isfinite(m_new), m_new, 0.0)
+        corr = np.exp(m - m_use)
+        f_j = np.log2(sv[j])
+        f_new = max(f_run, f_j)
+        v_corr = np.exp2(f_run - f_new)
+        pt = np.exp(s - m_use[:, None])
+        l = corr * l + pt.sum(axis=1)
+        p8 = e4m3_decode(e4m3_encode(pt * np.exp2(p_shift + f_j - f_new)))
+        acc = (corr * v_corr)[:, None] * acc + p8 @ vf[cols]
+        m, f_run = m_new, f_new
+    return acc * np.exp2(f_run - p_shift) / l[:, None], m + np.log(l)
+
+
 def attention_fp8(q8, k8, v8, sq, sk, sv, scale, causal=False, block=BLOCK, p_shift=4, tau=4.0, heads=None,
                   rows=None):
     """FP8 forward following Algorithm 1 tile by tile (Bc = block keys per tile).
@@ -226,30 +262,48 @@ def attention_fp8(q8, k8, v8, sq, sk, sv, scale, causal=False, block=BLOCK, p_sh
     rows = np.arange(n) if rows is None else np.asarray(rows)
     heads = [(b, h) for b in range(b_) for h in range(hq)] if heads is None else heads
     for b, h in heads:
-            kv = h // g
-            q_fac = sq[b, h, rows // block]
-            qrows = qf[b, h, rows]
-            m = np.full(len(rows), -np.inf)
-            l = np.zeros(len(rows))
-            acc = np.zeros((len(rows), d))
-            f_run = -np.inf
-            for j in range((n + block - 1) // block):
-                cols = np.arange(j * block, min(n, (j + 1) * block))
-                s = scale * q_fac[:, None] * sk[b, kv, j] * (qrows @ kf[b, kv, cols].T)
-                if causal:
-                    s = np.where(cols[None, :] > rows[:, None], -np.inf, s)
-                mx = s.max(axis=1)
-                m_new = np.where(mx > m + tau * np.log(2.0), mx, m)   # stale max within 2^tau
-                m_use = np.where(np.isfinite(m_new), m_new, 0.0)
-                corr = np.exp(m - m_use)
-                f_j = np.log2(sv[b, kv, j])
-                f_new = max(f_run, f_j)
-                v_corr = np.exp2(f_run - f_new)
-                pt = np.exp(s - m_use[:, None])
-                l = corr * l + pt.sum(axis=1)
-                p8 = e4m3_decode(e4m3_encode(pt * np.exp2(p_shift + f_j - f_new)))
-                acc = (corr * v_corr)[:, None] * acc + p8 @ vf[b, kv, cols]
-                m, f_run = m_new, f_new
-            o[b, h, rows] = acc * np.exp2(f_run - p_shift) / l[:, None]
-            lse[b, h, rows] = m + np.log(l)
+        kv = h // g
+        o[b, h, rows], lse[b, h, rows] = _fp8_rows(
+            qf[b, h, rows], sq[b, h, rows // block], kf[b, kv], vf[b, kv], sk[b, kv], sv[b, kv],
+            range((n + block - 1) // block), n, scale, causal, rows, block, p_shift, tau)
+    return o, lse
+
+
+def combine_splits(o_parts, lse_parts):
+    """Partial results of disjoint key ranges -> the result over their union:
+    LSE = log sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s (float64).
+    o_parts [S, ..., d], lse_parts [S, ...]; a part with LSE = -inf adds nothing."""
+    o_parts = np.asarray(o_parts, dtype=np.float64)
+    lse_parts = np.asarray(lse_parts, dtype=np.float64)
+    mx = lse_parts.max(axis=0)
+    w = np.exp(lse_parts - mx[None])
+    tot = w.sum(axis=0)
+    o = (w[..., None] * np.nan_to_num(o_parts)).sum(axis=0) / tot[..., None]
+    return o, mx + np.log(tot)
+
+
+def decode_fp8(q8, sq, k8, v8, sk, sv, lens, scale, tiles_per_split, block=BLOCK, p_shift=4, tau=4.0):
+    """FP8 decode over a block-quantised KV cache, split by key tiles.
+
+    q8 [B, Hkv, g, d]: E4M3 codes of the g query heads of each KV group at the
+    decoded position (query head h = kv * g + i), sq [B, Hkv] their factors;
+    k8/v8 [B, Hkv, Nmax, d] and sk/sv [B, Hkv, ceil(Nmax/block)] the cache;
+    lens[b] the valid cache length of sequence b. Split s holds key tiles
+    [s * tiles_per_split, (s + 1) * tiles_per_split) below ceil(lens[b]/block);
+    each split runs the FP8 form of Algorithm 1 on its own and the splits are
+    combined with combine_splits. Returns (O [B, Hkv, g, d], LSE [B, Hkv, g]).
+    """
+    qf, kf, vf = e4m3_decode(q8), e4m3_decode(k8), e4m3_decode(v8)
+    sq, sk, sv = (np.asarray(a, dtype=np.float64) for a in (sq, sk, sv))
+    b_, hkv, g, d = qf.shape
+    o = np.empty((b_, hkv, g, d))
+    lse = np.empty((b_, hkv, g))
+    for b in range(b_):
+        n = int(lens[b])
+        nt = (n + block - 1) // block
+        splits = [range(t, min(t + tiles_per_split, nt)) for t in range(0, nt, tiles_per_split)]
+        for kv in range(hkv):
+            parts = [_fp8_rows(qf[b, kv], np.full(g, sq[b, kv]), kf[b, kv], vf[b, kv], sk[b, kv], sv[b, kv],
+                               tiles, n, scale, block=block, p_shift=p_shift, tau=tau) for tiles in splits]
+            o[b, kv], lse[b, kv] = combine_splits([p[0] for p in parts], [p[1] for p in parts])
     return o, lse

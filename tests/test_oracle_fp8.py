@@ -269,3 +269,62 @@ def test_quantize_with_rope_applies_rope_first():
     a = F.quantize_blocks(x, signs, rope=(c, s))
     b = F.quantize_blocks(F.rope_fp32(x, c, s), signs)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# -------------------------------------------------------------------- decode
+
+def test_combine_splits_is_exact():
+    """Attention over disjoint key ranges, combined by LSE weights, is the
+    attention over their union (plain float64, no FP8)."""
+    rng = np.random.default_rng(70)
+    n, d = 300, 16
+    q, k, v = rng.standard_normal((5, d)), rng.standard_normal((n, d)), rng.standard_normal((n, d))
+    o, lse, _ = A.head_forward(q, k, v, 0.3, False)
+    cuts = [0, 1, 128, 200, 300]
+    parts = [A.head_forward(q, k[a:b], v[a:b], 0.3, False)[:2] for a, b in zip(cuts, cuts[1:])]
+    o2, lse2 = F.combine_splits([p[0] for p in parts], [p[1] for p in parts])
+    np.testing.assert_allclose(o2, o, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(lse2, lse, atol=1e-12, rtol=0)
+
+
+def _decode_case(seed, b_, hkv, g, nmax, d):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((b_, hkv, g, d)).astype(np.float32)
+    k = rng.standard_normal((b_, hkv, nmax, d)).astype(np.float32)
+    v = rng.standard_normal((b_, hkv, nmax, d)).astype(np.float32)
+    q8, sq = F.quantize_blocks(q)
+    k8, sk = F.quantize_blocks(k)
+    v8, sv = F.quantize_blocks(v)
+    return q8, sq[:, :, 0], k8, v8, sk, sv
+
+
+def test_decode_single_split_is_the_fp8_forward():
+    g, nmax, d = 4, 300, 32
+    q8, sq, k8, v8, sk, sv = _decode_case(71, 1, 1, g, nmax, d)
+    o, lse = F.decode_fp8(q8, sq, k8, v8, sk, sv, [nmax], 0.2, tiles_per_split=100)
+    qpad = np.zeros((1, 1, nmax, d), dtype=np.uint8)
+    qpad[0, 0, :g] = q8[0, 0]
+    sqpad = np.ones((1, 1, (nmax + 127) // 128), dtype=np.float32)
+    sqpad[0, 0, 0] = sq[0, 0]
+    o2, lse2 = F.attention_fp8(qpad, k8, v8, sqpad, sk, sv, 0.2, rows=np.arange(g))
+    np.testing.assert_array_equal(o[0, 0], o2[0, 0, :g])
+    np.testing.assert_array_equal(lse[0, 0], lse2[0, 0, :g])
+
+
+def test_decode_splits_and_lengths_close_to_exact():
+    """Several splits and ragged cache lengths against float64 attention of
+    the dequantised values: only the E4M3 rounding of P~ differs."""
+    b_, hkv, g, nmax, d = 2, 2, 3, 700, 32
+    q8, sq, k8, v8, sk, sv = _decode_case(72, b_, hkv, g, nmax, d)
+    lens = [700, 259]
+    o, lse = F.decode_fp8(q8, sq, k8, v8, sk, sv, lens, 0.25, tiles_per_split=2)
+    deq = lambda c, f: F.e4m3_decode(c) * np.repeat(f, 128, axis=-1)[..., :c.shape[2], None]
+    qf = F.e4m3_decode(q8) * sq[:, :, None, None]
+    kf, vf = deq(k8, sk), deq(v8, sv)
+    for b in range(b_):
+        n = lens[b]
+        for kv in range(hkv):
+            ro, rl, _ = A.head_forward(qf[b, kv], kf[b, kv, :n], vf[b, kv, :n], 0.25, False)
+            err = o[b, kv] - ro
+            assert np.sqrt((err ** 2).mean()) < 1e-2 and np.abs(err).max() < 5e-2
+            assert np.abs(lse[b, kv] - rl).max() < 1e-2
