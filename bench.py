@@ -16,6 +16,11 @@ Sliding-window workloads (name starting "window_") time a step of
 attn_fwd_window + attn_bwd_window (BF16) instead; their FLOPs count only the
 visible (query, key) pairs: 4 B H d * pairs forward, 2.5x that backward.
 
+Decode workloads (name starting "decode_") time attn_decode_fp8, one new
+token per sequence over a resident block-quantised FP8 KV cache; the metric is
+cache bytes read per second (HBM-bound), with the measured copy bandwidth as
+the roofline peak.
+
 --impl reference times the float64 CPU oracle on a bounded sample of the same
 workload (one head per step) in the same units.
 Under torchrun every rank runs the same workload on its own GPU (replicas, no
@@ -46,6 +51,10 @@ WORKLOADS = {
     "window_b1_h16_n16384_w1024": (1, 16, 16, 16384, 128, False, (1024, 0)),
 }
 DEFAULT = "bf16_sweep_d128_n8192"
+DECODE_WORKLOADS = {
+    # name: (B, Hq, Hkv, Nmax, d, splits): a 1 GiB FP8 cache, GQA groups of 4
+    "decode_fp8_b16_hq32_hkv8_n32768_d128": (16, 32, 8, 32768, 128, 8),
+}
 LAUNCHES_PER_STEP = 8   # fwd 1, bwd 3, quantise 3, fp8 fwd 1
 
 
@@ -323,6 +332,154 @@ def cpu_sample(wl, steps=1):
     return per_step * steps, dt
 
 
+def bench_decode(args, wl, rank, world):
+    """Time attn_decode_fp8 on a resident cache; returns the JSON line's fields."""
+    import numpy as np
+    import torch
+    from exact_attention_73_gb300 import binding as L
+    from exact_attention_73_gb300 import inputs
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    L.load(build_if_missing=True)
+    B, Hq, Hkv, N, d, splits = wl
+    g = Hq // Hkv
+    gen = torch.Generator(device=dev).manual_seed(7)   # a 1 GiB cache is drawn on the device
+    q = torch.randn((B, Hq, d), generator=gen, device=dev).to(torch.bfloat16)
+    k = torch.randn((B, Hkv, N, d), generator=gen, device=dev).to(torch.bfloat16)
+    v = torch.randn((B, Hkv, N, d), generator=gen, device=dev).to(torch.bfloat16)
+    signs = inputs.random_signs(4, d).to(dev)
+    nb = (N + 127) // 128
+    k8 = torch.empty(k.shape, dtype=torch.uint8, device=dev)
+    v8 = torch.empty(v.shape, dtype=torch.uint8, device=dev)
+    sk = torch.empty((B, Hkv, nb), device=dev)
+    sv = torch.empty((B, Hkv, nb), device=dev)
+    L.attn_quantize_fp8(k, k8, sk, signs)
+    L.attn_quantize_fp8(v, v8, sv)
+    q8 = torch.empty((B, Hq, d), dtype=torch.uint8, device=dev)
+    sq3 = torch.empty((B, Hkv, 1), device=dev)
+    L.attn_quantize_fp8(q.view(B, Hkv, g, d), q8.view(B, Hkv, g, d), sq3, signs)
+    sq = sq3[:, :, 0].contiguous()
+    del k, v
+    o = torch.empty((B, Hq, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, Hq), device=dev)
+    ws = torch.empty((L.attn_decode_fp8_workspace_size(B, Hq, d, splits),), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        L.attn_decode_fp8(q8, sq, k8, v8, sk, sv, o, lse, ws, splits)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    clocks = Clocks(dev.index)
+    barrier()
+    clocks.start()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    # end to end: the new token's codes and factors in, O and LSE out, every step
+    hq8, hsq = q8.cpu().pin_memory(), sq.cpu().pin_memory()
+    ho, hl = torch.empty(o.shape, dtype=o.dtype, pin_memory=True), torch.empty(lse.shape, pin_memory=True)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        q8.copy_(hq8, non_blocking=True)
+        sq.copy_(hsq, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    ms_e2e = e0.elapsed_time(e1)
+    if L.attn_get_device_status() != 0:
+        raise RuntimeError("device-side wait timed out during the decode run")
+    ms, ms_e2e = max_over_ranks([ms, ms_e2e], world, dev)
+    h2d = hq8.numel() + hsq.numel() * 4
+    d2h = ho.numel() * 2 + hl.numel() * 4
+    cache_bytes = 2 * B * Hkv * N * d + 2 * B * Hkv * nb * 4
+    line = {"ms_total": ms, "ms_e2e": ms_e2e, "clocks": clk, "h2d": h2d, "d2h": d2h,
+            "bytes": cache_bytes, "flops": 4.0 * B * Hq * N * d}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        qn, kn, vn = q8[0:1].cpu().numpy(), k8[0:1].cpu().numpy(), v8[0:1].cpu().numpy()
+        t = time.perf_counter()
+        from oracle import fp8 as F
+        F.decode_fp8(qn.reshape(1, Hkv, g, d), sq[0:1].cpu().numpy(), kn, vn, sk[0:1].cpu().numpy(),
+                     sv[0:1].cpu().numpy(), [N], d ** -0.5, -(-nb // splits))
+        sec = time.perf_counter() - t
+        line["cpu"] = (2 * Hkv * N * d + 2 * Hkv * nb * 4) / sec / 1e9, sec
+    return line
+
+
+def decode_main(args, world, rank):
+    import numpy as np
+    wl = DECODE_WORKLOADS[args.workload]
+    B, Hq, Hkv, N, d, splits = wl
+    config = {"workload": args.workload, "B": B, "Hq": Hq, "Hkv": Hkv, "Nmax": N, "d": d, "splits": splits,
+              "step": "attn_decode_fp8: one token per sequence over the whole FP8 cache (+ split combine)",
+              "l2": "cache (1 GiB) larger than L2 (no flush)", "parallelism": f"replicas x{world}"}
+    metric = "FP8 KV-cache decode: cache bytes read per second on GB300"
+    pk = peaks()
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        from oracle import fp8 as F
+        rng = np.random.default_rng(7)
+        g, nb = Hq // Hkv, (N + 127) // 128
+        q8 = rng.integers(0, 120, (1, Hkv, g, d), dtype=np.uint8)
+        k8 = rng.integers(0, 120, (1, Hkv, N, d), dtype=np.uint8)
+        v8 = rng.integers(0, 120, (1, Hkv, N, d), dtype=np.uint8)
+        f = np.ones((1, Hkv, nb), dtype=np.float32)
+        t = time.perf_counter()
+        for _ in range(args.steps):
+            F.decode_fp8(q8, np.ones((1, Hkv), dtype=np.float32), k8, v8, f, f, [N], d ** -0.5, -(-nb // splits))
+        sec = time.perf_counter() - t
+        val = args.steps * (2 * Hkv * N * d + 2 * Hkv * nb * 4) / sec / 1e9
+        print(json.dumps({"impl": "reference", "metric": metric, "value": val, "unit": "GB/s", "n_gpus": world,
+                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic", "config": config,
+                          "cpu_baseline": {"kind": "oracle", "value": val, "unit": "GB/s", "cores": cpu_cores(),
+                                           "sample": "one sequence (b = 0) of the workload per step"},
+                          "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+              flush=True)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    r = bench_decode(args, wl, rank, world)
+    gbs = world * r["bytes"] * args.steps / (r["ms_total"] * 1e-3) / 1e9
+    line = {"metric": metric, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": r["ms_total"] / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic", "config": config,
+            "tokens_per_s": world * B * args.steps / (r["ms_total"] * 1e-3),
+            "roofline": {"bound": "hbm", "kernel": "attn_decode_fp8 (split kernel + combine)",
+                         "achieved": gbs / world, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / world / pk["hbm_gbs"], "peak_source": pk["source"] + " copy bandwidth",
+                         "traffic": None},
+            "e2e": {"value": world * r["bytes"] * args.steps / (r["ms_e2e"] * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+            "gpu_launches": 2 * args.steps, "clocks": r["clocks"]}
+    if "cpu" in r:
+        line["cpu_baseline"] = {"value": r["cpu"][0], "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+                                "sample": f"one sequence (b = 0) of the workload: {r['cpu'][1]:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -336,15 +493,17 @@ def main():
     ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT)
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(DECODE_WORKLOADS), default=DEFAULT)
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle timing")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    wl = WORKLOADS[args.workload]
-    B, Hq, Hkv, N, d, causal, window = wl
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.workload in DECODE_WORKLOADS:
+        return decode_main(args, world, rank)
+    wl = WORKLOADS[args.workload]
+    B, Hq, Hkv, N, d, causal, window = wl
     config = {"workload": args.workload, "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d, "causal": causal,
               "step": "fwd bf16 + bwd bf16 + fp8 quantise (Q,K rotated) + fwd fp8",
               "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"}

@@ -26,7 +26,8 @@ EXPORTS = ("attn_status_string", "attn_version", "attn_fwd", "attn_fwd_varlen", 
            "attn_fwd_fp8", "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_varlen_workspace_size",
            "attn_bwd_varlen", "attn_get_device_status", "attn_bwd_noalloc", "attn_selftest_wait_timeout",
            "attn_fwd_window", "attn_bwd_window", "attn_bwd_deterministic_workspace_size",
-           "attn_bwd_deterministic", "attn_quantize_fp8_rope")
+           "attn_bwd_deterministic", "attn_quantize_fp8_rope", "attn_decode_fp8_workspace_size",
+           "attn_decode_fp8")
 
 
 class AttnError(RuntimeError):
@@ -54,6 +55,8 @@ _SIGS = {
     "attn_bwd_window": ([_P] * 9 + [_P, _Z, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P], _I),
     "attn_bwd_deterministic_workspace_size": ([_I, _I, _I, _I, _I], _Z),
     "attn_quantize_fp8_rope": ([_P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
+    "attn_decode_fp8_workspace_size": ([_I, _I, _I, _I], _Z),
+    "attn_decode_fp8": ([_P] * 10 + [_Z, _I, _I, _I, _I, _I, _F, _I, _P], _I),
     "attn_bwd_deterministic": ([_P] * 9 + [_P, _Z, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P], _I),
 }
 
@@ -153,6 +156,22 @@ def attn_fwd_fp8(q8, k8, v8, sq, sk, sv, o, lse, scale=None, causal=False, strea
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     _check(load().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(sq), _ptr(sk), _ptr(sv), _ptr(o), _ptr(lse),
                                B, Hq, Hkv, N, d, scale, int(bool(causal)), _stream(stream)), "attn_fwd_fp8")
+
+
+def attn_decode_fp8_workspace_size(B, Hq, d, num_splits):
+    return load().attn_decode_fp8_workspace_size(B, Hq, d, num_splits)
+
+
+def attn_decode_fp8(q8, sq, k8, v8, sk, sv, o, lse, workspace, num_splits, seqlens=None, scale=None, stream=None):
+    """One decoded token per sequence: q8 [B,Hq,d] codes, sq [B,Hkv]; cache k8/v8
+    [B,Hkv,Nmax,d] with sk/sv [B,Hkv,ceil(Nmax/128)]; seqlens int32 [B] or None;
+    o [B,Hq,d] bf16, lse [B,Hq]."""
+    B, Hq, d = q8.shape
+    _, Hkv, Nmax, _ = k8.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    _check(load().attn_decode_fp8(_ptr(q8), _ptr(sq), _ptr(k8), _ptr(v8), _ptr(sk), _ptr(sv), _ptr(seqlens), _ptr(o),
+                                  _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  B, Hq, Hkv, Nmax, d, scale, int(num_splits), _stream(stream)), "attn_decode_fp8")
 
 
 def attn_bwd_workspace_size(B, Hq, Hkv, N, d):

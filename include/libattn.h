@@ -155,6 +155,34 @@ ATTN_API attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8
                          int B, int Hq, int Hkv, int N, int d, float scale, int causal,
                          void* stream);
 
+/* Bytes of workspace attn_decode_fp8 needs: per split, a float32 partial O
+ * [B, Hq, d] and LSE [B, Hq], each area rounded up to 256 bytes. */
+ATTN_API size_t attn_decode_fp8_workspace_size(int B, int Hq, int d, int num_splits);
+
+/*
+ * FP8 decode over a block-quantised KV cache, split-KV (§3.5 FP8 forward of
+ * Algorithm 1 applied to one new token per sequence; the pages do not give a
+ * decode kernel — this is the forward's split form). One query token per
+ * sequence and query head:
+ *   q8 [B, Hq, d] E4M3 codes and sq [B, Hkv] float32 power-of-two factors, one
+ *   per KV group (quantise q viewed as [B, Hkv, g, d] with attn_quantize_fp8);
+ *   k8, v8 [B, Hkv, Nmax, d] E4M3 cache, sk, sv [B, Hkv, ceil(Nmax/128)]
+ *   factors (attn_quantize_fp8 of the cache);
+ *   seqlens: int32 [B] on the device, valid cache length of each sequence
+ *   (1 <= seqlens[b] <= Nmax), or NULL for Nmax everywhere;
+ *   o [B, Hq, d] BF16 and lse [B, Hq] float32 (natural log) are written.
+ * The cache's KV tiles are cut into num_splits runs of ceil(ceil(Nmax/128) /
+ * num_splits) tiles (1 <= num_splits <= ceil(Nmax/128)); each run of each
+ * (sequence, KV group) is one CTA computing the FP8 forward for the group's
+ * g = Hq / Hkv query heads (g <= 128) from a fresh state, and a second kernel
+ * combines the runs by their log-sum-exp weights. Runs past a sequence's
+ * length contribute nothing. workspace: attn_decode_fp8_workspace_size bytes.
+ */
+ATTN_API attn_status attn_decode_fp8(const void* q8, const float* sq, const void* k8, const void* v8,
+                                     const float* sk, const float* sv, const int* seqlens, void* o, float* lse,
+                                     void* workspace, size_t ws_bytes, int B, int Hq, int Hkv, int Nmax, int d,
+                                     float scale, int num_splits, void* stream);
+
 /* Bytes of device workspace attn_bwd needs: FP32 dQ accumulator [B,Hq,N,d]
  * plus D = rowsum(dO o O) [B,Hq,N], each rounded up to 256 bytes. */
 ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d);

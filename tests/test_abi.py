@@ -53,6 +53,16 @@ def test_argument_checks_before_any_device_work(lib):
     assert lib.attn_fwd_varlen(P(16), P(16), P(16), P(16), P(16), P(16), 0, 10, 5, 2, 1, 64, 0.1, 0, 0, None) == 3
     assert lib.attn_fwd_varlen(P(16), P(16), P(16), P(16), P(16), P(16), 2, 10, 11, 2, 1, 64, 0.1, 0, 0, None) == 3
     assert lib.attn_fwd_varlen(P(16), P(16), P(16), P(16), P(16), None, 2, 10, 5, 2, 1, 64, 0.1, 0, 0, None) == 1
+    # decode: splits within [1, ceil(Nmax/128)], group size <= 128, workspace
+    wdec = binding.attn_decode_fp8_workspace_size(2, 8, 128, 3)
+    assert wdec == (3 * 2 * 8 * 128 * 4 + 255) // 256 * 256 + 256
+    dargs = [P(16)] * 6 + [None, P(16), P(16), P(16)]
+    assert lib.attn_decode_fp8(*dargs, wdec, 2, 8, 2, 300, 128, 0.1, 4, None) == 3            # > ceil(300/128) splits
+    assert lib.attn_decode_fp8(*dargs, wdec, 2, 8, 2, 300, 128, 0.1, 0, None) == 3
+    assert lib.attn_decode_fp8(*dargs, wdec - 1, 2, 8, 2, 300, 128, 0.1, 3, None) == 7
+    assert lib.attn_decode_fp8(*dargs, wdec, 2, 8, 3, 300, 128, 0.1, 3, None) == 5
+    assert lib.attn_decode_fp8(*dargs, wdec, 2, 8, 2, 300, 96, 0.1, 3, None) == 4
+    assert lib.attn_decode_fp8(*dargs, wdec, 1, 256, 1, 300, 128, 0.1, 1, None) == 3        # g > 128
     # fused RoPE producer: the tables are required and aligned
     assert lib.attn_quantize_fp8_rope(P(16), 0, P(16), P(16), 1, 1, 8, 64, None, P(16), None, None) == 1
     assert lib.attn_quantize_fp8_rope(P(16), 0, P(16), P(16), 1, 1, 8, 64, P(16), P(20), None, None) == 2
