@@ -5,7 +5,7 @@
 // by diag(random signs) * Hadamard / sqrt(d) to spread outliers.
 // m.xxqk.cn FA3 walkthrough §4.2: power-of-two scale factors.
 //
-// One CTA per (128-row block, head, batch), 16 warps, each warp owns 8 rows;
+// One CTA per (128-row block, head, batch), 8 warps, each warp owns 16 rows;
 // lane l holds elements [l*c, l*c + c) of a row (c = d / 32), so loads and
 // stores are coalesced. The fast Walsh-Hadamard transform runs in FP32 in
 // radix-2 stages of stride 1, 2, 4, ...: strides below c inside a lane,
@@ -13,11 +13,13 @@
 // and a - b exactly once, so the result does not depend on which lane holds
 // which operand. This kernel is HBM-bound: it reads 2 bytes and writes 1
 // byte per element.
-// Optional rotary position embedding first (the paper fuses quantisation into
-// the RoPE step that produces Q and K): rotate-half pairs (i, i + d/2) with
-// the caller's cos/sin tables [N, d/2]; lanes 0-15 hold the first half of a
-// row and lanes 16-31 the second, so a lane's partner is 16 lanes away. Each
-// product and sum is rounded on its own (no fused multiply-add).
+// Optional rotary position embedding first (kRope; the paper fuses
+// quantisation into the RoPE step that produces Q and K): rotate-half pairs
+// (i, i + d/2) with the caller's cos/sin tables [N, d/2]; lanes 0-15 hold the
+// first half of a row and lanes 16-31 the second, so a lane's partner is 16
+// lanes away. Each product and sum is rounded on its own (no fused
+// multiply-add). It is a separate instance so that the plain quantiser's code
+// is unchanged by it.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -62,14 +64,19 @@ __device__ __forceinline__ int e4m3_scale_exponent(float amax) {
   return (m <= 0.875f) ? 9 - k : 8 - k;
 }
 
-template <typename T, int D>
-__global__ void __launch_bounds__(512) quant_kernel(const T* __restrict__ x, uint8_t* __restrict__ x8,
+// warps per CTA: 8 rows of 16 for the plain quantiser; the RoPE instance uses
+// 16 warps of 8 rows, so more rows' table loads are in flight at once
+template <bool kRope>
+__host__ __device__ constexpr int quant_warps() { return kRope ? 16 : 8; }
+
+template <typename T, int D, bool kRope>
+__global__ void __launch_bounds__(32 * quant_warps<kRope>()) quant_kernel(const T* __restrict__ x, uint8_t* __restrict__ x8,
                                                     float* __restrict__ scales, int H, int N,
                                                     const int8_t* __restrict__ signs, float inv_sqrt_d,
                                                     const float* __restrict__ rope_cos,
                                                     const float* __restrict__ rope_sin) {
   constexpr int c = D / 32;
-  constexpr int NW = 16;    // warps
+  constexpr int NW = quant_warps<kRope>();
   constexpr int RPW = 128 / NW;   // rows per warp
   __shared__ float red[NW];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -86,33 +93,33 @@ __global__ void __launch_bounds__(512) quant_kernel(const T* __restrict__ x, uin
     const int row = row0 + r;
     if (row < N) {
       const T* src = x + (head_off + row) * D + lane * c;
-      // c consecutive 16-bit elements: one 4-, 8- or 16-byte load
-      uint32_t raw[c / 2];
-      if constexpr (c == 2) {
-        raw[0] = *reinterpret_cast<const uint32_t*>(src);
-      } else if constexpr (c == 4) {
-        const uint2 w = *reinterpret_cast<const uint2*>(src);
-        raw[0] = w.x;
-        raw[1] = w.y;
-      } else {
-        const uint4 w = *reinterpret_cast<const uint4*>(src);
-        raw[0] = w.x;
-        raw[1] = w.y;
-        raw[2] = w.z;
-        raw[3] = w.w;
-      }
 #pragma unroll
       for (int e = 0; e < c; ++e) {
-        const uint16_t bits = static_cast<uint16_t>(raw[e / 2] >> (16 * (e & 1)));
-        if constexpr (std::is_same<T, __nv_bfloat16>::value) v[r][e] = __uint_as_float(static_cast<uint32_t>(bits) << 16);
-        else v[r][e] = __half2float(__ushort_as_half(bits));
+        if constexpr (sizeof(T) == 2 && std::is_same<T, __nv_bfloat16>::value) v[r][e] = __bfloat162float(src[e]);
+        else v[r][e] = __half2float(src[e]);
       }
-      if (rope_cos) {   // row < N is the same for the whole warp
+      if constexpr (kRope) {   // row < N is the same for the whole warp
         const long long t = static_cast<long long>(row) * (D / 2) + (lane & 15) * c;
+        float cs4[c], sn4[c];
+        if constexpr (c % 4 == 0) {
+#pragma unroll
+          for (int e = 0; e < c; e += 4) {
+            const float4 a = *reinterpret_cast<const float4*>(rope_cos + t + e);
+            const float4 b = *reinterpret_cast<const float4*>(rope_sin + t + e);
+            cs4[e] = a.x; cs4[e + 1] = a.y; cs4[e + 2] = a.z; cs4[e + 3] = a.w;
+            sn4[e] = b.x; sn4[e + 1] = b.y; sn4[e + 2] = b.z; sn4[e + 3] = b.w;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < c; ++e) {
+            cs4[e] = rope_cos[t + e];
+            sn4[e] = rope_sin[t + e];
+          }
+        }
 #pragma unroll
         for (int e = 0; e < c; ++e) {
           const float other = __shfl_xor_sync(0xffffffffu, v[r][e], 16);
-          const float cs = rope_cos[t + e], sn = rope_sin[t + e];
+          const float cs = cs4[e], sn = sn4[e];
           v[r][e] = lane < 16 ? __fsub_rn(__fmul_rn(v[r][e], cs), __fmul_rn(other, sn))
                               : __fadd_rn(__fmul_rn(v[r][e], cs), __fmul_rn(other, sn));
         }
@@ -162,15 +169,15 @@ __global__ void __launch_bounds__(512) quant_kernel(const T* __restrict__ x, uin
   }
 }
 
-template <typename T>
+template <typename T, bool kRope>
 cudaError_t launch_typed(const void* x, uint8_t* x8, float* scales, int B, int H, int N, int d, const int8_t* signs,
                          float inv_sqrt_d, const float* rc, const float* rs, cudaStream_t st) {
   const dim3 grid((N + 127) / 128, H, B);
   const T* xt = static_cast<const T*>(x);
   switch (d) {
-    case 64: quant_kernel<T, 64><<<grid, 512, 0, st>>>(xt, x8, scales, H, N, signs, inv_sqrt_d, rc, rs); break;
-    case 128: quant_kernel<T, 128><<<grid, 512, 0, st>>>(xt, x8, scales, H, N, signs, inv_sqrt_d, rc, rs); break;
-    case 256: quant_kernel<T, 256><<<grid, 512, 0, st>>>(xt, x8, scales, H, N, signs, inv_sqrt_d, rc, rs); break;
+    case 64: quant_kernel<T, 64, kRope><<<grid, 32 * quant_warps<kRope>(), 0, st>>>(xt, x8, scales, H, N, signs, inv_sqrt_d, rc, rs); break;
+    case 128: quant_kernel<T, 128, kRope><<<grid, 32 * quant_warps<kRope>(), 0, st>>>(xt, x8, scales, H, N, signs, inv_sqrt_d, rc, rs); break;
+    case 256: quant_kernel<T, 256, kRope><<<grid, 32 * quant_warps<kRope>(), 0, st>>>(xt, x8, scales, H, N, signs, inv_sqrt_d, rc, rs); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -181,9 +188,12 @@ cudaError_t launch_typed(const void* x, uint8_t* x8, float* scales, int B, int H
 cudaError_t launch_quant_fp8(const void* x, int in_dt, uint8_t* x8, float* scales, int B, int H, int N, int d,
                              const int8_t* signs, float inv_sqrt_d, const float* rope_cos, const float* rope_sin,
                              cudaStream_t st) {
+  const bool rope = rope_cos != nullptr;
   if (in_dt == 0)
-    return launch_typed<__nv_bfloat16>(x, x8, scales, B, H, N, d, signs, inv_sqrt_d, rope_cos, rope_sin, st);
-  return launch_typed<__half>(x, x8, scales, B, H, N, d, signs, inv_sqrt_d, rope_cos, rope_sin, st);
+    return rope ? launch_typed<__nv_bfloat16, true>(x, x8, scales, B, H, N, d, signs, inv_sqrt_d, rope_cos, rope_sin, st)
+                : launch_typed<__nv_bfloat16, false>(x, x8, scales, B, H, N, d, signs, inv_sqrt_d, nullptr, nullptr, st);
+  return rope ? launch_typed<__half, true>(x, x8, scales, B, H, N, d, signs, inv_sqrt_d, rope_cos, rope_sin, st)
+              : launch_typed<__half, false>(x, x8, scales, B, H, N, d, signs, inv_sqrt_d, nullptr, nullptr, st);
 }
 
 }  // namespace attn
