@@ -466,7 +466,7 @@ def decode_main(args, world, rank):
             "roofline": {"bound": "hbm", "kernel": "attn_decode_fp8 (split kernel + combine)",
                          "achieved": gbs / world, "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / world / pk["hbm_gbs"], "peak_source": pk["source"] + " copy bandwidth",
-                         "traffic": None},
+                         "traffic": measured_traffic(f"{args.workload}:decode")},
             "e2e": {"value": world * r["bytes"] * args.steps / (r["ms_e2e"] * 1e-3) / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
             "gpu_launches": 2 * args.steps, "clocks": r["clocks"]}
@@ -485,6 +485,15 @@ def cpu_cores():
         return len(os.sched_getaffinity(0))
     except AttributeError:
         return os.cpu_count()
+
+
+def measured_traffic(key):
+    """DRAM bytes (read + write) per launch from the committed ncu summary, or
+    None when that kernel has no capture."""
+    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(tp):
+        return None
+    return json.load(open(tp)).get(key)
 
 
 def main():
@@ -557,10 +566,7 @@ def main():
     dom_flops = {"fwd": f, "bwd": 2.5 * f, "fwd_fp8": f}[dom]
     dom_peak = pk["bf16_burst"] * (2 if dom == "fwd_fp8" else 1)
     achieved = dom_flops / st[dom] / 1e9
-    traffic = None
-    tp = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tp):
-        traffic = json.load(open(tp)).get(f"{args.workload}:{dom}")
+    traffic = measured_traffic(f"{args.workload}:{dom}")
     line = {
         "metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
