@@ -82,6 +82,8 @@ struct FwdCfg {
   static constexpr int O_COL = NSB * 128;                   // O_t at O_COL + t * D
   static_assert(O_COL + QT * D <= 512, "tensor memory overflow");
   static constexpr int NTHREADS = 128 + 128 * QT;
+  static constexpr uint32_t kRegsCtl = 96, kRegsSoft = 200;   // QT = 2 register split
+  static_assert(QT != 2 || 128 * kRegsCtl + 256 * kRegsSoft <= 384 * 168, "register split");
   static constexpr int NBAR = 1 + 2 * NSLOT + 2 * NSB + 2;
   static constexpr int SMEM_BYTES = 1024 + Q_B + NSLOT * TILE_B + NBAR * 8 + 16;
   static constexpr uint32_t FMT = DT == kBF16 ? 1u : 0u;    // BF16=1, F16=0, E4M3=0
@@ -217,6 +219,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
   tc_fence_after();
   const uint32_t tbase = *tmem_holder;
 
+  // With two query tiles (384 threads, 168 registers each at launch) the
+  // load/MMA warpgroup hands registers to the two softmax warpgroups; each
+  // role changes its budget inside its own branch, so the compiler sizes
+  // every role's code for the budget it runs with.
+  if (warp < 4) {
+  if constexpr (QT == 2) regs_dec<C::kRegsCtl>();
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -343,7 +351,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       mma_commit(o_final);
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  }
+  } else {
+    if constexpr (QT == 2) regs_inc<C::kRegsSoft>();
     // ------------------------------------------------------- softmax
     const int t = (warp - 4) >> 2;
     const int quarter = warp & 3;

@@ -364,16 +364,16 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
 // chains of three-input max (short dependency chains).
 template <int N>
 __device__ __forceinline__ float rowmax(const uint32_t (&v)[N]) {
-  static_assert(N % 8 == 0, "row chunk must be a multiple of 8");
-  float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+  static_assert(N % 16 == 0, "row chunk must be a multiple of 16");
+  // eight independent chains of three-input max: depth N / 16 + 2
+  float m[8];
 #pragma unroll
-  for (int c = 0; c < N; c += 8) {
-    m0 = fmax3(m0, __uint_as_float(v[c + 0]), __uint_as_float(v[c + 1]));
-    m1 = fmax3(m1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
-    m2 = fmax3(m2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
-    m3 = fmax3(m3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
-  }
-  return fmax3(fmaxf(m0, m1), m2, m3);
+  for (int i = 0; i < 8; ++i) m[i] = fmaxf(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+#pragma unroll
+  for (int c = 16; c < N; c += 16)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m[i] = fmax3(m[i], __uint_as_float(v[c + 2 * i]), __uint_as_float(v[c + 2 * i + 1]));
+  return fmax3(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
 }
 
 }  // namespace attn

@@ -204,8 +204,9 @@ def check_fp8_vs_emulation(o, o_ref):
 
 @pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
-def test_fp8_forward_matches_emulation(d, causal):
-    q, k, v = inputs.outliers(3, [(1, 4, 700, d), (1, 2, 700, d), (1, 2, 700, d)])
+@pytest.mark.parametrize("n", [100, 700])   # one KV tile; several tiles and a ragged tail
+def test_fp8_forward_matches_emulation(d, causal, n):
+    q, k, v = inputs.outliers(3, [(1, 4, n, d), (1, 2, n, d), (1, 2, n, d)])
     o, lse, (q8, k8, v8, sq, sk, sv) = run_fp8(q, k, v, causal)
     o_ref, lse_ref = F.attention_fp8(q8, k8, v8, sq, sk, sv, d ** -0.5, causal)
     check_fp8_vs_emulation(o.double().numpy(), o_ref)
