@@ -30,6 +30,9 @@ Readings (the pages leave these open):
   the accumulated O is multiplied by 2^(F_old - F_new) whenever F grows (the
   same correction as for the running row max m). The rounded value lies in
   (0, 256]. At the end O = O_acc * 2^(F - 4) / l; l sums the unrounded P~.
+  The KV tile (Bc keys) need not equal the quantisation block: a tile that
+  spans two blocks gives each key its own block's K and V factors, and F is
+  raised once per tile, to the largest f among the tile's keys.
 * Decode over a KV cache: the g query heads of one KV group at the decoded
   position are one block of g query rows with one factor; the cache keys are
   split into runs of whole 128-key tiles, each run is processed as Algorithm 1
@@ -213,39 +216,46 @@ def quantize_tensor(x, signs=None, block=BLOCK):
 
 
 def _fp8_rows(qrows, q_fac, kf, vf, sk, sv, tiles, n, scale, causal=False, rows=None, block=BLOCK, p_shift=4,
-              tau=4.0):
+              tau=4.0, kv_tile=None):
     """Algorithm 1 in its FP8 form for query rows ``qrows`` [R, d] (decoded,
-    with per-row factors q_fac) over the key tiles ``tiles`` (in order) of one
-    KV head: kf/vf [N, d] decoded, sk/sv per-tile factors. Starts from m = -inf,
-    l = 0, O = 0. Returns (O [R, d], LSE [R])."""
+    with per-row factors q_fac) over the key tiles ``tiles`` (indices of tiles
+    of kv_tile keys, in order) of one KV head: kf/vf [N, d] decoded, sk/sv the
+    factors of the ``block``-key quantisation blocks. A tile may span blocks:
+    each key takes its own block's factors, and F is raised to the largest V
+    exponent among the tile's keys. Starts from m = -inf, l = 0, O = 0.
+    Returns (O [R, d], LSE [R])."""
+    kv_tile = block if kv_tile is None else kv_tile
     d = qrows.shape[1]
     m = np.full(len(qrows), -np.inf)
     l = np.zeros(len(qrows))
     acc = np.zeros((len(qrows), d))
     f_run = -np.inf
     for j in tiles:
-        cols = np.arange(j * block, min(n, (j + 1) * block))
-        s = scale * q_fac[:, None] * sk[j] * (qrows @ kf[cols].T)
+        cols = np.arange(j * kv_tile, min(n, (j + 1) * kv_tile))
+        blk = cols // block
+        s = scale * q_fac[:, None] * sk[blk][None, :] * (qrows @ kf[cols].T)
         if causal:
             s = np.where(cols[None, :] > rows[:, None], -np.inf, s)
         mx = s.max(axis=1)
         m_new = np.where(mx > m + tau * np.log(2.0), mx, m)   # stale max within 2^tau
         m_use = np.where(np.isfinite(m_new), m_new, 0.0)
         corr = np.exp(m - m_use)
-        f_j = np.log2(sv[j])
-        f_new = max(f_run, f_j)
+        f_c = np.log2(sv[blk])                                # V exponent of each key
+        f_new = max(f_run, f_c.max())
         v_corr = np.exp2(f_run - f_new)
         pt = np.exp(s - m_use[:, None])
         l = corr * l + pt.sum(axis=1)
-        p8 = e4m3_decode(e4m3_encode(pt * np.exp2(p_shift + f_j - f_new)))
+        p8 = e4m3_decode(e4m3_encode(pt * np.exp2(p_shift + f_c - f_new)[None, :]))
         acc = (corr * v_corr)[:, None] * acc + p8 @ vf[cols]
         m, f_run = m_new, f_new
     return acc * np.exp2(f_run - p_shift) / l[:, None], m + np.log(l)
 
 
 def attention_fp8(q8, k8, v8, sq, sk, sv, scale, causal=False, block=BLOCK, p_shift=4, tau=4.0, heads=None,
-                  rows=None):
-    """FP8 forward following Algorithm 1 tile by tile (Bc = block keys per tile).
+                  rows=None, kv_tile=None):
+    """FP8 forward following Algorithm 1 tile by tile (Bc = kv_tile keys per
+    tile, by default the quantisation block; the stale max and the V exponent
+    F move at tile granularity, so the E4M3 rounding of P~ depends on it).
 
     q8 [B, Hq, N, d], k8/v8 [B, Hkv, N, d] are E4M3 codes; sq/sk/sv are the
     dequantisation factors per 128-row block. Arithmetic is float64 except the
@@ -261,11 +271,12 @@ def attention_fp8(q8, k8, v8, sq, sk, sv, scale, causal=False, block=BLOCK, p_sh
     lse = np.full((b_, hq, n), np.nan)
     rows = np.arange(n) if rows is None else np.asarray(rows)
     heads = [(b, h) for b in range(b_) for h in range(hq)] if heads is None else heads
+    kvt = block if kv_tile is None else kv_tile
     for b, h in heads:
         kv = h // g
         o[b, h, rows], lse[b, h, rows] = _fp8_rows(
             qf[b, h, rows], sq[b, h, rows // block], kf[b, kv], vf[b, kv], sk[b, kv], sv[b, kv],
-            range((n + block - 1) // block), n, scale, causal, rows, block, p_shift, tau)
+            range((n + kvt - 1) // kvt), n, scale, causal, rows, block, p_shift, tau, kvt)
     return o, lse
 
 

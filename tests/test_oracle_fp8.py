@@ -122,7 +122,8 @@ def test_rotation_preserves_attention_in_float64(d):
     np.testing.assert_allclose(l2, l1, atol=1e-12)
 
 
-def test_fp8_attention_zero_query_is_mean_of_dequantised_v():
+@pytest.mark.parametrize("kv_tile", [None, 96, 64])
+def test_fp8_attention_zero_query_is_mean_of_dequantised_v(kv_tile):
     rng = np.random.default_rng(7)
     b, h, n, d = 1, 2, 300, 32
     v = torch.from_numpy(rng.standard_normal((b, h, n, d)).astype(np.float32))
@@ -134,7 +135,7 @@ def test_fp8_attention_zero_query_is_mean_of_dequantised_v():
     v8, sv = F.quantize_blocks(v)
     assert len(set(sv[0, 0].tolist())) > 1
     for causal in (False, True):
-        o, lse = F.attention_fp8(q8, k8, v8, sq, sk, sv, d ** -0.5, causal)
+        o, lse = F.attention_fp8(q8, k8, v8, sq, sk, sv, d ** -0.5, causal, kv_tile=kv_tile)
         vd = F.e4m3_decode(v8) * np.repeat(sv, 128, axis=2)[:, :, :n, None]
         for i in (0, 17, 128, 299):
             vis = i + 1 if causal else n
@@ -156,6 +157,30 @@ def test_fp8_attention_on_grid_inputs_is_close_to_exact():
     np.testing.assert_allclose(lse, l_ref, atol=1e-12)
     err = np.abs(o - o_ref).max()
     assert 0 < err < 2 ** -4 * np.abs(v).max()
+
+
+@pytest.mark.parametrize("kv_tile", [None, 96, 64])
+def test_fp8_attention_tiles_spanning_blocks_use_each_keys_factors(kv_tile):
+    """Codes on the E4M3 grid with power-of-two block factors that differ per
+    128-key block (so 96- and 64-key tiles span blocks): both products are
+    exact in float64, so the LSE equals float64 attention of the dequantised
+    inputs to rounding (a key given another block's factor moves it), and O is
+    within the E4M3 rounding of P~ (2^-4 relative) of it."""
+    rng = np.random.default_rng(9)
+    n, d = 300, 16
+    grid = lambda a: F.e4m3_decode(F.e4m3_encode(a))
+    q, k, v = (grid(rng.standard_normal((1, 1, n, d))) for _ in range(3))
+    sq = np.ones((1, 1, 3))
+    sk = np.exp2(np.array([1.0, -2.0, 3.0]))[None, None]
+    sv = np.exp2(np.array([-1.0, 2.0, 0.0]))[None, None]
+    kd = k * np.repeat(sk, 128, axis=2)[:, :, :n, None]
+    vd = v * np.repeat(sv, 128, axis=2)[:, :, :n, None]
+    for causal in (False, True):
+        o, lse = F.attention_fp8(F.e4m3_encode(q), F.e4m3_encode(k), F.e4m3_encode(v), sq, sk, sv, 0.25, causal,
+                                 kv_tile=kv_tile)
+        o_ref, l_ref = A.forward(q, kd, vd, 0.25, causal)
+        np.testing.assert_allclose(lse, l_ref, atol=1e-12)
+        assert np.abs(o - o_ref).max() < 2 ** -4 * np.abs(vd).max()
 
 
 def _emulated_rms(q, k, v, signs, quant, causal=False, rows=slice(None)):
