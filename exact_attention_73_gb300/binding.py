@@ -27,7 +27,7 @@ EXPORTS = ("attn_status_string", "attn_version", "attn_fwd", "attn_fwd_varlen", 
            "attn_bwd_varlen", "attn_get_device_status", "attn_bwd_noalloc", "attn_selftest_wait_timeout",
            "attn_fwd_window", "attn_bwd_window", "attn_bwd_deterministic_workspace_size",
            "attn_bwd_deterministic", "attn_quantize_fp8_rope", "attn_decode_fp8_workspace_size",
-           "attn_decode_fp8")
+           "attn_decode_fp8", "attn_fwd_fp8_kv_tile")
 
 
 class AttnError(RuntimeError):
@@ -44,6 +44,7 @@ _SIGS = {
     "attn_fwd_varlen": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P], _I),
     "attn_quantize_fp8": ([_P, _I, _P, _P, _I, _I, _I, _I, _P, _P], _I),
     "attn_fwd_fp8": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P], _I),
+    "attn_fwd_fp8_kv_tile": ([_I], _I),
     "attn_bwd_workspace_size": ([_I, _I, _I, _I, _I], _Z),
     "attn_bwd": ([_P] * 9 + [_P, _Z, _I, _I, _I, _I, _I, _F, _I, _I, _P], _I),
     "attn_bwd_varlen_workspace_size": ([_I, _I, _I, _I], _Z),
@@ -156,6 +157,11 @@ def attn_fwd_fp8(q8, k8, v8, sq, sk, sv, o, lse, scale=None, causal=False, strea
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     _check(load().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(sq), _ptr(sk), _ptr(sv), _ptr(o), _ptr(lse),
                                B, Hq, Hkv, N, d, scale, int(bool(causal)), _stream(stream)), "attn_fwd_fp8")
+
+
+def attn_fwd_fp8_kv_tile(d):
+    """Keys per KV tile of attn_fwd_fp8 for head dimension d (0: unsupported)."""
+    return load().attn_fwd_fp8_kv_tile(d)
 
 
 def attn_decode_fp8_workspace_size(B, Hq, d, num_splits):

@@ -287,8 +287,10 @@ attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8,
   int* status;
   if ((s = device_context(&status)) != ATTN_OK) return s;
   CUtensorMap tq, tk, tv;
-  if (!operand_map(&tq, q8, kE4M3, d, false, B, Hq, N, 128) || !operand_map(&tk, k8, kE4M3, d, false, B, Hkv, N, 128) ||
-      !operand_map(&tv, v8, kE4M3, d, false, B, Hkv, N, 128))
+  const int kv_rows = fwd_e4m3_kv_rows(d);
+  if (!operand_map(&tq, q8, kE4M3, d, false, B, Hq, N, 128) ||
+      !operand_map(&tk, k8, kE4M3, d, false, B, Hkv, N, kv_rows) ||
+      !operand_map(&tv, v8, kE4M3, d, false, B, Hkv, N, kv_rows))
     return ATTN_ERR_CUDA;
   FwdArgs a{};
   a.o = o;
@@ -314,6 +316,8 @@ attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8,
   a.status = status;
   return from_cuda(launch_fwd(kE4M3, d, tq, tk, tv, a, N, Hq, B, static_cast<cudaStream_t>(stream)));
 }
+
+int attn_fwd_fp8_kv_tile(int d) { return fwd_e4m3_kv_rows(d); }
 
 attn_status attn_get_device_status(void* stream) {
   int* status;

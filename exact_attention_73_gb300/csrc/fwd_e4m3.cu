@@ -1,5 +1,6 @@
 // Forward instances with e4m3 operands: d = 64 and 128 with two query tiles
-// per CTA, d = 256 with one (tensor memory holds S and O for 512 columns).
+// per CTA, d = 256 with one (tensor memory holds S and O for 512 columns);
+// all with 128-key KV tiles.
 #include "fwd_launch.cuh"
 
 namespace attn {
@@ -13,5 +14,7 @@ cudaError_t launch_fwd_e4m3(int d, const CUtensorMap& q, const CUtensorMap& k, c
     default: return cudaErrorInvalidValue;
   }
 }
+
+int fwd_e4m3_kv_rows(int d) { return d == 64 || d == 128 || d == 256 ? 128 : 0; }
 
 }  // namespace attn

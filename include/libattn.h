@@ -147,13 +147,23 @@ ATTN_API attn_status attn_quantize_fp8_rope(const void* x, attn_dtype in_dtype, 
  * max is raised only when a tile's max exceeds it by more than 4 (log2
  * units), so P~ = exp2(x - m) <= 16; P~ is rounded to E4M3 as
  * e4m3(P~ * 2^(4 + f_j - F)) with sv_j = 2^f_j and F the running maximum of
- * f over the KV tiles seen (O rescaled when F grows).
+ * f over the KV tiles seen (O rescaled when F grows). The KV tile holds
+ * attn_fwd_fp8_kv_tile(d) keys; a tile that spans two 128-row blocks gives
+ * each key its own block's factors and raises F to the larger exponent.
  */
 ATTN_API attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8,
                          const float* sq, const float* sk, const float* sv,
                          void* o, float* lse,
                          int B, int Hq, int Hkv, int N, int d, float scale, int causal,
                          void* stream);
+
+/*
+ * Keys per KV tile of attn_fwd_fp8 for head dimension d (128 for d = 64,
+ * 128, 256), 0 for an unsupported d. The stale running max and F move
+ * once per KV tile (§3.2 Algorithm 1, Bc), so the E4M3 rounding of P~, and
+ * with it the result's last bits, depends on this blocking. No device work.
+ */
+ATTN_API int attn_fwd_fp8_kv_tile(int d);
 
 /* Bytes of workspace attn_decode_fp8 needs: per split, a float32 partial O
  * [B, Hq, d] and LSE [B, Hq], each area rounded up to 256 bytes. */

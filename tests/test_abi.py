@@ -53,6 +53,8 @@ def test_argument_checks_before_any_device_work(lib):
     assert lib.attn_fwd_varlen(P(16), P(16), P(16), P(16), P(16), P(16), 0, 10, 5, 2, 1, 64, 0.1, 0, 0, None) == 3
     assert lib.attn_fwd_varlen(P(16), P(16), P(16), P(16), P(16), P(16), 2, 10, 11, 2, 1, 64, 0.1, 0, 0, None) == 3
     assert lib.attn_fwd_varlen(P(16), P(16), P(16), P(16), P(16), None, 2, 10, 5, 2, 1, 64, 0.1, 0, 0, None) == 1
+    # FP8 forward blocking: keys per KV tile by head dimension (no device work)
+    assert [binding.attn_fwd_fp8_kv_tile(d) for d in (64, 128, 256, 100)] == [128, 128, 128, 0]
     # decode: splits within [1, ceil(Nmax/128)], group size <= 128, workspace
     wdec = binding.attn_decode_fp8_workspace_size(2, 8, 128, 3)
     assert wdec == (3 * 2 * 8 * 128 * 4 + 255) // 256 * 256 + 256

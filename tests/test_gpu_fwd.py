@@ -208,7 +208,7 @@ def check_fp8_vs_emulation(o, o_ref):
 def test_fp8_forward_matches_emulation(d, causal, n):
     q, k, v = inputs.outliers(3, [(1, 4, n, d), (1, 2, n, d), (1, 2, n, d)])
     o, lse, (q8, k8, v8, sq, sk, sv) = run_fp8(q, k, v, causal)
-    o_ref, lse_ref = F.attention_fp8(q8, k8, v8, sq, sk, sv, d ** -0.5, causal)
+    o_ref, lse_ref = F.attention_fp8(q8, k8, v8, sq, sk, sv, d ** -0.5, causal, kv_tile=L.attn_fwd_fp8_kv_tile(d))
     check_fp8_vs_emulation(o.double().numpy(), o_ref)
     assert np.abs(lse.double().numpy() - lse_ref).max() <= 1e-3
 
@@ -230,7 +230,8 @@ def test_fp8_config_accuracy_sampled(d, causal):
     kt, skt = F.quantize_tensor(k, signs.numpy())
     vt, svt = F.quantize_tensor(v)
     o_ten, _ = F.attention_fp8(qt, kt, vt, sqt, skt, svt, d ** -0.5, causal, heads=heads, rows=rows)
-    o_emu, _ = F.attention_fp8(q8, k8, v8, sq, sk, sv, d ** -0.5, causal, heads=heads, rows=rows)
+    o_emu, _ = F.attention_fp8(q8, k8, v8, sq, sk, sv, d ** -0.5, causal, heads=heads, rows=rows,
+                               kv_tile=L.attn_fwd_fp8_kv_tile(d))
     gpu, ten, emu, ref = [], [], [], []
     for (b, h) in heads:
         r, _ = A.forward_rows(q[b, h], k[b, h], v[b, h], rows, d ** -0.5, causal)
