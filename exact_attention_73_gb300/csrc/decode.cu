@@ -9,6 +9,7 @@
 #include <cuda_bf16.h>
 
 #include "../../include/libattn.h"
+#include "decode_kernel.cuh"
 #include "internal.h"
 #include "ops.h"
 
@@ -41,14 +42,20 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const float* __rest
   if (t == 0) lse[r] = mx + logf(tot);
 }
 
+// persistent: at most one CTA per SM, each walking the (split, KV head,
+// batch) items with a stride of the grid size
 template <int D>
 cudaError_t launch_decode_inst(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdArgs& a,
-                               int splits, cudaStream_t st) {
-  using C = FwdCfg<kE4M3, D, 1>;
-  auto kern = fwd_kernel<kE4M3, D, 1, true>;
+                               int splits, int items, cudaStream_t st) {
+  using C = DecCfg<D>;
+  auto kern = decode_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(splits, a.Hkv, a.batch), C::NTHREADS, C::SMEM_BYTES, st>>>(q, k, v, a);
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const int grid = items < sms ? items : sms;
+  kern<<<grid, C::NTHREADS, C::SMEM_BYTES, st>>>(q, k, v, a, splits, items);
   return cudaGetLastError();
 }
 
@@ -115,11 +122,13 @@ extern "C" attn_status attn_decode_fp8(const void* q8, const float* sq, const vo
   a.status = status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int splits = (ntiles + tps - 1) / tps;   // splits that hold a tile of a full-length cache
+  const long long items = static_cast<long long>(splits) * Hkv * B;
+  if (items > 0x7fffffffLL) return ATTN_ERR_SHAPE;
   cudaError_t e;
   switch (d) {
-    case 64: e = launch_decode_inst<64>(tq, tk, tv, a, splits, st); break;
-    case 128: e = launch_decode_inst<128>(tq, tk, tv, a, splits, st); break;
-    default: e = launch_decode_inst<256>(tq, tk, tv, a, splits, st); break;
+    case 64: e = launch_decode_inst<64>(tq, tk, tv, a, splits, static_cast<int>(items), st); break;
+    case 128: e = launch_decode_inst<128>(tq, tk, tv, a, splits, static_cast<int>(items), st); break;
+    default: e = launch_decode_inst<256>(tq, tk, tv, a, splits, static_cast<int>(items), st); break;
   }
   if (e == cudaSuccess) {
     decode_combine_kernel<<<static_cast<unsigned>(B * Hq), d, 0, st>>>(o_part, lse_part,

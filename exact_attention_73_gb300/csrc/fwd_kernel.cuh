@@ -48,7 +48,7 @@ struct FwdArgs {
   const float* sk;
   const float* sv;
   int nblk;                     // blocks per (batch, head) in sq/sk/sv
-  // decode over a KV cache (kDecode): one CTA per (split, KV head, batch)
+  // decode over a KV cache (decode_kernel): items of (split, KV head, batch)
   const int* seqlens;           // valid cache length per sequence (null: N)
   int tiles_per_split;          // KV tiles per split
   int batch;                    // B
@@ -124,11 +124,7 @@ __device__ __forceinline__ int kv_index_v(int qt, int j, int nkv) {
   return nkv == 1 ? 1 : (j == nkv - 1 ? 2 * nkv - 1 : 2 + 2 * j);
 }
 
-// kDecode (E4M3, QT = 1): the query tile holds the g = Hq / Hkv query heads
-// of one KV group at the decoded position (the Q map views q as
-// [B, Hkv, g, d]); the CTA runs Algorithm 1 over one split of the cache's KV
-// tiles and writes a per-split partial O (normalised) and LSE for the g rows.
-template <int DT, int D, int QT, bool kDecode = false>
+template <int DT, int D, int QT>
 __global__ void __launch_bounds__(FwdCfg<DT, D, QT>::NTHREADS, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
            const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
@@ -147,51 +143,32 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
   uint64_t* o_done = o_final + 1;                  // one phase per O += P V (single-tile CTAs)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(o_done + 1);
 
-  static_assert(!kDecode || (C::kFp8 && QT == 1), "decode runs the E4M3 single-tile form");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const bool packed = !kDecode && a.cu_seqlens != nullptr;
+  const bool packed = a.cu_seqlens != nullptr;
   int h, hkv, b, seq0, L, nqt, qt0, kv0, nkv;
-  if constexpr (kDecode) {
-    hkv = blockIdx.y;
-    h = hkv;                                    // Q map coordinate: the group
+  h = blockIdx.y;
+  if (packed) {
+    b = 0;
+    seq0 = a.cu_seqlens[blockIdx.z];
+    L = a.cu_seqlens[blockIdx.z + 1] - seq0;
+  } else {
     b = blockIdx.z;
     seq0 = 0;
-    L = a.seqlens ? min(a.seqlens[b], a.N) : a.N;   // valid cache length, at most the cache
-    nqt = 1;
-    qt0 = 0;
-    kv0 = static_cast<int>(blockIdx.x) * a.tiles_per_split;
-    nkv = min((L + 127) >> 7, kv0 + a.tiles_per_split) - kv0;
-    if (nkv <= 0) {   // a split past the cache: a neutral partial, no set-up
-      const long long base = (static_cast<long long>(blockIdx.x) * a.batch + b) * a.Hq + static_cast<long long>(hkv) * a.group;
-      for (int i = threadIdx.x; i < a.group * D; i += blockDim.x) a.o_part[base * D + i] = 0.f;
-      for (int i = threadIdx.x; i < a.group; i += blockDim.x) a.lse_part[base + i] = -INFINITY;
-      return;
-    }
-  } else {
-    h = blockIdx.y;
-    if (packed) {
-      b = 0;
-      seq0 = a.cu_seqlens[blockIdx.z];
-      L = a.cu_seqlens[blockIdx.z + 1] - seq0;
-    } else {
-      b = blockIdx.z;
-      seq0 = 0;
-      L = a.N;
-    }
-    nqt = (L + 127) >> 7;
-    // Causal CTAs with the most KV tiles start first.
-    const int cblk = a.causal ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
-    qt0 = cblk * QT;
-    if (qt0 >= nqt) return;   // whole CTA leaves before any set-up
-    // KV tiles that hold a key visible to some query row of this CTA
-    const int r0 = qt0 * 128, r1 = min((qt0 + QT) * 128, L);
-    const int klo = a.win_left < 0 ? 0 : max(0, r0 - a.win_left);
-    const int khi = a.win_right < 0 ? L : min(L, r1 + a.win_right);   // exclusive
-    kv0 = klo >> 7;
-    nkv = ((khi + 127) >> 7) - kv0;
-    hkv = h / a.group;
+    L = a.N;
   }
+  nqt = (L + 127) >> 7;
+  // Causal CTAs with the most KV tiles start first.
+  const int cblk = a.causal ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
+  qt0 = cblk * QT;
+  if (qt0 >= nqt) return;   // whole CTA leaves before any set-up
+  // KV tiles that hold a key visible to some query row of this CTA
+  const int r0 = qt0 * 128, r1 = min((qt0 + QT) * 128, L);
+  const int klo = a.win_left < 0 ? 0 : max(0, r0 - a.win_left);
+  const int khi = a.win_right < 0 ? L : min(L, r1 + a.win_right);   // exclusive
+  kv0 = klo >> 7;
+  nkv = ((khi + 127) >> 7) - kv0;
+  hkv = h / a.group;
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmQ);
@@ -367,10 +344,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     int f_run = -1000;       // FP8: running max exponent of the V factors
     float q_fac = 1.f;
     long long vs_base = 0;
-    if constexpr (kDecode) {
-      q_fac = a.sq[static_cast<long long>(b) * a.Hkv + hkv];   // one factor per group
-      vs_base = (static_cast<long long>(b) * a.Hkv + hkv) * a.nblk + kv0;
-    } else if constexpr (C::kFp8) {
+    if constexpr (C::kFp8) {
       q_fac = a.sq[(static_cast<long long>(b) * a.Hq + h) * a.nblk + min(qtile, nqt - 1)];
       vs_base = (static_cast<long long>(b) * a.Hkv + hkv) * a.nblk + kv0;
     }
@@ -501,31 +475,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_final, 0, a.status));
     tc_fence_after();
-    if (ok && kDecode) {   // rows 0 .. g-1: FP32 partial O and LSE of this split
-      float inv = 1.f / l;
-      inv *= exp2i(f_run - C::kPShift);
-      const bool prow_ok = row < a.group;             // the warp's loads stay collective
-      const long long prow = (static_cast<long long>(blockIdx.x) * a.batch + b) * a.Hq +
-                             static_cast<long long>(hkv) * a.group + row;
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tO + 32 * c, r);
-        tmem_wait_ld();
-        reg_fence(r);
-        if (prow_ok) {
-          float4* dst = reinterpret_cast<float4*>(a.o_part + prow * D + 32 * c);
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
-                                 __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
-        }
-      }
-      if (prow_ok) {
-        const float lse2 = (m == -INFINITY ? 0.f : m) + __log2f(l);
-        a.lse_part[prow] = lse2 * 0.69314718055994530942f;
-      }
-    } else if (ok) {
+    if (ok) {
       float inv = 1.f / l;
       if constexpr (C::kFp8) inv *= exp2i(f_run - C::kPShift);
       const bool valid = qrow < L;
