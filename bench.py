@@ -55,6 +55,11 @@ DECODE_WORKLOADS = {
     # name: (B, Hq, Hkv, Nmax, d, splits): a 1 GiB FP8 cache, GQA groups of 4
     "decode_fp8_b16_hq32_hkv8_n32768_d128": (16, 32, 8, 32768, 128, 8),
 }
+VARLEN_WORKLOADS = {
+    # name: (lengths seed, sequences, Hq, Hkv, d): packed causal BF16 forward + backward,
+    # 8 sequences of 1k..32k tokens (T = 129511), GQA groups of 4
+    "varlen_t129511_hq32_hkv8_d128_causal": (18, 8, 32, 8, 128),
+}
 LAUNCHES_PER_STEP = 8   # fwd 1, bwd 3, quantise 3, fp8 fwd 1
 
 
@@ -480,6 +485,160 @@ def decode_main(args, world, rank):
         dist.destroy_process_group()
 
 
+def bench_varlen(args, wl, rank, world):
+    """Time attn_fwd_varlen + attn_bwd_varlen (causal, BF16) on resident packed
+    inputs; returns the JSON line's fields."""
+    import torch
+    from exact_attention_73_gb300 import binding as L
+    from exact_attention_73_gb300 import inputs
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    L.load(build_if_missing=True)
+    seed, nseq, Hq, Hkv, d = wl
+    lens = inputs.varlen_lengths(seed, nseq)
+    cu = inputs.cu_seqlens(lens).to(dev)
+    T, mx = int(sum(lens)), int(max(lens))
+    gen = torch.Generator(device=dev).manual_seed(5)   # 2.7 GB of inputs are drawn on the device
+    q = torch.randn((T, Hq, d), generator=gen, device=dev).to(torch.bfloat16)
+    k = torch.randn((T, Hkv, d), generator=gen, device=dev).to(torch.bfloat16)
+    v = torch.randn((T, Hkv, d), generator=gen, device=dev).to(torch.bfloat16)
+    do = torch.randn((T, Hq, d), generator=gen, device=dev).to(torch.bfloat16)
+    o, dq = torch.empty_like(q), torch.empty_like(q)
+    dk, dv = torch.empty_like(k), torch.empty_like(v)
+    lse = torch.empty((Hq, T), device=dev)
+    ws = torch.empty((L.attn_bwd_varlen_workspace_size(T, Hq, Hkv, d),), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(m=None):
+        if m is not None:
+            m[0].record(stream)
+        L.attn_fwd_varlen(q, k, v, o, lse, cu, mx, causal=True)
+        if m is not None:
+            m[1].record(stream)
+        L.attn_bwd_varlen(q, k, v, o, lse, do, dq, dk, dv, ws, cu, mx, causal=True)
+        if m is not None:
+            m[2].record(stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = Clocks(dev.index)
+    barrier()
+    clocks.start()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s_ in range(args.steps):
+        step(marks[s_])
+    t1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    stage = {n: sum(m[i].elapsed_time(m[i + 1]) for m in marks) / args.steps for i, n in enumerate(("fwd", "bwd"))}
+    # end to end: Q, K, V, dO in from pinned host memory and O, LSE, dQ, dK, dV out, every step
+    hin = [x.cpu().pin_memory() for x in (q, k, v, do)]
+    hout = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (o, lse, dq, dk, dv)]
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        for dst, src in zip((q, k, v, do), hin):
+            dst.copy_(src, non_blocking=True)
+        step()
+        for dst, src in zip(hout, (o, lse, dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    ms_e2e = e0.elapsed_time(e1)
+    if L.attn_get_device_status() != 0:
+        raise RuntimeError("device-side wait timed out during the varlen run")
+    ms, ms_e2e = max_over_ranks([ms, ms_e2e], world, dev)
+    fwd_flops = sum(4.0 * Hq * n * n * d / 2 for n in lens)
+    line = {"ms_total": ms, "ms_e2e": ms_e2e, "clocks": clk, "stage_ms": stage, "fwd_flops": fwd_flops,
+            "h2d": sum(x.numel() * x.element_size() for x in hin),
+            "d2h": sum(x.numel() * x.element_size() for x in hout), "lens": lens}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu"] = varlen_cpu_sample(min(lens), d)
+    return line
+
+
+def varlen_cpu_sample(n, d):
+    """The oracle's forward and backward on one head of one sequence of n
+    tokens (causal): (TFLOP/s, seconds)."""
+    from exact_attention_73_gb300 import inputs
+    from oracle import attention as A
+    q, k, v, do = inputs.normal(5, [(1, 1, n, d)] * 4)
+    t = time.perf_counter()
+    A.forward(q, k, v, d ** -0.5, True)
+    A.backward(q, k, v, do, d ** -0.5, True)
+    sec = time.perf_counter() - t
+    return 3.5 * 4.0 * n * n * d / 2 / sec / 1e12, sec
+
+
+def varlen_main(args, world, rank):
+    seed, nseq, Hq, Hkv, d = VARLEN_WORKLOADS[args.workload]
+    from exact_attention_73_gb300 import inputs
+    lens = [int(x) for x in inputs.varlen_lengths(seed, nseq)]
+    config = {"workload": args.workload, "lengths": lens, "T": sum(lens), "Hq": Hq, "Hkv": Hkv, "d": d,
+              "causal": True, "step": "attn_fwd_varlen + attn_bwd_varlen (BF16, packed [T, H, d])",
+              "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"}
+    metric = "attention fwd+bwd (BF16, packed variable length) TFLOP/s on GB300"
+    pk = peaks()
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        n = min(lens)
+        t = time.perf_counter()
+        for _ in range(args.steps):
+            varlen_cpu_sample(n, d)
+        sec = time.perf_counter() - t
+        val = args.steps * 3.5 * 4.0 * n * n * d / 2 / sec / 1e12
+        print(json.dumps({"impl": "reference", "metric": metric, "value": val, "unit": "TFLOP/s", "n_gpus": world,
+                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic", "config": config,
+                          "cpu_baseline": {"kind": "oracle", "value": val, "unit": "TFLOP/s", "cores": cpu_cores(),
+                                           "sample": f"one head of the {n}-token sequence per step"},
+                          "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+              flush=True)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    r = bench_varlen(args, VARLEN_WORKLOADS[args.workload], rank, world)
+    f = r["fwd_flops"]
+    value = job_tflops(3.5 * f, args.steps, world, r["ms_total"])
+    st = r["stage_ms"]
+    line = {"metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": r["ms_total"] / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
+            "stages": {"fwd_bf16": {"ms": st["fwd"], "tflops": f / st["fwd"] / 1e9,
+                                    "frac_of_bf16_peak": f / st["fwd"] / 1e9 / pk["bf16_burst"]},
+                       "bwd_bf16": {"ms": st["bwd"], "tflops": 2.5 * f / st["bwd"] / 1e9,
+                                    "frac_of_bf16_peak": 2.5 * f / st["bwd"] / 1e9 / pk["bf16_burst"]}},
+            "roofline": {"bound": "tensor", "kernel": "attn_bwd_varlen (main + 2 helpers)",
+                         "achieved": 2.5 * f / st["bwd"] / 1e9, "peak": pk["bf16_burst"], "unit": "TFLOP/s",
+                         "frac": 2.5 * f / st["bwd"] / 1e9 / pk["bf16_burst"], "peak_source": pk["source"],
+                         "traffic": measured_traffic(f"{args.workload}:bwd")},
+            "e2e": {"value": job_tflops(3.5 * f, args.steps, world, r["ms_e2e"]), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+            "gpu_launches": 4 * args.steps, "clocks": r["clocks"]}
+    if "cpu" in r:
+        line["cpu_baseline"] = {"value": r["cpu"][0], "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                                "sample": f"one head of the {min(r['lens'])}-token sequence, fwd + bwd: "
+                                          f"{r['cpu'][1]:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -502,7 +661,8 @@ def main():
     ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(DECODE_WORKLOADS), default=DEFAULT)
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(DECODE_WORKLOADS) + sorted(VARLEN_WORKLOADS),
+                    default=DEFAULT)
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle timing")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -511,6 +671,8 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", 1))
     if args.workload in DECODE_WORKLOADS:
         return decode_main(args, world, rank)
+    if args.workload in VARLEN_WORKLOADS:
+        return varlen_main(args, world, rank)
     wl = WORKLOADS[args.workload]
     B, Hq, Hkv, N, d, causal, window = wl
     config = {"workload": args.workload, "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d, "causal": causal,
