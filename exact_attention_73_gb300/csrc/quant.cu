@@ -5,21 +5,21 @@
 // by diag(random signs) * Hadamard / sqrt(d) to spread outliers.
 // m.xxqk.cn FA3 walkthrough §4.2: power-of-two scale factors.
 //
-// One CTA per (128-row block, head, batch), 8 warps, each warp owns 16 rows;
-// lane l holds elements [l*c, l*c + c) of a row (c = d / 32), so loads and
-// stores are coalesced. The fast Walsh-Hadamard transform runs in FP32 in
-// radix-2 stages of stride 1, 2, 4, ...: strides below c inside a lane,
-// larger strides across lanes with shuffles; each butterfly computes a + b
-// and a - b exactly once, so the result does not depend on which lane holds
-// which operand. This kernel is HBM-bound: it reads 2 bytes and writes 1
-// byte per element.
+// One CTA per (128-row block, head, batch), 8 warps of 16 rows. A lane holds
+// 32 consecutive elements of a row (d / 32 lanes per row, 32 / (d / 32) rows
+// per warp at a time), loaded and stored with 16-byte accesses. The fast
+// Walsh-Hadamard transform runs in FP32 in radix-2 stages of stride 1, 2, 4,
+// ...: strides below 32 inside a lane, larger ones across the lanes of a row
+// with shuffles; each butterfly computes a + b and a - b exactly once, so the
+// result does not depend on which lane holds which operand. This kernel is
+// HBM-bound: it reads 2 bytes and writes 1 byte per element.
 // Optional rotary position embedding first (kRope; the paper fuses
 // quantisation into the RoPE step that produces Q and K): rotate-half pairs
-// (i, i + d/2) with the caller's cos/sin tables [N, d/2]; lanes 0-15 hold the
-// first half of a row and lanes 16-31 the second, so a lane's partner is 16
-// lanes away. Each product and sum is rounded on its own (no fused
-// multiply-add). It is a separate instance so that the plain quantiser's code
-// is unchanged by it.
+// (i, i + d/2) with the caller's cos/sin tables [N, d/2]; the first half of a
+// row sits in the row's first d/64 lanes, so a lane's partner is d/64 lanes
+// away. Each product and sum is rounded on its own (no fused multiply-add).
+#include <type_traits>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -30,14 +30,15 @@ namespace attn {
 
 namespace {
 
+// Radix-2 FWHT of one row held as 32 consecutive elements per lane over
+// R = D / 32 lanes; li is the lane's position within its row.
 template <int D>
-__device__ __forceinline__ void fwht_row(float (&x)[D / 32], int lane) {
-  constexpr int c = D / 32;
+__device__ __forceinline__ void fwht_row(float (&x)[32], int li) {
 #pragma unroll
   for (int h = 1; h < D; h <<= 1) {
-    if (h < c) {
+    if (h < 32) {
 #pragma unroll
-      for (int e = 0; e < c; ++e) {
+      for (int e = 0; e < 32; ++e) {
         if ((e & h) == 0) {
           const float a = x[e], b = x[e + h];
           x[e] = a + b;
@@ -45,10 +46,10 @@ __device__ __forceinline__ void fwht_row(float (&x)[D / 32], int lane) {
         }
       }
     } else {
-      const int lm = h / c;
-      const bool upper = (lane & lm) != 0;
+      const int lm = h / 32;
+      const bool upper = (li & lm) != 0;
 #pragma unroll
-      for (int e = 0; e < c; ++e) {
+      for (int e = 0; e < 32; ++e) {
         const float other = __shfl_xor_sync(0xffffffffu, x[e], lm);
         x[e] = upper ? (other - x[e]) : (x[e] + other);
       }
@@ -64,79 +65,86 @@ __device__ __forceinline__ int e4m3_scale_exponent(float amax) {
   return (m <= 0.875f) ? 9 - k : 8 - k;
 }
 
-// warps per CTA: 8 rows of 16 for the plain quantiser; the RoPE instance uses
-// 16 warps of 8 rows, so more rows' table loads are in flight at once
-template <bool kRope>
-__host__ __device__ constexpr int quant_warps() { return kRope ? 16 : 8; }
+template <typename T>
+__device__ __forceinline__ float to_f32(uint32_t bits16) {
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) return __uint_as_float(bits16 << 16);
+  else return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16)));
+}
+
+constexpr int kQuantThreads = 256;
 
 template <typename T, int D, bool kRope>
-__global__ void __launch_bounds__(32 * quant_warps<kRope>()) quant_kernel(const T* __restrict__ x, uint8_t* __restrict__ x8,
-                                                    float* __restrict__ scales, int H, int N,
-                                                    const int8_t* __restrict__ signs, float inv_sqrt_d,
-                                                    const float* __restrict__ rope_cos,
-                                                    const float* __restrict__ rope_sin) {
-  constexpr int c = D / 32;
-  constexpr int NW = quant_warps<kRope>();
-  constexpr int RPW = 128 / NW;   // rows per warp
+__global__ void __launch_bounds__(kQuantThreads) quant_kernel(const T* __restrict__ x, uint8_t* __restrict__ x8,
+                                                             float* __restrict__ scales, int H, int N,
+                                                             const int8_t* __restrict__ signs, float inv_sqrt_d,
+                                                             const float* __restrict__ rope_cos,
+                                                             const float* __restrict__ rope_sin) {
+  constexpr int R = D / 32;            // lanes per row
+  constexpr int RP = 32 / R;           // rows per warp at a time
+  constexpr int NW = kQuantThreads / 32;
+  constexpr int RPW = 128 / NW;        // rows per warp
+  constexpr int NPASS = RPW / RP;
   __shared__ float red[NW];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lr = lane / R, li = lane % R;
   const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const long long head_off = (static_cast<long long>(b) * H + h) * N;
   const int row0 = blk * 128 + warp * RPW;
-  float v[RPW][c];
-  float sg[c];
-#pragma unroll
-  for (int e = 0; e < c; ++e) sg[e] = signs ? static_cast<float>(signs[lane * c + e]) : 1.f;
+  float v[NPASS][32];
   float amax = 0.f;
 #pragma unroll
-  for (int r = 0; r < RPW; ++r) {
-    const int row = row0 + r;
-    if (row < N) {
-      const T* src = x + (head_off + row) * D + lane * c;
+  for (int p = 0; p < NPASS; ++p) {
+    const int row = row0 + p * RP + lr;
+    const bool valid = row < N;
+    if (valid) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + (head_off + row) * D + li * 32);
 #pragma unroll
-      for (int e = 0; e < c; ++e) {
-        if constexpr (sizeof(T) == 2 && std::is_same<T, __nv_bfloat16>::value) v[r][e] = __bfloat162float(src[e]);
-        else v[r][e] = __half2float(src[e]);
-      }
-      if constexpr (kRope) {   // row < N is the same for the whole warp
-        const long long t = static_cast<long long>(row) * (D / 2) + (lane & 15) * c;
-        float cs4[c], sn4[c];
-        if constexpr (c % 4 == 0) {
+      for (int q = 0; q < 4; ++q) {
+        const uint4 w = src[q];
+        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-          for (int e = 0; e < c; e += 4) {
-            const float4 a = *reinterpret_cast<const float4*>(rope_cos + t + e);
-            const float4 b = *reinterpret_cast<const float4*>(rope_sin + t + e);
-            cs4[e] = a.x; cs4[e + 1] = a.y; cs4[e + 2] = a.z; cs4[e + 3] = a.w;
-            sn4[e] = b.x; sn4[e + 1] = b.y; sn4[e + 2] = b.z; sn4[e + 3] = b.w;
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < c; ++e) {
-            cs4[e] = rope_cos[t + e];
-            sn4[e] = rope_sin[t + e];
-          }
-        }
-#pragma unroll
-        for (int e = 0; e < c; ++e) {
-          const float other = __shfl_xor_sync(0xffffffffu, v[r][e], 16);
-          const float cs = cs4[e], sn = sn4[e];
-          v[r][e] = lane < 16 ? __fsub_rn(__fmul_rn(v[r][e], cs), __fmul_rn(other, sn))
-                              : __fadd_rn(__fmul_rn(v[r][e], cs), __fmul_rn(other, sn));
+        for (int u = 0; u < 4; ++u) {
+          v[p][8 * q + 2 * u] = to_f32<T>(wv[u] & 0xFFFFu);
+          v[p][8 * q + 2 * u + 1] = to_f32<T>(wv[u] >> 16);
         }
       }
     } else {
 #pragma unroll
-      for (int e = 0; e < c; ++e) v[r][e] = 0.f;
+      for (int e = 0; e < 32; ++e) v[p][e] = 0.f;
+    }
+    if constexpr (kRope) {   // partner d/2 elements away: R/2 lanes away; every lane shuffles
+      float cs[32], sn[32];
+      if (valid) {
+        const long long t = static_cast<long long>(row) * (D / 2) + (li % (R / 2)) * 32;
+        const float4* c4 = reinterpret_cast<const float4*>(rope_cos + t);
+        const float4* s4 = reinterpret_cast<const float4*>(rope_sin + t);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 a = c4[q], bq = s4[q];
+          cs[4 * q] = a.x; cs[4 * q + 1] = a.y; cs[4 * q + 2] = a.z; cs[4 * q + 3] = a.w;
+          sn[4 * q] = bq.x; sn[4 * q + 1] = bq.y; sn[4 * q + 2] = bq.z; sn[4 * q + 3] = bq.w;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) cs[e] = sn[e] = 0.f;
+      }
+      const bool second = li >= R / 2;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const float other = __shfl_xor_sync(0xffffffffu, v[p][e], R / 2);
+        v[p][e] = second ? __fadd_rn(__fmul_rn(v[p][e], cs[e]), __fmul_rn(other, sn[e]))
+                         : __fsub_rn(__fmul_rn(v[p][e], cs[e]), __fmul_rn(other, sn[e]));
+      }
     }
     if (signs) {
 #pragma unroll
-      for (int e = 0; e < c; ++e) v[r][e] *= sg[e];
-      fwht_row<D>(v[r], lane);
+      for (int e = 0; e < 32; ++e) v[p][e] *= static_cast<float>(signs[li * 32 + e]);
+      fwht_row<D>(v[p], li);
 #pragma unroll
-      for (int e = 0; e < c; ++e) v[r][e] *= inv_sqrt_d;
+      for (int e = 0; e < 32; ++e) v[p][e] *= inv_sqrt_d;
     }
 #pragma unroll
-    for (int e = 0; e < c; ++e) amax = fmaxf(amax, fabsf(v[r][e]));
+    for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(v[p][e]));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -150,21 +158,19 @@ __global__ void __launch_bounds__(32 * quant_warps<kRope>()) quant_kernel(const 
   const float f1 = ldexpf(1.f, e1), f2 = ldexpf(1.f, e2);
   if (threadIdx.x == 0) scales[(static_cast<long long>(b) * H + h) * gridDim.x + blk] = ldexpf(1.f, -e);
 #pragma unroll
-  for (int r = 0; r < RPW; ++r) {
-    const int row = row0 + r;
-    if (row >= N) break;
-    uint8_t* dst = x8 + (head_off + row) * D + lane * c;
-    if constexpr (c == 2) {
-      uint16_t p;
-      asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(p) : "f"(v[r][1] * f1 * f2), "f"(v[r][0] * f1 * f2));
-      *reinterpret_cast<uint16_t*>(dst) = p;
-    } else {
+  for (int p = 0; p < NPASS; ++p) {
+    const int row = row0 + p * RP + lr;
+    if (row >= N) continue;
+    uint4* dst = reinterpret_cast<uint4*>(x8 + (head_off + row) * D + li * 32);
 #pragma unroll
-      for (int q = 0; q < c / 4; ++q) {
-        const uint32_t p = pack_e4m3x4(v[r][4 * q] * f1 * f2, v[r][4 * q + 1] * f1 * f2,
-                                       v[r][4 * q + 2] * f1 * f2, v[r][4 * q + 3] * f1 * f2);
-        reinterpret_cast<uint32_t*>(dst)[q] = p;
+    for (int q = 0; q < 2; ++q) {
+      uint32_t pk[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = 16 * q + 4 * u;
+        pk[u] = pack_e4m3x4(v[p][i] * f1 * f2, v[p][i + 1] * f1 * f2, v[p][i + 2] * f1 * f2, v[p][i + 3] * f1 * f2);
       }
+      dst[q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
   }
 }
@@ -175,9 +181,9 @@ cudaError_t launch_typed(const void* x, uint8_t* x8, float* scales, int B, int H
   const dim3 grid((N + 127) / 128, H, B);
   const T* xt = static_cast<const T*>(x);
   switch (d) {
-    case 64: quant_kernel<T, 64, kRope><<<grid, 32 * quant_warps<kRope>(), 0, st>>>(xt, x8, scales, H, N, signs, inv_sqrt_d, rc, rs); break;
-    case 128: quant_kernel<T, 128, kRope><<<grid, 32 * quant_warps<kRope>(), 0, st>>>(xt, x8, scales, H, N, signs, inv_sqrt_d, rc, rs); break;
-    case 256: quant_kernel<T, 256, kRope><<<grid, 32 * quant_warps<kRope>(), 0, st>>>(xt, x8, scales, H, N, signs, inv_sqrt_d, rc, rs); break;
+    case 64: quant_kernel<T, 64, kRope><<<grid, kQuantThreads, 0, st>>>(xt, x8, scales, H, N, signs, inv_sqrt_d, rc, rs); break;
+    case 128: quant_kernel<T, 128, kRope><<<grid, kQuantThreads, 0, st>>>(xt, x8, scales, H, N, signs, inv_sqrt_d, rc, rs); break;
+    case 256: quant_kernel<T, 256, kRope><<<grid, kQuantThreads, 0, st>>>(xt, x8, scales, H, N, signs, inv_sqrt_d, rc, rs); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
