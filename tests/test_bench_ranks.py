@@ -53,3 +53,24 @@ def test_flop_formula_of_the_pages():
     # 4 * seqlen^2 * head_dim * heads per batch element, halved when causal
     assert bench.fwd_flops(4, 16, 8448, 128, False) == 4 * 4 * 16 * 8448 ** 2 * 128
     assert bench.fwd_flops(1, 1, 1000, 64, True) == 2 * 1000 ** 2 * 64
+
+
+@pytest.mark.parametrize("workload", ["varlen_t129511_hq32_hkv8_d128_causal", "decode_fp8_b16_hq32_hkv8_n32768_d128"])
+def test_reference_arm_prints_one_contract_line(workload):
+    """The reference arm (the oracle on a bounded sample of the workload) runs
+    on the host alone and prints one JSON line with the contract's keys."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--workload", workload,
+                        "--steps", "1", "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"]["value"] == d["value"] and d["config"]["workload"] == workload
