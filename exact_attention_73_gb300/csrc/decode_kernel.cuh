@@ -12,9 +12,9 @@
 // order, so barrier phases follow from running counters: ri counts the items
 // with at least one KV tile, tg the KV tiles before the current item. The K/V
 // ring, the two score buffers and the two Q buffers run on across items, so
-// the TMA loads of the next item stream while the current one drains; a CTA
-// per item would leave its SM's share of HBM idle from the last tile of one
-// item to the first tile of the next.
+// the TMA loads of the next item stream while the current one drains and the
+// cost of starting and draining a CTA is not paid once per item (which made
+// high split counts slow with one CTA per item).
 //
 // Roles (256 threads): warp 0 loads Q (double-buffered per item) and K/V
 // tiles (ring of NSLOT slots, order K0 K1 V0 K2 V1 ... per item); warp 1
