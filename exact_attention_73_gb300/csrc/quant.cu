@@ -5,19 +5,20 @@
 // by diag(random signs) * Hadamard / sqrt(d) to spread outliers.
 // m.xxqk.cn FA3 walkthrough §4.2: power-of-two scale factors.
 //
-// One CTA per (128-row block, head, batch), 8 warps of 16 rows. A lane holds
-// 32 consecutive elements of a row (d / 32 lanes per row, 32 / (d / 32) rows
-// per warp at a time), loaded and stored with 16-byte accesses. The fast
+// One CTA per (128-row block, head, batch). A lane holds EPL consecutive
+// elements of a row (d / EPL lanes per row): EPL = 32 for the plain and
+// rotation instances (8 warps of 16 rows, 16-byte loads), EPL = d / 32 for
+// the RoPE instance (a warp per row, 16 warps of 8 rows). The fast
 // Walsh-Hadamard transform runs in FP32 in radix-2 stages of stride 1, 2, 4,
-// ...: strides below 32 inside a lane, larger ones across the lanes of a row
+// ...: strides below EPL inside a lane, larger ones across the lanes of a row
 // with shuffles; each butterfly computes a + b and a - b exactly once, so the
 // result does not depend on which lane holds which operand. This kernel is
 // HBM-bound: it reads 2 bytes and writes 1 byte per element.
 // Optional rotary position embedding first (kRope; the paper fuses
 // quantisation into the RoPE step that produces Q and K): rotate-half pairs
 // (i, i + d/2) with the caller's cos/sin tables [N, d/2]; the first half of a
-// row sits in the row's first d/64 lanes, so a lane's partner is d/64 lanes
-// away. Each product and sum is rounded on its own (no fused multiply-add).
+// row sits in the first half of the row's lanes, so a lane's partner is half
+// the row's lanes away. Each product and sum is rounded on its own (no fused multiply-add).
 #include <type_traits>
 
 #include <cuda_bf16.h>
@@ -30,15 +31,15 @@ namespace attn {
 
 namespace {
 
-// Radix-2 FWHT of one row held as 32 consecutive elements per lane over
-// R = D / 32 lanes; li is the lane's position within its row.
-template <int D>
-__device__ __forceinline__ void fwht_row(float (&x)[32], int li) {
+// Radix-2 FWHT of one row held as EPL consecutive elements per lane over
+// D / EPL lanes; li is the lane's position within its row.
+template <int D, int EPL>
+__device__ __forceinline__ void fwht_row(float (&x)[EPL], int li) {
 #pragma unroll
   for (int h = 1; h < D; h <<= 1) {
-    if (h < 32) {
+    if (h < EPL) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
+      for (int e = 0; e < EPL; ++e) {
         if ((e & h) == 0) {
           const float a = x[e], b = x[e + h];
           x[e] = a + b;
@@ -46,10 +47,10 @@ __device__ __forceinline__ void fwht_row(float (&x)[32], int li) {
         }
       }
     } else {
-      const int lm = h / 32;
+      const int lm = h / EPL;
       const bool upper = (li & lm) != 0;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
+      for (int e = 0; e < EPL; ++e) {
         const float other = __shfl_xor_sync(0xffffffffu, x[e], lm);
         x[e] = upper ? (other - x[e]) : (x[e] + other);
       }
@@ -71,18 +72,60 @@ __device__ __forceinline__ float to_f32(uint32_t bits16) {
   else return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16)));
 }
 
-constexpr int kQuantThreads = 256;
+// Layout per instance. The plain and rotation instances: a lane holds 32
+// consecutive elements of a row (d/32 lanes per row), so five Hadamard stages
+// run in registers, with 16-byte loads; 8 warps of 16 rows. The RoPE
+// instance: a warp holds one row at a time (d/32 elements per lane); 16 warps
+// of 8 rows, which keeps more cos/sin table loads in flight (measured faster
+// for it than the 32-per-lane layout).
+template <int D, bool kRope>
+__host__ __device__ constexpr int quant_epl() { return kRope ? D / 32 : 32; }
+template <int D, bool kRope>
+__host__ __device__ constexpr int quant_threads() { return kRope ? 512 : 256; }
+
+// n consecutive 16-bit elements (n = 2, 4 or a multiple of 8) as floats
+template <typename T, int n>
+__device__ __forceinline__ void load_row_part(const T* src, float* v) {
+  if constexpr (n % 8 == 0) {
+#pragma unroll
+    for (int q = 0; q < n / 8; ++q) {
+      const uint4 w = reinterpret_cast<const uint4*>(src)[q];
+      const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        v[8 * q + 2 * u] = to_f32<T>(wv[u] & 0xFFFFu);
+        v[8 * q + 2 * u + 1] = to_f32<T>(wv[u] >> 16);
+      }
+    }
+  } else {
+    uint32_t wv[n / 2];
+    if constexpr (n == 4) {
+      const uint2 w = *reinterpret_cast<const uint2*>(src);
+      wv[0] = w.x;
+      wv[1] = w.y;
+    } else {
+      wv[0] = *reinterpret_cast<const uint32_t*>(src);
+    }
+#pragma unroll
+    for (int u = 0; u < n / 2; ++u) {
+      v[2 * u] = to_f32<T>(wv[u] & 0xFFFFu);
+      v[2 * u + 1] = to_f32<T>(wv[u] >> 16);
+    }
+  }
+}
 
 template <typename T, int D, bool kRope>
-__global__ void __launch_bounds__(kQuantThreads) quant_kernel(const T* __restrict__ x, uint8_t* __restrict__ x8,
+__global__ void __launch_bounds__(quant_threads<D, kRope>()) quant_kernel(const T* __restrict__ x, uint8_t* __restrict__ x8,
                                                              float* __restrict__ scales, int H, int N,
                                                              const int8_t* __restrict__ signs, float inv_sqrt_d,
                                                              const float* __restrict__ rope_cos,
                                                              const float* __restrict__ rope_sin) {
-  constexpr int R = D / 32;            // lanes per row
+  constexpr int EPL = quant_epl<D, kRope>();   // elements per lane
+  constexpr int R = D / EPL;           // lanes per row
   constexpr int RP = 32 / R;           // rows per warp at a time
-  constexpr int NW = kQuantThreads / 32;
+  constexpr int NW = quant_threads<D, kRope>() / 32;
   constexpr int RPW = 128 / NW;        // rows per warp
+  static_assert(RPW >= RP && RPW % RP == 0, "a warp's rows must cover whole rows of lanes");
   constexpr int NPASS = RPW / RP;
   __shared__ float red[NW];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -90,47 +133,44 @@ __global__ void __launch_bounds__(kQuantThreads) quant_kernel(const T* __restric
   const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const long long head_off = (static_cast<long long>(b) * H + h) * N;
   const int row0 = blk * 128 + warp * RPW;
-  float v[NPASS][32];
+  float v[NPASS][EPL];
   float amax = 0.f;
 #pragma unroll
   for (int p = 0; p < NPASS; ++p) {
     const int row = row0 + p * RP + lr;
     const bool valid = row < N;
     if (valid) {
-      const uint4* src = reinterpret_cast<const uint4*>(x + (head_off + row) * D + li * 32);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 w = src[q];
-        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          v[p][8 * q + 2 * u] = to_f32<T>(wv[u] & 0xFFFFu);
-          v[p][8 * q + 2 * u + 1] = to_f32<T>(wv[u] >> 16);
-        }
-      }
+      load_row_part<T, EPL>(x + (head_off + row) * D + li * EPL, v[p]);
     } else {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) v[p][e] = 0.f;
+      for (int e = 0; e < EPL; ++e) v[p][e] = 0.f;
     }
     if constexpr (kRope) {   // partner d/2 elements away: R/2 lanes away; every lane shuffles
-      float cs[32], sn[32];
+      float cs[EPL], sn[EPL];
       if (valid) {
-        const long long t = static_cast<long long>(row) * (D / 2) + (li % (R / 2)) * 32;
-        const float4* c4 = reinterpret_cast<const float4*>(rope_cos + t);
-        const float4* s4 = reinterpret_cast<const float4*>(rope_sin + t);
+        const long long t = static_cast<long long>(row) * (D / 2) + (li % (R / 2)) * EPL;
+        if constexpr (EPL % 4 == 0) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 a = c4[q], bq = s4[q];
-          cs[4 * q] = a.x; cs[4 * q + 1] = a.y; cs[4 * q + 2] = a.z; cs[4 * q + 3] = a.w;
-          sn[4 * q] = bq.x; sn[4 * q + 1] = bq.y; sn[4 * q + 2] = bq.z; sn[4 * q + 3] = bq.w;
+          for (int q = 0; q < EPL / 4; ++q) {
+            const float4 a = reinterpret_cast<const float4*>(rope_cos + t)[q];
+            const float4 bq = reinterpret_cast<const float4*>(rope_sin + t)[q];
+            cs[4 * q] = a.x; cs[4 * q + 1] = a.y; cs[4 * q + 2] = a.z; cs[4 * q + 3] = a.w;
+            sn[4 * q] = bq.x; sn[4 * q + 1] = bq.y; sn[4 * q + 2] = bq.z; sn[4 * q + 3] = bq.w;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) {
+            cs[e] = rope_cos[t + e];
+            sn[e] = rope_sin[t + e];
+          }
         }
       } else {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) cs[e] = sn[e] = 0.f;
+        for (int e = 0; e < EPL; ++e) cs[e] = sn[e] = 0.f;
       }
       const bool second = li >= R / 2;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
+      for (int e = 0; e < EPL; ++e) {
         const float other = __shfl_xor_sync(0xffffffffu, v[p][e], R / 2);
         v[p][e] = second ? __fadd_rn(__fmul_rn(v[p][e], cs[e]), __fmul_rn(other, sn[e]))
                          : __fsub_rn(__fmul_rn(v[p][e], cs[e]), __fmul_rn(other, sn[e]));
@@ -138,13 +178,13 @@ __global__ void __launch_bounds__(kQuantThreads) quant_kernel(const T* __restric
     }
     if (signs) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) v[p][e] *= static_cast<float>(signs[li * 32 + e]);
-      fwht_row<D>(v[p], li);
+      for (int e = 0; e < EPL; ++e) v[p][e] *= static_cast<float>(signs[li * EPL + e]);
+      fwht_row<D, EPL>(v[p], li);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) v[p][e] *= inv_sqrt_d;
+      for (int e = 0; e < EPL; ++e) v[p][e] *= inv_sqrt_d;
     }
 #pragma unroll
-    for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(v[p][e]));
+    for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(v[p][e]));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -161,16 +201,25 @@ __global__ void __launch_bounds__(kQuantThreads) quant_kernel(const T* __restric
   for (int p = 0; p < NPASS; ++p) {
     const int row = row0 + p * RP + lr;
     if (row >= N) continue;
-    uint4* dst = reinterpret_cast<uint4*>(x8 + (head_off + row) * D + li * 32);
+    uint8_t* dst = x8 + (head_off + row) * D + li * EPL;
+    if constexpr (EPL == 2) {
+      uint16_t pq;
+      asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pq) : "f"(v[p][1] * f1 * f2), "f"(v[p][0] * f1 * f2));
+      *reinterpret_cast<uint16_t*>(dst) = pq;
+    } else {
+      uint32_t pk[EPL / 4];
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      uint32_t pk[4];
+      for (int u = 0; u < EPL / 4; ++u)
+        pk[u] = pack_e4m3x4(v[p][4 * u] * f1 * f2, v[p][4 * u + 1] * f1 * f2, v[p][4 * u + 2] * f1 * f2,
+                            v[p][4 * u + 3] * f1 * f2);
+      if constexpr (EPL % 16 == 0) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = 16 * q + 4 * u;
-        pk[u] = pack_e4m3x4(v[p][i] * f1 * f2, v[p][i + 1] * f1 * f2, v[p][i + 2] * f1 * f2, v[p][i + 3] * f1 * f2);
+        for (int q = 0; q < EPL / 16; ++q)
+          reinterpret_cast<uint4*>(dst)[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      } else {
+#pragma unroll
+        for (int u = 0; u < EPL / 4; ++u) reinterpret_cast<uint32_t*>(dst)[u] = pk[u];
       }
-      dst[q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
   }
 }
@@ -181,9 +230,9 @@ cudaError_t launch_typed(const void* x, uint8_t* x8, float* scales, int B, int H
   const dim3 grid((N + 127) / 128, H, B);
   const T* xt = static_cast<const T*>(x);
   switch (d) {
-    case 64: quant_kernel<T, 64, kRope><<<grid, kQuantThreads, 0, st>>>(xt, x8, scales, H, N, signs, inv_sqrt_d, rc, rs); break;
-    case 128: quant_kernel<T, 128, kRope><<<grid, kQuantThreads, 0, st>>>(xt, x8, scales, H, N, signs, inv_sqrt_d, rc, rs); break;
-    case 256: quant_kernel<T, 256, kRope><<<grid, kQuantThreads, 0, st>>>(xt, x8, scales, H, N, signs, inv_sqrt_d, rc, rs); break;
+    case 64: quant_kernel<T, 64, kRope><<<grid, quant_threads<64, kRope>(), 0, st>>>(xt, x8, scales, H, N, signs, inv_sqrt_d, rc, rs); break;
+    case 128: quant_kernel<T, 128, kRope><<<grid, quant_threads<128, kRope>(), 0, st>>>(xt, x8, scales, H, N, signs, inv_sqrt_d, rc, rs); break;
+    case 256: quant_kernel<T, 256, kRope><<<grid, quant_threads<256, kRope>(), 0, st>>>(xt, x8, scales, H, N, signs, inv_sqrt_d, rc, rs); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
