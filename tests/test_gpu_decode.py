@@ -108,3 +108,25 @@ def test_decode_without_seqlens_uses_the_whole_cache():
         torch.cuda.synchronize()
         outs.append((o, lse))
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+def test_decode_more_items_than_sms():
+    """480 (split, KV head, batch) items: each CTA of the persistent kernel
+    walks several, across items of different lengths and empty splits (the
+    K/V ring, score buffers and Q buffers run on from one item to the next)."""
+    B, Hq, Hkv, nmax, d, splits = 20, 16, 8, 384, 128, 3
+    rng = np.random.default_rng(81)
+    lens = [int(x) for x in rng.integers(1, nmax + 1, B)]
+    lens[0], lens[1] = nmax, 1
+    o, lse, o_ref, lse_ref, _ = run_case(B, Hq, Hkv, nmax, d, lens, splits, 910)
+    check_vs_emulation(o, o_ref)
+    assert np.abs(lse - lse_ref).max() <= 1e-3
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_largest_group(d):
+    """g = 128 query heads per KV head: every row of the 128-row query tile is real."""
+    lens = [500, 130]
+    o, lse, o_ref, lse_ref, _ = run_case(2, 128, 1, 500, d, lens, 2, 920 + d)
+    check_vs_emulation(o, o_ref)
+    assert np.abs(lse - lse_ref).max() <= 1e-3
