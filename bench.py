@@ -52,8 +52,10 @@ WORKLOADS = {
 }
 DEFAULT = "bf16_sweep_d128_n8192"
 DECODE_WORKLOADS = {
-    # name: (B, Hq, Hkv, Nmax, d, splits): a 1 GiB FP8 cache, GQA groups of 4
+    # name: (B, Hq, Hkv, Nmax, d, splits): an FP8 cache of 2 * B * Hkv * Nmax * d bytes, GQA groups of 4
     "decode_fp8_b16_hq32_hkv8_n32768_d128": (16, 32, 8, 32768, 128, 8),
+    # a quarter of it (268 MB of cache, still above L2): the size used for ncu --set full
+    "decode_fp8_b4_hq32_hkv8_n32768_d128": (4, 32, 8, 32768, 128, 8),
 }
 VARLEN_WORKLOADS = {
     # name: (lengths seed, sequences, Hq, Hkv, d): packed causal BF16 forward + backward,
@@ -348,7 +350,7 @@ def bench_decode(args, wl, rank, world):
     L.load(build_if_missing=True)
     B, Hq, Hkv, N, d, splits = wl
     g = Hq // Hkv
-    gen = torch.Generator(device=dev).manual_seed(7)   # a 1 GiB cache is drawn on the device
+    gen = torch.Generator(device=dev).manual_seed(7)   # the cache is drawn on the device
     q = torch.randn((B, Hq, d), generator=gen, device=dev).to(torch.bfloat16)
     k = torch.randn((B, Hkv, N, d), generator=gen, device=dev).to(torch.bfloat16)
     v = torch.randn((B, Hkv, N, d), generator=gen, device=dev).to(torch.bfloat16)
@@ -432,7 +434,8 @@ def decode_main(args, world, rank):
     B, Hq, Hkv, N, d, splits = wl
     config = {"workload": args.workload, "B": B, "Hq": Hq, "Hkv": Hkv, "Nmax": N, "d": d, "splits": splits,
               "step": "attn_decode_fp8: one token per sequence over the whole FP8 cache (+ split combine)",
-              "l2": "cache (1 GiB) larger than L2 (no flush)", "parallelism": f"replicas x{world}"}
+              "l2": f"cache ({2 * B * Hkv * N * d / 2**20:.0f} MiB) larger than L2 (no flush)",
+              "parallelism": f"replicas x{world}"}
     metric = "FP8 KV-cache decode: cache bytes read per second on GB300"
     pk = peaks()
     if args.impl == "reference":
