@@ -228,6 +228,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tO = tbase + lane_off + F::O_COL;
+    // rows quarter*32 .. +31 hold real query heads only if quarter*32 < g; a
+    // warp of padding rows skips the softmax and the epilogue (its rows of P
+    // and O are never read) but keeps every barrier's arrival count, waiting
+    // for each tile's S so that it never runs ahead by two phases
+    const bool active = quarter * 32 < a.group;
     int ri = 0, tg = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < items && ok; w += gridDim.x) {
@@ -256,6 +261,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const uint32_t tS = tbase + lane_off + sb * 128;
         ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (jg >> 1) & 1, a.status));
         if (!ok) break;
+        if (!active) {
+          mbar_arrive(&p_ready[sb]);
+          continue;
+        }
         tc_fence_after();
         uint32_t sr[128];
 #pragma unroll
@@ -326,6 +335,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         mbar_arrive(&p_ready[sb]);
       }
       if (!ok) break;
+      if (!active) {   // no rows of this warp to write; o_final(ri) first, so that
+                       // this arrival cannot count toward an earlier o_free phase
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(o_final, ri & 1, a.status)))) break;
+        mbar_arrive(o_free);
+        tg += t.nkv;
+        ++ri;
+        continue;
+      }
       ok = __all_sync(0xffffffffu, mbar_wait(o_final, ri & 1, a.status));
       if (!ok) break;
       tc_fence_after();
