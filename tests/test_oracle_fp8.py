@@ -183,6 +183,26 @@ def test_fp8_attention_tiles_spanning_blocks_use_each_keys_factors(kv_tile):
         assert np.abs(o - o_ref).max() < 2 ** -4 * np.abs(vd).max()
 
 
+@pytest.mark.parametrize("jump", [2.5, 3.5, 6.0])
+def test_fp8_attention_running_max_keeps_p_below_its_shift(jump):
+    """The running max moves only when a tile's row max exceeds it by more than
+    4 log2 units (4 ln 2 ~ 2.77 in score units), so P~ <= 2^4 and P~ * 2^4
+    never reaches E4M3's saturation at 448. Scores: one key at 0 in tile 0, one
+    key at `jump` in tile 1, every other key at -96 (weight below e^-90). With
+    V = 1 the exact output is 1; a saturated P~ would lose over 10 %."""
+    n, d = 256, 16
+    q = np.zeros((1, 1, n, d))
+    q[..., 0] = 1.0
+    k = np.zeros((1, 1, n, d))
+    k[0, 0, 1:, 0] = -96.0
+    k[0, 0, 128, 0] = jump
+    v = np.ones((1, 1, n, d))
+    ones = np.ones((1, 1, 2))
+    o, lse = F.attention_fp8(F.e4m3_encode(q), F.e4m3_encode(k), F.e4m3_encode(v), ones, ones, ones, 1.0, False)
+    assert abs(lse - np.log(1.0 + np.exp(jump))).max() < 1e-12
+    assert np.abs(o - 1.0).max() < 2 ** -4
+
+
 def _emulated_rms(q, k, v, signs, quant, causal=False, rows=slice(None)):
     d = q.shape[-1]
     o_ref, _ = A.forward(q, k, v, d ** -0.5, causal)
