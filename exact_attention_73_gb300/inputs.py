@@ -12,7 +12,9 @@ Recipes
   even, done by torch's CPU cast).
 * Outlier distribution (FP8 accuracy protocol of the FlashAttention-3 paper,
   zenmind summary §10.3 / Table 3): N(0,1) where a Bernoulli(0.001) subset of
-  entries is replaced by N(0, 10^2).
+  entries is replaced by N(0, 10^2); with ``additive=True`` the N(0, 10^2)
+  draw is added to those entries instead (the paper's own wording of the
+  protocol), from the same random draws.
 * Variable-length packing: sequence lengths drawn uniformly from [lo, hi] with
   ``integers(lo, hi + 1, n)``; ``cu_seqlens`` is their exclusive prefix sum.
 * Random signs for the incoherent-processing rotation: +-1 drawn from the seed.
@@ -38,14 +40,17 @@ def normal(seed: int, shapes, dtype: str = "bf16"):
     return out
 
 
-def outliers(seed: int, shapes, dtype: str = "bf16", frac: float = 1e-3, sigma: float = 10.0):
-    """N(0,1) with a Bernoulli(frac) subset of entries replaced by N(0, sigma^2)."""
+def outliers(seed: int, shapes, dtype: str = "bf16", frac: float = 1e-3, sigma: float = 10.0,
+             additive: bool = False):
+    """N(0,1) with a Bernoulli(frac) subset of entries replaced by N(0, sigma^2)
+    (``additive``: with N(0, sigma^2) added to them)."""
     rng = np.random.default_rng(seed)
     out = []
     for shp in shapes:
         x = rng.standard_normal(size=tuple(shp), dtype=np.float32)
         hit = rng.random(size=tuple(shp)) < frac
-        x[hit] = (sigma * rng.standard_normal(size=int(hit.sum()))).astype(np.float32)
+        extra = (sigma * rng.standard_normal(size=int(hit.sum()))).astype(np.float32)
+        x[hit] = x[hit] + extra if additive else extra
         out.append(torch.from_numpy(x).to(_TORCH_DTYPES[dtype]))
     return out
 

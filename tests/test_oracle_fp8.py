@@ -228,6 +228,21 @@ def test_fp8_emulation_on_outliers_with_rotation():
     assert blk < plain            # the rotation spreads the outliers
 
 
+def test_fp8_emulation_on_additive_outliers_with_rotation():
+    """The same protocol with the outliers added to the N(0,1) entries instead
+    of replacing them: the same bounds hold."""
+    from exact_attention_73_gb300 import inputs
+    q, k, v = inputs.outliers(3, [(1, 2, 1024, 128)] * 3, additive=True)
+    q0, _, _ = inputs.outliers(3, [(1, 2, 1024, 128)] * 3)
+    diff = (q.float() - q0.float()).abs()
+    assert 0 < int((diff > 0).sum()) < 0.002 * q.numel()     # only the outlier entries differ
+    signs = inputs.random_signs(4, 128).numpy()
+    blk = _emulated_rms(q, k, v, signs, F.quantize_blocks)
+    ten = _emulated_rms(q, k, v, signs, F.quantize_tensor)
+    assert blk < 1.5e-2
+    assert blk <= ten * (1 + 1e-3)
+
+
 def test_fp8_block_scales_beat_tensor_scale_when_one_block_is_large():
     """One V block 10^4 times larger: with a single scale the other blocks fall into
     E4M3's subnormal range; causal rows that never see the large block show it."""
