@@ -169,9 +169,8 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
                      const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
                      int B, int Hq, int Hkv, int N, int d, float scale, int causal, attn_dtype dtype,
                      void* stream) {
-  if (B < 1 || B > 65535 || N < 1) return ATTN_ERR_SHAPE;
-  attn_status s = check_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, ws_bytes,
-                               attn_bwd_workspace_size(B, Hq, Hkv, N, d), Hq, Hkv, d, dtype);
+  attn_status s = attn::bwd_check_dense(q, k, v, o, lse, dout, dq, dk, dv, workspace, ws_bytes, B, Hq, Hkv, N, d,
+                                        dtype);
   if (s != ATTN_OK) return s;
   int* status;
   if ((s = attn::device_context(&status)) != ATTN_OK) return s;
@@ -210,3 +209,15 @@ attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const v
 }
 
 }  // extern "C"
+
+namespace attn {
+
+attn_status bwd_check_dense(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                            const void* dout, const void* dq, const void* dk, const void* dv, const void* ws,
+                            size_t ws_bytes, int B, int Hq, int Hkv, int N, int d, attn_dtype dtype) {
+  if (B < 1 || B > 65535 || N < 1) return ATTN_ERR_SHAPE;
+  return check_common(q, k, v, o, lse, dout, dq, dk, dv, ws, ws_bytes, attn_bwd_workspace_size(B, Hq, Hkv, N, d),
+                      Hq, Hkv, d, dtype);
+}
+
+}  // namespace attn

@@ -25,6 +25,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/libattn.h"
+#include "ops.h"
 
 namespace {
 
@@ -56,12 +57,14 @@ extern "C" attn_status attn_bwd_noalloc(const void* q, const void* k, const void
                                         const float* lse, const void* dout, void* dq, void* dk, void* dv,
                                         int B, int Hq, int Hkv, int N, int d, float scale, int causal,
                                         attn_dtype dtype, void* stream) {
-  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return ATTN_ERR_NULL;
-  const size_t need = attn_bwd_workspace_size(B, Hq, Hkv, N, d);
-  if (need > kScratchBytes) return ATTN_ERR_WORKSPACE;   // problem too large for the built-in array
-  void* ws = nullptr;
-  attn_status s = scratch_on_current_device(&ws);
+  // Every argument error, a problem too large for the array included, is
+  // reported before the array's address is looked up. q stands in for the
+  // workspace pointer here (the array itself is non-null and aligned).
+  attn_status s = attn::bwd_check_dense(q, k, v, o, lse, dout, dq, dk, dv, q, kScratchBytes, B, Hq, Hkv, N, d,
+                                        dtype);
   if (s != ATTN_OK) return s;
+  void* ws = nullptr;
+  if ((s = scratch_on_current_device(&ws)) != ATTN_OK) return s;
   return attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, ws, kScratchBytes, B, Hq, Hkv, N, d, scale, causal, dtype,
                   stream);
 }

@@ -10,6 +10,12 @@ namespace attn {
 
 attn_status device_context(int** status);
 
+// Argument checks of the dense backward (pointers, alignment, shape, head
+// dimension, GQA, dtype, workspace), all on the host before any device work.
+attn_status bwd_check_dense(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                            const void* dout, const void* dq, const void* dk, const void* dv, const void* ws,
+                            size_t ws_bytes, int B, int Hq, int Hkv, int N, int d, attn_dtype dtype);
+
 struct BwdArgs;
 bool operand_map(CUtensorMap* m, const void* base, int dt, int d, bool packed, int B, int H, long long rows,
                  int box_rows);

@@ -72,6 +72,20 @@ def test_argument_checks_before_any_device_work(lib):
     # quantiser: head dim and dtype
     assert lib.attn_quantize_fp8(P(16), 0, P(16), P(16), 1, 1, 8, 32, None, None) == 4
     assert lib.attn_quantize_fp8(P(16), 2, P(16), P(16), 1, 1, 8, 64, None, None) == 6
+    # FP8 forward: scales are required and aligned; head dim and GQA as attn_fwd
+    f8 = [P(16)] * 3
+    assert lib.attn_fwd_fp8(*f8, None, P(16), P(16), P(16), P(16), 1, 2, 1, 8, 128, 0.1, 0, None) == 1
+    assert lib.attn_fwd_fp8(*f8, P(16), P(20), P(16), P(16), P(16), 1, 2, 1, 8, 128, 0.1, 0, None) == 2
+    assert lib.attn_fwd_fp8(*f8, P(16), P(16), P(16), P(16), P(16), 1, 2, 1, 0, 128, 0.1, 0, None) == 3
+    assert lib.attn_fwd_fp8(*f8, P(16), P(16), P(16), P(16), P(16), 1, 2, 1, 8, 96, 0.1, 0, None) == 4
+    assert lib.attn_fwd_fp8(*f8, P(16), P(16), P(16), P(16), P(16), 1, 3, 2, 8, 128, 0.1, 0, None) == 5
+    # varlen backward: cu_seqlens, sequence counts and the workspace are checked
+    wv = binding.attn_bwd_varlen_workspace_size(10, 2, 1, 128)
+    vargs = [P(16)] * 9
+    assert lib.attn_bwd_varlen(*vargs, P(16), wv, None, 2, 10, 5, 2, 1, 128, 0.1, 0, 0, None) == 1
+    assert lib.attn_bwd_varlen(*vargs, P(16), wv, P(16), 0, 10, 5, 2, 1, 128, 0.1, 0, 0, None) == 3
+    assert lib.attn_bwd_varlen(*vargs, P(16), wv, P(16), 2, 10, 11, 2, 1, 128, 0.1, 0, 0, None) == 3
+    assert lib.attn_bwd_varlen(*vargs, P(16), wv - 1, P(16), 2, 10, 5, 2, 1, 128, 0.1, 0, 0, None) == 7
     # backward: workspace must be present and large enough
     ws = binding.attn_bwd_workspace_size(1, 2, 1, 8, 128)
     args = [P(16)] * 9

@@ -64,3 +64,10 @@ def test_noalloc_refuses_problems_larger_than_its_array():
     # 2 x 32 heads x 8192 rows x 128 dims of FP32 accumulator is far above 32 MiB
     assert lib.attn_bwd_noalloc(*args, 2, 32, 8, 8192, 128, 0.1, 1, 0, None) == 7   # ATTN_ERR_WORKSPACE
     assert lib.attn_bwd_noalloc(None, *args[1:], 1, 2, 1, 8, 128, 0.1, 0, 0, None) == 1
+    # the other argument errors, as attn_bwd reports them, before the array is looked up
+    assert lib.attn_bwd_noalloc(*args, 1, 2, 1, 0, 128, 0.1, 0, 0, None) == 3         # N = 0
+    assert lib.attn_bwd_noalloc(P(20), *args[1:], 1, 2, 1, 8, 128, 0.1, 0, 0, None) == 2
+    assert lib.attn_bwd_noalloc(*args, 1, 2, 1, 8, 64, 0.1, 0, 0, None) == 4          # d = 128 only
+    assert lib.attn_bwd_noalloc(*args, 1, 3, 2, 8, 128, 0.1, 0, 0, None) == 5
+    assert lib.attn_bwd_noalloc(*args, 1, 2, 1, 8, 128, 0.1, 0, 2, None) == 6         # E4M3 has no backward
+    assert lib.attn_bwd_noalloc(*args, 1, 2, 1, 8, 128, 0.1, 0, 0, None) == 11        # valid: no device here
