@@ -51,8 +51,16 @@ def run_case(B, Hq, Hkv, nmax, d, lens, splits, seed):
     assert L.attn_get_device_status() == 0
     ntiles = (nmax + 127) // 128
     tps = -(-ntiles // splits)
-    o_ref, lse_ref = F.decode_fp8(q8.cpu().numpy(), sq.cpu().numpy(), k8.cpu().numpy(), v8.cpu().numpy(),
-                                  sk.cpu().numpy(), sv.cpu().numpy(), lens, d ** -0.5, tps)
+    # the oracle quantises the same seeded inputs itself; the GPU's codes must equal its own
+    s = signs.cpu().numpy()
+    rq8, rsq = F.quantize_blocks(q.view(B, Hkv, g, d), s)
+    rk8, rsk = F.quantize_blocks(k, s)
+    rv8, rsv = F.quantize_blocks(v)
+    rsq = rsq[:, :, 0]
+    for name, a, b in (("q8", q8.view(B, Hkv, g, d), rq8), ("sq", sq, rsq), ("k8", k8, rk8), ("sk", sk, rsk),
+                       ("v8", v8, rv8), ("sv", sv, rsv)):
+        assert np.array_equal(a.cpu().numpy(), b), name
+    o_ref, lse_ref = F.decode_fp8(rq8, rsq, rk8, rv8, rsk, rsv, lens, d ** -0.5, tps)
     return o.double().cpu().numpy().reshape(B, Hkv, g, d), lse.cpu().numpy().reshape(B, Hkv, g), o_ref, lse_ref, \
         (q, k, v)
 

@@ -172,6 +172,8 @@ def test_quantizer_zero_block_gets_unit_scale():
 
 
 def run_fp8(q, k, v, causal, signs=None):
+    """GPU quantiser then GPU FP8 forward. Returns O, LSE and the GPU's codes
+    and factors (q8, k8, v8, sq, sk, sv) as numpy arrays."""
     q8, sq = quantize_gpu(q, signs)
     k8, sk = quantize_gpu(k, signs)
     v8, sv = quantize_gpu(v)
@@ -182,6 +184,23 @@ def run_fp8(q, k, v, causal, signs=None):
     torch.cuda.synchronize()
     return o.cpu(), lse.cpu(), (q8.cpu().numpy(), k8.cpu().numpy(), v8.cpu().numpy(),
                                 sq.cpu().numpy(), sk.cpu().numpy(), sv.cpu().numpy())
+
+
+def oracle_fp8_inputs(q, k, v, signs=None, gpu=None):
+    """The oracle's own block quantisation of the seeded inputs (Q and K
+    rotated when signs are given): the codes and factors its emulation runs
+    on. With ``gpu`` (the GPU's codes and factors of the same inputs), first
+    check that the two are equal bit for bit, so that both sides run on the
+    same codes without the oracle taking any input from the GPU."""
+    s = None if signs is None else signs.numpy()
+    q8, sq = F.quantize_blocks(q, s)
+    k8, sk = F.quantize_blocks(k, s)
+    v8, sv = F.quantize_blocks(v)
+    ref = (q8, k8, v8, sq, sk, sv)
+    if gpu is not None:
+        for name, a, b in zip(("q8", "k8", "v8", "sq", "sk", "sv"), gpu, ref):
+            assert np.array_equal(a, b), name
+    return ref
 
 
 # The emulation rounds P~ to E4M3 from float64 scores, the kernel from
@@ -207,8 +226,9 @@ def check_fp8_vs_emulation(o, o_ref):
 @pytest.mark.parametrize("n", [100, 700])   # one KV tile; several tiles and a ragged tail
 def test_fp8_forward_matches_emulation(d, causal, n):
     q, k, v = inputs.outliers(3, [(1, 4, n, d), (1, 2, n, d), (1, 2, n, d)])
-    o, lse, (q8, k8, v8, sq, sk, sv) = run_fp8(q, k, v, causal)
-    o_ref, lse_ref = F.attention_fp8(q8, k8, v8, sq, sk, sv, d ** -0.5, causal, kv_tile=L.attn_fwd_fp8_kv_tile(d))
+    o, lse, gpu_codes = run_fp8(q, k, v, causal)
+    codes = oracle_fp8_inputs(q, k, v, gpu=gpu_codes)
+    o_ref, lse_ref = F.attention_fp8(*codes, d ** -0.5, causal, kv_tile=L.attn_fwd_fp8_kv_tile(d))
     check_fp8_vs_emulation(o.double().numpy(), o_ref)
     assert np.abs(lse.double().numpy() - lse_ref).max() <= 1e-3
 
@@ -223,22 +243,24 @@ def test_fp8_config_accuracy_sampled(d, causal):
     B, H, N = 4, 16, 8192
     q, k, v = inputs.outliers(3, [(B, H, N, d)] * 3)
     signs = inputs.random_signs(4, d)
-    o, lse, (q8, k8, v8, sq, sk, sv) = run_fp8(q, k, v, causal, signs)
+    o, lse, gpu_codes = run_fp8(q, k, v, causal, signs)
     heads = [(0, 0), (3, 15)]
     rows = sampled_rows(N, 64, d)
     qt, sqt = F.quantize_tensor(q, signs.numpy())
     kt, skt = F.quantize_tensor(k, signs.numpy())
     vt, svt = F.quantize_tensor(v)
     o_ten, _ = F.attention_fp8(qt, kt, vt, sqt, skt, svt, d ** -0.5, causal, heads=heads, rows=rows)
-    o_emu, _ = F.attention_fp8(q8, k8, v8, sq, sk, sv, d ** -0.5, causal, heads=heads, rows=rows,
-                               kv_tile=L.attn_fwd_fp8_kv_tile(d))
     gpu, ten, emu, ref = [], [], [], []
     for (b, h) in heads:
+        # block factors belong to one (batch, head), so one head's slice is quantised on its own
+        one = lambda x: x[b:b + 1, h:h + 1]
+        codes = oracle_fp8_inputs(one(q), one(k), one(v), signs, gpu=[one(x) for x in gpu_codes])
+        o_emu, _ = F.attention_fp8(*codes, d ** -0.5, causal, rows=rows, kv_tile=L.attn_fwd_fp8_kv_tile(d))
         r, _ = A.forward_rows(q[b, h], k[b, h], v[b, h], rows, d ** -0.5, causal)
         ref.append(r)
         gpu.append(o[b, h, rows].double().numpy())
         ten.append(o_ten[b, h, rows])
-        emu.append(o_emu[b, h, rows])
+        emu.append(o_emu[0, 0, rows])
     ref, gpu, ten, emu = (np.concatenate(x) for x in (ref, gpu, ten, emu))
     rms = lambda x: math.sqrt(((x - ref) ** 2).mean())
     assert rms(gpu) <= 1.5e-2, rms(gpu)
@@ -255,13 +277,14 @@ def test_fp8_accuracy_additive_outliers(causal):
     d = 128
     q, k, v = inputs.outliers(6, [(1, 4, 1024, d)] * 3, additive=True)
     signs = inputs.random_signs(4, d)
-    o, _, (q8, k8, v8, sq, sk, sv) = run_fp8(q, k, v, causal, signs)
+    o, _, gpu_codes = run_fp8(q, k, v, causal, signs)
     ref, _ = A.forward(q, k, v, d ** -0.5, causal)
     qt, sqt = F.quantize_tensor(q, signs.numpy())
     kt, skt = F.quantize_tensor(k, signs.numpy())
     vt, svt = F.quantize_tensor(v)
     o_ten, _ = F.attention_fp8(qt, kt, vt, sqt, skt, svt, d ** -0.5, causal)
-    o_emu, _ = F.attention_fp8(q8, k8, v8, sq, sk, sv, d ** -0.5, causal, kv_tile=L.attn_fwd_fp8_kv_tile(d))
+    codes = oracle_fp8_inputs(q, k, v, signs, gpu=gpu_codes)
+    o_emu, _ = F.attention_fp8(*codes, d ** -0.5, causal, kv_tile=L.attn_fwd_fp8_kv_tile(d))
     gpu = o.double().numpy()
     rms = lambda x: math.sqrt(((x - ref) ** 2).mean())
     assert rms(gpu) <= 1.5e-2, rms(gpu)
