@@ -55,7 +55,8 @@ def test_flop_formula_of_the_pages():
     assert bench.fwd_flops(1, 1, 1000, 64, True) == 2 * 1000 ** 2 * 64
 
 
-@pytest.mark.parametrize("workload", ["varlen_t129511_hq32_hkv8_d128_causal", "decode_fp8_b16_hq32_hkv8_n32768_d128"])
+@pytest.mark.parametrize("workload", [None, "varlen_t129511_hq32_hkv8_d128_causal",
+                                      "decode_fp8_b16_hq32_hkv8_n32768_d128"])
 def test_reference_arm_prints_one_contract_line(workload):
     """The reference arm (the oracle on a bounded sample of the workload) runs
     on the host alone and prints one JSON line with the contract's keys."""
@@ -63,8 +64,10 @@ def test_reference_arm_prints_one_contract_line(workload):
     import subprocess
     import sys
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--workload", workload,
-                        "--steps", "1", "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=root)
+    cmd = [sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "1", "--warmup", "3"]
+    if workload is not None:
+        cmd += ["--workload", workload]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=root)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
     assert len(lines) == 1
@@ -73,4 +76,5 @@ def test_reference_arm_prints_one_contract_line(workload):
                 "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
         assert key in d, key
     assert d["impl"] == "reference" and d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
-    assert d["e2e"]["value"] == d["value"] and d["config"]["workload"] == workload
+    assert d["e2e"]["value"] == d["value"] and d["config"]["workload"] == (workload or bench.DEFAULT)
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
