@@ -12,8 +12,13 @@ fp8       : the E4M3 codec, power-of-two block scales, the random-sign
             Hadamard rotation and an emulation of block-quantised FP8
             attention that follows the tiled algorithm step by step.
 
-Parity status: every function is pinned by ``tests/test_oracle_*.py`` except
-``fp8.attention_fp8`` beyond its closed-form special cases (parity unpinned
-for general inputs: only the stated tolerance and the ordering against the
-per-tensor emulation are checked).
+Parity status: every function is pinned by ``tests/test_oracle_*.py``. For
+``fp8.attention_fp8`` and ``fp8.decode_fp8`` everything but the E4M3 rounding
+of P~ is pinned on arbitrary inputs (with ``round_p=False`` they equal float64
+attention of the dequantised inputs); which value is rounded is pinned only by
+a worked example, the saturation bound and inputs on the E4M3 grid (parity
+partly unpinned: on general inputs the rounding's effect is checked through
+the stated tolerance and the ordering against the per-tensor emulation).
+``tests/test_oracle_mutations.py`` plants mistakes in copies of both modules
+and checks that a pin fails for each.
 """

@@ -216,14 +216,15 @@ def quantize_tensor(x, signs=None, block=BLOCK):
 
 
 def _fp8_rows(qrows, q_fac, kf, vf, sk, sv, tiles, n, scale, causal=False, rows=None, block=BLOCK, p_shift=4,
-              tau=4.0, kv_tile=None):
+              tau=4.0, kv_tile=None, round_p=True):
     """Algorithm 1 in its FP8 form for query rows ``qrows`` [R, d] (decoded,
     with per-row factors q_fac) over the key tiles ``tiles`` (indices of tiles
     of kv_tile keys, in order) of one KV head: kf/vf [N, d] decoded, sk/sv the
     factors of the ``block``-key quantisation blocks. A tile may span blocks:
     each key takes its own block's factors, and F is raised to the largest V
     exponent among the tile's keys. Starts from m = -inf, l = 0, O = 0.
-    Returns (O [R, d], LSE [R])."""
+    ``round_p=False`` leaves out the E4M3 rounding of P~ (for pins: the rest
+    is then exact). Returns (O [R, d], LSE [R])."""
     kv_tile = block if kv_tile is None else kv_tile
     d = qrows.shape[1]
     m = np.full(len(qrows), -np.inf)
@@ -245,14 +246,16 @@ def _fp8_rows(qrows, q_fac, kf, vf, sk, sv, tiles, n, scale, causal=False, rows=
         v_corr = np.exp2(f_run - f_new)
         pt = np.exp(s - m_use[:, None])
         l = corr * l + pt.sum(axis=1)
-        p8 = e4m3_decode(e4m3_encode(pt * np.exp2(p_shift + f_c - f_new)[None, :]))
+        p8 = pt * np.exp2(p_shift + f_c - f_new)[None, :]
+        if round_p:
+            p8 = e4m3_decode(e4m3_encode(p8))
         acc = (corr * v_corr)[:, None] * acc + p8 @ vf[cols]
         m, f_run = m_new, f_new
     return acc * np.exp2(f_run - p_shift) / l[:, None], m + np.log(l)
 
 
 def attention_fp8(q8, k8, v8, sq, sk, sv, scale, causal=False, block=BLOCK, p_shift=4, tau=4.0, heads=None,
-                  rows=None, kv_tile=None):
+                  rows=None, kv_tile=None, round_p=True):
     """FP8 forward following Algorithm 1 tile by tile (Bc = kv_tile keys per
     tile, by default the quantisation block; the stale max and the V exponent
     F move at tile granularity, so the E4M3 rounding of P~ depends on it).
@@ -262,6 +265,7 @@ def attention_fp8(q8, k8, v8, sq, sk, sv, scale, causal=False, block=BLOCK, p_sh
     E4M3 rounding of P~ before the second product. Returns (O, LSE).
     ``heads`` (list of (b, h)) and ``rows`` restrict the work to those query
     heads and rows (rows are independent); other entries are left as NaN.
+    ``round_p=False`` leaves out the E4M3 rounding of P~ (for pins).
     """
     qf, kf, vf = e4m3_decode(q8), e4m3_decode(k8), e4m3_decode(v8)
     sq, sk, sv = (np.asarray(a, dtype=np.float64) for a in (sq, sk, sv))
@@ -276,7 +280,7 @@ def attention_fp8(q8, k8, v8, sq, sk, sv, scale, causal=False, block=BLOCK, p_sh
         kv = h // g
         o[b, h, rows], lse[b, h, rows] = _fp8_rows(
             qf[b, h, rows], sq[b, h, rows // block], kf[b, kv], vf[b, kv], sk[b, kv], sv[b, kv],
-            range((n + kvt - 1) // kvt), n, scale, causal, rows, block, p_shift, tau, kvt)
+            range((n + kvt - 1) // kvt), n, scale, causal, rows, block, p_shift, tau, kvt, round_p)
     return o, lse
 
 
@@ -293,7 +297,8 @@ def combine_splits(o_parts, lse_parts):
     return o, mx + np.log(tot)
 
 
-def decode_fp8(q8, sq, k8, v8, sk, sv, lens, scale, tiles_per_split, block=BLOCK, p_shift=4, tau=4.0):
+def decode_fp8(q8, sq, k8, v8, sk, sv, lens, scale, tiles_per_split, block=BLOCK, p_shift=4, tau=4.0,
+               round_p=True):
     """FP8 decode over a block-quantised KV cache, split by key tiles.
 
     q8 [B, Hkv, g, d]: E4M3 codes of the g query heads of each KV group at the
@@ -302,7 +307,8 @@ def decode_fp8(q8, sq, k8, v8, sk, sv, lens, scale, tiles_per_split, block=BLOCK
     lens[b] the valid cache length of sequence b. Split s holds key tiles
     [s * tiles_per_split, (s + 1) * tiles_per_split) below ceil(lens[b]/block);
     each split runs the FP8 form of Algorithm 1 on its own and the splits are
-    combined with combine_splits. Returns (O [B, Hkv, g, d], LSE [B, Hkv, g]).
+    combined with combine_splits. ``round_p=False`` leaves out the E4M3
+    rounding of P~ (for pins). Returns (O [B, Hkv, g, d], LSE [B, Hkv, g]).
     """
     qf, kf, vf = e4m3_decode(q8), e4m3_decode(k8), e4m3_decode(v8)
     sq, sk, sv = (np.asarray(a, dtype=np.float64) for a in (sq, sk, sv))
@@ -315,6 +321,7 @@ def decode_fp8(q8, sq, k8, v8, sk, sv, lens, scale, tiles_per_split, block=BLOCK
         splits = [range(t, min(t + tiles_per_split, nt)) for t in range(0, nt, tiles_per_split)]
         for kv in range(hkv):
             parts = [_fp8_rows(qf[b, kv], np.full(g, sq[b, kv]), kf[b, kv], vf[b, kv], sk[b, kv], sv[b, kv],
-                               tiles, n, scale, block=block, p_shift=p_shift, tau=tau) for tiles in splits]
+                               tiles, n, scale, block=block, p_shift=p_shift, tau=tau, round_p=round_p)
+                     for tiles in splits]
             o[b, kv], lse[b, kv] = combine_splits([p[0] for p in parts], [p[1] for p in parts])
     return o, lse

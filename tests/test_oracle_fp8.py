@@ -183,6 +183,76 @@ def test_fp8_attention_tiles_spanning_blocks_use_each_keys_factors(kv_tile):
         assert np.abs(o - o_ref).max() < 2 ** -4 * np.abs(vd).max()
 
 
+def _dequantised(codes, fac):
+    """Decoded codes times their block's factor (the values the FP8 path represents)."""
+    return F.e4m3_decode(codes) * np.repeat(np.asarray(fac, dtype=np.float64), F.BLOCK, axis=2)[:, :, :codes.shape[2], None]
+
+
+def _blocky(seed, shape):
+    """Outlier-distributed values whose 128-row blocks differ in magnitude by
+    up to 2^6, so the block factors (and the scores between tiles) differ."""
+    from exact_attention_73_gb300 import inputs
+    (x,) = inputs.outliers(seed, [shape], dtype="fp32")
+    mag = np.exp2(np.random.default_rng(seed).integers(-3, 4, (shape[0], shape[1], -(-shape[2] // 128))))
+    return torch.from_numpy(x.numpy() * np.repeat(mag, 128, axis=2)[:, :, :shape[2], None].astype(np.float32))
+
+
+@pytest.mark.parametrize("kv_tile", [None, 96, 64])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_emulation_without_p_rounding_is_exact_attention(kv_tile, causal):
+    """Leaving out only the E4M3 rounding of P~, the emulation's bookkeeping
+    (stale max and its corrections, per-key K and V factors, the V-exponent
+    F, the 2^4 shift, the final division) must give float64 attention of the
+    dequantised inputs, for any inputs: GQA, a ragged tail, rotated Q and K,
+    block factors that differ by up to 2^6."""
+    from exact_attention_73_gb300 import inputs
+    n, d = 300, 64
+    q, k, v = _blocky(20, (1, 4, n, d)), _blocky(21, (1, 2, n, d)), _blocky(22, (1, 2, n, d))
+    signs = inputs.random_signs(4, d).numpy()
+    (q8, sq), (k8, sk), (v8, sv) = F.quantize_blocks(q, signs), F.quantize_blocks(k, signs), F.quantize_blocks(v)
+    assert len(np.unique(sk)) > 2 and len(np.unique(sv)) > 2
+    o, lse = F.attention_fp8(q8, k8, v8, sq, sk, sv, d ** -0.5, causal, kv_tile=kv_tile, round_p=False)
+    o_ref, l_ref = A.forward(_dequantised(q8, sq), _dequantised(k8, sk), _dequantised(v8, sv), d ** -0.5, causal)
+    np.testing.assert_allclose(lse, l_ref, rtol=0, atol=1e-10)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-10 * np.abs(o_ref).max())
+
+
+def test_decode_without_p_rounding_is_exact_attention():
+    """The split decode with the E4M3 rounding of P~ left out: float64
+    attention of the g query rows over each sequence's valid keys, whatever
+    the split size."""
+    B, Hkv, g, nmax, d = 3, 2, 4, 600, 64
+    q = _blocky(23, (B, Hkv, g, d))
+    k, v = _blocky(24, (B, Hkv, nmax, d)), _blocky(25, (B, Hkv, nmax, d))
+    (q8, sq), (k8, sk), (v8, sv) = F.quantize_blocks(q), F.quantize_blocks(k), F.quantize_blocks(v)
+    qd, kd, vd = _dequantised(q8, sq), _dequantised(k8, sk), _dequantised(v8, sv)
+    lens = [600, 1, 300]
+    for tps in (1, 2, 5):
+        o, lse = F.decode_fp8(q8, sq[:, :, 0], k8, v8, sk, sv, lens, d ** -0.5, tps, round_p=False)
+        for b in range(B):
+            for h in range(Hkv):
+                ro, rl, _ = A.head_forward(qd[b, h], kd[b, h, :lens[b]], vd[b, h, :lens[b]], d ** -0.5, False)
+                np.testing.assert_allclose(lse[b, h], rl, rtol=0, atol=1e-10)
+                np.testing.assert_allclose(o[b, h], ro, rtol=0, atol=1e-10 * np.abs(ro).max())
+
+
+def test_fp8_p_rounding_worked_example():
+    """Two keys (and two equal queries), unit factors, scale ln 3: scores -ln 3 and 0, so
+    P~ = (1/3, 1) and P~ * 2^4 = (16/3, 16). E4M3 has steps of 1/2 in [4, 8):
+    16/3 rounds to 5.5, 16 is exact. l sums the unrounded P~ (4/3), so with
+    V rows e_0 and e_1: O = (5.5/16, 16/16) * 3/4 = (33/128, 3/4) (exact
+    attention gives (1/4, 3/4)) and LSE = ln(4/3)."""
+    d = 16
+    q = np.zeros((1, 1, 2, d)); q[..., 0] = 1.0
+    k = np.zeros((1, 1, 2, d)); k[0, 0, 0, 0] = -1.0
+    v = np.zeros((1, 1, 2, d)); v[0, 0, 0, 0] = 1.0; v[0, 0, 1, 1] = 1.0
+    one = np.ones((1, 1, 1))
+    o, lse = F.attention_fp8(F.e4m3_encode(q), F.e4m3_encode(k), F.e4m3_encode(v), one, one, one, math.log(3.0))
+    want = np.zeros(d); want[0], want[1] = 33 / 128, 3 / 4
+    np.testing.assert_allclose(o[0, 0], np.stack([want, want]), rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse[0, 0], math.log(4 / 3), rtol=0, atol=1e-15)
+
+
 @pytest.mark.parametrize("jump", [2.5, 3.5, 6.0])
 def test_fp8_attention_running_max_keeps_p_below_its_shift(jump):
     """The running max moves only when a tile's row max exceeds it by more than

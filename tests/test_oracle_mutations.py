@@ -141,6 +141,8 @@ FP8_MUTANTS = {
     "causal mask off by one": ("s = np.where(cols[None, :] > rows[:, None], -np.inf, s)",
                                "s = np.where(cols[None, :] >= rows[:, None], -np.inf, s)"),
     "O not rescaled when F grows": ("v_corr = np.exp2(f_run - f_new)", "v_corr = 1.0"),
+    "F correction with the wrong sign": ("v_corr = np.exp2(f_run - f_new)", "v_corr = np.exp2(f_new - f_run)"),
+    "row max correction with the wrong sign": ("corr = np.exp(m - m_use)", "corr = np.exp(m_use - m)"),
     "O not rescaled when m grows": ("acc = (corr * v_corr)[:, None] * acc + p8 @ vf[cols]",
                                     "acc = v_corr * acc + p8 @ vf[cols]"),
     "l not rescaled when m grows": ("l = corr * l + pt.sum(axis=1)", "l = l + pt.sum(axis=1)"),
@@ -148,8 +150,10 @@ FP8_MUTANTS = {
                            "return acc * np.exp2(f_run) / l[:, None], m + np.log(l)"),
     "stale-max threshold in the wrong units": ("m_new = np.where(mx > m + tau * np.log(2.0), mx, m)",
                                               "m_new = np.where(mx > m + tau, mx, m)"),
-    "V factor taken per tile, not per key": ("p8 = e4m3_decode(e4m3_encode(pt * np.exp2(p_shift + f_c - f_new)[None, :]))",
-                                             "p8 = e4m3_decode(e4m3_encode(pt * np.exp2(p_shift + f_c.max() - f_new)))"),
+    "V factor taken per tile, not per key": ("p8 = pt * np.exp2(p_shift + f_c - f_new)[None, :]",
+                                             "p8 = pt * np.exp2(p_shift + f_c.max() - f_new)"),
+    "P~ not rounded to E4M3": ("        if round_p:\n            p8 = e4m3_decode(e4m3_encode(p8))",
+                               "        pass"),
     "split combine without normalisation": ("o = (w[..., None] * np.nan_to_num(o_parts)).sum(axis=0) / tot[..., None]",
                                             "o = (w[..., None] * np.nan_to_num(o_parts)).sum(axis=0)"),
     "split combine LSE in base 2": ("return o, mx + np.log(tot)", "return o, mx + np.log2(tot)"),
