@@ -313,6 +313,28 @@ def test_fp8_emulation_on_additive_outliers_with_rotation():
     assert blk <= ten * (1 + 1e-3)
 
 
+def test_fp8_emulation_reproduces_the_published_ablation_qualitatively():
+    """The pages' FP8 accuracy ablation (tests/golden/fp8_table3_ablation.json,
+    shapes not given) on its own additive outlier distribution, at B=1, H=2,
+    N=1024, d=128: the rotation is the main effect (published: 2.4e-2 without
+    it against 9.1e-3 with it; here at least a factor 1.5), block scales alone
+    change little (9.3e-3 against 9.1e-3; here within 5 %), and the RMSE is of
+    the published order (within a factor 2 of 9.1e-3)."""
+    from exact_attention_73_gb300 import inputs
+    g = json.load(open(os.path.join(GOLD, "fp8_table3_ablation.json")))["rmse"]
+    q, k, v = inputs.outliers(3, [(1, 2, 1024, 128)] * 3, additive=True)
+    signs = inputs.random_signs(4, 128).numpy()
+    both = _emulated_rms(q, k, v, signs, F.quantize_blocks)
+    no_rotation = _emulated_rms(q, k, v, None, F.quantize_blocks)
+    no_blocks = _emulated_rms(q, k, v, signs, F.quantize_tensor)
+    assert no_rotation > 1.5 * both, (no_rotation, both)
+    assert abs(no_blocks - both) <= 0.05 * both, (no_blocks, both)
+    ref = g["fp8_fa3_block_quantisation_and_incoherent_processing"]
+    assert ref / 2 < both < 2 * ref, both
+    pub = g["fp8_without_incoherent_processing"] / ref
+    assert pub > 1.5 and abs(g["fp8_without_block_quantisation"] - ref) <= 0.05 * ref   # the fixture's own reading
+
+
 def test_fp8_block_scales_beat_tensor_scale_when_one_block_is_large():
     """One V block 10^4 times larger: with a single scale the other blocks fall into
     E4M3's subnormal range; causal rows that never see the large block show it."""
