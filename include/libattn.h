@@ -259,10 +259,9 @@ ATTN_API attn_status attn_bwd_deterministic(const void* q, const void* k, const 
  * keeps until the process exits. A problem whose attn_bwd_workspace_size
  * exceeds that returns ATTN_ERR_WORKSPACE before any device work, and every
  * other argument error returns attn_bwd's code, also before any device work.
- * The first
- * call on a device looks up the array's device address (do it before any
- * stream capture). All calls share the array: calls that overlap on the GPU
- * race and must not be issued. Nothing is allocated or freed.
+ * The first call on a device looks up the array's device address (do it
+ * before any stream capture). All calls share the array: calls that overlap
+ * on the GPU race and must not be issued. Nothing is allocated or freed.
  */
 ATTN_API attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                                       const float* lse, const void* dout,
