@@ -80,8 +80,52 @@ def load(build_if_missing: bool = True):
     return lib
 
 
-def _ptr(t):
-    return None if t is None else C.c_void_p(t.data_ptr())
+# The C ABI sees only pointers, so the layout its kernels assume is checked
+# here: every tensor handed to the library is a contiguous tensor on the GPU
+# with the documented number of elements and element type. A mismatch would
+# otherwise make a kernel read or write past the end of a buffer.
+_DEVICE_TYPE = "cuda"
+
+
+def _ptr(t, name="tensor", numel=None, dtype=None, shape=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+    if t.device.type != _DEVICE_TYPE:
+        raise ValueError(f"{name} must be a {_DEVICE_TYPE} tensor, not on {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (the library reads it as a dense array)")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} must hold {numel} elements, got {t.numel()}")
+    return C.c_void_p(t.data_ptr())
+
+
+def _dims(t, name, n):
+    if not isinstance(t, torch.Tensor) or t.dim() != n:
+        raise ValueError(f"{name} must be a {n}-D tensor")
+    return tuple(t.shape)
+
+
+def _nb(n):
+    return (n + 127) // 128
+
+
+def _bwd_ptrs(q, k, v, o, lse, dout, dq, dk, dv):
+    """Pointers of a dense backward call: q [B,Hq,N,d], k/v [B,Hkv,N,d], o, dout,
+    dq like q, dk/dv like k (all of q's type), lse [B,Hq,N] float32."""
+    B, Hq, N, d = _dims(q, "q", 4)
+    Hkv = _dims(k, "k", 4)[1]
+    dt = q.dtype
+    kv = (B, Hkv, N, d)
+    return [_ptr(q, "q"), _ptr(k, "k", dtype=dt, shape=kv), _ptr(v, "v", dtype=dt, shape=kv),
+            _ptr(o, "o", q.numel(), dt), _ptr(lse, "lse", B * Hq * N, torch.float32),
+            _ptr(dout, "dout", q.numel(), dt), _ptr(dq, "dq", q.numel(), dt), _ptr(dk, "dk", k.numel(), dt),
+            _ptr(dv, "dv", k.numel(), dt)]
 
 
 def _stream(stream):
@@ -104,58 +148,82 @@ def _dtype(t):
     return _DT[t.dtype]
 
 
+def _fwd_ptrs(q, k, v, o, lse):
+    """Pointers of a dense forward call: q [B,Hq,N,d], k/v [B,Hkv,N,d] of q's
+    type, o like q, lse [B,Hq,N] float32."""
+    B, Hq, N, d = _dims(q, "q", 4)
+    Hkv = _dims(k, "k", 4)[1]
+    kv = (B, Hkv, N, d)
+    return [_ptr(q, "q"), _ptr(k, "k", dtype=q.dtype, shape=kv), _ptr(v, "v", dtype=q.dtype, shape=kv),
+            _ptr(o, "o", q.numel(), q.dtype), _ptr(lse, "lse", B * Hq * N, torch.float32)]
+
+
 def attn_fwd(q, k, v, o, lse, scale=None, causal=False, stream=None):
     """Dense forward: q [B,Hq,N,d], k/v [B,Hkv,N,d], o like q, lse [B,Hq,N] fp32."""
-    B, Hq, N, d = q.shape
-    Hkv = k.shape[1]
+    B, Hq, N, d = _dims(q, "q", 4)
+    Hkv = _dims(k, "k", 4)[1]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
-    _check(load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d, scale,
+    _check(load().attn_fwd(*_fwd_ptrs(q, k, v, o, lse), B, Hq, Hkv, N, d, scale,
                            int(bool(causal)), _dtype(q), _stream(stream)), "attn_fwd")
 
 
 def attn_fwd_window(q, k, v, o, lse, window, scale=None, stream=None):
     """Dense forward with a key window (left, right): key j is visible to
     query i iff i - left <= j <= i + right; -1 means no bound on that side."""
-    B, Hq, N, d = q.shape
-    Hkv = k.shape[1]
+    B, Hq, N, d = _dims(q, "q", 4)
+    Hkv = _dims(k, "k", 4)[1]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     left, right = (int(w) for w in window)
-    _check(load().attn_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d, scale,
+    _check(load().attn_fwd_window(*_fwd_ptrs(q, k, v, o, lse), B, Hq, Hkv, N, d, scale,
                                   left, right, _dtype(q), _stream(stream)), "attn_fwd_window")
 
 
 def attn_fwd_varlen(q, k, v, o, lse, cu_seqlens, max_seqlen, scale=None, causal=False, stream=None):
     """Packed forward: q [T,Hq,d], k/v [T,Hkv,d], o like q, lse [Hq,T]; cu_seqlens int32 on the device."""
-    T, Hq, d = q.shape
-    Hkv = k.shape[1]
+    T, Hq, d = _dims(q, "q", 3)
+    Hkv = _dims(k, "k", 3)[1]
+    kv = (T, Hkv, d)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
-    _check(load().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens),
+    _check(load().attn_fwd_varlen(_ptr(q, "q"), _ptr(k, "k", dtype=q.dtype, shape=kv),
+                                  _ptr(v, "v", dtype=q.dtype, shape=kv), _ptr(o, "o", q.numel(), q.dtype),
+                                  _ptr(lse, "lse", Hq * T, torch.float32),
+                                  _ptr(cu_seqlens, "cu_seqlens", dtype=torch.int32),
                                   cu_seqlens.numel() - 1, T, int(max_seqlen), Hq, Hkv, d, scale,
                                   int(bool(causal)), _dtype(q), _stream(stream)), "attn_fwd_varlen")
 
 
 def attn_quantize_fp8(x, x8, scales, hadamard_signs=None, stream=None):
     """x [B,H,N,d] bf16/fp16 -> x8 uint8 codes (same shape), scales [B,H,ceil(N/128)] fp32."""
-    B, H, N, d = x.shape
-    _check(load().attn_quantize_fp8(_ptr(x), _dtype(x), _ptr(x8), _ptr(scales), B, H, N, d,
-                                    _ptr(hadamard_signs), _stream(stream)), "attn_quantize_fp8")
+    B, H, N, d = _dims(x, "x", 4)
+    _check(load().attn_quantize_fp8(_ptr(x, "x"), _dtype(x), _ptr(x8, "x8", x.numel(), torch.uint8),
+                                    _ptr(scales, "scales", B * H * _nb(N), torch.float32), B, H, N, d,
+                                    _ptr(hadamard_signs, "hadamard_signs", d, torch.int8), _stream(stream)),
+           "attn_quantize_fp8")
 
 
 def attn_quantize_fp8_rope(x, x8, scales, rope_cos, rope_sin, hadamard_signs=None, stream=None):
     """RoPE (rotate-half, float32 cos/sin tables [N, d/2] on the device), then
     the optional rotation and block quantisation, in one pass."""
-    B, H, N, d = x.shape
-    _check(load().attn_quantize_fp8_rope(_ptr(x), _dtype(x), _ptr(x8), _ptr(scales), B, H, N, d, _ptr(rope_cos),
-                                         _ptr(rope_sin), _ptr(hadamard_signs), _stream(stream)),
+    B, H, N, d = _dims(x, "x", 4)
+    _check(load().attn_quantize_fp8_rope(_ptr(x, "x"), _dtype(x), _ptr(x8, "x8", x.numel(), torch.uint8),
+                                         _ptr(scales, "scales", B * H * _nb(N), torch.float32), B, H, N, d,
+                                         _ptr(rope_cos, "rope_cos", N * (d // 2), torch.float32),
+                                         _ptr(rope_sin, "rope_sin", N * (d // 2), torch.float32),
+                                         _ptr(hadamard_signs, "hadamard_signs", d, torch.int8), _stream(stream)),
            "attn_quantize_fp8_rope")
 
 
 def attn_fwd_fp8(q8, k8, v8, sq, sk, sv, o, lse, scale=None, causal=False, stream=None):
     """FP8 forward on E4M3 codes (uint8) with block factors; o bf16, lse fp32."""
-    B, Hq, N, d = q8.shape
-    Hkv = k8.shape[1]
+    B, Hq, N, d = _dims(q8, "q8", 4)
+    Hkv = _dims(k8, "k8", 4)[1]
+    kv = (B, Hkv, N, d)
+    u8, f32 = torch.uint8, torch.float32
     scale = 1.0 / math.sqrt(d) if scale is None else scale
-    _check(load().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(sq), _ptr(sk), _ptr(sv), _ptr(o), _ptr(lse),
+    _check(load().attn_fwd_fp8(_ptr(q8, "q8", dtype=u8), _ptr(k8, "k8", dtype=u8, shape=kv),
+                               _ptr(v8, "v8", dtype=u8, shape=kv), _ptr(sq, "sq", B * Hq * _nb(N), f32),
+                               _ptr(sk, "sk", B * Hkv * _nb(N), f32), _ptr(sv, "sv", B * Hkv * _nb(N), f32),
+                               _ptr(o, "o", q8.numel(), torch.bfloat16), _ptr(lse, "lse", B * Hq * N, f32),
                                B, Hq, Hkv, N, d, scale, int(bool(causal)), _stream(stream)), "attn_fwd_fp8")
 
 
@@ -172,11 +240,17 @@ def attn_decode_fp8(q8, sq, k8, v8, sk, sv, o, lse, workspace, num_splits, seqle
     """One decoded token per sequence: q8 [B,Hq,d] codes, sq [B,Hkv]; cache k8/v8
     [B,Hkv,Nmax,d] with sk/sv [B,Hkv,ceil(Nmax/128)]; seqlens int32 [B] or None;
     o [B,Hq,d] bf16, lse [B,Hq]."""
-    B, Hq, d = q8.shape
-    _, Hkv, Nmax, _ = k8.shape
+    B, Hq, d = _dims(q8, "q8", 3)
+    Hkv, Nmax = _dims(k8, "k8", 4)[1:3]
+    kv = (B, Hkv, Nmax, d)
+    u8, f32 = torch.uint8, torch.float32
     scale = 1.0 / math.sqrt(d) if scale is None else scale
-    _check(load().attn_decode_fp8(_ptr(q8), _ptr(sq), _ptr(k8), _ptr(v8), _ptr(sk), _ptr(sv), _ptr(seqlens), _ptr(o),
-                                  _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+    _check(load().attn_decode_fp8(_ptr(q8, "q8", dtype=u8), _ptr(sq, "sq", B * Hkv, f32),
+                                  _ptr(k8, "k8", dtype=u8, shape=kv), _ptr(v8, "v8", dtype=u8, shape=kv),
+                                  _ptr(sk, "sk", B * Hkv * _nb(Nmax), f32), _ptr(sv, "sv", B * Hkv * _nb(Nmax), f32),
+                                  _ptr(seqlens, "seqlens", B, torch.int32), _ptr(o, "o", B * Hq * d, torch.bfloat16),
+                                  _ptr(lse, "lse", B * Hq, f32), _ptr(workspace, "workspace"),
+                                  workspace.numel() * workspace.element_size(),
                                   B, Hq, Hkv, Nmax, d, scale, int(num_splits), _stream(stream)), "attn_decode_fp8")
 
 
@@ -186,22 +260,22 @@ def attn_bwd_workspace_size(B, Hq, Hkv, N, d):
 
 def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, scale=None, causal=False, stream=None):
     """Dense backward; workspace is a byte tensor of at least attn_bwd_workspace_size bytes."""
-    B, Hq, N, d = q.shape
-    Hkv = k.shape[1]
+    B, Hq, N, d = _dims(q, "q", 4)
+    Hkv = _dims(k, "k", 4)[1]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
-    _check(load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
-                           _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(),
+    _check(load().attn_bwd(*_bwd_ptrs(q, k, v, o, lse, dout, dq, dk, dv), _ptr(workspace, "workspace"),
+                           workspace.numel() * workspace.element_size(),
                            B, Hq, Hkv, N, d, scale, int(bool(causal)), _dtype(q), _stream(stream)), "attn_bwd")
 
 
 def attn_bwd_window(q, k, v, o, lse, dout, dq, dk, dv, workspace, window, scale=None, stream=None):
     """Dense backward with the key window of attn_fwd_window."""
-    B, Hq, N, d = q.shape
-    Hkv = k.shape[1]
+    B, Hq, N, d = _dims(q, "q", 4)
+    Hkv = _dims(k, "k", 4)[1]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     left, right = (int(w) for w in window)
-    _check(load().attn_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
-                                  _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(),
+    _check(load().attn_bwd_window(*_bwd_ptrs(q, k, v, o, lse, dout, dq, dk, dv), _ptr(workspace, "workspace"),
+                                  workspace.numel() * workspace.element_size(),
                                   B, Hq, Hkv, N, d, scale, left, right, _dtype(q), _stream(stream)),
            "attn_bwd_window")
 
@@ -215,14 +289,13 @@ def attn_bwd_deterministic(q, k, v, o, lse, dout, dq, dk, dv, workspace, window=
     """Dense backward with one writer and one summation order per output
     element (identical bits on every call); window as attn_fwd_window, and
     causal=True means the window (-1, 0)."""
-    B, Hq, N, d = q.shape
-    Hkv = k.shape[1]
+    B, Hq, N, d = _dims(q, "q", 4)
+    Hkv = _dims(k, "k", 4)[1]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     left, right = (int(w) for w in window)
     if causal:
         right = 0 if right < 0 else min(right, 0)
-    _check(load().attn_bwd_deterministic(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
-                                         _ptr(dk), _ptr(dv), _ptr(workspace),
+    _check(load().attn_bwd_deterministic(*_bwd_ptrs(q, k, v, o, lse, dout, dq, dk, dv), _ptr(workspace, "workspace"),
                                          workspace.numel() * workspace.element_size(),
                                          B, Hq, Hkv, N, d, scale, left, right, _dtype(q), _stream(stream)),
            "attn_bwd_deterministic")
@@ -234,12 +307,11 @@ def attn_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, scale=None, causal=False
     For callers that cannot allocate device memory; see include/libattn.h.
     Calls that overlap on the GPU share that workspace and must not be issued.
     """
-    B, Hq, N, d = q.shape
-    Hkv = k.shape[1]
+    B, Hq, N, d = _dims(q, "q", 4)
+    Hkv = _dims(k, "k", 4)[1]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
-    _check(load().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
-                                   _ptr(dv), B, Hq, Hkv, N, d, scale, int(bool(causal)), _dtype(q),
-                                   _stream(stream)), "attn_bwd_noalloc")
+    _check(load().attn_bwd_noalloc(*_bwd_ptrs(q, k, v, o, lse, dout, dq, dk, dv), B, Hq, Hkv, N, d, scale,
+                                   int(bool(causal)), _dtype(q), _stream(stream)), "attn_bwd_noalloc")
 
 
 def attn_bwd_varlen_workspace_size(T, Hq, Hkv, d):
@@ -248,13 +320,18 @@ def attn_bwd_varlen_workspace_size(T, Hq, Hkv, d):
 
 def attn_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, workspace, cu_seqlens, max_seqlen, scale=None,
                     causal=False, stream=None):
-    T, Hq, d = q.shape
-    Hkv = k.shape[1]
+    T, Hq, d = _dims(q, "q", 3)
+    Hkv = _dims(k, "k", 3)[1]
+    kv, dt = (T, Hkv, d), q.dtype
     scale = 1.0 / math.sqrt(d) if scale is None else scale
-    _check(load().attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
-                                  _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(),
-                                  _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, int(max_seqlen), Hq, Hkv, d, scale,
-                                  int(bool(causal)), _dtype(q), _stream(stream)), "attn_bwd_varlen")
+    _check(load().attn_bwd_varlen(_ptr(q, "q"), _ptr(k, "k", dtype=dt, shape=kv), _ptr(v, "v", dtype=dt, shape=kv),
+                                  _ptr(o, "o", q.numel(), dt), _ptr(lse, "lse", Hq * T, torch.float32),
+                                  _ptr(dout, "dout", q.numel(), dt), _ptr(dq, "dq", q.numel(), dt),
+                                  _ptr(dk, "dk", k.numel(), dt), _ptr(dv, "dv", k.numel(), dt),
+                                  _ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+                                  _ptr(cu_seqlens, "cu_seqlens", dtype=torch.int32), cu_seqlens.numel() - 1, T,
+                                  int(max_seqlen), Hq, Hkv, d, scale, int(bool(causal)), _dtype(q), _stream(stream)),
+           "attn_bwd_varlen")
 
 
 def attn_get_device_status(stream=None):
