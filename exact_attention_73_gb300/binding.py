@@ -1,8 +1,9 @@
 """ctypes binding of libattn: the C entry points under the same names.
 
-Argument marshalling only: tensors become device pointers and sizes, the
-current torch stream becomes the stream handle, and a non-OK status raises
-``AttnError``. Every step of the computation runs in the library's kernels;
+Argument marshalling only: tensors become device pointers and sizes (after a
+check that each is a contiguous GPU tensor of the documented element type and
+count, since the C ABI cannot see strides), the current torch stream becomes
+the stream handle, and a non-OK status raises ``AttnError``. Every step of the computation runs in the library's kernels;
 there is no other code path. The library must have been built (``build()``);
 loading fails loudly otherwise.
 """
