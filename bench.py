@@ -103,7 +103,8 @@ def job_tflops(step_flops, steps, world, ms):
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
-        m = json.load(open(p))
+        with open(p) as f:
+            m = json.load(f)
         return {"bf16_burst": m["bf16_tflops"], "bf16_sustained": m.get("bf16_tflops_sustained"),
                 "hbm_gbs": m["hbm_gbs"], "source": "measured"}
     return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
@@ -119,35 +120,49 @@ class Clocks:
         self.index = index
         self.proc = None
         self.path = None
+        self.out = None
 
     def start(self):
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
+            self.out = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
                                           "--format=csv,noheader,nounits", "-lms", "50"],
-                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
 
     def stop(self):
         if self.proc is None:
+            if self.out is not None:
+                self.out.close()
+                os.unlink(self.path)
             return None
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        rows = [r.split(",") for r in open(self.path).read().strip().splitlines() if r.strip()]
+        self.out.close()
+        with open(self.path) as f:
+            text = f.read()
         os.unlink(self.path)
-        if not rows:
-            return None
-        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if "Active" in v and "Not" not in v})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+        return parse_clock_samples(text)
+
+
+def parse_clock_samples(text):
+    """Median SM clock, the largest max clock and the throttle reasons seen in
+    nvidia-smi CSV rows (the fields of Clocks.Q, no header, no units)."""
+    rows = [r.split(",") for r in text.strip().splitlines() if r.strip()]
+    if not rows:
+        return None
+    sm = [float(r[1]) for r in rows if len(r) > 2 and r[1].strip().replace(".", "").isdigit()]
+    mx = [float(r[2]) for r in rows if len(r) > 2 and r[2].strip().replace(".", "").isdigit()]
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if "Active" in v and "Not" not in v})
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+            "reasons": reasons, "samples": len(rows)}
 
 
 def make_inputs(wl, device):

@@ -78,3 +78,15 @@ def test_reference_arm_prints_one_contract_line(workload):
     assert d["impl"] == "reference" and d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["value"] == d["value"] and d["config"]["workload"] == (workload or bench.DEFAULT)
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_clock_samples_are_parsed():
+    """nvidia-smi rows (fields of Clocks.Q): median SM clock, max clock, active reasons."""
+    text = ("0, 2070, 2070, 900.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active\n"
+            "0, 1980, 2070, 1390.1, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n"
+            "0, 2010, 2070, 1200.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active\n")
+    r = bench.parse_clock_samples(text)
+    assert r == {"sm_mhz": 2010.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    assert bench.parse_clock_samples("") is None
+    hot = bench.parse_clock_samples("0, 1500, 2070, 1400, 0x8, Active, Not Active, Active, Not Active\n")
+    assert hot["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
