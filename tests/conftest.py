@@ -13,6 +13,11 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "slow: large parity cases")
 
 
+def pytest_collection_modifyitems(config, items):
+    """The guard-canary tests run after every parity test."""
+    items.sort(key=lambda it: os.path.basename(str(it.fspath)) == "test_gpu_canaries.py")
+
+
 @pytest.fixture(scope="session")
 def lib():
     """The built C-ABI library through its Python binding (built on demand)."""
