@@ -90,3 +90,21 @@ def test_clock_samples_are_parsed():
     assert bench.parse_clock_samples("") is None
     hot = bench.parse_clock_samples("0, 1500, 2070, 1400, 0x8, Active, Not Active, Active, Not Active\n")
     assert hot["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+
+
+@pytest.mark.parametrize("workload", [None, "varlen_t129511_hq32_hkv8_d128_causal",
+                                      "decode_fp8_b16_hq32_hkv8_n32768_d128"])
+def test_reference_arm_other_ranks_exit_quietly(workload):
+    """Under a launcher with two ranks, rank 1 of the reference arm does no
+    work and prints nothing (rank 0 alone prints the line)."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--gpus", "2", "--steps", "1",
+           "--warmup", "3"]
+    if workload is not None:
+        cmd += ["--workload", workload]
+    env = dict(os.environ, RANK="1", LOCAL_RANK="1", WORLD_SIZE="2")
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=120, cwd=root, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip() == ""
