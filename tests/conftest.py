@@ -13,9 +13,16 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "slow: large parity cases")
 
 
+LAST = ("test_gpu_bench_config.py", "test_gpu_canaries.py")
+
+
 def pytest_collection_modifyitems(config, items):
-    """The guard-canary tests run after every parity test."""
-    items.sort(key=lambda it: os.path.basename(str(it.fspath)) == "test_gpu_canaries.py")
+    """The benchmark-configuration and guard-canary tests run after every
+    other test, in that order."""
+    def rank(item):
+        name = os.path.basename(str(item.fspath))
+        return LAST.index(name) + 1 if name in LAST else 0
+    items.sort(key=rank)
 
 
 @pytest.fixture(scope="session")
