@@ -116,3 +116,57 @@ def test_workspace_size_arithmetic():
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
 def test_valid_call_without_gpu_fails_loudly(lib):
     assert _fwd(lib) == 11                          # ATTN_ERR_NODEVICE, nothing launched
+
+
+C_CLIENT = r"""
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+#include "libattn.h"
+
+int main(void) {
+  int bad = 0;
+  for (int s = ATTN_OK; s <= ATTN_ERR_NODEVICE; ++s) {
+    const char* n = attn_status_string((attn_status)s);
+    printf("%d %s\n", s, n ? n : "(null)");
+    if (!n || strncmp(n, "ATTN_", 5) != 0) bad = 1;
+  }
+  printf("version %s\n", attn_version());
+  /* argument checks return before any device work; host memory stands in for device pointers */
+  static char buf[64];
+  void* p = (void*)(((uintptr_t)buf + 15) & ~(uintptr_t)15);
+  if (attn_fwd(NULL, p, p, p, (float*)p, 1, 2, 1, 8, 64, 0.125f, 0, ATTN_BF16, NULL) != ATTN_ERR_NULL) bad = 2;
+  if (attn_fwd(p, p, p, p, (float*)p, 1, 2, 1, 8, 96, 0.125f, 0, ATTN_BF16, NULL) != ATTN_ERR_HEADDIM) bad = 3;
+  if (attn_fwd(p, p, p, p, (float*)p, 1, 3, 2, 8, 64, 0.125f, 0, ATTN_BF16, NULL) != ATTN_ERR_GQA) bad = 4;
+  if (attn_fwd_fp8_kv_tile(128) != 128) bad = 5;
+  if (attn_bwd_workspace_size(2, 32, 8, 8192, 128) != (size_t)2 * 32 * 8192 * 128 * 4 + (size_t)2 * 32 * 8192 * 4)
+    bad = 6;
+  if (ATTN_BWD_NOALLOC_MAX_BYTES != 32u * 1024u * 1024u) bad = 7;
+  printf("%s %d\n", bad ? "FAIL" : "OK", bad);
+  return bad;
+}
+"""
+
+
+def test_plain_c_client_compiles_links_and_runs(lib, tmp_path):
+    """The header is plain C (gcc -std=c11 -Wall -Werror) and a C program
+    links against libattn.so and gets the documented answers without a GPU."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    from exact_attention_73_gb300 import build
+    src, exe = tmp_path / "client.c", tmp_path / "client"
+    src.write_text(C_CLIENT)
+    libdir = os.path.dirname(build.LIB)
+    r = subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-I", os.path.dirname(HEADER), str(src),
+                        "-o", str(exe), f"-L{libdir}", f"-l:{os.path.basename(build.LIB)}", f"-Wl,-rpath,{libdir}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stdout + r.stderr
+    lines = r.stdout.splitlines()
+    for code, name in binding.STATUS.items():
+        assert lines[code].split()[1].rstrip(":") == name, lines[code]
+    assert lines[-1] == "OK 0"
