@@ -380,3 +380,39 @@ def test_window_pins_catch_off_by_one():
     finally:
         A.visible = good
     assert not np.allclose(bad, ref, atol=1e-12)
+
+
+# ------------------------------------------------------- property-based check
+
+def test_random_problems_match_torch_float64():
+    """Random small problems (batch, KV heads, GQA group, length, head dim,
+    scale, causal flag and window): the oracle's O, LSE and gradients equal
+    torch's float64 SDPA with an explicit mask built by loops, its autograd,
+    and torch.logsumexp of the masked scores, to 1e-12."""
+    hyp = pytest.importorskip("hypothesis")
+    st = hyp.strategies
+
+    @hyp.settings(max_examples=40, deadline=None, derandomize=True)
+    @hyp.given(b=st.integers(1, 2), hkv=st.integers(1, 2), g=st.integers(1, 3), n=st.integers(1, 40),
+               d=st.integers(1, 9), scale=st.floats(0.05, 2.0), causal=st.booleans(),
+               left=st.integers(-1, 12), right=st.integers(-1, 12), seed=st.integers(0, 10 ** 6))
+    def check(b, hkv, g, n, d, scale, causal, left, right, seed):
+        rng = np.random.default_rng(seed)
+        q = torch.from_numpy(rng.standard_normal((b, hkv * g, n, d)))
+        k, v = (torch.from_numpy(rng.standard_normal((b, hkv, n, d))) for _ in range(2))
+        do = torch.from_numpy(rng.standard_normal((b, hkv * g, n, d)))
+        r = right if not causal else (0 if right < 0 else min(right, 0))
+        mask = torch.from_numpy(_mask_loops(n, left, r))
+        qt, kt, vt = (x.clone().requires_grad_(True) for x in (q, k, v))
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            qt, kt.repeat_interleave(g, 1), vt.repeat_interleave(g, 1), attn_mask=mask, scale=scale)
+        ref.backward(do)
+        s = scale * q @ k.repeat_interleave(g, 1).transpose(-1, -2)
+        lse_ref = torch.logsumexp(s.masked_fill(~mask, float("-inf")), dim=-1)
+        o, lse = A.forward(q, k, v, scale, causal, (left, right))
+        np.testing.assert_allclose(o, ref.detach().numpy(), atol=1e-12, rtol=0)
+        np.testing.assert_allclose(lse, lse_ref.numpy(), atol=1e-12, rtol=0)
+        for got, want in zip(A.backward(q, k, v, do, scale, causal, (left, right)), (qt.grad, kt.grad, vt.grad)):
+            np.testing.assert_allclose(got, want.numpy(), atol=1e-11, rtol=0)
+
+    check()
