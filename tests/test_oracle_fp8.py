@@ -480,3 +480,45 @@ def test_decode_splits_and_lengths_close_to_exact():
             err = o[b, kv] - ro
             assert np.sqrt((err ** 2).mean()) < 1e-2 and np.abs(err).max() < 5e-2
             assert np.abs(lse[b, kv] - rl).max() < 1e-2
+
+
+def test_random_problems_without_p_rounding_are_exact():
+    """Random small FP8 problems (GQA, ragged lengths, causal, KV tiles of 128,
+    96 or 64 keys, block factors up to 2^6 apart, rotation on or off; and the
+    split decode with random cache lengths and split sizes): with only the E4M3
+    rounding of P~ left out, the emulation equals float64 attention of the
+    dequantised inputs."""
+    hyp = pytest.importorskip("hypothesis")
+    st = hyp.strategies
+    from exact_attention_73_gb300 import inputs
+
+    @hyp.settings(max_examples=25, deadline=None, derandomize=True)
+    @hyp.given(hkv=st.integers(1, 2), g=st.integers(1, 3), n=st.integers(1, 400), d=st.sampled_from([16, 32]),
+               causal=st.booleans(), kv_tile=st.sampled_from([None, 96, 64]), rotate=st.booleans(),
+               seed=st.integers(0, 10 ** 6))
+    def forward(hkv, g, n, d, causal, kv_tile, rotate, seed):
+        q, k, v = _blocky(seed, (1, hkv * g, n, d)), _blocky(seed + 1, (1, hkv, n, d)), _blocky(seed + 2, (1, hkv, n, d))
+        s = inputs.random_signs(seed, d).numpy() if rotate else None
+        (q8, sq), (k8, sk), (v8, sv) = F.quantize_blocks(q, s), F.quantize_blocks(k, s), F.quantize_blocks(v)
+        o, lse = F.attention_fp8(q8, k8, v8, sq, sk, sv, d ** -0.5, causal, kv_tile=kv_tile, round_p=False)
+        o_ref, l_ref = A.forward(_dequantised(q8, sq), _dequantised(k8, sk), _dequantised(v8, sv), d ** -0.5, causal)
+        np.testing.assert_allclose(lse, l_ref, rtol=0, atol=1e-10)
+        np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-10 * max(1.0, np.abs(o_ref).max()))
+
+    @hyp.settings(max_examples=25, deadline=None, derandomize=True)
+    @hyp.given(b=st.integers(1, 3), g=st.integers(1, 8), nmax=st.integers(1, 700), tps=st.integers(1, 4),
+               seed=st.integers(0, 10 ** 6), data=st.data())
+    def decode(b, g, nmax, tps, seed, data):
+        lens = [data.draw(st.integers(1, nmax)) for _ in range(b)]
+        q = _blocky(seed, (b, 1, g, 16))
+        k, v = _blocky(seed + 1, (b, 1, nmax, 16)), _blocky(seed + 2, (b, 1, nmax, 16))
+        (q8, sq), (k8, sk), (v8, sv) = F.quantize_blocks(q), F.quantize_blocks(k), F.quantize_blocks(v)
+        qd, kd, vd = _dequantised(q8, sq), _dequantised(k8, sk), _dequantised(v8, sv)
+        o, lse = F.decode_fp8(q8, sq[:, :, 0], k8, v8, sk, sv, lens, 0.25, tps, round_p=False)
+        for i in range(b):
+            ro, rl, _ = A.head_forward(qd[i, 0], kd[i, 0, :lens[i]], vd[i, 0, :lens[i]], 0.25, False)
+            np.testing.assert_allclose(lse[i, 0], rl, rtol=0, atol=1e-10)
+            np.testing.assert_allclose(o[i, 0], ro, rtol=0, atol=1e-10 * max(1.0, np.abs(ro).max()))
+
+    forward()
+    decode()
