@@ -15,10 +15,13 @@ fp8       : the E4M3 codec, power-of-two block scales, the random-sign
 Parity status: every function is pinned by ``tests/test_oracle_*.py``. For
 ``fp8.attention_fp8`` and ``fp8.decode_fp8`` everything but the E4M3 rounding
 of P~ is pinned on arbitrary inputs (with ``round_p=False`` they equal float64
-attention of the dequantised inputs); which value is rounded is pinned only by
-a worked example, the saturation bound and inputs on the E4M3 grid (parity
-partly unpinned: on general inputs the rounding's effect is checked through
-the stated tolerance and the ordering against the per-tensor emulation).
+attention of the dequantised inputs). The rounding itself is pinned by worked
+examples (one per running-max rule), the saturation bound, inputs on the E4M3
+grid, and on arbitrary inputs by its own bound: every rounded entry moves by
+at most half an E4M3 step (``fp8.half_step``), so O moves by at most the
+returned E. The default running max is the one of Algorithm 1 (tau = 0);
+``STALE_MAX_TAU`` selects the stale-max variant, which differs from it only in
+which values are rounded, by at most one step per entry in total.
 ``tests/test_oracle_mutations.py`` plants mistakes in copies of both modules
 and checks that a pin fails for each.
 """

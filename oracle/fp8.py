@@ -20,16 +20,20 @@ Readings (the pages leave these open):
 * The rotation is y = fp32(FWHT_fp32(sigma o x) * fp32(1/sqrt(d))), with the
   fast Walsh-Hadamard transform taken in the textbook radix-2 order (stride
   1, 2, 4, ...), every add and subtract rounded to float32. Sylvester order.
-* The running max m of Algorithm 1 is raised only when a KV tile's row max
-  exceeds it by more than tau = 4 (log2 units, i.e. S units of 4 ln 2); then
-  P~ = exp(S - m) <= 2^4, O and l are rescaled as in Algorithm 1, and the
-  result is unchanged in exact arithmetic.
+* The running max m is the one of Algorithm 1: m_new = max(m_old, rowmax S_j)
+  at every KV tile (``tau = 0``, the default). ``tau > 0`` selects the
+  stale-max variant (STALE_MAX_TAU): m is raised only when a tile's row max
+  exceeds it by more than tau log2 units, so P~ = exp(S - m) <= 2^tau and O
+  is rescaled less often. Both give the same result in exact arithmetic; they
+  differ only in which values are rounded to E4M3, by at most one E4M3 step
+  per entry of P~ (half a step on each side, see ``half_step``).
 * The V factor of KV tile j, sv_j = 2^f_j, is folded into P~ before its
   E4M3 rounding, relative to F, the running maximum of f over the tiles seen
   so far: P~ enters the second product as e4m3(P~ * 2^(4 + f_j - F)), and
   the accumulated O is multiplied by 2^(F_old - F_new) whenever F grows (the
   same correction as for the running row max m). The rounded value lies in
-  (0, 256]. At the end O = O_acc * 2^(F - 4) / l; l sums the unrounded P~.
+  (0, 2^(4 + tau)]. At the end O = O_acc * 2^(F - 4) / l; l sums the
+  unrounded P~.
   The KV tile (Bc keys) need not equal the quantisation block: a tile that
   spans two blocks gives each key its own block's K and V factors, and F is
   raised once per tile, to the largest f among the tile's keys.
@@ -51,6 +55,10 @@ import numpy as np
 
 E4M3_MAX = 448.0
 BLOCK = 128
+# Stale-max variant of the running max (log2 units): m moves only when a
+# tile's row max exceeds it by more than this. Not the pages' rule (tau = 0);
+# it changes which values are rounded to E4M3, not the exact result.
+STALE_MAX_TAU = 4.0
 
 
 def e4m3_decode(codes):
@@ -82,6 +90,15 @@ def e4m3_encode(x):
     code = code + np.where(neg, 128, 0)
     code = np.where(nan, 0x7F, code)
     return code.astype(np.uint8)
+
+
+def half_step(x):
+    """Largest rounding error of e4m3_encode at x >= 0 (below saturation):
+    half the spacing of the E4M3 grid in the binade of x, 2^(e - 4) for
+    x in [2^e, 2^(e+1)) with e >= -6, and 2^-10 in the subnormal range."""
+    x = np.asarray(x, dtype=np.float64)
+    _, ex = np.frexp(np.where(x > 0, x, 1.0))     # x = mant * 2^ex, mant in [0.5, 1)
+    return np.where(x >= 2.0 ** -6, np.exp2(ex - 5.0), 2.0 ** -10)
 
 
 def pow2_exponent(amax):
@@ -216,7 +233,7 @@ def quantize_tensor(x, signs=None, block=BLOCK):
 
 
 def _fp8_rows(qrows, q_fac, kf, vf, sk, sv, tiles, n, scale, causal=False, rows=None, block=BLOCK, p_shift=4,
-              tau=4.0, kv_tile=None, round_p=True):
+              tau=0.0, kv_tile=None, round_p=True, bound=False):
     """Algorithm 1 in its FP8 form for query rows ``qrows`` [R, d] (decoded,
     with per-row factors q_fac) over the key tiles ``tiles`` (indices of tiles
     of kv_tile keys, in order) of one KV head: kf/vf [N, d] decoded, sk/sv the
@@ -224,12 +241,15 @@ def _fp8_rows(qrows, q_fac, kf, vf, sk, sv, tiles, n, scale, causal=False, rows=
     each key takes its own block's factors, and F is raised to the largest V
     exponent among the tile's keys. Starts from m = -inf, l = 0, O = 0.
     ``round_p=False`` leaves out the E4M3 rounding of P~ (for pins: the rest
-    is then exact). Returns (O [R, d], LSE [R])."""
+    is then exact). Returns (O [R, d], LSE [R]); with ``bound`` also E [R, d],
+    the sum over keys of each rounded entry's half_step times |V|, carried
+    through the same corrections as O: |O - O_unrounded| <= E elementwise."""
     kv_tile = block if kv_tile is None else kv_tile
     d = qrows.shape[1]
     m = np.full(len(qrows), -np.inf)
     l = np.zeros(len(qrows))
     acc = np.zeros((len(qrows), d))
+    err = np.zeros((len(qrows), d))
     f_run = -np.inf
     for j in tiles:
         cols = np.arange(j * kv_tile, min(n, (j + 1) * kv_tile))
@@ -238,7 +258,7 @@ def _fp8_rows(qrows, q_fac, kf, vf, sk, sv, tiles, n, scale, causal=False, rows=
         if causal:
             s = np.where(cols[None, :] > rows[:, None], -np.inf, s)
         mx = s.max(axis=1)
-        m_new = np.where(mx > m + tau * np.log(2.0), mx, m)   # stale max within 2^tau
+        m_new = np.where(mx > m + tau * np.log(2.0), mx, m)   # tau = 0: the running max itself
         m_use = np.where(np.isfinite(m_new), m_new, 0.0)
         corr = np.exp(m - m_use)
         f_c = np.log2(sv[blk])                                # V exponent of each key
@@ -247,15 +267,20 @@ def _fp8_rows(qrows, q_fac, kf, vf, sk, sv, tiles, n, scale, causal=False, rows=
         pt = np.exp(s - m_use[:, None])
         l = corr * l + pt.sum(axis=1)
         p8 = pt * np.exp2(p_shift + f_c - f_new)[None, :]
+        hs = half_step(p8)
         if round_p:
             p8 = e4m3_decode(e4m3_encode(p8))
         acc = (corr * v_corr)[:, None] * acc + p8 @ vf[cols]
+        err = (corr * v_corr)[:, None] * err + hs @ np.abs(vf[cols])
         m, f_run = m_new, f_new
-    return acc * np.exp2(f_run - p_shift) / l[:, None], m + np.log(l)
+    out = acc * np.exp2(f_run - p_shift) / l[:, None], m + np.log(l)
+    if bound:
+        return out + (err * np.exp2(f_run - p_shift) / l[:, None],)
+    return out
 
 
-def attention_fp8(q8, k8, v8, sq, sk, sv, scale, causal=False, block=BLOCK, p_shift=4, tau=4.0, heads=None,
-                  rows=None, kv_tile=None, round_p=True):
+def attention_fp8(q8, k8, v8, sq, sk, sv, scale, causal=False, block=BLOCK, p_shift=4, tau=0.0, heads=None,
+                  rows=None, kv_tile=None, round_p=True, bound=False):
     """FP8 forward following Algorithm 1 tile by tile (Bc = kv_tile keys per
     tile, by default the quantisation block; the stale max and the V exponent
     F move at tile granularity, so the E4M3 rounding of P~ depends on it).
@@ -266,22 +291,26 @@ def attention_fp8(q8, k8, v8, sq, sk, sv, scale, causal=False, block=BLOCK, p_sh
     ``heads`` (list of (b, h)) and ``rows`` restrict the work to those query
     heads and rows (rows are independent); other entries are left as NaN.
     ``round_p=False`` leaves out the E4M3 rounding of P~ (for pins).
+    ``tau`` = 0 is the running max of Algorithm 1; STALE_MAX_TAU the stale-max
+    variant. With ``bound`` a third array E (like O) bounds the effect of the
+    E4M3 rounding of P~: |O - O(round_p=False)| <= E elementwise.
     """
     qf, kf, vf = e4m3_decode(q8), e4m3_decode(k8), e4m3_decode(v8)
     sq, sk, sv = (np.asarray(a, dtype=np.float64) for a in (sq, sk, sv))
     b_, hq, n, d = qf.shape
     g = hq // kf.shape[1]
     o = np.full(qf.shape, np.nan)
+    e = np.full(qf.shape, np.nan)
     lse = np.full((b_, hq, n), np.nan)
     rows = np.arange(n) if rows is None else np.asarray(rows)
     heads = [(b, h) for b in range(b_) for h in range(hq)] if heads is None else heads
     kvt = block if kv_tile is None else kv_tile
     for b, h in heads:
         kv = h // g
-        o[b, h, rows], lse[b, h, rows] = _fp8_rows(
+        o[b, h, rows], lse[b, h, rows], e[b, h, rows] = _fp8_rows(
             qf[b, h, rows], sq[b, h, rows // block], kf[b, kv], vf[b, kv], sk[b, kv], sv[b, kv],
-            range((n + kvt - 1) // kvt), n, scale, causal, rows, block, p_shift, tau, kvt, round_p)
-    return o, lse
+            range((n + kvt - 1) // kvt), n, scale, causal, rows, block, p_shift, tau, kvt, round_p, bound=True)
+    return (o, lse, e) if bound else (o, lse)
 
 
 def combine_splits(o_parts, lse_parts):
@@ -297,7 +326,7 @@ def combine_splits(o_parts, lse_parts):
     return o, mx + np.log(tot)
 
 
-def decode_fp8(q8, sq, k8, v8, sk, sv, lens, scale, tiles_per_split, block=BLOCK, p_shift=4, tau=4.0,
+def decode_fp8(q8, sq, k8, v8, sk, sv, lens, scale, tiles_per_split, block=BLOCK, p_shift=4, tau=0.0,
                round_p=True):
     """FP8 decode over a block-quantised KV cache, split by key tiles.
 

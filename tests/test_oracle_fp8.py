@@ -253,13 +253,16 @@ def test_fp8_p_rounding_worked_example():
     np.testing.assert_allclose(lse[0, 0], math.log(4 / 3), rtol=0, atol=1e-15)
 
 
+@pytest.mark.parametrize("tau", [0.0, F.STALE_MAX_TAU])
 @pytest.mark.parametrize("jump", [2.5, 3.5, 6.0])
-def test_fp8_attention_running_max_keeps_p_below_its_shift(jump):
-    """The running max moves only when a tile's row max exceeds it by more than
-    4 log2 units (4 ln 2 ~ 2.77 in score units), so P~ <= 2^4 and P~ * 2^4
-    never reaches E4M3's saturation at 448. Scores: one key at 0 in tile 0, one
-    key at `jump` in tile 1, every other key at -96 (weight below e^-90). With
-    V = 1 the exact output is 1; a saturated P~ would lose over 10 %."""
+def test_fp8_attention_running_max_keeps_p_below_its_shift(jump, tau):
+    """With the running max of Algorithm 1 (tau = 0) P~ <= 1; in the stale-max
+    variant the max moves only when a tile's row max exceeds it by more than
+    4 log2 units (4 ln 2 ~ 2.77 in score units), so P~ <= 2^4. Either way
+    P~ * 2^4 never reaches E4M3's saturation at 448. Scores: one key at 0 in
+    tile 0, one key at `jump` in tile 1, every other key at -96 (weight below
+    e^-90). With V = 1 the exact output is 1; a saturated P~ would lose over
+    10 %."""
     n, d = 256, 16
     q = np.zeros((1, 1, n, d))
     q[..., 0] = 1.0
@@ -268,9 +271,91 @@ def test_fp8_attention_running_max_keeps_p_below_its_shift(jump):
     k[0, 0, 128, 0] = jump
     v = np.ones((1, 1, n, d))
     ones = np.ones((1, 1, 2))
-    o, lse = F.attention_fp8(F.e4m3_encode(q), F.e4m3_encode(k), F.e4m3_encode(v), ones, ones, ones, 1.0, False)
+    o, lse = F.attention_fp8(F.e4m3_encode(q), F.e4m3_encode(k), F.e4m3_encode(v), ones, ones, ones, 1.0, False,
+                             tau=tau)
     assert abs(lse - np.log(1.0 + np.exp(jump))).max() < 1e-12
     assert np.abs(o - 1.0).max() < 2 ** -4
+
+
+def test_fp8_running_max_worked_example():
+    """Which value is rounded to E4M3 depends on the running max. Scale
+    ln(5/3), q = e_0; key 0 (tile 0) has k = 0, key 128 (tile 1) has k = e_0,
+    every other key k = -96 e_0 (weight below e^-49); V_0 = e_0, V_128 = e_1,
+    other rows 0. Scores 0 and ln(5/3), exact O = (3/8, 5/8).
+    * Algorithm 1's running max (the default): tile 1 raises m to ln(5/3), so
+      both rounded values are P~ * 2^4 = 16, exact, and O = (3/8, 5/8).
+    * Stale max (tau = 4): m stays 0, key 128 enters as 16 * 5/3 = 26.67,
+      which E4M3 (step 2 in [16, 32)) rounds to 26; l = 8/3 is unrounded, so
+      O = (16/16, 26/16) * 3/8 = (3/8, 39/64).
+    The rounding bound E sums each rounded entry's half step (1 in [16, 32))
+    times |V|, scaled like O: running max (3/5 e_0 + e_1) / 16 / (8/5) =
+    (3/128, 5/128), the tile-0 term carrying the correction 3/5; stale max
+    (e_0 + e_1) / 16 / (8/3) = (3/128, 3/128)."""
+    n, d = 129, 16
+    q = np.zeros((1, 1, n, d)); q[..., 0] = 1.0
+    k = np.zeros((1, 1, n, d)); k[0, 0, 1:, 0] = -96.0; k[0, 0, 128, 0] = 1.0
+    v = np.zeros((1, 1, n, d)); v[0, 0, 0, 0] = 1.0; v[0, 0, 128, 1] = 1.0
+    ones = np.ones((1, 1, 2))
+    enc = F.e4m3_encode
+    args = (enc(q), enc(k), enc(v), ones, ones, ones, math.log(5.0 / 3.0), False)
+    for tau, want, bound in ((None, (3 / 8, 5 / 8), (3 / 128, 5 / 128)), (0.0, (3 / 8, 5 / 8), (3 / 128, 5 / 128)),
+                             (F.STALE_MAX_TAU, (3 / 8, 39 / 64), (3 / 128, 3 / 128))):
+        kw = {} if tau is None else {"tau": tau}
+        o, lse, e = F.attention_fp8(*args, bound=True, **kw)
+        np.testing.assert_allclose(o[0, 0, :, :2], np.tile(want, (n, 1)), rtol=0, atol=1e-15)
+        np.testing.assert_allclose(o[0, 0, :, 2:], 0.0, rtol=0, atol=0)
+        np.testing.assert_allclose(lse[0, 0], math.log(8.0 / 3.0), rtol=0, atol=1e-14)
+        np.testing.assert_allclose(e[0, 0, :, :2], np.tile(bound, (n, 1)), rtol=1e-12, atol=0)
+
+
+def test_half_step_bounds_e4m3_rounding():
+    """half_step(x) is the largest error of the E4M3 rounding at x: every
+    random value rounds within it, and every midpoint between two neighbouring
+    codes (below saturation) lies exactly half a step from both."""
+    rng = np.random.default_rng(80)
+    x = np.exp2(rng.uniform(-14, 8.7, 200000))
+    err = np.abs(F.e4m3_decode(F.e4m3_encode(x)) - x)
+    assert np.all(err <= F.half_step(x))
+    c = _finite_codes()
+    pos = np.sort(F.e4m3_decode(c[c < 128]))
+    mids = (pos[:-1] + pos[1:]) / 2
+    np.testing.assert_array_equal(F.half_step(mids), (pos[1:] - pos[:-1]) / 2)
+    # and the bound is reached: the largest observed error per binade is the half step
+    assert np.isclose(err.max() / F.half_step(x[np.argmax(err)]), 1.0, rtol=1e-3)
+
+
+def _outlier_codes(causal_seed=3, n=1024, d=128, additive=False):
+    from exact_attention_73_gb300 import inputs
+    q, k, v = inputs.outliers(causal_seed, [(1, 2, n, d)] * 3, additive=additive)
+    signs = inputs.random_signs(4, d).numpy()
+    (q8, sq), (k8, sk), (v8, sv) = F.quantize_blocks(q, signs), F.quantize_blocks(k, signs), F.quantize_blocks(v)
+    return q8, k8, v8, sq, sk, sv
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("additive", [False, True])
+def test_running_max_and_stale_max_differ_by_at_most_one_step_per_entry(causal, additive):
+    """The outlier accuracy configuration (0.1 % outliers of std 10, rotation
+    on, B=1, H=2, N=1024, d=128): the rounding of P~ under either running max
+    stays within half an E4M3 step per entry of the unrounded result (the E
+    each emulation returns), so the two emulations differ by at most E_0 + E_4
+    elementwise -- one step per entry in total. In exact arithmetic they are
+    the same; the bound is reached only if every entry's error has the same
+    sign, so in practice the gap is far below it."""
+    codes = _outlier_codes(additive=additive)
+    d = codes[0].shape[-1]
+    o0, l0, e0 = F.attention_fp8(*codes, d ** -0.5, causal, bound=True)
+    o4, l4, e4 = F.attention_fp8(*codes, d ** -0.5, causal, tau=F.STALE_MAX_TAU, bound=True)
+    ou, lu = F.attention_fp8(*codes, d ** -0.5, causal, round_p=False)
+    np.testing.assert_allclose(l0, lu, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l4, lu, rtol=0, atol=1e-12)
+    tiny = 1e-12 * np.abs(ou).max()
+    assert np.all(np.abs(o0 - ou) <= e0 + tiny)
+    assert np.all(np.abs(o4 - ou) <= e4 + tiny)
+    gap = np.abs(o0 - o4)
+    assert np.all(gap <= e0 + e4 + tiny)
+    assert 0 < gap.max()                                       # the two rules do round different values
+    assert math.sqrt((gap ** 2).mean()) < 0.25 * math.sqrt(((e0 + e4) ** 2).mean())
 
 
 def _emulated_rms(q, k, v, signs, quant, causal=False, rows=slice(None)):

@@ -146,10 +146,15 @@ FP8_MUTANTS = {
     "O not rescaled when m grows": ("acc = (corr * v_corr)[:, None] * acc + p8 @ vf[cols]",
                                     "acc = v_corr * acc + p8 @ vf[cols]"),
     "l not rescaled when m grows": ("l = corr * l + pt.sum(axis=1)", "l = l + pt.sum(axis=1)"),
-    "P shift not undone": ("return acc * np.exp2(f_run - p_shift) / l[:, None], m + np.log(l)",
-                           "return acc * np.exp2(f_run) / l[:, None], m + np.log(l)"),
+    "P shift not undone": ("out = acc * np.exp2(f_run - p_shift) / l[:, None], m + np.log(l)",
+                           "out = acc * np.exp2(f_run) / l[:, None], m + np.log(l)"),
     "stale-max threshold in the wrong units": ("m_new = np.where(mx > m + tau * np.log(2.0), mx, m)",
                                               "m_new = np.where(mx > m + tau, mx, m)"),
+    "stale running max as the default": ("p_shift=4, tau=0.0, heads=None,", "p_shift=4, tau=STALE_MAX_TAU, heads=None,"),
+    "half step a binade too small": ("return np.where(x >= 2.0 ** -6, np.exp2(ex - 5.0), 2.0 ** -10)",
+                                     "return np.where(x >= 2.0 ** -6, np.exp2(ex - 6.0), 2.0 ** -10)"),
+    "rounding bound not rescaled with O": ("err = (corr * v_corr)[:, None] * err + hs @ np.abs(vf[cols])",
+                                           "err = err + hs @ np.abs(vf[cols])"),
     "V factor taken per tile, not per key": ("p8 = pt * np.exp2(p_shift + f_c - f_new)[None, :]",
                                              "p8 = pt * np.exp2(p_shift + f_c.max() - f_new)"),
     "P~ not rounded to E4M3": ("        if round_p:\n            p8 = e4m3_decode(e4m3_encode(p8))",
