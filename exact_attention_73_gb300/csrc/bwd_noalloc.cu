@@ -15,6 +15,11 @@
 // a stand-in symbol, not a device address), so the first call on each device
 // looks up its device address with cudaGetSymbolAddress while that device is
 // current, and caches it. Make that first call before any stream capture.
+// With lazy module loading (CUDA's default) that lookup is also when the
+// driver loads this file's module and reserves the array on the device, so
+// the first call can fail with ATTN_ERR_CUDA if the device is already full:
+// callers whose memory pool takes nearly all of HBM should make one call at
+// start-up, before the pool reserves its memory.
 // All calls share the one array: calls whose kernels overlap on the GPU (two
 // streams, or two host threads) race on it and give wrong results. The
 // backward's first kernel clears the dQ accumulator and writes D, so nothing
@@ -63,6 +68,9 @@ extern "C" attn_status attn_bwd_noalloc(const void* q, const void* k, const void
   attn_status s = attn::bwd_check_dense(q, k, v, o, lse, dout, dq, dk, dv, q, kScratchBytes, B, Hq, Hkv, N, d,
                                         dtype);
   if (s != ATTN_OK) return s;
+  // a device that is not sm_103 is reported as every other entry point does
+  int* status = nullptr;
+  if ((s = attn::device_context(&status)) != ATTN_OK) return s;
   void* ws = nullptr;
   if ((s = scratch_on_current_device(&ws)) != ATTN_OK) return s;
   return attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, ws, kScratchBytes, B, Hq, Hkv, N, d, scale, causal, dtype,

@@ -260,8 +260,12 @@ ATTN_API attn_status attn_bwd_deterministic(const void* q, const void* k, const 
  * exceeds that returns ATTN_ERR_WORKSPACE before any device work, and every
  * other argument error returns attn_bwd's code, also before any device work.
  * The first call on a device looks up the array's device address (do it
- * before any stream capture). All calls share the array: calls that overlap
- * on the GPU race and must not be issued. Nothing is allocated or freed.
+ * before any stream capture). Under lazy module loading (CUDA's default) that
+ * first call is also when the driver reserves the array on the device, so it
+ * can fail with ATTN_ERR_CUDA on a device that is already full: make one call
+ * at start-up, before a memory pool reserves the device's memory. All calls
+ * share the array: calls that overlap on the GPU race and must not be issued.
+ * The entry point itself allocates and frees nothing.
  */
 ATTN_API attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                                       const float* lse, const void* dout,

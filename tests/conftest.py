@@ -13,12 +13,12 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "slow: large parity cases")
 
 
-LAST = ("test_gpu_bench_config.py", "test_gpu_canaries.py")
+LAST = ("test_gpu_bench_config.py", "test_gpu_canaries.py", "test_zz_no_alloc.py")
 
 
 def pytest_collection_modifyitems(config, items):
-    """The benchmark-configuration and guard-canary tests run after every
-    other test, in that order."""
+    """The benchmark-configuration, guard-canary and allocation-free backward
+    tests run after every other test, in that order."""
     def rank(item):
         name = os.path.basename(str(item.fspath))
         return LAST.index(name) + 1 if name in LAST else 0

@@ -7,7 +7,9 @@ These tests check, through the C ABI, that it returns what attn_bwd returns
 with a caller-provided workspace, on two calls in a row (the shared array keeps
 the previous call's contents, so the second call also checks that nothing
 carries over), and that oversized problems are refused.
-This file is collected last on purpose.
+The test session runs this file last (tests/conftest.py orders it after
+every other file), so a run that stops at its first failure has already run
+every other test when one of these fails.
 """
 import ctypes as C
 
@@ -44,7 +46,8 @@ def _case(seed, B, Hq, Hkv, N, causal):
 
 @pytest.mark.gpu
 def test_noalloc_backward_matches_workspace_backward_on_two_calls():
-    cases = [(31, 1, 4, 2, 1000, True), (32, 1, 8, 4, 4096, False)]
+    # the last case needs 33,552,384 of the array's 33,554,432 bytes
+    cases = [(31, 1, 4, 2, 1000, True), (32, 1, 8, 4, 4096, False), (33, 1, 16, 4, 4064, True)]
     for seed, B, Hq, Hkv, N, causal in cases:
         assert L.attn_bwd_workspace_size(B, Hq, Hkv, N, 128) <= MAX_BYTES
         args, ref = _case(seed, B, Hq, Hkv, N, causal)
@@ -54,6 +57,20 @@ def test_noalloc_backward_matches_workspace_backward_on_two_calls():
         assert L.attn_get_device_status() == 0
         for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
             assert rel_rms(g, r) <= 1e-2, (name, seed, rel_rms(g, r))
+
+
+@pytest.mark.gpu
+def test_noalloc_refuses_oversized_problem_on_a_gpu():
+    """Where the array is actually loaded: a problem one row too large for it
+    is refused with ATTN_ERR_WORKSPACE before any device work (the pointers
+    are aligned stand-ins that are never dereferenced)."""
+    lib = L.load()
+    P = C.c_void_p
+    args = [P(256)] * 9
+    assert L.attn_bwd_workspace_size(1, 16, 4, 4065, 128) > MAX_BYTES
+    assert lib.attn_bwd_noalloc(*args, 1, 16, 4, 4065, 128, 0.1, 1, 0, None) == 7
+    assert lib.attn_bwd_noalloc(*args, 2, 32, 8, 8192, 128, 0.1, 1, 0, None) == 7
+    assert L.attn_get_device_status() == 0
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="argument check only, run where no GPU is present")
