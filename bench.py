@@ -47,6 +47,9 @@ WORKLOADS = {
     "gqa_b2_hq32_hkv8_n8192_causal": (2, 32, 8, 8192, 128, True, None),
     # same token count as the default, shorter rows: the size used for ncu --set full captures
     "bf16_b4_h16_n4096": (4, 16, 16, 4096, 128, False, None),
+    # other points of the BF16 sweep (B*N = 16384 tokens): the memory-bound short rows and head dim 64
+    "bf16_sweep_d128_n512": (32, 16, 16, 512, 128, False, None),
+    "bf16_sweep_d64_n8192": (2, 32, 32, 8192, 64, False, None),
     # sliding window: each query sees itself and the 1024 keys before it
     "window_b1_h16_n16384_w1024": (1, 16, 16, 16384, 128, False, (1024, 0)),
 }
@@ -63,6 +66,10 @@ VARLEN_WORKLOADS = {
     "varlen_t129511_hq32_hkv8_d128_causal": (18, 8, 32, 8, 128),
 }
 LAUNCHES_PER_STEP = 8   # fwd 1, bwd 3, quantise 3, fp8 fwd 1
+# The FP8 accuracy configuration, timed on its own inputs after the step:
+# B=4, H=16, N=8192, d=128, N(0,1) with 0.1 % of entries replaced by
+# N(0, 10^2) (seed 3), Q and K rotated with the random signs of seed 4.
+FP8_CONFIG = (4, 16, 8192, 128)
 
 
 def visible_pairs(N, left, right):
@@ -128,7 +135,7 @@ class Clocks:
             os.close(fd)
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=self.out, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -260,7 +267,6 @@ def bench_ours(args, wl, rank, world):
         step(marks[s])
     t1.record(stream)
     barrier()
-    clk = clocks.stop()
     ms_total = t0.elapsed_time(t1)
     stage = {n: sum(m[i].elapsed_time(m[i + 1]) for m in marks) / args.steps
              for i, n in enumerate(("fwd", "bwd", "quant", "fwd_fp8"))}
@@ -322,9 +328,52 @@ def bench_ours(args, wl, rank, world):
     if L.attn_get_device_status() != 0:
         raise RuntimeError("device-side wait timed out during the end-to-end run")
 
+    fp8cfg = None
+    if window is None:
+        fp8cfg = time_fp8_config(L, dev, stream, args.steps, barrier)
+    clk = clocks.stop()
     ms_total, ms_e2e = max_over_ranks([ms_total, ms_e2e], world, dev)
     return {"ms_total": ms_total, "ms_e2e": ms_e2e, "stage_ms": stage, "clocks": clk,
-            "h2d": h2d, "d2h": d2h}
+            "h2d": h2d, "d2h": d2h, "fp8_config": fp8cfg}
+
+
+def time_fp8_config(L, dev, stream, steps, barrier):
+    """attn_fwd_fp8 on the FP8 accuracy configuration's own inputs (FP8_CONFIG:
+    outliers, Q and K rotated; the GPU quantiser runs first, untimed), non-causal
+    and causal, `steps` launches each after 3 warm-up launches. Each launch
+    reads 201 MB of codes and writes 134 MB of O (above L2, no flush).
+    Returns {causal flag: ms per launch}."""
+    import torch
+    from exact_attention_73_gb300 import inputs
+    B, H, N, d = FP8_CONFIG
+    nb = (N + 127) // 128
+    q, k, v = (x.to(dev) for x in inputs.outliers(3, [(B, H, N, d)] * 3))
+    signs = inputs.random_signs(4, d).to(dev)
+    codes = []
+    for x, sg in ((q, signs), (k, signs), (v, None)):
+        x8 = torch.empty(x.shape, dtype=torch.uint8, device=dev)
+        sc = torch.empty((B, H, nb), device=dev)
+        L.attn_quantize_fp8(x, x8, sc, sg)
+        codes += [x8, sc]
+    del q, k, v
+    q8, sq, k8, sk, v8, sv = codes
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, N), device=dev)
+    out = {}
+    for causal in (False, True):
+        for _ in range(3):
+            L.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, o, lse, causal=causal)
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            L.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, o, lse, causal=causal)
+        e1.record(stream)
+        barrier()
+        out[causal] = e0.elapsed_time(e1) / steps
+    if L.attn_get_device_status() != 0:
+        raise RuntimeError("device-side wait timed out during the FP8 configuration run")
+    return out
 
 
 def cpu_sample(wl, steps=1):
@@ -670,13 +719,58 @@ def cpu_cores():
         return os.cpu_count()
 
 
+def kernel_source_sha16():
+    """Hash of every kernel and launcher source of the library: a DRAM capture
+    is valid only for the source it was taken from."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_attention_73_gb300", "csrc")
+    for f in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh")) +
+                    glob.glob(os.path.join(csrc, "*.h"))):
+        h.update(os.path.basename(f).encode())
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+
+
 def measured_traffic(key):
-    """DRAM bytes (read + write) per launch from the committed ncu summary, or
-    None when that kernel has no capture."""
-    tp = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(tp):
+    """DRAM bytes (read + write) per launch of one ncu capture (profiles/traffic.json),
+    or None when the kernel has no capture or the capture was taken from other
+    kernel sources than the current ones."""
+    if not os.path.exists(TRAFFIC):
         return None
-    return json.load(open(tp)).get(key)
+    t = json.load(open(TRAFFIC))
+    e = t.get("launches", {}).get(key)
+    if e is None or t.get("source_sha16") != kernel_source_sha16():
+        return None
+    return e
+
+
+def write_traffic(csv_path, keys):
+    """Write profiles/traffic.json from an ncu --csv launch list holding
+    dram__bytes_read.sum and dram__bytes_write.sum: `keys` maps a kernel-name
+    regex to the traffic key; the last captured launch of each kernel is used.
+    Records the current kernel source hash with the numbers."""
+    import csv
+    import re
+    rows = list(csv.reader(l for l in open(csv_path) if l.startswith('"')))
+    head = rows[0]
+    ki, mi, vi, ui = head.index("Kernel Name"), head.index("Metric Name"), head.index("Metric Value"), \
+        head.index("Metric Unit")
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    per = {}
+    for r in rows[1:]:
+        for pat, key in keys.items():
+            if re.search(pat, r[ki]) and r[mi] in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+                per.setdefault(key, {})[r[mi]] = float(r[vi].replace(",", "")) * scale[r[ui]]
+    out = {"source_sha16": kernel_source_sha16(), "capture": os.path.basename(csv_path),
+           "launches": {k: int(v["dram__bytes_read.sum"] + v["dram__bytes_write.sum"]) for k, v in per.items()}}
+    with open(TRAFFIC, "w") as f:
+        json.dump(out, f, indent=1)
+    return out
 
 
 def main():
@@ -688,7 +782,15 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(DECODE_WORKLOADS) + sorted(VARLEN_WORKLOADS),
                     default=DEFAULT)
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle timing")
+    ap.add_argument("--write-traffic", metavar="CSV",
+                    help="write profiles/traffic.json from an ncu --csv capture of the default workload's "
+                         "dram__bytes_read.sum/dram__bytes_write.sum, then exit")
     args = ap.parse_args()
+    if args.write_traffic:
+        print(json.dumps(write_traffic(args.write_traffic, {
+            r"fwd_kernel<\(?int\)?0|fwd_kernel<0": f"{DEFAULT}:fwd", r"bwd_kernel": f"{DEFAULT}:bwd",
+            r"fwd_kernel<\(?int\)?2|fwd_kernel<2": f"{DEFAULT}:fwd_fp8"})))
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank = int(os.environ.get("RANK", 0))
@@ -762,11 +864,26 @@ def main():
                                                     "fwd_fp8": "attn_fwd_fp8"}[dom],
                      "achieved": achieved, "peak": dom_peak, "unit": "TFLOP/s", "frac": achieved / dom_peak,
                      "peak_source": pk["source"] + (" bf16 burst x2 (fp8 nominal ratio)" if dom == "fwd_fp8" else " bf16 burst"),
-                     "traffic": traffic},
+                     "traffic": traffic,
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, captured "
+                                       "from the current kernel sources" if traffic is not None else
+                                       "no ncu capture of the current kernel sources"},
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": (4 if window is not None else LAUNCHES_PER_STEP) * args.steps,
         "clocks": r["clocks"],
     }
+    if r.get("fp8_config"):
+        fb, fh, fn, fd = FP8_CONFIG
+        ff = fwd_flops(fb, fh, fn, fd, False)
+        line["fp8_config"] = {
+            "workload": f"fp8_b{fb}_h{fh}_n{fn}_d{fd}_outliers_rotated",
+            "kernel": "attn_fwd_fp8", "peak": 2 * pk["bf16_burst"],
+            "peak_source": pk["source"] + " bf16 burst x2 (fp8 nominal ratio)",
+            **{name: {"ms": ms, "tflops": ff / (2 if c else 1) / ms / 1e9,
+                      "frac_of_fp8_peak": ff / (2 if c else 1) / ms / 1e9 / (2 * pk["bf16_burst"])}
+               for c, name, ms in ((False, "non_causal", r["fp8_config"][False]),
+                                   (True, "causal", r["fp8_config"][True]))}}
+        line["gpu_launches"] += 2 * (args.steps + 3) + 3
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         fl, sec = cpu_sample(wl)
         line["cpu_baseline"] = {"value": fl / sec / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",

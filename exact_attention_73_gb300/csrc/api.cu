@@ -65,17 +65,62 @@ attn_status current_device(int* dev_out, int** status_out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Encoded maps, keyed by everything the encode reads: a caller that repeats a
+// call on the same buffers (a training or serving loop) skips the encode. A
+// map holds only the address, shape and box, so a hit is the same map the
+// encode would produce.
+struct MapKey {
+  int dev, dt, sw;
+  const void* base;
+  uint64_t dims[4], strides[3];
+  uint32_t box[4];
+  bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
+};
+struct MapEntry {
+  bool used = false;
+  MapKey key;
+  CUtensorMap map;
+};
+constexpr int kMapCache = 64;
+MapEntry g_maps[kMapCache];
+int g_map_next = 0;
+std::mutex g_map_mu;
+
 // 4-D tiled map over a tensor whose rows hold d contiguous elements.
 // dims (innermost first) and byte strides of dims 1..3; box = (box_e, b1, b2, 1).
 bool encode_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, const uint64_t dims[4],
                 const uint64_t strides[3], const uint32_t box[4], CUtensorMapSwizzle sw) {
+  MapKey key;
+  std::memset(&key, 0, sizeof(key));   // padding takes part in the comparison
+  if (cudaGetDevice(&key.dev) != cudaSuccess) return false;
+  key.dt = static_cast<int>(dt);
+  key.sw = static_cast<int>(sw);
+  key.base = base;
+  std::memcpy(key.dims, dims, sizeof(key.dims));
+  std::memcpy(key.strides, strides, sizeof(key.strides));
+  std::memcpy(key.box, box, sizeof(key.box));
+  {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (const MapEntry& e : g_maps)
+      if (e.used && e.key == key) {
+        *m = e.map;
+        return true;
+      }
+  }
   cuuint64_t gd[4] = {dims[0], dims[1], dims[2], dims[3]};
   cuuint64_t gs[3] = {strides[0], strides[1], strides[2]};
   cuuint32_t bx[4] = {box[0], box[1], box[2], box[3]};
   cuuint32_t es[4] = {1, 1, 1, 1};
   CUresult r = g_encode(m, dt, 4, const_cast<void*>(base), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  if (r != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  MapEntry& e = g_maps[g_map_next];
+  g_map_next = (g_map_next + 1) % kMapCache;
+  e.used = true;
+  e.key = key;
+  e.map = *m;
+  return true;
 }
 
 CUtensorMapDataType tma_type(int dt) {

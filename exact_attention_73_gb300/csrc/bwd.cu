@@ -1,5 +1,6 @@
 // Backward launchers: D = rowsum(dO o O) with the dQ accumulator cleared,
-// the tcgen05 main kernel, and the FP32 -> BF16/FP16 dQ conversion.
+// the tcgen05 main kernel (head dim 64 or 128), and the FP32 -> BF16/FP16 dQ
+// conversion.
 //
 // The two helper kernels are HBM-bound streams: one warp per row of d
 // elements (pre) and four elements per thread (convert), coalesced.
@@ -37,9 +38,15 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ o, c
 #pragma unroll
   for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
   if (dq_acc) {   // absent for the deterministic backward (dQ written directly)
-    float4* z = reinterpret_cast<float4*>(dq_acc + r * D + lane * c);
+    float* z = dq_acc + r * D + lane * c;
+    if constexpr (c % 4 == 0) {
 #pragma unroll
-    for (int e = 0; e < c / 4; ++e) z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int e = 0; e < c / 4; ++e) reinterpret_cast<float4*>(z)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      static_assert(c % 2 == 0, "row chunk per lane");
+#pragma unroll
+      for (int e = 0; e < c / 2; ++e) reinterpret_cast<float2*>(z)[e] = make_float2(0.f, 0.f);
+    }
   }
   if (lane == 0) {
     long long idx = r;
@@ -65,16 +72,29 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
   }
 }
 
-template <int DT, bool kDQ>
+template <int DT, int D, bool kDQ>
 cudaError_t launch_main(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q, const CUtensorMap& d,
                         const CUtensorMap& dq, const BwdArgs& a, int max_len, int nz, cudaStream_t st) {
-  using C = BwdCfg<DT, 128>;
-  auto kern = bwd_kernel<DT, 128, kDQ>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  using C = BwdCfg<DT, D>;
+  auto kern = bwd_kernel<DT, D, kDQ>;
+  cudaError_t e = smem_attr_once<bwd_kernel<DT, D, kDQ>>(C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const dim3 grid((max_len + C::BC - 1) / C::BC, a.Hkv, nz);
   kern<<<grid, C::NTHREADS, C::SMEM_BYTES, st>>>(k, v, q, d, dq, a);
   return cudaGetLastError();
+}
+
+template <bool kDQ>
+cudaError_t launch_main_dt(int dt, int hd, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
+                           const CUtensorMap& d, const CUtensorMap& dq, const BwdArgs& a, int max_len, int nz,
+                           cudaStream_t st) {
+  if (hd == 128)
+    return dt == kBF16 ? launch_main<kBF16, 128, kDQ>(k, v, q, d, dq, a, max_len, nz, st)
+                       : launch_main<kFP16, 128, kDQ>(k, v, q, d, dq, a, max_len, nz, st);
+  if (hd == 64)
+    return dt == kBF16 ? launch_main<kBF16, 64, kDQ>(k, v, q, d, dq, a, max_len, nz, st)
+                       : launch_main<kFP16, 64, kDQ>(k, v, q, d, dq, a, max_len, nz, st);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -82,28 +102,34 @@ cudaError_t launch_main(const CUtensorMap& k, const CUtensorMap& v, const CUtens
 cudaError_t launch_bwd_pre(int dt, int d, const void* o, const void* dout, float* dvec, float* dq_acc, long long rows,
                            int Hq, int T_tokens, int packed, cudaStream_t st) {
   const dim3 grid(static_cast<unsigned>((rows + 7) / 8));
-  if (d != 128) return cudaErrorInvalidValue;
-  if (dt == kBF16)
-    bwd_pre_kernel<__nv_bfloat16, 128><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(o),
-        static_cast<const __nv_bfloat16*>(dout), dvec, dq_acc, rows, Hq, T_tokens, packed);
-  else
-    bwd_pre_kernel<__half, 128><<<grid, 256, 0, st>>>(static_cast<const __half*>(o), static_cast<const __half*>(dout),
-        dvec, dq_acc, rows, Hq, T_tokens, packed);
+  const auto* ob = static_cast<const __nv_bfloat16*>(o);
+  const auto* db = static_cast<const __nv_bfloat16*>(dout);
+  const auto* oh = static_cast<const __half*>(o);
+  const auto* dh = static_cast<const __half*>(dout);
+  if (d == 128) {
+    if (dt == kBF16) bwd_pre_kernel<__nv_bfloat16, 128><<<grid, 256, 0, st>>>(ob, db, dvec, dq_acc, rows, Hq, T_tokens, packed);
+    else bwd_pre_kernel<__half, 128><<<grid, 256, 0, st>>>(oh, dh, dvec, dq_acc, rows, Hq, T_tokens, packed);
+  } else if (d == 64) {
+    if (dt == kBF16) bwd_pre_kernel<__nv_bfloat16, 64><<<grid, 256, 0, st>>>(ob, db, dvec, dq_acc, rows, Hq, T_tokens, packed);
+    else bwd_pre_kernel<__half, 64><<<grid, 256, 0, st>>>(oh, dh, dvec, dq_acc, rows, Hq, T_tokens, packed);
+  } else {
+    return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_main(int dt, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
+cudaError_t launch_bwd_main(int dt, int d, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
                             const CUtensorMap& dout, const CUtensorMap& dq_acc, const BwdArgs& a, int max_len, int nz,
                             cudaStream_t st) {
-  return dt == kBF16 ? launch_main<kBF16, true>(k, v, q, dout, dq_acc, a, max_len, nz, st)
-                     : launch_main<kFP16, true>(k, v, q, dout, dq_acc, a, max_len, nz, st);
+  return launch_main_dt<true>(dt, d, k, v, q, dout, dq_acc, a, max_len, nz, st);
 }
 
-cudaError_t launch_bwd_dkdv(int dt, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
+int bwd_dq_rows(int d) { return d == 64 ? BwdCfg<kBF16, 64>::DQ_ROWS : BwdCfg<kBF16, 128>::DQ_ROWS; }
+
+cudaError_t launch_bwd_dkdv(int dt, int d, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
                             const CUtensorMap& dout, const BwdArgs& a, int max_len, int nz, cudaStream_t st) {
   // the dQ map is never read without the dQ product; K's map stands in for it
-  return dt == kBF16 ? launch_main<kBF16, false>(k, v, q, dout, k, a, max_len, nz, st)
-                     : launch_main<kFP16, false>(k, v, q, dout, k, a, max_len, nz, st);
+  return launch_main_dt<false>(dt, d, k, v, q, dout, k, a, max_len, nz, st);
 }
 
 cudaError_t launch_dq_convert(int dt, const float* acc, void* dq, long long n, float scale, cudaStream_t st) {

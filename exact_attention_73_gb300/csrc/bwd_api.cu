@@ -18,7 +18,7 @@ attn_status check_common(const void* q, const void* k, const void* v, const void
   for (const void* p : ptrs)
     if (!aligned16(p)) return ATTN_ERR_ALIGN;
   if (Hq < 1 || Hkv < 1 || Hq > 65535) return ATTN_ERR_SHAPE;
-  if (d != 128) return ATTN_ERR_HEADDIM;   // the backward kernel is built for d = 128
+  if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;   // the backward kernel is built for d = 64 and 128
   if (Hq % Hkv) return ATTN_ERR_GQA;
   if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_DTYPE;
   if (ws_bytes < ws_need) return ATTN_ERR_WORKSPACE;
@@ -51,7 +51,7 @@ attn_status run_bwd(const void* q, const void* k, const void* v, const void* o, 
       !operand_map(&tv, v, dtype, d, packed, B, Hkv, rows_or_T, 128) ||
       !operand_map(&tq, q, dtype, d, packed, B, Hq, rows_or_T, 64) ||
       !operand_map(&tdo, dout, dtype, d, packed, B, Hq, rows_or_T, 64) ||
-      !accum_map(&tdq, dq_acc, d, packed, B, Hq, rows_or_T, 32))
+      !accum_map(&tdq, dq_acc, d, packed, B, Hq, rows_or_T, bwd_dq_rows(d)))
     return ATTN_ERR_CUDA;
   BwdArgs a{};
   a.lse = lse;
@@ -81,7 +81,7 @@ attn_status run_bwd(const void* q, const void* k, const void* v, const void* o, 
   a.causal = (win_left < 0 && win_right == 0) ? 1 : 0;
   a.status = status;
   cudaError_t e = launch_bwd_pre(dtype, d, o, dout, dvec, dq_acc, rows, Hq, rows_or_T, packed ? 1 : 0, st);
-  if (e == cudaSuccess) e = launch_bwd_main(dtype, tk, tv, tq, tdo, tdq, a, max_len, nz, st);
+  if (e == cudaSuccess) e = launch_bwd_main(dtype, d, tk, tv, tq, tdo, tdq, a, max_len, nz, st);
   if (e == cudaSuccess) e = launch_dq_convert(dtype, dq_acc, dq, rows * d, scale, st);
   return from_cuda(e);
 }
@@ -124,7 +124,7 @@ attn_status run_bwd_det(const void* q, const void* k, const void* v, const void*
   a.causal = (win_left < 0 && win_right == 0) ? 1 : 0;
   a.status = status;
   cudaError_t e = launch_bwd_pre(dtype, d, o, dout, dvec, nullptr, rows, Hq, N, 0, st);
-  if (e == cudaSuccess) e = launch_bwd_dkdv(dtype, tk, tv, tq, tdo, a, N, B, st);
+  if (e == cudaSuccess) e = launch_bwd_dkdv(dtype, d, tk, tv, tq, tdo, a, N, B, st);
   if (e == cudaSuccess) e = launch_bwd_dq(dtype, tq128, tdo128, tk, tv, a, N, B, st);
   return from_cuda(e);
 }
@@ -148,6 +148,7 @@ attn_status attn_bwd_deterministic(const void* q, const void* k, const void* v, 
   attn_status s = check_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, ws_bytes,
                                attn_bwd_deterministic_workspace_size(B, Hq, Hkv, N, d), Hq, Hkv, d, dtype);
   if (s != ATTN_OK) return s;
+  if (d != 128) return ATTN_ERR_HEADDIM;   // the query-stationary dQ kernel is built for d = 128
   int* status;
   if ((s = attn::device_context(&status)) != ATTN_OK) return s;
   return run_bwd_det(q, k, v, o, lse, dout, dq, dk, dv, workspace, B, N, Hq, Hkv, d, scale, window_left,

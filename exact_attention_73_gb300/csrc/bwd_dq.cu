@@ -11,7 +11,7 @@ cudaError_t launch(const CUtensorMap& q, const CUtensorMap& dout, const CUtensor
                    const BwdArgs& a, int max_len, int nz, cudaStream_t st) {
   using C = DqCfg<DT>;
   auto kern = bwd_dq_kernel<DT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  cudaError_t e = smem_attr_once<bwd_dq_kernel<DT>>(C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const dim3 grid((max_len + 127) / 128, a.Hq, nz);
   kern<<<grid, C::NTHREADS, C::SMEM_BYTES, st>>>(q, dout, k, v, a);

@@ -1,4 +1,4 @@
-// Backward attention kernels for sm_103a (BF16 / FP16, head dim 128).
+// Backward attention kernels for sm_103a (BF16 / FP16, head dim 64 or 128).
 //
 // Method: FlashAttention-3 (zenmind.me summary) §3.1 backward chain with P
 // recomputed from the forward's log-sum-exp, and §4 step 5 (paper App. B.1):
@@ -29,8 +29,11 @@
 // and writing P^T/dS^T over them) and also store dS^T to shared memory
 // (double-buffered, 128-byte swizzle) for the dQ product, warps 8-11 drain
 // dQ^T (one head-dim index per thread) into
-// a [64 queries][128 dims] FP32 tile in shared memory, which one thread adds
-// into the global dQ accumulator with a single TMA reduce-add.
+// a [rows][D] FP32 tile in shared memory, which one thread adds into the
+// global dQ accumulator with TMA reduce-adds.
+// D = 64: dK and dV take 64 columns each; the dQ^T product keeps M = 128 with
+// its A operand running from K into V (the next 64-dim box in shared memory),
+// so tensor-memory lanes 64..127 hold V^T dS^T, which the drain ignores.
 #pragma once
 #include <cmath>
 #include <cstdint>
@@ -62,7 +65,7 @@ struct BwdArgs {
 
 template <int DT, int D>
 struct BwdCfg {
-  static_assert(D == 128, "backward kernel is written for head dim 128");
+  static_assert(D == 64 || D == 128, "backward kernel is written for head dim 64 or 128");
   static constexpr int BR = 64;                     // query rows per iteration
   static constexpr int BC = 128;                    // keys per CTA
   static constexpr int NBOX = D / 64;               // 64-element (128-byte) boxes per row
@@ -71,10 +74,11 @@ struct BwdCfg {
   static constexpr int Q_B = BR * D * 2;            // Q_i or dO_i tile
   static constexpr int Q_BOX_B = BR * 128;
   static constexpr int DS_B = BC * BR * 2;          // dS^T tile [128 keys][64 queries]
-  static constexpr int NQ = 4;                      // stages of the Q/dO ring
+  static constexpr int NQ = D == 64 ? 6 : 4;        // stages of the Q/dO ring
   static constexpr int LD_B = 2 * BR * 4;           // LSE*log2e and D for one tile
-  static constexpr int DQ_ROWS = BR / 2;            // rows of dQ per reduce-add (two per tile)
-  static constexpr int DQ_STAGE_B = DQ_ROWS * D * 4;  // FP32 staging for one reduce-add
+  static constexpr int DQ_ROWS = D == 64 ? BR : BR / 2;   // rows of dQ per reduce-add
+  static constexpr int DQ_PARTS = BR / DQ_ROWS;            // reduce-adds per tile
+  static constexpr int DQ_STAGE_B = DQ_ROWS * D * 4;       // FP32 staging for one reduce-add
   static constexpr int SMEM_BYTES =
       2 * KV_B + DS_B + NQ * (2 * Q_B) + DQ_STAGE_B + NQ * LD_B + 18 * 8 + 16;   // base is 1024-aligned
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeded");
@@ -88,10 +92,10 @@ struct BwdCfg {
   static constexpr uint32_t FMT = DT == kBF16 ? 1u : 0u;
   static constexpr uint32_t IDESC_SP = instr_desc(128, BR, FMT, FMT, 0, 0);
   static constexpr uint32_t IDESC_KV = instr_desc(128, D, FMT, FMT, 0, 1);
-  static constexpr uint32_t IDESC_DQ = instr_desc(D, BR, FMT, FMT, 1, 1);
+  static constexpr uint32_t IDESC_DQ = instr_desc(128, BR, FMT, FMT, 1, 1);   // M = 128 also for D = 64
   // within score buffer X (base 128X)
   static constexpr uint32_t COL_S = 0, COL_DP = 64, COL_P = 0, COL_DQ = 32, COL_DS = 96;
-  static constexpr uint32_t COL_DV = 256, COL_DK = 384;
+  static constexpr uint32_t COL_DV = 256, COL_DK = 256 + D;
 };
 
 // kDQ = false: dK and dV only (the deterministic backward computes dQ in a
@@ -439,11 +443,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(done, 0, a.status));
     tc_fence_after();
-    if (ok) {   // dV rows, columns 64*half .. +63
+    if (ok) {   // dV rows, columns D/2*half .. +D/2-1
       const long long off = static_cast<long long>(b) * a.k_sb + static_cast<long long>(hkv) * a.k_sh +
                             static_cast<long long>(seq0 + kloc) * a.k_sn;
 #pragma unroll 1
-      for (int c = 2 * half; c < 2 * half + 2; ++c) {
+      for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
         uint32_t v[32];
         tmem_ld32(tbase + lane_off + C::COL_DV + 32 * c, v);
         tmem_wait_ld();
@@ -483,21 +487,32 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       mbar_arrive(dq_empty);
       const int h = hkv * a.group + it / per_head;
       const int q0 = q_tile(it) * C::BR;
-      // two reduce-adds of 32 rows through one FP32 staging buffer; rows past
+      // reduce-adds of DQ_ROWS rows through one FP32 staging buffer; rows past
       // the sequence hold exact zeros (P = 0 there): for the dense layout the
       // map clips them, for the packed layout they add 0 to the next
       // sequence's rows
 #pragma unroll
-      for (int part = 0; part < 2; ++part) {
+      for (int part = 0; part < C::DQ_PARTS; ++part) {
         if (threadIdx.x == 256) bulk_wait_read_all();   // previous reduce-add has read the buffer
         named_bar_sync(1, 128);
+        if (dim < D) {                                  // D = 64: lanes 64..127 are not dQ
+          if constexpr (C::DQ_PARTS == 2) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) sDQ[e * D + dim] = __uint_as_float(part == 0 ? x0[e] : x1[e]);
+            for (int e = 0; e < 32; ++e) sDQ[e * D + dim] = __uint_as_float(part == 0 ? x0[e] : x1[e]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              sDQ[e * D + dim] = __uint_as_float(x0[e]);
+              sDQ[(e + 32) * D + dim] = __uint_as_float(x1[e]);
+            }
+          }
+        }
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
         if (threadIdx.x == 256) {
-          if (packed) tma_reduce_add_4d(&tmdQ, sDQ, 0, h, seq0 + q0 + 32 * part, 0);
-          else tma_reduce_add_4d(&tmdQ, sDQ, 0, q0 + 32 * part, h, b);
+          const int row = q0 + C::DQ_ROWS * part;
+          if (packed) tma_reduce_add_4d(&tmdQ, sDQ, 0, h, seq0 + row, 0);
+          else tma_reduce_add_4d(&tmdQ, sDQ, 0, row, h, b);
           bulk_commit();
         }
       }

@@ -49,7 +49,7 @@ cudaError_t launch_decode_inst(const CUtensorMap& q, const CUtensorMap& k, const
                                int splits, int items, cudaStream_t st) {
   using C = DecCfg<D>;
   auto kern = decode_kernel<D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  cudaError_t e = smem_attr_once<decode_kernel<D>>(C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;

@@ -9,7 +9,7 @@ cudaError_t launch_fwd_inst(const CUtensorMap& q, const CUtensorMap& k, const CU
                             const FwdArgs& a, int rows, int gy, int gz, cudaStream_t st) {
   using C = FwdCfg<DT, D, QT>;
   auto kern = fwd_kernel<DT, D, QT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  cudaError_t e = smem_attr_once<fwd_kernel<DT, D, QT>>(C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const dim3 grid((rows + 128 * QT - 1) / (128 * QT), gy, gz);
   kern<<<grid, C::NTHREADS, C::SMEM_BYTES, st>>>(q, k, v, a);

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include "fwd_kernel.cuh"
+#include "launch_util.h"
 
 namespace attn {
 

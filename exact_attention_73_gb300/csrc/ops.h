@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/libattn.h"
+#include "launch_util.h"
 
 namespace attn {
 
@@ -21,12 +22,14 @@ bool operand_map(CUtensorMap* m, const void* base, int dt, int d, bool packed, i
                  int box_rows);
 cudaError_t launch_bwd_pre(int dt, int d, const void* o, const void* dout, float* dvec, float* dq_acc,
                            long long rows, int Hq, int T_tokens, int packed, cudaStream_t st);
-cudaError_t launch_bwd_main(int dt, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
+cudaError_t launch_bwd_main(int dt, int d, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
                             const CUtensorMap& dout, const CUtensorMap& dq_acc, const BwdArgs& a, int max_len, int nz,
                             cudaStream_t st);
 // FP32 accumulator map (layout of the operands, no swizzle), boxes of d x box_rows.
 bool accum_map(CUtensorMap* m, const float* base, int d, bool packed, int B, int H, long long rows, int box_rows);
-cudaError_t launch_bwd_dkdv(int dt, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
+// Rows of the dQ accumulator per reduce-add of the main kernel (the box of its map).
+int bwd_dq_rows(int d);
+cudaError_t launch_bwd_dkdv(int dt, int d, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
                             const CUtensorMap& dout, const BwdArgs& a, int max_len, int nz, cudaStream_t st);
 cudaError_t launch_bwd_dq(int dt, const CUtensorMap& q, const CUtensorMap& dout, const CUtensorMap& k,
                           const CUtensorMap& v, const BwdArgs& a, int max_len, int nz, cudaStream_t st);

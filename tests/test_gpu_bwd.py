@@ -42,11 +42,12 @@ def run_dense(q, k, v, do, causal):
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("n", [1, 64, 200, 640, 1000])
-def test_dense_gqa_ragged(dtype, causal, n):
-    q, k, v, do = inputs.normal(200 + n, [(2, 4, n, 128), (2, 2, n, 128), (2, 2, n, 128), (2, 4, n, 128)],
+@pytest.mark.parametrize("d", [64, 128])
+def test_dense_gqa_ragged(dtype, causal, n, d):
+    q, k, v, do = inputs.normal(200 + n + d, [(2, 4, n, d), (2, 2, n, d), (2, 2, n, d), (2, 4, n, d)],
                                 dtype=dtype)
     got = run_dense(q, k, v, do, causal)
-    ref = A.backward(q, k, v, do, 128 ** -0.5, causal)
+    ref = A.backward(q, k, v, do, d ** -0.5, causal)
     for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
         assert rel_rms(g, r) <= 1e-2, (name, rel_rms(g, r))
 
@@ -61,20 +62,21 @@ def test_two_calls_reuse_workspace():
 
 
 @pytest.mark.parametrize("causal", [False, True])
-def test_varlen_small(causal):
+@pytest.mark.parametrize("d", [64, 128])
+def test_varlen_small(causal, d):
     lens = [1, 127, 128, 300, 1000, 5]
     cu = inputs.cu_seqlens(lens)
     T = int(cu[-1])
-    q, k, v, do = inputs.normal(12, [(T, 4, 128), (T, 2, 128), (T, 2, 128), (T, 4, 128)])
+    q, k, v, do = inputs.normal(12, [(T, 4, d), (T, 2, d), (T, 2, d), (T, 4, d)])
     qd, kd, vd, dod, cud = (x.cuda() for x in (q, k, v, do, cu))
     o = torch.empty_like(qd)
     lse = torch.empty((4, T), device="cuda")
     L.attn_fwd_varlen(qd, kd, vd, o, lse, cud, max(lens), causal=causal)
     dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
-    ws = torch.empty((L.attn_bwd_varlen_workspace_size(T, 4, 2, 128),), dtype=torch.uint8, device="cuda")
+    ws = torch.empty((L.attn_bwd_varlen_workspace_size(T, 4, 2, d),), dtype=torch.uint8, device="cuda")
     L.attn_bwd_varlen(qd, kd, vd, o, lse, dod, dq, dk, dv, ws, cud, max(lens), causal=causal)
     torch.cuda.synchronize()
-    ref = A.backward_varlen(q, k, v, do, cu.numpy(), 128 ** -0.5, causal)
+    ref = A.backward_varlen(q, k, v, do, cu.numpy(), d ** -0.5, causal)
     for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
         assert rel_rms(g, r) <= 1e-2, (name, rel_rms(g, r))
 

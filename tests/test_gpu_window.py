@@ -98,10 +98,11 @@ def run_bwd(q, k, v, do, window):
 
 @pytest.mark.parametrize("window", WINDOWS)
 @pytest.mark.parametrize("n", [200, 700])
-def test_backward_window(window, n):
-    q, k, v, do = inputs.normal(320 + n, [(2, 4, n, 128), (2, 2, n, 128), (2, 2, n, 128), (2, 4, n, 128)])
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_window(window, n, d):
+    q, k, v, do = inputs.normal(320 + n, [(2, 4, n, d), (2, 2, n, d), (2, 2, n, d), (2, 4, n, d)])
     got = run_bwd(q, k, v, do, window)
-    ref = A.backward(q, k, v, do, 128 ** -0.5, False, window)
+    ref = A.backward(q, k, v, do, d ** -0.5, False, window)
     for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
         assert rel_rms(g, r) <= 1e-2, (name, window, rel_rms(g, r))
 
