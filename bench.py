@@ -118,8 +118,11 @@ def peaks():
 
 
 class Clocks:
-    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampling of SM clock and throttle reasons. The sampler is
+    started before the warm-up (its start-up competes with the first launches
+    for the CPU and the driver, which would stretch a short timed region) and
+    only the samples taken inside the timed regions (begin/end) are kept."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -128,6 +131,8 @@ class Clocks:
         self.proc = None
         self.path = None
         self.out = None
+        self.windows = []
+        self._t = None
 
     def start(self):
         try:
@@ -139,6 +144,14 @@ class Clocks:
                                          stdout=self.out, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+
+    def begin(self):
+        self._t = time.time()
+
+    def end(self):
+        if self._t is not None:
+            self.windows.append((self._t, time.time()))
+            self._t = None
 
     def stop(self):
         if self.proc is None:
@@ -155,17 +168,35 @@ class Clocks:
         with open(self.path) as f:
             text = f.read()
         os.unlink(self.path)
-        return parse_clock_samples(text)
+        return parse_clock_samples(text, self.windows)
 
 
-def parse_clock_samples(text):
+def parse_clock_samples(text, windows=None):
     """Median SM clock, the largest max clock and the throttle reasons seen in
-    nvidia-smi CSV rows (the fields of Clocks.Q, no header, no units)."""
-    rows = [r.split(",") for r in text.strip().splitlines() if r.strip()]
+    nvidia-smi CSV rows (the fields of Clocks.Q without the leading timestamp,
+    or with it). With `windows` (wall-clock (start, end) pairs) and timestamped
+    rows, only the rows inside a window count (all rows if none does)."""
+    import datetime
+    rows = [[f.strip() for f in r.split(",")] for r in text.strip().splitlines() if r.strip()]
     if not rows:
         return None
-    sm = [float(r[1]) for r in rows if len(r) > 2 and r[1].strip().replace(".", "").isdigit()]
-    mx = [float(r[2]) for r in rows if len(r) > 2 and r[2].strip().replace(".", "").isdigit()]
+    stamped = []
+    for r in rows:
+        t = None
+        if "/" in r[0]:
+            try:
+                t = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                t = None
+            r = r[1:]
+        stamped.append((t, r))
+    if windows:
+        inside = [r for t, r in stamped if t is not None and any(a - 0.05 <= t <= b + 0.05 for a, b in windows)]
+        rows = inside or [r for _, r in stamped]
+    else:
+        rows = [r for _, r in stamped]
+    sm = [float(r[1]) for r in rows if len(r) > 2 and r[1].replace(".", "").isdigit()]
+    mx = [float(r[2]) for r in rows if len(r) > 2 and r[2].replace(".", "").isdigit()]
     names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
     reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if "Active" in v and "Not" not in v})
     return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
@@ -249,6 +280,8 @@ def bench_ours(args, wl, rank, world):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
+    clocks = Clocks(dev.index)
+    clocks.start()
     for _ in range(args.warmup):
         step()
     status = L.attn_get_device_status()
@@ -257,9 +290,8 @@ def bench_ours(args, wl, rank, world):
 
     # ---------------------------------------------------------- device-timed
     marks = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    clocks = Clocks(dev.index)
     barrier()
-    clocks.start()
+    clocks.begin()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -267,6 +299,7 @@ def bench_ours(args, wl, rank, world):
         step(marks[s])
     t1.record(stream)
     barrier()
+    clocks.end()
     ms_total = t0.elapsed_time(t1)
     stage = {n: sum(m[i].elapsed_time(m[i + 1]) for m in marks) / args.steps
              for i, n in enumerate(("fwd", "bwd", "quant", "fwd_fp8"))}
@@ -320,24 +353,26 @@ def bench_ours(args, wl, rank, world):
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    clocks.begin()
     e0.record(stream)
     e2e(args.steps, e0)
     e1.record(stream)
     barrier()
+    clocks.end()
     ms_e2e = e0.elapsed_time(e1)
     if L.attn_get_device_status() != 0:
         raise RuntimeError("device-side wait timed out during the end-to-end run")
 
     fp8cfg = None
     if window is None:
-        fp8cfg = time_fp8_config(L, dev, stream, args.steps, barrier)
+        fp8cfg = time_fp8_config(L, dev, stream, args.steps, barrier, clocks)
     clk = clocks.stop()
     ms_total, ms_e2e = max_over_ranks([ms_total, ms_e2e], world, dev)
     return {"ms_total": ms_total, "ms_e2e": ms_e2e, "stage_ms": stage, "clocks": clk,
             "h2d": h2d, "d2h": d2h, "fp8_config": fp8cfg}
 
 
-def time_fp8_config(L, dev, stream, steps, barrier):
+def time_fp8_config(L, dev, stream, steps, barrier, clocks):
     """attn_fwd_fp8 on the FP8 accuracy configuration's own inputs (FP8_CONFIG:
     outliers, Q and K rotated; the GPU quantiser runs first, untimed), non-causal
     and causal, `steps` launches each after 3 warm-up launches. Each launch
@@ -364,12 +399,14 @@ def time_fp8_config(L, dev, stream, steps, barrier):
         for _ in range(3):
             L.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, o, lse, causal=causal)
         barrier()
+        clocks.begin()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(steps):
             L.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, o, lse, causal=causal)
         e1.record(stream)
         barrier()
+        clocks.end()
         out[causal] = e0.elapsed_time(e1) / steps
     if L.attn_get_device_status() != 0:
         raise RuntimeError("device-side wait timed out during the FP8 configuration run")
@@ -445,17 +482,19 @@ def bench_decode(args, wl, rank, world):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
+    clocks = Clocks(dev.index)
+    clocks.start()
     for _ in range(args.warmup):
         step()
-    clocks = Clocks(dev.index)
     barrier()
-    clocks.start()
+    clocks.begin()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for _ in range(args.steps):
         step()
     t1.record(stream)
     barrier()
+    clocks.end()
     clk = clocks.stop()
     ms = t0.elapsed_time(t1)
     # end to end: the new token's codes and factors in, O and LSE out, every step
@@ -598,18 +637,20 @@ def bench_varlen(args, wl, rank, world):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
+    clocks = Clocks(dev.index)
+    clocks.start()
     for _ in range(args.warmup):
         step()
     marks = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    clocks = Clocks(dev.index)
     barrier()
-    clocks.start()
+    clocks.begin()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for s_ in range(args.steps):
         step(marks[s_])
     t1.record(stream)
     barrier()
+    clocks.end()
     clk = clocks.stop()
     ms = t0.elapsed_time(t1)
     stage = {n: sum(m[i].elapsed_time(m[i + 1]) for m in marks) / args.steps for i, n in enumerate(("fwd", "bwd"))}

@@ -92,6 +92,19 @@ def test_clock_samples_are_parsed():
     assert hot["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
 
 
+def test_clock_samples_outside_the_timed_windows_are_dropped():
+    """Timestamped rows: only those inside a (start, end) wall-clock window count."""
+    import datetime
+    t0 = datetime.datetime(2026, 1, 2, 3, 4, 5, 0)
+    row = lambda dt, mhz: (f"{(t0 + datetime.timedelta(seconds=dt)).strftime('%Y/%m/%d %H:%M:%S.%f')[:-3]}, "
+                           f"0, {mhz}, 2070, 900, 0x0, Not Active, Not Active, Not Active, Not Active\n")
+    text = row(0.0, 900) + row(1.0, 2070) + row(1.2, 2050) + row(3.0, 1000)
+    w = [(t0.timestamp() + 0.9, t0.timestamp() + 1.3)]
+    r = bench.parse_clock_samples(text, w)
+    assert r["samples"] == 2 and r["sm_mhz"] == 2060.0
+    assert bench.parse_clock_samples(text)["samples"] == 4
+
+
 @pytest.mark.parametrize("workload", [None, "varlen_t129511_hq32_hkv8_d128_causal",
                                       "decode_fp8_b16_hq32_hkv8_n32768_d128"])
 def test_reference_arm_other_ranks_exit_quietly(workload):
