@@ -50,6 +50,7 @@ WORKLOADS = {
     # other points of the BF16 sweep (B*N = 16384 tokens): the memory-bound short rows and head dim 64
     "bf16_sweep_d128_n512": (32, 16, 16, 512, 128, False, None),
     "bf16_sweep_d64_n8192": (2, 32, 32, 8192, 64, False, None),
+    "bf16_sweep_d256_n8192": (2, 8, 8, 8192, 256, False, None),
     # sliding window: each query sees itself and the 1024 keys before it
     "window_b1_h16_n16384_w1024": (1, 16, 16, 16384, 128, False, (1024, 0)),
 }

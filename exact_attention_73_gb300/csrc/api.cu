@@ -163,19 +163,21 @@ attn_status device_context(int** status) {
   return current_device(&dev, status);
 }
 
-bool accum_map(CUtensorMap* m, const float* base, int d, bool packed, int B, int H, long long rows, int box_rows) {
+bool accum_map(CUtensorMap* m, const float* base, int d, bool packed, int B, int H, long long rows, int box_rows,
+               int box_e) {
   const uint64_t esz = 4;
   const uint32_t br = static_cast<uint32_t>(box_rows);
+  const uint32_t be = static_cast<uint32_t>(box_e);
   if (packed) {   // dims (d, H, T, 1)
     const uint64_t dims[4] = {static_cast<uint64_t>(d), static_cast<uint64_t>(H), static_cast<uint64_t>(rows), 1};
     const uint64_t str[3] = {d * esz, static_cast<uint64_t>(H) * d * esz, static_cast<uint64_t>(rows) * H * d * esz};
-    const uint32_t box[4] = {static_cast<uint32_t>(d), 1, br, 1};
+    const uint32_t box[4] = {be, 1, br, 1};
     return encode_map(m, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE);
   }
   const uint64_t dims[4] = {static_cast<uint64_t>(d), static_cast<uint64_t>(rows), static_cast<uint64_t>(H),
                             static_cast<uint64_t>(B)};
   const uint64_t str[3] = {d * esz, static_cast<uint64_t>(rows) * d * esz, static_cast<uint64_t>(H) * rows * d * esz};
-  const uint32_t box[4] = {static_cast<uint32_t>(d), br, 1, 1};
+  const uint32_t box[4] = {be, br, 1, 1};
   return encode_map(m, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 

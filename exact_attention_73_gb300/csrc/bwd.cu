@@ -1,6 +1,6 @@
 // Backward launchers: D = rowsum(dO o O) with the dQ accumulator cleared,
-// the tcgen05 main kernel (head dim 64 or 128), and the FP32 -> BF16/FP16 dQ
-// conversion.
+// the tcgen05 main kernel (head dim 64, 128 or 256), and the FP32 -> BF16/FP16
+// dQ conversion.
 //
 // The two helper kernels are HBM-bound streams: one warp per row of d
 // elements (pre) and four elements per thread (convert), coalesced.
@@ -79,7 +79,7 @@ cudaError_t launch_main(const CUtensorMap& k, const CUtensorMap& v, const CUtens
   auto kern = bwd_kernel<DT, D, kDQ>;
   cudaError_t e = smem_attr_once<bwd_kernel<DT, D, kDQ>>(C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const dim3 grid((max_len + C::BC - 1) / C::BC, a.Hkv, nz);
+  const dim3 grid((max_len + C::BC - 1) / C::BC * C::DSPLIT, a.Hkv, nz);
   kern<<<grid, C::NTHREADS, C::SMEM_BYTES, st>>>(k, v, q, d, dq, a);
   return cudaGetLastError();
 }
@@ -94,6 +94,9 @@ cudaError_t launch_main_dt(int dt, int hd, const CUtensorMap& k, const CUtensorM
   if (hd == 64)
     return dt == kBF16 ? launch_main<kBF16, 64, kDQ>(k, v, q, d, dq, a, max_len, nz, st)
                        : launch_main<kFP16, 64, kDQ>(k, v, q, d, dq, a, max_len, nz, st);
+  if (hd == 256 && kDQ)
+    return dt == kBF16 ? launch_main<kBF16, 256, true>(k, v, q, d, dq, a, max_len, nz, st)
+                       : launch_main<kFP16, 256, true>(k, v, q, d, dq, a, max_len, nz, st);
   return cudaErrorInvalidValue;
 }
 
@@ -112,6 +115,9 @@ cudaError_t launch_bwd_pre(int dt, int d, const void* o, const void* dout, float
   } else if (d == 64) {
     if (dt == kBF16) bwd_pre_kernel<__nv_bfloat16, 64><<<grid, 256, 0, st>>>(ob, db, dvec, dq_acc, rows, Hq, T_tokens, packed);
     else bwd_pre_kernel<__half, 64><<<grid, 256, 0, st>>>(oh, dh, dvec, dq_acc, rows, Hq, T_tokens, packed);
+  } else if (d == 256) {
+    if (dt == kBF16) bwd_pre_kernel<__nv_bfloat16, 256><<<grid, 256, 0, st>>>(ob, db, dvec, dq_acc, rows, Hq, T_tokens, packed);
+    else bwd_pre_kernel<__half, 256><<<grid, 256, 0, st>>>(oh, dh, dvec, dq_acc, rows, Hq, T_tokens, packed);
   } else {
     return cudaErrorInvalidValue;
   }
@@ -124,7 +130,12 @@ cudaError_t launch_bwd_main(int dt, int d, const CUtensorMap& k, const CUtensorM
   return launch_main_dt<true>(dt, d, k, v, q, dout, dq_acc, a, max_len, nz, st);
 }
 
-int bwd_dq_rows(int d) { return d == 64 ? BwdCfg<kBF16, 64>::DQ_ROWS : BwdCfg<kBF16, 128>::DQ_ROWS; }
+int bwd_dq_rows(int d) {
+  return d == 64 ? BwdCfg<kBF16, 64>::DQ_ROWS : d == 256 ? BwdCfg<kBF16, 256>::DQ_ROWS : BwdCfg<kBF16, 128>::DQ_ROWS;
+}
+int bwd_dq_dims(int d) {
+  return d == 64 ? BwdCfg<kBF16, 64>::DH : d == 256 ? BwdCfg<kBF16, 256>::DH : BwdCfg<kBF16, 128>::DH;
+}
 
 cudaError_t launch_bwd_dkdv(int dt, int d, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
                             const CUtensorMap& dout, const BwdArgs& a, int max_len, int nz, cudaStream_t st) {

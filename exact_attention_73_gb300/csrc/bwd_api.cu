@@ -18,7 +18,7 @@ attn_status check_common(const void* q, const void* k, const void* v, const void
   for (const void* p : ptrs)
     if (!aligned16(p)) return ATTN_ERR_ALIGN;
   if (Hq < 1 || Hkv < 1 || Hq > 65535) return ATTN_ERR_SHAPE;
-  if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;   // the backward kernel is built for d = 64 and 128
+  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_HEADDIM;
   if (Hq % Hkv) return ATTN_ERR_GQA;
   if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_DTYPE;
   if (ws_bytes < ws_need) return ATTN_ERR_WORKSPACE;
@@ -51,7 +51,7 @@ attn_status run_bwd(const void* q, const void* k, const void* v, const void* o, 
       !operand_map(&tv, v, dtype, d, packed, B, Hkv, rows_or_T, 128) ||
       !operand_map(&tq, q, dtype, d, packed, B, Hq, rows_or_T, 64) ||
       !operand_map(&tdo, dout, dtype, d, packed, B, Hq, rows_or_T, 64) ||
-      !accum_map(&tdq, dq_acc, d, packed, B, Hq, rows_or_T, bwd_dq_rows(d)))
+      !accum_map(&tdq, dq_acc, d, packed, B, Hq, rows_or_T, bwd_dq_rows(d), bwd_dq_dims(d)))
     return ATTN_ERR_CUDA;
   BwdArgs a{};
   a.lse = lse;

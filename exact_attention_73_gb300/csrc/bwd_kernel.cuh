@@ -1,4 +1,4 @@
-// Backward attention kernels for sm_103a (BF16 / FP16, head dim 64 or 128).
+// Backward attention kernels for sm_103a (BF16 / FP16, head dim 64, 128 or 256).
 //
 // Method: FlashAttention-3 (zenmind.me summary) §3.1 backward chain with P
 // recomputed from the forward's log-sum-exp, and §4 step 5 (paper App. B.1):
@@ -34,6 +34,12 @@
 // D = 64: dK and dV take 64 columns each; the dQ^T product keeps M = 128 with
 // its A operand running from K into V (the next 64-dim box in shared memory),
 // so tensor-memory lanes 64..127 hold V^T dS^T, which the drain ignores.
+// D = 256: dK and dV of 128 keys at 256 dims would need all 512 columns, so
+// two CTAs share a key tile and each owns half of the head dimensions of dK,
+// dV and dQ (blockIdx.x = 2 * key tile + half); both compute the full S^T and
+// dP^T (the contraction runs over all 256 dims). K and V of 256 dims leave
+// room for one Q/dO stage only, so the products of one query tile are issued
+// after the previous tile's, without overlap.
 #pragma once
 #include <cmath>
 #include <cstdint>
@@ -65,7 +71,9 @@ struct BwdArgs {
 
 template <int DT, int D>
 struct BwdCfg {
-  static_assert(D == 64 || D == 128, "backward kernel is written for head dim 64 or 128");
+  static_assert(D == 64 || D == 128 || D == 256, "backward kernel is written for head dim 64, 128 or 256");
+  static constexpr int DSPLIT = D == 256 ? 2 : 1;   // CTAs per key tile (each owns DH dims of dK, dV, dQ)
+  static constexpr int DH = D / DSPLIT;
   static constexpr int BR = 64;                     // query rows per iteration
   static constexpr int BC = 128;                    // keys per CTA
   static constexpr int NBOX = D / 64;               // 64-element (128-byte) boxes per row
@@ -74,11 +82,11 @@ struct BwdCfg {
   static constexpr int Q_B = BR * D * 2;            // Q_i or dO_i tile
   static constexpr int Q_BOX_B = BR * 128;
   static constexpr int DS_B = BC * BR * 2;          // dS^T tile [128 keys][64 queries]
-  static constexpr int NQ = D == 64 ? 6 : 4;        // stages of the Q/dO ring
+  static constexpr int NQ = D == 64 ? 6 : (D == 128 ? 4 : 1);   // stages of the Q/dO ring
   static constexpr int LD_B = 2 * BR * 4;           // LSE*log2e and D for one tile
   static constexpr int DQ_ROWS = D == 64 ? BR : BR / 2;   // rows of dQ per reduce-add
   static constexpr int DQ_PARTS = BR / DQ_ROWS;            // reduce-adds per tile
-  static constexpr int DQ_STAGE_B = DQ_ROWS * D * 4;       // FP32 staging for one reduce-add
+  static constexpr int DQ_STAGE_B = DQ_ROWS * DH * 4;      // FP32 staging for one reduce-add
   static constexpr int SMEM_BYTES =
       2 * KV_B + DS_B + NQ * (2 * Q_B) + DQ_STAGE_B + NQ * LD_B + 18 * 8 + 16;   // base is 1024-aligned
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeded");
@@ -91,11 +99,12 @@ struct BwdCfg {
   static_assert(128 * (kRegsCtl + kRegsDrain + 2 * kRegsMath) <= NTHREADS * 128, "register split");
   static constexpr uint32_t FMT = DT == kBF16 ? 1u : 0u;
   static constexpr uint32_t IDESC_SP = instr_desc(128, BR, FMT, FMT, 0, 0);
-  static constexpr uint32_t IDESC_KV = instr_desc(128, D, FMT, FMT, 0, 1);
+  static constexpr uint32_t IDESC_KV = instr_desc(128, DH, FMT, FMT, 0, 1);
   static constexpr uint32_t IDESC_DQ = instr_desc(128, BR, FMT, FMT, 1, 1);   // M = 128 also for D = 64
   // within score buffer X (base 128X)
   static constexpr uint32_t COL_S = 0, COL_DP = 64, COL_P = 0, COL_DQ = 32, COL_DS = 96;
-  static constexpr uint32_t COL_DV = 256, COL_DK = 256 + D;
+  static constexpr uint32_t COL_DV = 256, COL_DK = 256 + DH;
+  static_assert(COL_DK + DH <= 512, "tensor memory overflow");
 };
 
 // kDQ = false: dK and dV only (the deterministic backward computes dQ in a
@@ -148,7 +157,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     seq0 = 0;
     L = a.N;
   }
-  const int j = blockIdx.x;                 // key tile; with causal masking tile 0 has the most work
+  const int j = blockIdx.x / C::DSPLIT;     // key tile; with causal masking tile 0 has the most work
+  const int dh = blockIdx.x % C::DSPLIT;    // which DH head dims of dK, dV, dQ this CTA owns
   if (j * C::BC >= L) return;
   // query tiles holding a query that sees a key of this tile
   const int klast = min(j * C::BC + C::BC, L) - 1;
@@ -263,11 +273,15 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       // start-address field (16-byte units) for each K step and stage.
       const uint64_t dK_kmaj = smem_desc(smem_u32(sK), 16, 1024, kSwizzle128);
       const uint64_t dV_kmaj = smem_desc(smem_u32(sV), 16, 1024, kSwizzle128);
-      const uint64_t dK_mn = smem_desc(smem_u32(sK), C::KV_BOX_B, 1024, kSwizzle128);
+      // K^T for this CTA's head dims (boxes of 64 dims, KV_BOX_B apart)
+      const uint64_t dK_mn = smem_desc(smem_u32(sK) + dh * (C::DH / 64) * C::KV_BOX_B, C::KV_BOX_B, 1024,
+                                       kSwizzle128);
       const uint64_t dQ0_kmaj = smem_desc(smem_u32(sQ), 16, 1024, kSwizzle128);
       const uint64_t ddO0_kmaj = smem_desc(smem_u32(sdO), 16, 1024, kSwizzle128);
-      const uint64_t dQ0_mn = smem_desc(smem_u32(sQ), C::Q_BOX_B, 1024, kSwizzle128);
-      const uint64_t ddO0_mn = smem_desc(smem_u32(sdO), C::Q_BOX_B, 1024, kSwizzle128);
+      // Q_i and dO_i as MN-major B of dK and dV: this CTA's head dims only
+      const uint32_t dh_off = dh * (C::DH / 64) * C::Q_BOX_B;
+      const uint64_t dQ0_mn = smem_desc(smem_u32(sQ) + dh_off, C::Q_BOX_B, 1024, kSwizzle128);
+      const uint64_t ddO0_mn = smem_desc(smem_u32(sdO) + dh_off, C::Q_BOX_B, 1024, kSwizzle128);
       const uint64_t dDS0_mn = smem_desc(smem_u32(sDS), C::DS_B, 1024, kSwizzle128);
       auto dadd = [](uint64_t d, uint32_t bytes) { return d + (bytes >> 4); };
       auto issue_sdp = [&](int it) {   // S^T = K Q^T and dP^T = V dO^T into buffer it % 2
@@ -287,31 +301,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         }
         mma_commit(&sp_full[it & 1]);
       };
-      bool ok = mbar_wait(kv_full, 0, a.status) && mbar_wait(&q_full[0], 0, a.status);
-      if (ok) {
-        tc_fence_after();
-        issue_sdp(0);
-      }
-      for (int it = 0; it < niter && ok; ++it) {
-        const int st = it % C::NQ;
+      // dQ^T first, so the drain warps can read it while dV and dK run and
+      // the next S^T/dP^T never waits for an empty tensor pipe
+      auto issue_grads = [&](int it) {
         const uint32_t xb = tbase + 128u * (it & 1);
-        if (it + 1 < niter) {
-          // buffer (it+1)%2 was last used by it-1: its dQ^T halves must be drained
-          const int sn = (it + 1) % C::NQ;
-          if (!(ok = mbar_wait(&q_full[sn], ((it + 1) / C::NQ) & 1, a.status))) break;
-          if (kDQ && !(ok = mbar_wait(dq_empty, (it & 1) ^ 1, a.status))) break;
-          tc_fence_after();
-          issue_sdp(it + 1);
-        }
-        if (!(ok = mbar_wait(ds_ready, it & 1, a.status))) break;
-        // The drain warps wait on dq_full by parity. On the last tile there is
-        // no S^T/dP^T issue (and no dq_empty wait) above, so wait here for the
-        // drain of it-1: dq_full then never runs two phases ahead of them.
-        if (kDQ && it + 1 >= niter && it > 0 && !(ok = mbar_wait(dq_empty, (it & 1) ^ 1, a.status))) break;
-        tc_fence_after();
-        const uint32_t so = st * C::Q_B;
-        // dQ^T first, so the drain warps can read it while dV and dK run and
-        // the next S^T/dP^T never waits for an empty tensor pipe
+        const uint32_t so = (it % C::NQ) * C::Q_B;
         if constexpr (kDQ) {
 #pragma unroll
           for (int kk = 0; kk < C::BC / 16; ++kk) {   // dQ^T = K^T dS^T, both MN-major
@@ -330,7 +324,44 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
           mma_ts<false>(tbase + C::COL_DK, xb + C::COL_DS + kk * 8, dadd(dQ0_mn, so + kk * 2048), C::IDESC_KV,
                         (it > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&q_empty[st]);
+        mma_commit(&q_empty[it % C::NQ]);
+      };
+      bool ok = mbar_wait(kv_full, 0, a.status);
+      if constexpr (C::NQ == 1) {
+        // one Q/dO stage: tile it's products, then tile it+1's
+        for (int it = 0; it < niter && ok; ++it) {
+          if (!(ok = mbar_wait(&q_full[0], it & 1, a.status))) break;
+          // buffer it%2 was last used by it-2, whose dQ^T was drained before it-1's
+          if (kDQ && it > 0 && !(ok = mbar_wait(dq_empty, (it - 1) & 1, a.status))) break;
+          tc_fence_after();
+          issue_sdp(it);
+          if (!(ok = mbar_wait(ds_ready, it & 1, a.status))) break;
+          tc_fence_after();
+          issue_grads(it);
+        }
+      } else {
+        ok = ok && mbar_wait(&q_full[0], 0, a.status);
+        if (ok) {
+          tc_fence_after();
+          issue_sdp(0);
+        }
+        for (int it = 0; it < niter && ok; ++it) {
+          if (it + 1 < niter) {
+            // buffer (it+1)%2 was last used by it-1: its dQ^T halves must be drained
+            const int sn = (it + 1) % C::NQ;
+            if (!(ok = mbar_wait(&q_full[sn], ((it + 1) / C::NQ) & 1, a.status))) break;
+            if (kDQ && !(ok = mbar_wait(dq_empty, (it & 1) ^ 1, a.status))) break;
+            tc_fence_after();
+            issue_sdp(it + 1);
+          }
+          if (!(ok = mbar_wait(ds_ready, it & 1, a.status))) break;
+          // The drain warps wait on dq_full by parity. On the last tile there is
+          // no S^T/dP^T issue (and no dq_empty wait) above, so wait here for the
+          // drain of it-1: dq_full then never runs two phases ahead of them.
+          if (kDQ && it + 1 >= niter && it > 0 && !(ok = mbar_wait(dq_empty, (it & 1) ^ 1, a.status))) break;
+          tc_fence_after();
+          issue_grads(it);
+        }
       }
       mma_commit(done);
     }
@@ -443,11 +474,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(done, 0, a.status));
     tc_fence_after();
-    if (ok) {   // dV rows, columns D/2*half .. +D/2-1
+    if (ok) {   // dV rows, this CTA's columns, DH/2 per group
       const long long off = static_cast<long long>(b) * a.k_sb + static_cast<long long>(hkv) * a.k_sh +
                             static_cast<long long>(seq0 + kloc) * a.k_sn;
 #pragma unroll 1
-      for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
+      for (int c = half * (C::DH / 64); c < (half + 1) * (C::DH / 64); ++c) {
         uint32_t v[32];
         tmem_ld32(tbase + lane_off + C::COL_DV + 32 * c, v);
         tmem_wait_ld();
@@ -458,7 +489,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
           pk[e] = (DT == kBF16) ? pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]))
                                 : pack_f16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
         if (kvalid) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dv) + off + 32 * c);
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dv) + off + dh * C::DH + 32 * c);
 #pragma unroll
           for (int w = 0; w < 4; ++w) dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
         }
@@ -495,15 +526,15 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       for (int part = 0; part < C::DQ_PARTS; ++part) {
         if (threadIdx.x == 256) bulk_wait_read_all();   // previous reduce-add has read the buffer
         named_bar_sync(1, 128);
-        if (dim < D) {                                  // D = 64: lanes 64..127 are not dQ
+        if (dim < C::DH) {                              // D = 64: lanes 64..127 are not dQ
           if constexpr (C::DQ_PARTS == 2) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) sDQ[e * D + dim] = __uint_as_float(part == 0 ? x0[e] : x1[e]);
+            for (int e = 0; e < 32; ++e) sDQ[e * C::DH + dim] = __uint_as_float(part == 0 ? x0[e] : x1[e]);
           } else {
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-              sDQ[e * D + dim] = __uint_as_float(x0[e]);
-              sDQ[(e + 32) * D + dim] = __uint_as_float(x1[e]);
+              sDQ[e * C::DH + dim] = __uint_as_float(x0[e]);
+              sDQ[(e + 32) * C::DH + dim] = __uint_as_float(x1[e]);
             }
           }
         }
@@ -511,8 +542,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         named_bar_sync(1, 128);
         if (threadIdx.x == 256) {
           const int row = q0 + C::DQ_ROWS * part;
-          if (packed) tma_reduce_add_4d(&tmdQ, sDQ, 0, h, seq0 + row, 0);
-          else tma_reduce_add_4d(&tmdQ, sDQ, 0, row, h, b);
+          if (packed) tma_reduce_add_4d(&tmdQ, sDQ, dh * C::DH, h, seq0 + row, 0);
+          else tma_reduce_add_4d(&tmdQ, sDQ, dh * C::DH, row, h, b);
           bulk_commit();
         }
       }
@@ -525,7 +556,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       const long long off = static_cast<long long>(b) * a.k_sb + static_cast<long long>(hkv) * a.k_sh +
                             static_cast<long long>(seq0 + kloc) * a.k_sn;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < C::DH / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(tbase + lane_off + C::COL_DK + 32 * c, v);
         tmem_wait_ld();
@@ -537,7 +568,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
           pk[e] = (DT == kBF16) ? pack_bf16x2(x0, x1) : pack_f16x2(x0, x1);
         }
         if (kloc < L) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dk) + off + 32 * c);
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dk) + off + dh * C::DH + 32 * c);
 #pragma unroll
           for (int w = 0; w < 4; ++w) dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
         }

@@ -25,10 +25,13 @@ cudaError_t launch_bwd_pre(int dt, int d, const void* o, const void* dout, float
 cudaError_t launch_bwd_main(int dt, int d, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
                             const CUtensorMap& dout, const CUtensorMap& dq_acc, const BwdArgs& a, int max_len, int nz,
                             cudaStream_t st);
-// FP32 accumulator map (layout of the operands, no swizzle), boxes of d x box_rows.
-bool accum_map(CUtensorMap* m, const float* base, int d, bool packed, int B, int H, long long rows, int box_rows);
-// Rows of the dQ accumulator per reduce-add of the main kernel (the box of its map).
+// FP32 accumulator map (layout of the operands, no swizzle), boxes of box_e x box_rows.
+bool accum_map(CUtensorMap* m, const float* base, int d, bool packed, int B, int H, long long rows, int box_rows,
+               int box_e);
+// Rows and head dims of the dQ accumulator per reduce-add of the main kernel
+// (the box of its map).
 int bwd_dq_rows(int d);
+int bwd_dq_dims(int d);
 cudaError_t launch_bwd_dkdv(int dt, int d, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
                             const CUtensorMap& dout, const BwdArgs& a, int max_len, int nz, cudaStream_t st);
 cudaError_t launch_bwd_dq(int dt, const CUtensorMap& q, const CUtensorMap& dout, const CUtensorMap& k,

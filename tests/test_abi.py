@@ -91,7 +91,7 @@ def test_argument_checks_before_any_device_work(lib):
     args = [P(16)] * 9
     assert lib.attn_bwd(*args, None, ws, 1, 2, 1, 8, 128, 0.1, 0, 0, None) == 1
     assert lib.attn_bwd(*args, P(16), ws - 1, 1, 2, 1, 8, 128, 0.1, 0, 0, None) == 7
-    assert lib.attn_bwd(*args, P(16), ws, 1, 2, 1, 8, 256, 0.1, 0, 0, None) == 4  # backward: d = 64 or 128
+    assert lib.attn_bwd(*args, P(16), ws, 1, 2, 1, 8, 96, 0.1, 0, 0, None) == 4   # backward: d = 64, 128, 256
     assert lib.attn_bwd(*args, P(16), ws, 1, 2, 1, 8, 64, 0.1, 0, 0, None) == 11  # d = 64 valid: no device here
     # sliding window: bounds are -1 (unbounded) or >= 0
     assert lib.attn_fwd_window(P(16), P(16), P(16), P(16), P(16), 1, 2, 1, 8, 64, 0.1, -2, 0, 0, None) == 3

@@ -42,7 +42,7 @@ def run_dense(q, k, v, do, causal):
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("n", [1, 64, 200, 640, 1000])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_dense_gqa_ragged(dtype, causal, n, d):
     q, k, v, do = inputs.normal(200 + n + d, [(2, 4, n, d), (2, 2, n, d), (2, 2, n, d), (2, 4, n, d)],
                                 dtype=dtype)
@@ -62,7 +62,7 @@ def test_two_calls_reuse_workspace():
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_varlen_small(causal, d):
     lens = [1, 127, 128, 300, 1000, 5]
     cu = inputs.cu_seqlens(lens)

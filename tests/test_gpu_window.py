@@ -98,7 +98,7 @@ def run_bwd(q, k, v, do, window):
 
 @pytest.mark.parametrize("window", WINDOWS)
 @pytest.mark.parametrize("n", [200, 700])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_backward_window(window, n, d):
     q, k, v, do = inputs.normal(320 + n, [(2, 4, n, d), (2, 2, n, d), (2, 2, n, d), (2, 4, n, d)])
     got = run_bwd(q, k, v, do, window)
