@@ -145,20 +145,23 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int hkv = blockIdx.y;
+  // with causal masking key tile 0 has the most work: heavy tiles start first
+  int bx = blockIdx.x, by = blockIdx.y, bz = blockIdx.z;
+  if (a.causal) heavy_first_order<16>(bx, by, bz);
+  const int hkv = by;
   const bool packed = a.cu_seqlens != nullptr;
   int b, seq0, L;
   if (packed) {
     b = 0;
-    seq0 = a.cu_seqlens[blockIdx.z];
-    L = a.cu_seqlens[blockIdx.z + 1] - seq0;
+    seq0 = a.cu_seqlens[bz];
+    L = a.cu_seqlens[bz + 1] - seq0;
   } else {
-    b = blockIdx.z;
+    b = bz;
     seq0 = 0;
     L = a.N;
   }
-  const int j = blockIdx.x / C::DSPLIT;     // key tile; with causal masking tile 0 has the most work
-  const int dh = blockIdx.x % C::DSPLIT;    // which DH head dims of dK, dV, dQ this CTA owns
+  const int j = bx / C::DSPLIT;             // key tile
+  const int dh = bx % C::DSPLIT;            // which DH head dims of dK, dV, dQ this CTA owns
   if (j * C::BC >= L) return;
   // query tiles holding a query that sees a key of this tile
   const int klast = min(j * C::BC + C::BC, L) - 1;

@@ -151,19 +151,23 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
   const int lane = threadIdx.x & 31;
   const bool packed = a.cu_seqlens != nullptr;
   int h, hkv, b, seq0, L, nqt, qt0, kv0, nkv;
-  h = blockIdx.y;
+  // with causal masking the last query tiles have the most work: they start
+  // first, those of every (head, batch) in the first waves
+  int bx = blockIdx.x, by = blockIdx.y, bz = blockIdx.z;
+  if (a.causal) heavy_first_order<8>(bx, by, bz);
+  h = by;
   if (packed) {
     b = 0;
-    seq0 = a.cu_seqlens[blockIdx.z];
-    L = a.cu_seqlens[blockIdx.z + 1] - seq0;
+    seq0 = a.cu_seqlens[bz];
+    L = a.cu_seqlens[bz + 1] - seq0;
   } else {
-    b = blockIdx.z;
+    b = bz;
     seq0 = 0;
     L = a.N;
   }
   nqt = (L + 127) >> 7;
   // Causal CTAs with the most KV tiles start first.
-  const int cblk = a.causal ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
+  const int cblk = a.causal ? static_cast<int>(gridDim.x) - 1 - bx : bx;
   qt0 = cblk * QT;
   if (qt0 >= nqt) return;   // whole CTA leaves before any set-up
   // KV tiles that hold a key visible to some query row of this CTA

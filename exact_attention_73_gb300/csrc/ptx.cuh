@@ -327,6 +327,27 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 
 __device__ __forceinline__ int warp_any(int pred) { return __any_sync(0xffffffffu, pred); }
 
+// Dispatch order for grids whose CTAs do unequal work, heaviest at x = 0
+// (causal masking). CTAs start in linear order (x fastest), so with the plain
+// mapping the heavy CTAs of the last (y, z) pairs start last and set a long
+// tail. This maps the linear index to (x, y, z) in blocks of JB consecutive x
+// of one (y, z) pair, block by block from the heaviest x: every pair's heavy
+// CTAs start in the first waves, and the CTAs running together still share a
+// pair's data in L2 (JB of them per pair).
+template <int JB>
+__device__ __forceinline__ void heavy_first_order(int& x, int& y, int& z) {
+  const int nx = static_cast<int>(gridDim.x), ny = static_cast<int>(gridDim.y);
+  const int groups = ny * static_cast<int>(gridDim.z);
+  const int lin = static_cast<int>(blockIdx.x) + nx * (static_cast<int>(blockIdx.y) + ny * static_cast<int>(blockIdx.z));
+  const int blk = lin / (JB * groups);
+  const int width = min(JB, nx - blk * JB);       // the last block may be narrower
+  const int rem = lin - blk * JB * groups;
+  const int g = rem / width;
+  x = blk * JB + rem % width;
+  y = g % ny;
+  z = g / ny;
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
