@@ -586,7 +586,7 @@ def decode_main(args, world, rank):
                          "traffic": measured_traffic(f"{args.workload}:decode")},
             "e2e": {"value": world * r["bytes"] * args.steps / (r["ms_e2e"] * 1e-3) / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
-            "gpu_launches": 2 * args.steps, "clocks": r["clocks"]}
+            "gpu_launches": 2 * 2 * args.steps, "clocks": r["clocks"]}   # device-timed and e2e steps
     if "cpu" in r:
         line["cpu_baseline"] = {"value": r["cpu"][0], "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
                                 "sample": "one sequence of the workload (seeded E4M3 codes, unit factors): "
@@ -742,7 +742,7 @@ def varlen_main(args, world, rank):
                          "traffic": measured_traffic(f"{args.workload}:bwd")},
             "e2e": {"value": job_tflops(3.5 * f, args.steps, world, r["ms_e2e"]), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
-            "gpu_launches": 4 * args.steps, "clocks": r["clocks"]}
+            "gpu_launches": 2 * 4 * args.steps, "clocks": r["clocks"]}   # device-timed and e2e steps
     if "cpu" in r:
         line["cpu_baseline"] = {"value": r["cpu"][0], "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
                                 "sample": f"one head of the {min(r['lens'])}-token sequence, fwd + bwd: "
@@ -752,6 +752,66 @@ def varlen_main(args, world, rank):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+SWEEP = [  # (B, H, N, d): the BF16 sweep configuration, B * N = 16384 tokens
+    (32, 16, 512, 128), (16, 16, 1024, 128), (8, 16, 2048, 128), (4, 16, 4096, 128), (2, 16, 8192, 128),
+    (1, 16, 16384, 128), (2, 32, 8192, 64), (2, 8, 8192, 256)]
+
+
+def sweep(args):
+    """Forward (BF16 and FP8) and, at N = 8192, backward TFLOP/s of every sweep
+    point, causal and not: `steps` launches each after 3 warm-up launches,
+    CUDA events; inputs drawn on the device (N(0,1), bf16), above L2 at every
+    point. Prints one JSON line per point (not the benchmark line)."""
+    import torch
+    from exact_attention_73_gb300 import binding as L
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    L.load(build_if_missing=True)
+    stream = torch.cuda.current_stream(dev)
+    gen = torch.Generator(device=dev).manual_seed(1)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / args.steps
+
+    for B, H, N, d in SWEEP:
+        q, k, v, do = (torch.randn((B, H, N, d), generator=gen, device=dev).to(torch.bfloat16) for _ in range(4))
+        o, lse = torch.empty_like(q), torch.empty((B, H, N), device=dev)
+        nb = (N + 127) // 128
+        codes = []
+        for x in (q, k, v):
+            x8, sc = torch.empty(x.shape, dtype=torch.uint8, device=dev), torch.empty((B, H, nb), device=dev)
+            L.attn_quantize_fp8(x, x8, sc)
+            codes += [x8, sc]
+        q8, sq, k8, sk, v8, sv = codes
+        row = {"B": B, "H": H, "N": N, "d": d}
+        for causal in (False, True):
+            f = fwd_flops(B, H, N, d, causal)
+            tag = "causal" if causal else "non_causal"
+            ms = timed(lambda: L.attn_fwd(q, k, v, o, lse, causal=causal))
+            row[f"fwd_bf16_{tag}"] = round(f / ms / 1e9, 1)
+            ms = timed(lambda: L.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, o, lse, causal=causal))
+            row[f"fwd_fp8_{tag}"] = round(f / ms / 1e9, 1)
+            if N == 8192:
+                L.attn_fwd(q, k, v, o, lse, causal=causal)
+                dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+                ws = torch.empty((L.attn_bwd_workspace_size(B, H, H, N, d),), dtype=torch.uint8, device=dev)
+                ms = timed(lambda: L.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, ws, causal=causal))
+                row[f"bwd_bf16_{tag}"] = round(2.5 * f / ms / 1e9, 1)
+        if L.attn_get_device_status() != 0:
+            raise RuntimeError("device-side wait timed out during the sweep")
+        print(json.dumps(row), flush=True)
+        del q, k, v, do, o, lse, codes, q8, sq, k8, sk, v8, sv
 
 
 def cpu_cores():
@@ -827,7 +887,12 @@ def main():
     ap.add_argument("--write-traffic", metavar="CSV",
                     help="write profiles/traffic.json from an ncu --csv capture of the default workload's "
                          "dram__bytes_read.sum/dram__bytes_write.sum, then exit")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the forward (BF16, FP8) and backward over the sweep points instead, one JSON line "
+                         "per point")
     args = ap.parse_args()
+    if args.sweep:
+        return sweep(args)
     if args.write_traffic:
         print(json.dumps(write_traffic(args.write_traffic, {
             r"fwd_kernel<\(?int\)?0|fwd_kernel<0": f"{DEFAULT}:fwd", r"bwd_kernel": f"{DEFAULT}:bwd",
@@ -911,7 +976,9 @@ def main():
                                        "from the current kernel sources" if traffic is not None else
                                        "no ncu capture of the current kernel sources"},
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
-        "gpu_launches": (4 if window is not None else LAUNCHES_PER_STEP) * args.steps,
+        # the library's launches inside the timed regions: the device-timed
+        # steps and the end-to-end steps (plus the FP8 config's launches below)
+        "gpu_launches": 2 * (4 if window is not None else LAUNCHES_PER_STEP) * args.steps,
         "clocks": r["clocks"],
     }
     if r.get("fp8_config"):
@@ -925,7 +992,7 @@ def main():
                       "frac_of_fp8_peak": ff / (2 if c else 1) / ms / 1e9 / (2 * pk["bf16_burst"])}
                for c, name, ms in ((False, "non_causal", r["fp8_config"][False]),
                                    (True, "causal", r["fp8_config"][True]))}}
-        line["gpu_launches"] += 2 * (args.steps + 3) + 3
+        line["gpu_launches"] += 2 * args.steps
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         fl, sec = cpu_sample(wl)
         line["cpu_baseline"] = {"value": fl / sec / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
