@@ -89,14 +89,15 @@ struct FwdCfg {
   static constexpr uint32_t FMT = DT == kBF16 ? 1u : 0u;    // BF16=1, F16=0, E4M3=0
   static constexpr uint32_t IDESC_S = instr_desc(128, 128, FMT, FMT, 0, 0);
   static constexpr uint32_t IDESC_O = instr_desc(128, D, FMT, FMT, 0, 1);
-  // Rescale threshold (log2 units): keep a stale max while exp2(x - m) <= 2^kTau.
-  // BF16/FP16 keep a stale max (P~ <= 2^8 is rounded to 8 significant bits, and
-  // O is rescaled only when the max moves far). FP8 uses the running max of
-  // Algorithm 1 itself: each row's largest entry is then P~ = 1, exact in
-  // E4M3, and a stale max measurably raises the error of the E4M3 rounding.
-  static constexpr float kTau = kFp8 ? 0.0f : 8.0f;
+  // Rescale threshold (log2 units): keep a stale max while exp2(x - m) <= 2^kTau,
+  // so O in tensor memory is rescaled only when the max moves far. The exact
+  // running max of Algorithm 1 (kTau = 0) would rescale O in most KV steps;
+  // for FP8 it also rounds each row's largest entry of P~ exactly, so the
+  // stale max costs a little accuracy there (bounded by one E4M3 step per
+  // entry against the exact-max rounding).
+  static constexpr float kTau = kFp8 ? 4.0f : 8.0f;
   // Power-of-two shift of P~ before its E4M3 rounding.
-  static constexpr int kPShift = 4;   // FP8: P~ <= 1, so P~ * 2^kPShift <= 16 < 448
+  static constexpr int kPShift = 4;   // P~ <= 2^kTau, so P~ * 2^kPShift <= 256 < 448
 };
 
 __device__ __forceinline__ int pow2_exponent_of(float x) {   // x an exact power of two

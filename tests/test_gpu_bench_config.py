@@ -81,7 +81,7 @@ def test_fp8_forward_sampled_heads():
         for (c, f), (g8, gs) in zip(mine, codes):
             assert np.array_equal(one(g8).cpu().numpy(), c) and np.array_equal(one(gs).cpu().numpy(), f)
         (rq8, rsq), (rk8, rsk), (rv8, rsv) = mine
-        emu, _ = F.attention_fp8(rq8, rk8, rv8, rsq, rsk, rsv, D ** -0.5, rows=rows,
+        emu, _ = F.attention_fp8(rq8, rk8, rv8, rsq, rsk, rsv, D ** -0.5, rows=rows, tau=F.STALE_MAX_TAU,
                                  kv_tile=L.attn_fwd_fp8_kv_tile(D))
         exact, _ = A.forward_rows(q[b, h], k[b, h], v[b, h], rows, D ** -0.5)
         got = o[b, h, rows]

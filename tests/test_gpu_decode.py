@@ -60,7 +60,8 @@ def run_case(B, Hq, Hkv, nmax, d, lens, splits, seed):
     for name, a, b in (("q8", q8.view(B, Hkv, g, d), rq8), ("sq", sq, rsq), ("k8", k8, rk8), ("sk", sk, rsk),
                        ("v8", v8, rv8), ("sv", sv, rsv)):
         assert np.array_equal(a.cpu().numpy(), b), name
-    o_ref, lse_ref = F.decode_fp8(rq8, rsq, rk8, rv8, rsk, rsv, lens, d ** -0.5, tps)
+    # the emulation of the kernel's bookkeeping (stale running max)
+    o_ref, lse_ref = F.decode_fp8(rq8, rsq, rk8, rv8, rsk, rsv, lens, d ** -0.5, tps, tau=F.STALE_MAX_TAU)
     return o.double().cpu().numpy().reshape(B, Hkv, g, d), lse.cpu().numpy().reshape(B, Hkv, g), o_ref, lse_ref, \
         (q, k, v)
 
