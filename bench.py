@@ -851,17 +851,22 @@ def measured_traffic(key):
     return e
 
 
-def write_traffic(csv_path, keys):
+def write_traffic(csv_path, keys, step_launches=None):
     """Write profiles/traffic.json from an ncu --csv launch list holding
     dram__bytes_read.sum and dram__bytes_write.sum: `keys` maps a kernel-name
-    regex to the traffic key; the last captured launch of each kernel is used.
-    Records the current kernel source hash with the numbers."""
+    regex to the traffic key; the last captured launch of each kernel among
+    the first `step_launches` launches (the benchmark steps, before the FP8
+    configuration's launches) is used. Records the current kernel source hash
+    with the numbers."""
     import csv
     import re
     rows = list(csv.reader(l for l in open(csv_path) if l.startswith('"')))
     head = rows[0]
     ki, mi, vi, ui = head.index("Kernel Name"), head.index("Metric Name"), head.index("Metric Value"), \
         head.index("Metric Unit")
+    ii = head.index("ID")
+    if step_launches is not None:
+        rows = [head] + [r for r in rows[1:] if int(r[ii]) < step_launches]
     scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
     per = {}
     for r in rows[1:]:
@@ -894,9 +899,12 @@ def main():
     if args.sweep:
         return sweep(args)
     if args.write_traffic:
+        # a capture of `bench.py --steps S --warmup W`: (W + S + 2 + S) steps of
+        # LAUNCHES_PER_STEP launches come before the FP8 configuration's
+        steps = args.warmup + args.steps + 2 + args.steps
         print(json.dumps(write_traffic(args.write_traffic, {
             r"fwd_kernel<\(?int\)?0|fwd_kernel<0": f"{DEFAULT}:fwd", r"bwd_kernel": f"{DEFAULT}:bwd",
-            r"fwd_kernel<\(?int\)?2|fwd_kernel<2": f"{DEFAULT}:fwd_fp8"})))
+            r"fwd_kernel<\(?int\)?2|fwd_kernel<2": f"{DEFAULT}:fwd_fp8"}, steps * LAUNCHES_PER_STEP)))
         return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
