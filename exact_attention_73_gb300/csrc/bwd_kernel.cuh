@@ -15,18 +15,20 @@
 // with the score buffers doubled so that S^T/dP^T of the next query tile are
 // computed while the current one is being turned into P^T/dS^T:
 //   buffer X (X = 0, 1) at cols 128X: S^T [128 keys x 64 queries] at +0..63
-//   and dP^T at +64..127; once both are in registers they are replaced by
-//     +0..31   P^T  (BF16 pairs)
-//     +32..95  dQ^T [128 dims x 64 queries] (FP32, one N = 64 product)
-//     +96..127 dS^T (BF16 pairs)
-//   dV [128 keys x 128 dims] cols 256..383, dK cols 384..511.
+//   and dP^T at +64..127. Once they are in registers, P^T and dS^T (BF16
+//   pairs) and dQ^T [128 dims x 64 queries] (FP32, one N = 64 product) take
+//   their place: for D = 128 at +0..31, +96..127 and +32..95; for D = 64 and
+//   256 each group g (queries 32g..32g+31) writes P^T and dS^T over its own
+//   S^T columns (+32g+0..15, +32g+16..31) and dQ^T replaces dP^T (+64..127).
+//   dV [128 keys x D dims] from col 256, dK after it.
 // Registers are split per warpgroup (setmaxnreg): load/MMA 88, dQ drain 88,
 // each P^T/dS^T warpgroup 168 (launch: 128 for all 512 threads).
 // Warp roles: warp 0 loads (TMA for K, V, Q_i, dO_i; plain loads for LSE and
 // D), warp 1 issues tcgen05.mma, warps 4-7 and 12-15 turn S^T/dP^T into
 // P^T/dS^T (one key per thread; the first group takes queries 0..31 of the
-// tile, the second 32..63; the two meet at a barrier between loading S^T/dP^T
-// and writing P^T/dS^T over them) and also store dS^T to shared memory
+// tile, the second 32..63; for D = 128 they meet at a barrier between loading
+// S^T/dP^T and writing P^T/dS^T, for D = 64 and 256 neither writes columns the
+// other reads and they run independently) and also store dS^T to shared memory
 // (double-buffered, 128-byte swizzle) for the dQ product, warps 8-11 drain
 // dQ^T (one head-dim index per thread) into
 // a [rows][D] FP32 tile in shared memory, which one thread adds into the
@@ -87,8 +89,10 @@ struct BwdCfg {
   static constexpr int DQ_ROWS = D == 64 ? BR : BR / 2;   // rows of dQ per reduce-add
   static constexpr int DQ_PARTS = BR / DQ_ROWS;            // reduce-adds per tile
   static constexpr int DQ_STAGE_B = DQ_ROWS * DH * 4;      // FP32 staging for one reduce-add
+  // kv_full, q_full[NQ], q_empty[NQ], sp_full[2], ds_ready[2][2], dq_full, dq_empty, done
+  static constexpr int NBARS = 1 + 2 * NQ + 2 + 4 + 3;
   static constexpr int SMEM_BYTES =
-      2 * KV_B + DS_B + NQ * (2 * Q_B) + DQ_STAGE_B + NQ * LD_B + 18 * 8 + 16;   // base is 1024-aligned
+      2 * KV_B + DS_B + NQ * (2 * Q_B) + DQ_STAGE_B + NQ * LD_B + NBARS * 8 + 16;   // base is 1024-aligned
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeded");
   static constexpr int NTHREADS = 512;
   // Registers: the launch gives 128 per thread (the whole register file);
@@ -102,7 +106,17 @@ struct BwdCfg {
   static constexpr uint32_t IDESC_KV = instr_desc(128, DH, FMT, FMT, 0, 1);
   static constexpr uint32_t IDESC_DQ = instr_desc(128, BR, FMT, FMT, 1, 1);   // M = 128 also for D = 64
   // within score buffer X (base 128X)
-  static constexpr uint32_t COL_S = 0, COL_DP = 64, COL_P = 0, COL_DQ = 32, COL_DS = 96;
+  // Score buffer layout. D = 64, 256: group g's P^T and dS^T go over its own
+  // S^T columns (32g + 0..15 and 32g + 16..31) and dQ^T over dP^T, so neither
+  // group writes columns the other still has to read and the groups run
+  // independently. D = 128 (measured faster): P^T at +0..31, dQ^T at +32..95,
+  // dS^T at +96..127, and the groups meet at a barrier between loading their
+  // scores and overwriting them.
+  static constexpr bool kOwnCols = D != 128;
+  static constexpr uint32_t COL_S = 0, COL_DP = 64, COL_DQ = kOwnCols ? 64 : 32;
+  // columns of P^T and dS^T for the 16 queries of K step kk, and of group g's writes
+  __host__ __device__ static constexpr uint32_t col_p(int kk) { return kOwnCols ? 32 * (kk >> 1) + 8 * (kk & 1) : 8 * kk; }
+  __host__ __device__ static constexpr uint32_t col_ds(int kk) { return kOwnCols ? col_p(kk) + 16 : 96 + 8 * kk; }
   static constexpr uint32_t COL_DV = 256, COL_DK = 256 + DH;
   static_assert(COL_DK + DH <= 512, "tensor memory overflow");
 };
@@ -137,8 +151,12 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
   uint64_t* q_full = bars + 1;
   uint64_t* q_empty = q_full + C::NQ;
   uint64_t* sp_full = q_empty + C::NQ;             // [2], one per score buffer
+  // P^T/dS^T ready. With independent groups (kOwnCols) one barrier per score
+  // buffer and group, [buffer][group]: a group that runs a tile ahead of the
+  // other arrives on the other buffer's barrier, never on this tile's. For
+  // D = 128 the groups meet every tile and one barrier of 256 serves.
   uint64_t* ds_ready = sp_full + 2;
-  uint64_t* dq_full = ds_ready + 1;
+  uint64_t* dq_full = ds_ready + 4;
   uint64_t* dq_empty = dq_full + 1;
   uint64_t* done = dq_empty + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
@@ -192,7 +210,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     }
     mbar_init(&sp_full[0], 1);
     mbar_init(&sp_full[1], 1);
-    mbar_init(ds_ready, 256);
+    if constexpr (C::kOwnCols) {
+      for (int i = 0; i < 4; ++i) mbar_init(&ds_ready[i], 128);
+    } else {
+      mbar_init(&ds_ready[0], 256);
+    }
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 128);
     mbar_init(done, 1);
@@ -287,6 +309,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       const uint64_t ddO0_mn = smem_desc(smem_u32(sdO) + dh_off, C::Q_BOX_B, 1024, kSwizzle128);
       const uint64_t dDS0_mn = smem_desc(smem_u32(sDS), C::DS_B, 1024, kSwizzle128);
       auto dadd = [](uint64_t d, uint32_t bytes) { return d + (bytes >> 4); };
+      auto ds_wait = [&](int it) {   // P^T and dS^T of tile it are in tensor memory
+        if constexpr (C::kOwnCols)
+          return mbar_wait(&ds_ready[(it & 1) * 2], (it >> 1) & 1, a.status) &&
+                 mbar_wait(&ds_ready[(it & 1) * 2 + 1], (it >> 1) & 1, a.status);
+        else
+          return mbar_wait(&ds_ready[0], it & 1, a.status);
+      };
       auto issue_sdp = [&](int it) {   // S^T = K Q^T and dP^T = V dO^T into buffer it % 2
         const uint32_t so = (it % C::NQ) * C::Q_B;
         const uint32_t xb = tbase + 128u * (it & 1);
@@ -319,12 +348,12 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         }
 #pragma unroll
         for (int kk = 0; kk < C::BR / 16; ++kk) {   // dV += P^T dO_i
-          mma_ts<false>(tbase + C::COL_DV, xb + C::COL_P + kk * 8, dadd(ddO0_mn, so + kk * 2048), C::IDESC_KV,
+          mma_ts<false>(tbase + C::COL_DV, xb + C::col_p(kk), dadd(ddO0_mn, so + kk * 2048), C::IDESC_KV,
                         (it > 0 || kk > 0) ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < C::BR / 16; ++kk) {   // dK += dS^T Q_i
-          mma_ts<false>(tbase + C::COL_DK, xb + C::COL_DS + kk * 8, dadd(dQ0_mn, so + kk * 2048), C::IDESC_KV,
+          mma_ts<false>(tbase + C::COL_DK, xb + C::col_ds(kk), dadd(dQ0_mn, so + kk * 2048), C::IDESC_KV,
                         (it > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&q_empty[it % C::NQ]);
@@ -338,7 +367,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
           if (kDQ && it > 0 && !(ok = mbar_wait(dq_empty, (it - 1) & 1, a.status))) break;
           tc_fence_after();
           issue_sdp(it);
-          if (!(ok = mbar_wait(ds_ready, it & 1, a.status))) break;
+          if (!(ok = ds_wait(it))) break;
           tc_fence_after();
           issue_grads(it);
         }
@@ -357,7 +386,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
             tc_fence_after();
             issue_sdp(it + 1);
           }
-          if (!(ok = mbar_wait(ds_ready, it & 1, a.status))) break;
+          if (!(ok = ds_wait(it))) break;
           // The drain warps wait on dq_full by parity. On the last tile there is
           // no S^T/dP^T issue (and no dq_empty wait) above, so wait here for the
           // drain of it-1: dq_full then never runs two phases ahead of them.
@@ -412,9 +441,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         reg_fence(sv);
         reg_fence(dp);
       }
-      // Both groups have their scores in registers before either overwrites
-      // columns the other reads; one decision for both groups.
-      ok = named_bar_and(2, 256, got);
+      // D = 128: both groups have their scores in registers before either
+      // overwrites columns the other reads; one decision for both groups
+      if constexpr (!C::kOwnCols) ok = named_bar_and(2, 256, got);
+      else ok = got;
       if (!ok) break;
       const int q0 = q_tile(it) * C::BR + 32 * half;
       // this key against queries q0 .. q0 + 31: outside the sequence or the window?
@@ -456,8 +486,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
           dd[2 * e4 + 1] = pack_f16x2(g23.x, g23.y);
         }
       }
-      tmem_st16(xb + C::COL_P + 16 * half, pp);
-      tmem_st16(xb + C::COL_DS + 16 * half, dd);
+      tmem_st16(xb + C::col_p(2 * half), pp);
+      tmem_st16(xb + C::col_ds(2 * half), dd);
       // dS^T row r, queries 32*half .. +31: 16-byte chunks 4*half .. +3 of a
       // 128-byte row, 128-byte swizzle (chunk ^= row % 8). The tile is free:
       // dQ^T of the previous tile (its only reader) completed before the
@@ -473,7 +503,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       tmem_wait_st();
       if constexpr (kDQ) fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(ds_ready);
+      mbar_arrive(C::kOwnCols ? &ds_ready[(it & 1) * 2 + half] : &ds_ready[0]);
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(done, 0, a.status));
     tc_fence_after();
