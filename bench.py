@@ -66,7 +66,27 @@ VARLEN_WORKLOADS = {
     # 8 sequences of 1k..32k tokens (T = 129511), GQA groups of 4
     "varlen_t129511_hq32_hkv8_d128_causal": (18, 8, 32, 8, 128),
 }
-LAUNCHES_PER_STEP = 8   # fwd 1, bwd 3, quantise 3, fp8 fwd 1
+
+
+def bwd_launches(B, Hq, Hkv, N, d, causal, window, sms):
+    """Kernels one dense attn_bwd call launches: D and the dQ clearing, the
+    main kernel, the dQ conversion, plus a second main-kernel launch when the
+    library splits the last wave (no mask, the units of the last wave at most
+    half the SMs and more than one wave's worth of work before them)."""
+    if causal or window is not None:
+        return 3
+    units = -(-N // 128) * (2 if d == 256 else 1) * Hkv * B
+    tail = units % sms
+    split = sms >= 2 and 0 < tail and 2 * tail <= sms and (Hq // Hkv) * -(-N // 64) >= 2
+    return 4 if split and units > tail else 3
+
+
+def launches_per_step(B, Hq, Hkv, N, d, causal, window, sms):
+    """fwd 1, bwd 3 or 4, quantise 3, fp8 fwd 1 (window: fwd 1, bwd 3 or 4)"""
+    nb = bwd_launches(B, Hq, Hkv, N, d, causal, window, sms)
+    return 1 + nb if window is not None else 1 + nb + 3 + 1
+
+
 # The FP8 accuracy configuration, timed on its own inputs after the step:
 # B=4, H=16, N=8192, d=128, N(0,1) with 0.1 % of entries replaced by
 # N(0, 10^2) (seed 3), Q and K rotated with the random signs of seed 4.
@@ -116,6 +136,11 @@ def peaks():
         return {"bf16_burst": m["bf16_tflops"], "bf16_sustained": m.get("bf16_tflops_sustained"),
                 "hbm_gbs": m["hbm_gbs"], "source": "measured"}
     return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def sm_count():
+    import torch
+    return torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
 
 
 class Clocks:
@@ -851,13 +876,14 @@ def measured_traffic(key):
     return e
 
 
-def write_traffic(csv_path, keys, step_launches=None):
+def write_traffic(csv_path, keys, step_launches, per_step):
     """Write profiles/traffic.json from an ncu --csv launch list holding
     dram__bytes_read.sum and dram__bytes_write.sum: `keys` maps a kernel-name
-    regex to the traffic key; the last captured launch of each kernel among
-    the first `step_launches` launches (the benchmark steps, before the FP8
-    configuration's launches) is used. Records the current kernel source hash
-    with the numbers."""
+    regex to the traffic key. The first `step_launches` launches are the
+    benchmark steps (before the FP8 configuration's), `per_step` of them per
+    step; each key gets the summed bytes of its launches in the last of those
+    steps (the backward's main kernel is two launches when its last wave is
+    split). Records the current kernel source hash with the numbers."""
     import csv
     import re
     rows = list(csv.reader(l for l in open(csv_path) if l.startswith('"')))
@@ -865,14 +891,14 @@ def write_traffic(csv_path, keys, step_launches=None):
     ki, mi, vi, ui = head.index("Kernel Name"), head.index("Metric Name"), head.index("Metric Value"), \
         head.index("Metric Unit")
     ii = head.index("ID")
-    if step_launches is not None:
-        rows = [head] + [r for r in rows[1:] if int(r[ii]) < step_launches]
+    rows = [r for r in rows[1:] if step_launches - per_step <= int(r[ii]) < step_launches]
     scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
     per = {}
-    for r in rows[1:]:
+    for r in rows:
         for pat, key in keys.items():
             if re.search(pat, r[ki]) and r[mi] in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
-                per.setdefault(key, {})[r[mi]] = float(r[vi].replace(",", "")) * scale[r[ui]]
+                d = per.setdefault(key, {})
+                d[r[mi]] = d.get(r[mi], 0.0) + float(r[vi].replace(",", "")) * scale[r[ui]]
     out = {"source_sha16": kernel_source_sha16(), "capture": os.path.basename(csv_path),
            "launches": {k: int(v["dram__bytes_read.sum"] + v["dram__bytes_write.sum"]) for k, v in per.items()}}
     with open(TRAFFIC, "w") as f:
@@ -892,6 +918,8 @@ def main():
     ap.add_argument("--write-traffic", metavar="CSV",
                     help="write profiles/traffic.json from an ncu --csv capture of the default workload's "
                          "dram__bytes_read.sum/dram__bytes_write.sum, then exit")
+    ap.add_argument("--sms", type=int, default=152,
+                    help="SM count of the GPU the --write-traffic capture ran on")
     ap.add_argument("--sweep", action="store_true",
                     help="time the forward (BF16, FP8) and backward over the sweep points instead, one JSON line "
                          "per point")
@@ -899,12 +927,14 @@ def main():
     if args.sweep:
         return sweep(args)
     if args.write_traffic:
-        # a capture of `bench.py --steps S --warmup W`: (W + S + 2 + S) steps of
-        # LAUNCHES_PER_STEP launches come before the FP8 configuration's
+        # a capture of `bench.py --steps S --warmup W` on a GPU of `--sms` SMs:
+        # (W + S + 2 + S) steps come before the FP8 configuration's launches
         steps = args.warmup + args.steps + 2 + args.steps
+        B, Hq, Hkv, N, d, causal, window = WORKLOADS[DEFAULT]
+        lps = launches_per_step(B, Hq, Hkv, N, d, causal, window, args.sms)
         print(json.dumps(write_traffic(args.write_traffic, {
             r"fwd_kernel<\(?int\)?0|fwd_kernel<0": f"{DEFAULT}:fwd", r"bwd_kernel": f"{DEFAULT}:bwd",
-            r"fwd_kernel<\(?int\)?2|fwd_kernel<2": f"{DEFAULT}:fwd_fp8"}, steps * LAUNCHES_PER_STEP)))
+            r"fwd_kernel<\(?int\)?2|fwd_kernel<2": f"{DEFAULT}:fwd_fp8"}, steps * lps, lps)))
         return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -975,7 +1005,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if window is not None else "bf16+e4m3", "data": "synthetic",
         "config": config, "stages": stages,
-        "roofline": {"bound": "tensor", "kernel": {"fwd": "attn_fwd", "bwd": "attn_bwd (main + 2 helpers)",
+        "roofline": {"bound": "tensor", "kernel": {"fwd": "attn_fwd", "bwd": "attn_bwd (main kernel, its last wave split into a second launch where that pays, + 2 helpers)",
                                                     "fwd_fp8": "attn_fwd_fp8"}[dom],
                      "achieved": achieved, "peak": dom_peak, "unit": "TFLOP/s", "frac": achieved / dom_peak,
                      "peak_source": pk["source"] + (" bf16 burst x2 (fp8 nominal ratio)" if dom == "fwd_fp8" else " bf16 burst"),
@@ -986,7 +1016,7 @@ def main():
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         # the library's launches inside the timed regions: the device-timed
         # steps and the end-to-end steps (plus the FP8 config's launches below)
-        "gpu_launches": 2 * (4 if window is not None else LAUNCHES_PER_STEP) * args.steps,
+        "gpu_launches": 2 * launches_per_step(B, Hq, Hkv, N, d, causal, window, sm_count()) * args.steps,
         "clocks": r["clocks"],
     }
     if r.get("fp8_config"):

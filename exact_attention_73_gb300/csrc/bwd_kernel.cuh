@@ -42,6 +42,11 @@
 // dP^T (the contraction runs over all 256 dims). K and V of 256 dims leave
 // room for one Q/dO stage only, so the products of one query tile are issued
 // after the previous tile's, without overlap.
+// Split walk (BwdArgs::nsplit = 2, clusters of two CTAs): both CTAs of a
+// cluster own the same key tile and each walks half of its query tiles; at
+// the end CTA 1 copies its dV and dK into CTA 0's shared memory (distributed
+// shared memory) and CTA 0 writes the sums. The host uses it for the last,
+// partly filled wave of grids without masks.
 #pragma once
 #include <cmath>
 #include <cstdint>
@@ -69,6 +74,13 @@ struct BwdArgs {
   int causal;               // scheduling hint: window (-1, 0)
   int win_left, win_right;  // key j visible to query i iff i - left <= j <= i + right (-1: no bound)
   int* status;
+  // Linear unit order (tiles_x > 0): CTA blockIdx.x takes unit unit0 +
+  // blockIdx.x / nsplit of the units (key tile x DSPLIT, KV head, batch), x
+  // fastest, and part blockIdx.x % nsplit of its walk over the query tiles.
+  // nsplit = 2 is launched as clusters of two CTAs: part 1 hands its dK and
+  // dV to part 0 through distributed shared memory, part 0 writes the sums.
+  // tiles_x = 0: the grid is (tiles x DSPLIT, Hkv, batch or sequences).
+  int tiles_x, unit0, nsplit;
 };
 
 template <int DT, int D>
@@ -94,6 +106,9 @@ struct BwdCfg {
   static constexpr int SMEM_BYTES =
       2 * KV_B + DS_B + NQ * (2 * Q_B) + DQ_STAGE_B + NQ * LD_B + NBARS * 8 + 16;   // base is 1024-aligned
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeded");
+  // a split walk's hand-over of dV and dK ([2][BC][DH] FP32 from offset 0)
+  // stays below the barriers
+  static_assert(2 * BC * DH * 4 <= 2 * KV_B + DS_B + NQ * (2 * Q_B) + DQ_STAGE_B + NQ * LD_B, "hand-over area");
   static constexpr int NTHREADS = 512;
   // Registers: the launch gives 128 per thread (the whole register file);
   // the load/MMA warpgroup and the dQ drain warpgroup return part of theirs
@@ -120,6 +135,39 @@ struct BwdCfg {
   static constexpr uint32_t COL_DV = 256, COL_DK = 256 + DH;
   static_assert(COL_DK + DH <= 512, "tensor memory overflow");
 };
+
+// Split walk: dV (offset 0) and dK (offset BC * DH floats) of part 1 go to
+// part 0's shared memory as [BC keys][DH] FP32, 16-byte groups of each
+// 32-column chunk swizzled by key % 8 so that a warp's 32 keys hit distinct
+// banks. Key row `row` hands chunks c0 .. c1 - 1 from tensor memory `taddr`.
+template <class C>
+__device__ __forceinline__ void split_handover(const uint8_t* smem, uint32_t taddr, int row, int c0, int c1,
+                                               int off) {
+  const uint32_t dst = cluster_map(smem_u32(smem), 0) + 4u * static_cast<uint32_t>(off + row * C::DH);
+#pragma unroll 1
+  for (int c = c0; c < c1; ++c) {
+    uint32_t v[32];
+    tmem_ld32(taddr + 32 * c, v);
+    tmem_wait_ld();
+    reg_fence(v);
+#pragma unroll
+    for (int w = 0; w < 8; ++w)
+      st_cluster_v4(dst + 4u * (32 * c + 4 * (w ^ (row & 7))), v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
+  }
+}
+// Part 0: v (its own chunk c of key row `row`) += part 1's.
+template <class C>
+__device__ __forceinline__ void split_add(uint32_t (&v)[32], const float* part1, int row, int c) {
+  const float* src = part1 + row * C::DH + 32 * c;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const float4 x = *reinterpret_cast<const float4*>(src + 4 * (w ^ (row & 7)));
+    v[4 * w] = __float_as_uint(__uint_as_float(v[4 * w]) + x.x);
+    v[4 * w + 1] = __float_as_uint(__uint_as_float(v[4 * w + 1]) + x.y);
+    v[4 * w + 2] = __float_as_uint(__uint_as_float(v[4 * w + 2]) + x.z);
+    v[4 * w + 3] = __float_as_uint(__uint_as_float(v[4 * w + 3]) + x.w);
+  }
+}
 
 // kDQ = false: dK and dV only (the deterministic backward computes dQ in a
 // separate query-stationary kernel); the dQ^T product, its drain and the
@@ -163,9 +211,18 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // with causal masking key tile 0 has the most work: heavy tiles start first
-  int bx = blockIdx.x, by = blockIdx.y, bz = blockIdx.z;
-  if (a.causal) heavy_first_order<16>(bx, by, bz);
+  int bx = blockIdx.x, by = blockIdx.y, bz = blockIdx.z, part = 0;
+  const int nsplit = a.tiles_x > 0 ? a.nsplit : 1;
+  if (a.tiles_x > 0) {
+    const int u = a.unit0 + static_cast<int>(blockIdx.x) / nsplit;
+    part = static_cast<int>(blockIdx.x) % nsplit;
+    bx = u % a.tiles_x;
+    by = (u / a.tiles_x) % a.Hkv;
+    bz = u / a.tiles_x / a.Hkv;
+  } else if (a.causal) {
+    // with causal masking key tile 0 has the most work: heavy tiles start first
+    heavy_first_order<16>(bx, by, bz);
+  }
   const int hkv = by;
   const bool packed = a.cu_seqlens != nullptr;
   int b, seq0, L;
@@ -187,15 +244,19 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
   const int qhi = a.win_left < 0 ? L - 1 : min(L - 1, klast + a.win_left);
   const int i0 = qlo / C::BR;
   const int per_head = qhi / C::BR + 1 - i0;
-  const int niter = a.group * per_head;
-  // Query tile of iteration it. Each key tile starts its walk at a different
-  // query tile, so the CTAs of one head neither load the same Q/dO tile nor
-  // add into the same dQ rows at the same moment.
+  // this CTA's part of the walk over (query head, query tile): iterations
+  // it_base .. it_base + niter - 1 of the group * per_head
+  const int it_base = part * (a.group * per_head) / nsplit;
+  const int niter = (part + 1) * (a.group * per_head) / nsplit - it_base;
+  // Query tile and head of local iteration it. Each key tile starts its walk
+  // at a different query tile, so the CTAs of one head neither load the same
+  // Q/dO tile nor add into the same dQ rows at the same moment.
   const int rot = j % per_head;
   auto q_tile = [&](int it) {
-    const int r = it % per_head + rot;
+    const int r = (it_base + it) % per_head + rot;
     return i0 + (r >= per_head ? r - per_head : r);
   };
+  auto q_head = [&](int it) { return hkv * a.group + (it_base + it) / per_head; };
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmK);
@@ -229,6 +290,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
   tc_fence_after();
   const uint32_t tbase = *tmem_holder;
   const float kLog2e = 1.4426950408889634f;
+  // The split last wave is launched as a dependent of the whole-wave grid:
+  // its clusters may start on SMs that this grid's last CTAs free up (it
+  // reads nothing this grid writes, except dQ, which both only add into).
+  if (nsplit == 1) grid_launch_dependents();
 
   // Each role changes its register budget inside its own branch, so the
   // compiler sizes every role's code for the budget it runs with.
@@ -251,7 +316,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     }
     for (int it = 0; it < niter; ++it) {
       const int st = it % C::NQ;
-      const int h = hkv * a.group + it / per_head;
+      const int h = q_head(it);
       const int q0 = q_tile(it) * C::BR;
       // LSE and D of this tile are fetched before waiting for the stage (they
       // do not depend on it), so their latency hides behind that wait
@@ -399,6 +464,12 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     }
     __syncwarp();
   }
+  // the two barriers of the split-walk hand-over (see the dV and dK stores)
+  if (nsplit > 1) {
+    __syncwarp();
+    cluster_sync_all();
+    cluster_sync_all();
+  }
   } else if ((warp >= 4 && warp < 8) || warp >= 12) {
     regs_inc<C::kRegsMath>();
     // -------------------------------------------------- P^T and dS^T
@@ -507,7 +578,19 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(done, 0, a.status));
     tc_fence_after();
-    if (ok) {   // dV rows, this CTA's columns, DH/2 per group
+    // dV rows, this CTA's columns, DH/2 per group. With a split walk part 1
+    // hands its dV to part 0 (between the two cluster barriers, once both
+    // parts' products are complete and part 0's shared memory is idle), and
+    // part 0 stores the sum.
+    const float* add = nullptr;
+    if (nsplit > 1) {
+      cluster_sync_all();
+      if (ok && part == 1) split_handover<C>(smem, tbase + lane_off + C::COL_DV, r, half * (C::DH / 64),
+                                             (half + 1) * (C::DH / 64), 0);
+      cluster_sync_all();
+      add = reinterpret_cast<const float*>(smem);
+    }
+    if (ok && part == 0) {
       const long long off = static_cast<long long>(b) * a.k_sb + static_cast<long long>(hkv) * a.k_sh +
                             static_cast<long long>(seq0 + kloc) * a.k_sn;
 #pragma unroll 1
@@ -516,6 +599,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         tmem_ld32(tbase + lane_off + C::COL_DV + 32 * c, v);
         tmem_wait_ld();
         reg_fence(v);
+        if (add) split_add<C>(v, add, r, c);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
@@ -549,7 +633,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       reg_fence(x1);
       tc_fence_before();
       mbar_arrive(dq_empty);
-      const int h = hkv * a.group + it / per_head;
+      const int h = q_head(it);
       const int q0 = q_tile(it) * C::BR;
       // reduce-adds of DQ_ROWS rows through one FP32 staging buffer; rows past
       // the sequence hold exact zeros (P = 0 there): for the dense layout the
@@ -584,8 +668,17 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     if (threadIdx.x == 256) bulk_wait_all();
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(done, 0, a.status));
     tc_fence_after();
-    if (ok) {   // dK rows, times scale
-      const int kloc = j * C::BC + dim;             // here the lane indexes keys
+    // dK rows (here the lane indexes keys), times scale; a split walk's part 1
+    // hands its dK to part 0 as for dV
+    const float* add = nullptr;
+    if (nsplit > 1) {
+      cluster_sync_all();
+      if (ok && part == 1) split_handover<C>(smem, tbase + lane_off + C::COL_DK, dim, 0, C::DH / 32, C::BC * C::DH);
+      cluster_sync_all();
+      add = reinterpret_cast<const float*>(smem) + C::BC * C::DH;
+    }
+    if (ok && part == 0) {
+      const int kloc = j * C::BC + dim;
       const long long off = static_cast<long long>(b) * a.k_sb + static_cast<long long>(hkv) * a.k_sh +
                             static_cast<long long>(seq0 + kloc) * a.k_sn;
 #pragma unroll 1
@@ -594,6 +687,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         tmem_ld32(tbase + lane_off + C::COL_DK + 32 * c, v);
         tmem_wait_ld();
         reg_fence(v);
+        if (add) split_add<C>(v, add, dim, c);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -608,6 +702,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       }
     }
   }
+  // the split last wave completes only after the grid it depends on, so the
+  // work queued after it (the dQ conversion) sees both grids' results
+  if (nsplit > 1) grid_wait_prerequisites();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

@@ -136,6 +136,34 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Barrier over every thread of every CTA of the cluster (release on arrive,
+// acquire on wait: shared-memory writes made before it, also into another
+// CTA's shared memory, are visible after it). Warp-converged callers only. A
+// launch without a cluster is a cluster of one CTA, where this is a CTA barrier.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address in CTA `rank` of the cluster of the shared-memory location `addr`
+// has in this CTA.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+// Programmatic dependent launch: let a grid launched after this one with the
+// programmatic-serialisation attribute start once every CTA of this grid has
+// executed this (or exited); and, in such a dependent grid, wait until the
+// grids it depends on have completed and their memory is visible.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_wait_prerequisites() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Per-warpgroup register reallocation: all four warps of a warpgroup execute
 // it. An increase waits until enough registers have been released.
 template <uint32_t N>

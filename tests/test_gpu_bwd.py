@@ -122,3 +122,38 @@ def test_varlen_config_backward_sampled():
         ref = A.backward(tr(q[:, hs]), tr(k[:, g:g + 1]), tr(v[:, g:g + 1]), tr(do[:, hs]), 128 ** -0.5, True)
         for name, got, r in zip(("dQ", "dK", "dV"), (tr(dq[:, hs]), tr(dk[:, g:g + 1]), tr(dv[:, g:g + 1])), ref):
             assert rel_rms(got, r) <= 1e-2, (name, int(s), rel_rms(got, r))
+
+
+def _tail_case(sms, d, split):
+    """Heads H of a (B=1, H, N=1024) non-causal problem whose backward runs
+    as whole waves plus a split last wave (split=True: more units than SMs,
+    the remainder at most half the SMs) or as one unsplit launch (split=False:
+    the remainder above half the SMs)."""
+    per_head_units = 8 * (2 if d == 256 else 1)
+    for h in range(1, 4 * sms):
+        units = per_head_units * h
+        r = units % sms
+        if split and units > sms and 0 < r <= sms // 2:
+            return h
+        if not split and 2 * r > sms:
+            return h
+    raise AssertionError("no such head count")
+
+
+@pytest.mark.parametrize("split", [True, False])
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_last_wave_split(split, d):
+    """Without masks the backward's last partial wave is split in two (two
+    CTAs per unit, each walking half of the query tiles, dK/dV summed through
+    distributed shared memory). Both launch plans against the oracle, and the
+    split one twice: its dK and dV are bit-identical across calls."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    H = _tail_case(sms, d, split)
+    q, k, v, do = inputs.normal(31 + d, [(1, H, 1024, d)] * 4)
+    got = run_dense(q, k, v, do, False)
+    ref = A.backward(q, k, v, do, d ** -0.5, False)
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        assert rel_rms(g, r) <= 1e-2, (name, H, rel_rms(g, r))
+    if split:
+        again = run_dense(q, k, v, do, False)
+        assert torch.equal(got[1], again[1]) and torch.equal(got[2], again[2])
