@@ -363,10 +363,8 @@ __device__ __forceinline__ int warp_any(int pred) { return __any_sync(0xffffffff
 // CTAs start in the first waves, and the CTAs running together still share a
 // pair's data in L2 (JB of them per pair).
 template <int JB>
-__device__ __forceinline__ void heavy_first_order(int& x, int& y, int& z) {
-  const int nx = static_cast<int>(gridDim.x), ny = static_cast<int>(gridDim.y);
-  const int groups = ny * static_cast<int>(gridDim.z);
-  const int lin = static_cast<int>(blockIdx.x) + nx * (static_cast<int>(blockIdx.y) + ny * static_cast<int>(blockIdx.z));
+__device__ __forceinline__ void heavy_first_map(int lin, int nx, int ny, int nz, int& x, int& y, int& z) {
+  const int groups = ny * nz;
   const int blk = lin / (JB * groups);
   const int width = min(JB, nx - blk * JB);       // the last block may be narrower
   const int rem = lin - blk * JB * groups;
@@ -374,6 +372,13 @@ __device__ __forceinline__ void heavy_first_order(int& x, int& y, int& z) {
   x = blk * JB + rem % width;
   y = g % ny;
   z = g / ny;
+}
+// the same over this CTA's place in a 3-D grid
+template <int JB>
+__device__ __forceinline__ void heavy_first_order(int& x, int& y, int& z) {
+  const int nx = static_cast<int>(gridDim.x), ny = static_cast<int>(gridDim.y);
+  const int lin = static_cast<int>(blockIdx.x) + nx * (static_cast<int>(blockIdx.y) + ny * static_cast<int>(blockIdx.z));
+  heavy_first_map<JB>(lin, nx, ny, static_cast<int>(gridDim.z), x, y, z);
 }
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {

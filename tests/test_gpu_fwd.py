@@ -407,3 +407,59 @@ def test_rope_producer_feeds_fp8_attention():
     o_ref, _ = A.forward(qr, kr, v, d ** -0.5, False)
     err = o.double().cpu().numpy() - o_ref
     assert math.sqrt((err ** 2).mean()) <= 1.5e-2
+
+
+# heads checked one by one: spread over the batch and head range, so that in
+# the full launch they fall in different rounds of the CTAs' walks
+PERSIST_HEADS = [(0, 0), (0, 31), (1, 7), (2, 19), (3, 3), (4, 28), (5, 12), (6, 23), (7, 0), (7, 31)]
+
+
+@pytest.mark.parametrize("n", [512, 1000, 2048])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_persistent_walk_matches_one_head_launches(n, fp8):
+    """Rows of up to 2048 run the persistent forward: one CTA per SM walks
+    the (query-tile pair, head, batch) units, here 512 to 2048 of them, so
+    each CTA takes several in a row with barrier phases, tensor memory and
+    the K/V ring carried over. A unit's result must not depend on that: O and
+    LSE of sampled heads equal bit for bit those of a launch holding that head
+    alone (one unit per CTA), and two heads match the oracle."""
+    B, H, d = 8, 32, 128
+    q, k, v = inputs.normal(40 + n, [(B, H, n, d)] * 3)
+    qd, kd, vd = (x.cuda() for x in (q, k, v))
+    if fp8:
+        q8, sq = quantize_gpu(q)
+        k8, sk = quantize_gpu(k)
+        v8, sv = quantize_gpu(v)
+
+    def fwd(sel):
+        b, h = sel if sel is not None else (slice(None), slice(None))
+        bs, hs = (slice(b, b + 1), slice(h, h + 1)) if sel is not None else (b, h)
+        shape = (1, 1, n, d) if sel is not None else (B, H, n, d)
+        o = torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full(shape[:3], float("nan"), device="cuda")
+        if fp8:
+            L.attn_fwd_fp8(*(x[bs, hs].contiguous() for x in (q8, k8, v8, sq, sk, sv)), o, lse)
+        else:
+            L.attn_fwd(*(x[bs, hs].contiguous() for x in (qd, kd, vd)), o, lse)
+        torch.cuda.synchronize()
+        return o.cpu(), lse.cpu()
+
+    o, lse = fwd(None)
+    assert L.attn_get_device_status() == 0
+    for b, h in PERSIST_HEADS:
+        o1, lse1 = fwd((b, h))
+        assert torch.equal(o[b:b + 1, h:h + 1], o1), (b, h)
+        assert torch.equal(lse[b:b + 1, h:h + 1], lse1), (b, h)
+    if fp8:
+        for b, h in PERSIST_HEADS[:2]:
+            one = lambda x: x[b:b + 1, h:h + 1]
+            gpu = tuple(one(x).cpu().numpy() for x in (q8, k8, v8, sq, sk, sv))
+            codes = oracle_fp8_inputs(one(q), one(k), one(v), gpu=gpu)
+            o_ref, _ = F.attention_fp8(*codes, d ** -0.5, False, tau=F.STALE_MAX_TAU,
+                                       kv_tile=L.attn_fwd_fp8_kv_tile(d))
+            check_fp8_vs_emulation(o[b:b + 1, h:h + 1].double().numpy(), o_ref)
+    else:
+        for b, h in PERSIST_HEADS[:2]:
+            one = lambda x: x[b:b + 1, h:h + 1]
+            o_ref, lse_ref = A.forward(one(q), one(k), one(v), d ** -0.5, False)
+            check_o_lse(one(o), one(lse), o_ref, lse_ref, f"n{n} b{b} h{h}")
