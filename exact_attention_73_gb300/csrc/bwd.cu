@@ -75,10 +75,11 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
 // Tail split. Without masks every unit (key tile x DSPLIT, KV head, batch)
 // walks the same query tiles, so the grid runs in waves of one unit per SM
 // and the last wave holds units % SMs of them. When that remainder R is at
-// most half the SMs, the first units - R run as one launch (whole waves) and
-// the last R as a second launch of 2R CTAs in clusters of two, each CTA
-// walking half of its unit's query tiles: the last wave takes half as long.
-// The two halves' dK and dV are summed in a fixed order (deterministic).
+// most half the SMs, the common instance runs the first units - R as whole
+// waves (a 1-D grid) and the split instance the last R as 2R CTAs in
+// clusters of two, each CTA walking half of its unit's query tiles: the last
+// wave takes about half as long. The two halves' dK and dV are summed in a
+// fixed order (deterministic).
 int tail_split_units(const BwdArgs& a, long long units, int per_head, int sms) {
   if (a.cu_seqlens != nullptr || a.win_left >= 0 || a.win_right >= 0) return 0;
   if (sms < 2 || static_cast<long long>(a.group) * per_head < 2) return 0;
@@ -90,49 +91,37 @@ template <int DT, int D, bool kDQ>
 cudaError_t launch_main(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q, const CUtensorMap& d,
                         const CUtensorMap& dq, const BwdArgs& a, int max_len, int nz, cudaStream_t st) {
   using C = BwdCfg<DT, D>;
-  auto kern = bwd_kernel<DT, D, kDQ>;
-  cudaError_t e = smem_attr_once<bwd_kernel<DT, D, kDQ>>(C::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
+  // At d = 256 the kSplit instance runs every grid: its build of the common
+  // path measured 3 % faster there (at d = 64 9 % slower, so d = 64 and 128
+  // use the instance without the split code for their whole-unit grids).
+  constexpr bool kSplitAll = D == 256;
   const int tiles_x = (max_len + C::BC - 1) / C::BC * C::DSPLIT;
   const long long units = static_cast<long long>(tiles_x) * a.Hkv * nz;
   int dev = 0, sms = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const int tail = units <= INT32_MAX ? tail_split_units(a, units, (a.N + C::BR - 1) / C::BR, sms) : 0;
-  if (tail == 0) {
-    BwdArgs g = a;
-    g.tiles_x = 0;
-    const dim3 grid(tiles_x, a.Hkv, nz);
-    kern<<<grid, C::NTHREADS, C::SMEM_BYTES, st>>>(k, v, q, d, dq, g);
-    return cudaGetLastError();
-  }
+  auto whole = [&](dim3 grid, const BwdArgs& g) -> cudaError_t {
+    if constexpr (kSplitAll) {
+      return launch_bwd_split<DT, D, kDQ>(k, v, q, d, dq, g, 0, grid, st);
+    } else {
+      cudaError_t r = smem_attr_once<bwd_kernel<DT, D, kDQ, false>>(C::SMEM_BYTES);
+      if (r != cudaSuccess) return r;
+      bwd_kernel<DT, D, kDQ, false><<<grid, C::NTHREADS, C::SMEM_BYTES, st>>>(k, v, q, d, dq, g);
+      return cudaGetLastError();
+    }
+  };
   BwdArgs g = a;
-  g.tiles_x = tiles_x;
+  g.tiles_x = 0;
   g.unit0 = 0;
   g.nsplit = 1;
-  if (units > tail) {
-    kern<<<static_cast<unsigned>(units - tail), C::NTHREADS, C::SMEM_BYTES, st>>>(k, v, q, d, dq, g);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
+  if (tail == 0) return whole(dim3(tiles_x, a.Hkv, nz), g);
+  g.tiles_x = tiles_x;
+  if (units > tail && (e = whole(dim3(static_cast<unsigned>(units - tail)), g)) != cudaSuccess) return e;
   g.unit0 = static_cast<int>(units - tail);
   g.nsplit = 2;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * tail);
-  cfg.blockDim = dim3(C::NTHREADS);
-  cfg.dynamicSmemBytes = C::SMEM_BYTES;
-  cfg.stream = st;
-  cudaLaunchAttribute at[2];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = 2;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  // may start while the whole-wave grid's last CTAs run (it waits for that
-  // grid only at its end)
-  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[1].val.programmaticStreamSerializationAllowed = units > tail ? 1 : 0;
-  cfg.attrs = at;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, k, v, q, d, dq, g);
+  return launch_bwd_split<DT, D, kDQ>(k, v, q, d, dq, g, tail, dim3(), st);
 }
 
 template <bool kDQ>

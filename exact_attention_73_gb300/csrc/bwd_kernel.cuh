@@ -42,11 +42,14 @@
 // dP^T (the contraction runs over all 256 dims). K and V of 256 dims leave
 // room for one Q/dO stage only, so the products of one query tile are issued
 // after the previous tile's, without overlap.
-// Split walk (BwdArgs::nsplit = 2, clusters of two CTAs): both CTAs of a
-// cluster own the same key tile and each walks half of its query tiles; at
-// the end CTA 1 copies its dV and dK into CTA 0's shared memory (distributed
-// shared memory) and CTA 0 writes the sums. The host uses it for the last,
-// partly filled wave of grids without masks.
+// Split walk (BwdArgs::nsplit = 2, clusters of two CTAs; the kSplit
+// instance): both CTAs of a cluster own the same key tile and each walks
+// half of its query tiles; at the end CTA 1 copies its dV and dK into CTA
+// 0's shared memory (distributed shared memory) and CTA 0 writes the sums.
+// The host uses it for the last, partly filled wave of grids without masks.
+// The instance without kSplit carries none of that code; which instance
+// runs the other grids is the host's choice per head dim (both compute the
+// same values).
 #pragma once
 #include <cmath>
 #include <cstdint>
@@ -74,12 +77,12 @@ struct BwdArgs {
   int causal;               // scheduling hint: window (-1, 0)
   int win_left, win_right;  // key j visible to query i iff i - left <= j <= i + right (-1: no bound)
   int* status;
-  // Linear unit order (tiles_x > 0): CTA blockIdx.x takes unit unit0 +
-  // blockIdx.x / nsplit of the units (key tile x DSPLIT, KV head, batch), x
-  // fastest, and part blockIdx.x % nsplit of its walk over the query tiles.
-  // nsplit = 2 is launched as clusters of two CTAs: part 1 hands its dK and
-  // dV to part 0 through distributed shared memory, part 0 writes the sums.
-  // tiles_x = 0: the grid is (tiles x DSPLIT, Hkv, batch or sequences).
+  // Units are (key tile x DSPLIT, KV head, batch), x fastest, tiles_x of
+  // them along x. tiles_x = 0: the grid is (tiles x DSPLIT, Hkv, batch or
+  // sequences), one unit per CTA. tiles_x > 0: a 1-D grid, CTA blockIdx.x
+  // taking part blockIdx.x % nsplit of the walk of unit unit0 + blockIdx.x /
+  // nsplit (nsplit = 2 only in the kSplit instance, launched in clusters of
+  // two).
   int tiles_x, unit0, nsplit;
 };
 
@@ -172,7 +175,7 @@ __device__ __forceinline__ void split_add(uint32_t (&v)[32], const float* part1,
 // kDQ = false: dK and dV only (the deterministic backward computes dQ in a
 // separate query-stationary kernel); the dQ^T product, its drain and the
 // reduce-adds are left out.
-template <int DT, int D, bool kDQ = true>
+template <int DT, int D, bool kDQ = true, bool kSplit = false>
 __global__ void __launch_bounds__(512, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
            const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
@@ -182,6 +185,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
   // the base by hand: a base that is not 1024-byte aligned (needed by the
   // swizzled tiles) is reported and the CTA leaves before touching it.
   extern __shared__ __align__(1024) uint8_t bwd_smem[];
+  // A split launch follows a 1-D grid of whole units (tiles_x > 0, nsplit =
+  // 1) as its programmatic dependent: its clusters may take SMs as this
+  // grid's last CTAs leave (it reads nothing this grid writes; dQ both only
+  // add into). Every thread signals.
+  if constexpr (!kSplit) {
+    if (a.tiles_x > 0) grid_launch_dependents();
+  }
   if (smem_u32(bwd_smem) & 1023u) {
     if (threadIdx.x == 0 && a.status) atomicExch(a.status, kDevBadSmemAlign);
     return;
@@ -211,14 +221,18 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  int bx = blockIdx.x, by = blockIdx.y, bz = blockIdx.z, part = 0;
-  const int nsplit = a.tiles_x > 0 ? a.nsplit : 1;
-  if (a.tiles_x > 0) {
+  const int nsplit = kSplit && a.tiles_x > 0 ? a.nsplit : 1;   // CTAs per unit
+  int bx = blockIdx.x, by = blockIdx.y, bz = blockIdx.z, wp = 0;   // wp: this CTA's part of the walk
+  if (kSplit && a.tiles_x > 0) {
     const int u = a.unit0 + static_cast<int>(blockIdx.x) / nsplit;
-    part = static_cast<int>(blockIdx.x) % nsplit;
+    wp = static_cast<int>(blockIdx.x) % nsplit;
     bx = u % a.tiles_x;
     by = (u / a.tiles_x) % a.Hkv;
     bz = u / a.tiles_x / a.Hkv;
+  } else if (a.tiles_x > 0) {   // whole units from unit 0 (the instance without kSplit)
+    bx = static_cast<int>(blockIdx.x) % a.tiles_x;
+    by = static_cast<int>(blockIdx.x) / a.tiles_x % a.Hkv;
+    bz = static_cast<int>(blockIdx.x) / a.tiles_x / a.Hkv;
   } else if (a.causal) {
     // with causal masking key tile 0 has the most work: heavy tiles start first
     heavy_first_order<16>(bx, by, bz);
@@ -246,8 +260,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
   const int per_head = qhi / C::BR + 1 - i0;
   // this CTA's part of the walk over (query head, query tile): iterations
   // it_base .. it_base + niter - 1 of the group * per_head
-  const int it_base = part * (a.group * per_head) / nsplit;
-  const int niter = (part + 1) * (a.group * per_head) / nsplit - it_base;
+  const int it_base = wp * (a.group * per_head) / nsplit;
+  const int niter = (wp + 1) * (a.group * per_head) / nsplit - it_base;
   // Query tile and head of local iteration it. Each key tile starts its walk
   // at a different query tile, so the CTAs of one head neither load the same
   // Q/dO tile nor add into the same dQ rows at the same moment.
@@ -290,10 +304,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
   tc_fence_after();
   const uint32_t tbase = *tmem_holder;
   const float kLog2e = 1.4426950408889634f;
-  // The split last wave is launched as a dependent of the whole-wave grid:
-  // its clusters may start on SMs that this grid's last CTAs free up (it
-  // reads nothing this grid writes, except dQ, which both only add into).
-  if (nsplit == 1) grid_launch_dependents();
+  if constexpr (kSplit) {
+    if (nsplit == 1) grid_launch_dependents();   // as above, for this instance's own whole-unit grids
+  }
 
   // Each role changes its register budget inside its own branch, so the
   // compiler sizes every role's code for the budget it runs with.
@@ -465,7 +478,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     __syncwarp();
   }
   // the two barriers of the split-walk hand-over (see the dV and dK stores)
-  if (nsplit > 1) {
+  if (kSplit && nsplit > 1) {
     __syncwarp();
     cluster_sync_all();
     cluster_sync_all();
@@ -583,14 +596,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     // parts' products are complete and part 0's shared memory is idle), and
     // part 0 stores the sum.
     const float* add = nullptr;
-    if (nsplit > 1) {
+    if (kSplit && nsplit > 1) {
       cluster_sync_all();
-      if (ok && part == 1) split_handover<C>(smem, tbase + lane_off + C::COL_DV, r, half * (C::DH / 64),
-                                             (half + 1) * (C::DH / 64), 0);
+      if (ok && wp == 1) split_handover<C>(smem, tbase + lane_off + C::COL_DV, r, half * (C::DH / 64),
+                                           (half + 1) * (C::DH / 64), 0);
       cluster_sync_all();
       add = reinterpret_cast<const float*>(smem);
     }
-    if (ok && part == 0) {
+    if (ok && wp == 0) {
       const long long off = static_cast<long long>(b) * a.k_sb + static_cast<long long>(hkv) * a.k_sh +
                             static_cast<long long>(seq0 + kloc) * a.k_sn;
 #pragma unroll 1
@@ -599,7 +612,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         tmem_ld32(tbase + lane_off + C::COL_DV + 32 * c, v);
         tmem_wait_ld();
         reg_fence(v);
-        if (add) split_add<C>(v, add, r, c);
+        if (kSplit && add) split_add<C>(v, add, r, c);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
@@ -671,13 +684,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     // dK rows (here the lane indexes keys), times scale; a split walk's part 1
     // hands its dK to part 0 as for dV
     const float* add = nullptr;
-    if (nsplit > 1) {
+    if (kSplit && nsplit > 1) {
       cluster_sync_all();
-      if (ok && part == 1) split_handover<C>(smem, tbase + lane_off + C::COL_DK, dim, 0, C::DH / 32, C::BC * C::DH);
+      if (ok && wp == 1) split_handover<C>(smem, tbase + lane_off + C::COL_DK, dim, 0, C::DH / 32, C::BC * C::DH);
       cluster_sync_all();
       add = reinterpret_cast<const float*>(smem) + C::BC * C::DH;
     }
-    if (ok && part == 0) {
+    if (ok && wp == 0) {
       const int kloc = j * C::BC + dim;
       const long long off = static_cast<long long>(b) * a.k_sb + static_cast<long long>(hkv) * a.k_sh +
                             static_cast<long long>(seq0 + kloc) * a.k_sn;
@@ -687,7 +700,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         tmem_ld32(tbase + lane_off + C::COL_DK + 32 * c, v);
         tmem_wait_ld();
         reg_fence(v);
-        if (add) split_add<C>(v, add, dim, c);
+        if (kSplit && add) split_add<C>(v, add, dim, c);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -702,9 +715,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       }
     }
   }
-  // the split last wave completes only after the grid it depends on, so the
-  // work queued after it (the dQ conversion) sees both grids' results
-  if (nsplit > 1) grid_wait_prerequisites();
+  // the split grid completes only after the grid it depends on, so work
+  // queued after it (the dQ conversion) sees both grids' results
+  if (kSplit && nsplit > 1) grid_wait_prerequisites();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -712,5 +725,12 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     tmem_dealloc(tbase, 512);
   }
 }
+
+// Launches of the kSplit instance (bwd_split.cu): with nsplit = 2, 2 * n CTAs
+// in clusters of two over units a.unit0 .. a.unit0 + n - 1 (a.tiles_x units
+// along x); with nsplit = 1, the grid `grid` of whole units.
+template <int DT, int D, bool kDQ>
+cudaError_t launch_bwd_split(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q, const CUtensorMap& d,
+                             const CUtensorMap& dq, const BwdArgs& a, int n, dim3 grid, cudaStream_t st);
 
 }  // namespace attn

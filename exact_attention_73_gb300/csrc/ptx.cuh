@@ -155,10 +155,11 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_
                : "memory");
 }
 
-// Programmatic dependent launch: let a grid launched after this one with the
-// programmatic-serialisation attribute start once every CTA of this grid has
-// executed this (or exited); and, in such a dependent grid, wait until the
-// grids it depends on have completed and their memory is visible.
+// Programmatic dependent launch: a grid launched after this one with the
+// programmatic-serialisation attribute may start once every CTA of this grid
+// has executed launch_dependents or exited; in that
+// dependent grid, wait_prerequisites blocks until the grids it depends on
+// have completed and their memory is visible.
 __device__ __forceinline__ void grid_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
