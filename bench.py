@@ -185,6 +185,14 @@ class Clocks:
                 self.out.close()
                 os.unlink(self.path)
             return None
+        # a run shorter than the sampler's start-up would leave no row at all:
+        # wait (at most 3 s) for the first one
+        t_end = time.time() + 3.0
+        while time.time() < t_end and self.proc.poll() is None:
+            self.out.flush()
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.05)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
