@@ -140,6 +140,46 @@ def _tail_case(sms, d, split):
     raise AssertionError("no such head count")
 
 
+def test_last_wave_split_gqa_and_deterministic():
+    """The split walk with GQA (each half of a unit's walk covers two of its
+    four query heads) and in the deterministic backward (dK/dV-only kernel,
+    dQ from the query-stationary kernel): against the oracle, and the
+    deterministic result bit-identical across calls."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    hkv = next(h for h in range(1, 4 * sms) if 8 * h > sms and 0 < (8 * h) % sms <= sms // 2)
+    B, N, d = 1, 1024, 128
+    q, k, v, do = inputs.normal(77, [(B, 4 * hkv, N, d), (B, hkv, N, d), (B, hkv, N, d), (B, 4 * hkv, N, d)])
+    groups = [0, hkv // 2, hkv - 1]   # KV heads checked against the oracle, each with its 4 query heads
+
+    def sel(x, g, kv):
+        return x[:, g:g + 1] if kv else x[:, 4 * g:4 * g + 4]
+
+    refs = {g: A.backward(sel(q, g, 0), sel(k, g, 1), sel(v, g, 1), sel(do, g, 0), d ** -0.5, False) for g in groups}
+
+    def check(res):
+        for g in groups:
+            for name, x, r, kv in zip(("dQ", "dK", "dV"), res, refs[g], (0, 1, 1)):
+                assert rel_rms(sel(x, g, kv), r) <= 1e-2, (name, g, rel_rms(sel(x, g, kv), r))
+
+    check(run_dense(q, k, v, do, False))
+    qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
+    o = torch.empty_like(qd)
+    lse = torch.empty((B, 4 * hkv, N), device="cuda")
+    L.attn_fwd(qd, kd, vd, o, lse)
+    ws = torch.empty((L.attn_bwd_deterministic_workspace_size(B, 4 * hkv, hkv, N, d),), dtype=torch.uint8,
+                     device="cuda")
+    outs = []
+    for _ in range(2):
+        dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+        L.attn_bwd_deterministic(qd, kd, vd, o, lse, dod, dq, dk, dv, ws)
+        torch.cuda.synchronize()
+        outs.append((dq.cpu(), dk.cpu(), dv.cpu()))
+    assert L.attn_get_device_status() == 0
+    check(outs[0])
+    for x, y in zip(*outs):
+        assert torch.equal(x, y)
+
+
 @pytest.mark.parametrize("split", [True, False])
 @pytest.mark.parametrize("d", [64, 128, 256])
 def test_last_wave_split(split, d):

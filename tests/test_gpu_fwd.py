@@ -90,6 +90,32 @@ def test_varlen_small(causal, d):
     check_o_lse(o, lse, o_ref, lse_ref, "varlen")
 
 
+def test_varlen_persistent_many_sequences():
+    """Packed sequences of at most 2048 tokens run the persistent forward;
+    with 96 sequences of 1..2048 tokens (16 query heads, GQA 4:1) the 152
+    CTAs walk 12288 units, most of them past their sequence's end and
+    skipped. Every sequence of one query head against the oracle, eight
+    sequences with all heads."""
+    lens = [int(x) for x in np.random.default_rng(5).integers(1, 2049, size=96)]
+    lens[:4] = [1, 128, 2048, 257]
+    cu = inputs.cu_seqlens(lens)
+    T = int(cu[-1])
+    q, k, v = inputs.normal(13, [(T, 16, 128), (T, 4, 128), (T, 4, 128)])
+    o = torch.full((T, 16, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((16, T), float("nan"), device="cuda")
+    L.attn_fwd_varlen(q.cuda(), k.cuda(), v.cuda(), o, lse, cu.cuda(), max(lens))
+    torch.cuda.synchronize()
+    assert L.attn_get_device_status() == 0
+    o, lse = o.cpu(), lse.cpu()
+    for s_ in range(len(lens)):
+        a, e = int(cu[s_]), int(cu[s_ + 1])
+        heads = slice(None) if s_ < 8 else slice(13, 14)
+        kvh = slice(None) if s_ < 8 else slice(3, 4)
+        tr = lambda x, hs: x[a:e, hs].transpose(0, 1)[None]
+        o_ref, lse_ref = A.forward(tr(q, heads), tr(k, kvh), tr(v, kvh), 128 ** -0.5, False)
+        check_o_lse(tr(o, heads), lse[heads, a:e][None], o_ref, lse_ref, f"seq {s_}")
+
+
 def sampled_rows(n, count, seed):
     r = np.random.default_rng(seed).choice(n, size=min(n, count), replace=False)
     return np.unique(np.concatenate([r, [0, n - 1, min(n - 1, 127), min(n - 1, 128)]]))
