@@ -5,7 +5,9 @@
 // by diag(random signs) * Hadamard / sqrt(d) to spread outliers.
 // m.xxqk.cn FA3 walkthrough §4.2: power-of-two scale factors.
 //
-// One CTA per (128-row block, head, batch). A lane holds EPL consecutive
+// One CTA per (128-row block, head, batch). Without rotation and RoPE a
+// lighter instance keeps the inputs packed (quant_plain_kernel). Otherwise a
+// lane holds EPL consecutive
 // elements of a row (d / EPL lanes per row): EPL = 32 for the plain and
 // rotation instances (8 warps of 16 rows, 16-byte loads), EPL = d / 32 for
 // the RoPE instance (a warp per row, 16 warps of 8 rows). The fast
@@ -48,11 +50,14 @@ __device__ __forceinline__ void fwht_row(float (&x)[EPL], int li) {
       }
     } else {
       const int lm = h / EPL;
-      const bool upper = (li & lm) != 0;
+      // the upper lane of a pair computes other - x, the lower x + other:
+      // one fused multiply-add with x * (-1 or 1) exact, so the sum is
+      // rounded once, as the plain add or subtract would be
+      const float sgn = (li & lm) != 0 ? -1.f : 1.f;
 #pragma unroll
       for (int e = 0; e < EPL; ++e) {
         const float other = __shfl_xor_sync(0xffffffffu, x[e], lm);
-        x[e] = upper ? (other - x[e]) : (x[e] + other);
+        x[e] = fmaf(x[e], sgn, other);
       }
     }
   }
@@ -135,11 +140,38 @@ __global__ void __launch_bounds__(quant_threads<D, kRope>()) quant_kernel(const 
   const int row0 = blk * 128 + warp * RPW;
   float v[NPASS][EPL];
   float amax = 0.f;
+  // Without RoPE and with at most two passes (d <= 128) every pass's 16-byte
+  // loads are issued before the first pass is transformed, so their
+  // latencies overlap (at d = 256 the four passes' raw values would not fit
+  // in registers next to the transformed ones).
+  constexpr bool kPre = !kRope && NPASS <= 2;
+  constexpr int NRAW = kPre ? EPL / 8 : 1;
+  uint4 raw[kPre ? NPASS : 1][NRAW];
+  if constexpr (kPre) {
+#pragma unroll
+    for (int p = 0; p < NPASS; ++p) {
+      const int row = row0 + p * RP + lr;
+#pragma unroll
+      for (int q = 0; q < NRAW; ++q)
+        raw[p][q] = row < N ? reinterpret_cast<const uint4*>(x + (head_off + row) * D + li * EPL)[q]
+                            : make_uint4(0, 0, 0, 0);
+    }
+  }
 #pragma unroll
   for (int p = 0; p < NPASS; ++p) {
     const int row = row0 + p * RP + lr;
     const bool valid = row < N;
-    if (valid) {
+    if constexpr (kPre) {
+#pragma unroll
+      for (int q = 0; q < NRAW; ++q) {
+        const uint32_t wv[4] = {raw[p][q].x, raw[p][q].y, raw[p][q].z, raw[p][q].w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          v[p][8 * q + 2 * u] = to_f32<T>(wv[u] & 0xFFFFu);
+          v[p][8 * q + 2 * u + 1] = to_f32<T>(wv[u] >> 16);
+        }
+      }
+    } else if (valid) {
       load_row_part<T, EPL>(x + (head_off + row) * D + li * EPL, v[p]);
     } else {
 #pragma unroll
@@ -184,7 +216,8 @@ __global__ void __launch_bounds__(quant_threads<D, kRope>()) quant_kernel(const 
       for (int e = 0; e < EPL; ++e) v[p][e] *= inv_sqrt_d;
     }
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(v[p][e]));
+    for (int e = 0; e + 1 < EPL; e += 2) amax = fmax3(amax, fabsf(v[p][e]), fabsf(v[p][e + 1]));
+    if constexpr (EPL % 2 != 0) amax = fmaxf(amax, fabsf(v[p][EPL - 1]));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -194,9 +227,19 @@ __global__ void __launch_bounds__(quant_threads<D, kRope>()) quant_kernel(const 
 #pragma unroll
   for (int w = 1; w < NW; ++w) amax = fmaxf(amax, red[w]);
   const int e = e4m3_scale_exponent(amax);
-  const int e1 = e / 2, e2 = e - e1;
-  const float f1 = ldexpf(1.f, e1), f2 = ldexpf(1.f, e2);
   if (threadIdx.x == 0) scales[(static_cast<long long>(b) * H + h) * gridDim.x + blk] = ldexpf(1.f, -e);
+  // x * 2^e in one multiply when 2^e is a normal float (exact either way:
+  // a power-of-two scaling), else in two steps
+  const int e1 = e / 2, e2 = e - e1;
+  const bool one = e >= -126 && e <= 127;
+  if (!one) {
+    const float fa = ldexpf(1.f, e1);
+#pragma unroll
+    for (int p = 0; p < NPASS; ++p)
+#pragma unroll
+      for (int q = 0; q < EPL; ++q) v[p][q] *= fa;
+  }
+  const float f1 = ldexpf(1.f, one ? e : e2);   // the (last) factor applied at the store
 #pragma unroll
   for (int p = 0; p < NPASS; ++p) {
     const int row = row0 + p * RP + lr;
@@ -204,14 +247,13 @@ __global__ void __launch_bounds__(quant_threads<D, kRope>()) quant_kernel(const 
     uint8_t* dst = x8 + (head_off + row) * D + li * EPL;
     if constexpr (EPL == 2) {
       uint16_t pq;
-      asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pq) : "f"(v[p][1] * f1 * f2), "f"(v[p][0] * f1 * f2));
+      asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pq) : "f"(v[p][1] * f1), "f"(v[p][0] * f1));
       *reinterpret_cast<uint16_t*>(dst) = pq;
     } else {
       uint32_t pk[EPL / 4];
 #pragma unroll
       for (int u = 0; u < EPL / 4; ++u)
-        pk[u] = pack_e4m3x4(v[p][4 * u] * f1 * f2, v[p][4 * u + 1] * f1 * f2, v[p][4 * u + 2] * f1 * f2,
-                            v[p][4 * u + 3] * f1 * f2);
+        pk[u] = pack_e4m3x4(v[p][4 * u] * f1, v[p][4 * u + 1] * f1, v[p][4 * u + 2] * f1, v[p][4 * u + 3] * f1);
       if constexpr (EPL % 16 == 0) {
 #pragma unroll
         for (int q = 0; q < EPL / 16; ++q)
@@ -224,11 +266,87 @@ __global__ void __launch_bounds__(quant_threads<D, kRope>()) quant_kernel(const 
   }
 }
 
+// Plain instance (no rotation, no RoPE): the 16-bit inputs stay packed in
+// registers between the load and the store (a quarter of the registers of
+// the float layout above), so more CTAs fit on an SM and each issues all of
+// its block's loads before its first use; a lane holds 8 consecutive
+// elements per row part (one 16-byte load), 256 threads per 128-row block.
+// The codes and factors equal those of the float layout: the same amax (of
+// the same values), the same power-of-two factor, each element scaled once.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) quant_plain_kernel(const T* __restrict__ x, uint8_t* __restrict__ x8,
+                                                          float* __restrict__ scales, int H, int N) {
+  constexpr int VPR = D / 8;                 // 16-byte vectors per row
+  constexpr int NV = 128 * VPR / 256;        // vectors per thread
+  __shared__ float red[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const long long base = ((static_cast<long long>(b) * H + h) * N + static_cast<long long>(blk) * 128) * D;
+  const int rows = min(128, N - blk * 128);
+  uint4 w[NV];
+  // vector i of this thread: row (i * 256 + threadIdx.x) / VPR, consecutive
+  // threads on consecutive vectors (coalesced)
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int vi = i * 256 + static_cast<int>(threadIdx.x);
+    w[i] = vi / VPR < rows ? reinterpret_cast<const uint4*>(x + base)[vi] : make_uint4(0, 0, 0, 0);
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const uint32_t wv[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      amax = fmax3(amax, fabsf(to_f32<T>(wv[u] & 0xFFFFu)), fabsf(to_f32<T>(wv[u] >> 16)));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if (lane == 0) red[warp] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+  const int e = e4m3_scale_exponent(amax);
+  if (threadIdx.x == 0) scales[(static_cast<long long>(b) * H + h) * gridDim.x + blk] = ldexpf(1.f, -e);
+  // x * 2^e in one multiply when 2^e is a normal float (exact either way:
+  // a power-of-two scaling), else in two steps
+  const int e1 = e / 2, e2 = e - e1;
+  const bool one = e >= -126 && e <= 127;
+  const float f = one ? ldexpf(1.f, e) : ldexpf(1.f, e1), f2 = one ? 1.f : ldexpf(1.f, e2);
+  uint2* dst = reinterpret_cast<uint2*>(x8 + base);
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int vi = i * 256 + static_cast<int>(threadIdx.x);
+    if (vi / VPR >= rows) continue;
+    const uint32_t wv[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+    float y[8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      y[2 * u] = to_f32<T>(wv[u] & 0xFFFFu) * f;
+      y[2 * u + 1] = to_f32<T>(wv[u] >> 16) * f;
+    }
+    if (!one) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) y[u] *= f2;
+    }
+    dst[vi] = make_uint2(pack_e4m3x4(y[0], y[1], y[2], y[3]), pack_e4m3x4(y[4], y[5], y[6], y[7]));
+  }
+}
+
 template <typename T, bool kRope>
 cudaError_t launch_typed(const void* x, uint8_t* x8, float* scales, int B, int H, int N, int d, const int8_t* signs,
                          float inv_sqrt_d, const float* rc, const float* rs, cudaStream_t st) {
   const dim3 grid((N + 127) / 128, H, B);
   const T* xt = static_cast<const T*>(x);
+  if (!kRope && signs == nullptr) {
+    switch (d) {
+      case 64: quant_plain_kernel<T, 64><<<grid, 256, 0, st>>>(xt, x8, scales, H, N); break;
+      case 128: quant_plain_kernel<T, 128><<<grid, 256, 0, st>>>(xt, x8, scales, H, N); break;
+      case 256: quant_plain_kernel<T, 256><<<grid, 256, 0, st>>>(xt, x8, scales, H, N); break;
+      default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+  }
   switch (d) {
     case 64: quant_kernel<T, 64, kRope><<<grid, quant_threads<64, kRope>(), 0, st>>>(xt, x8, scales, H, N, signs, inv_sqrt_d, rc, rs); break;
     case 128: quant_kernel<T, 128, kRope><<<grid, quant_threads<128, kRope>(), 0, st>>>(xt, x8, scales, H, N, signs, inv_sqrt_d, rc, rs); break;
