@@ -125,7 +125,7 @@ attn_status run_bwd_det(const void* q, const void* k, const void* v, const void*
   a.status = status;
   cudaError_t e = launch_bwd_pre(dtype, d, o, dout, dvec, nullptr, rows, Hq, N, 0, st);
   if (e == cudaSuccess) e = launch_bwd_dkdv(dtype, d, tk, tv, tq, tdo, a, N, B, st);
-  if (e == cudaSuccess) e = launch_bwd_dq(dtype, tq128, tdo128, tk, tv, a, N, B, st);
+  if (e == cudaSuccess) e = launch_bwd_dq(dtype, d, tq128, tdo128, tk, tv, a, N, B, st);
   return from_cuda(e);
 }
 
@@ -148,7 +148,7 @@ attn_status attn_bwd_deterministic(const void* q, const void* k, const void* v, 
   attn_status s = check_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, ws_bytes,
                                attn_bwd_deterministic_workspace_size(B, Hq, Hkv, N, d), Hq, Hkv, d, dtype);
   if (s != ATTN_OK) return s;
-  if (d != 128) return ATTN_ERR_HEADDIM;   // the query-stationary dQ kernel is built for d = 128
+  if (d == 256) return ATTN_ERR_HEADDIM;   // the query-stationary dQ kernel is built for d = 64 and 128
   int* status;
   if ((s = attn::device_context(&status)) != ATTN_OK) return s;
   return run_bwd_det(q, k, v, o, lse, dout, dq, dk, dv, workspace, B, N, Hq, Hkv, d, scale, window_left,

@@ -1,4 +1,5 @@
-// dQ kernel of the deterministic backward for sm_103a (BF16 / FP16, head dim 128).
+// dQ kernel of the deterministic backward for sm_103a (BF16 / FP16, head dim 64
+// or 128).
 //
 // Method: FlashAttention-3 (zenmind.me summary) §3.1 backward chain with P
 // recomputed from the forward's log-sum-exp and §4 step 5 (paper App. B.1)
@@ -11,13 +12,14 @@
 // the key-stationary kernel with its dQ product left out.)
 //
 // Tensor memory (512 columns): S [128 q x 128 keys] FP32 at 0..127, dP at
-// 128..255, dQ [128 q x 128 dims] FP32 at 256..383, dS (16-bit pairs, two
+// 128..255, dQ [128 q x d dims] FP32 from 256, dS (16-bit pairs, two
 // buffers) at 384..447 and 448..511.
 // Shared memory: Q and dO tiles (loaded once), a ring of three K tiles and a
 // ring of two V tiles; 128-byte-swizzled boxes of 64 elements x 128 rows.
 // Warps: 0 TMA, 1 MMA (one lane), 4..11 two warpgroups; warpgroup g turns the
 // scores of keys 64g .. 64g + 63 into dS (thread = query row of its lane
-// quarter) and, at the end, writes dims 64g .. 64g + 63 of dQ.
+// quarter) and, at the end, writes dims 64g .. 64g + 63 of dQ (at d = 64 the
+// first warpgroup writes them all).
 // MMA order for KV step j: S(j) = Q K_j^T and dP(j) = dO V_j^T once the
 // compute warps hold S(j-1)/dP(j-1) in registers, then dQ += dS(j-1) K_{j-1}
 // once dS(j-1) is in tensor memory; so S(j)/dP(j) run while dS(j-1) is formed.
@@ -31,9 +33,11 @@
 
 namespace attn {
 
-template <int DT>
+template <int DT, int DIM>
 struct DqCfg {
-  static constexpr int D = 128;
+  static_assert(DIM == 64 || DIM == 128, "deterministic dQ kernel is written for head dim 64 or 128");
+  static constexpr int D = DIM;
+  static constexpr int NBOX = D / 64;               // 64-element boxes per row
   static constexpr int TILE_B = 128 * D * 2;        // one 128-row tile
   static constexpr int BOX_B = 128 * 128;           // one 64-element box of 128 rows
   static constexpr int SBO = 1024;                  // 8 rows of 128 bytes
@@ -52,12 +56,12 @@ struct DqCfg {
   static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 256, COL_DS = 384;
 };
 
-template <int DT>
+template <int DT, int DIM>
 __global__ void __launch_bounds__(384, 1)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
               const BwdArgs a) {
-  using C = DqCfg<DT>;
+  using C = DqCfg<DT, DIM>;
   constexpr int D = C::D;
   extern __shared__ __align__(1024) uint8_t dq_smem[];
   if (smem_u32(dq_smem) & 1023u) {
@@ -147,7 +151,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     if (lane == 0) {
       const int qrow = seq0 + r0;
       mbar_arrive_expect_tx(q_full, 2 * C::TILE_B);
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < C::NBOX; ++c) {
         if (packed) {
           tma_load_4d(sQ + c * C::BOX_B, &tmQ, q_full, c * 64, h, qrow, 0);
           tma_load_4d(sdO + c * C::BOX_B, &tmdO, q_full, c * 64, h, qrow, 0);
@@ -161,14 +165,14 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const int sk = j % C::NK, sv = j % C::NV;
         if (!mbar_wait(&k_empty[sk], ((j / C::NK) & 1) ^ 1, a.status)) break;
         mbar_arrive_expect_tx(&k_full[sk], C::TILE_B);
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < C::NBOX; ++c) {
           uint8_t* dst = sK + sk * C::TILE_B + c * C::BOX_B;
           if (packed) tma_load_4d(dst, &tmK, &k_full[sk], c * 64, hkv, krow, 0);
           else tma_load_4d(dst, &tmK, &k_full[sk], c * 64, krow, hkv, b);
         }
         if (!mbar_wait(&v_empty[sv], ((j / C::NV) & 1) ^ 1, a.status)) break;
         mbar_arrive_expect_tx(&v_full[sv], C::TILE_B);
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < C::NBOX; ++c) {
           uint8_t* dst = sV + sv * C::TILE_B + c * C::BOX_B;
           if (packed) tma_load_4d(dst, &tmV, &v_full[sv], c * 64, hkv, krow, 0);
           else tma_load_4d(dst, &tmV, &v_full[sv], c * 64, krow, hkv, b);
@@ -295,7 +299,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(dq_final, 0, a.status));
     tc_fence_after();
-    if (ok) {   // dQ row qi, dims 64g .. 64g + 63, times scale
+    if (ok && 64 * g < D) {   // dQ row qi, dims 64g .. 64g + 63, times scale
       const long long off = static_cast<long long>(b) * a.q_sb + static_cast<long long>(h) * a.q_sh +
                             static_cast<long long>(seq0 + qi) * a.q_sn + 64 * g;
 #pragma unroll 1

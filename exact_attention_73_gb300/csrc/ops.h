@@ -34,7 +34,7 @@ int bwd_dq_rows(int d);
 int bwd_dq_dims(int d);
 cudaError_t launch_bwd_dkdv(int dt, int d, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
                             const CUtensorMap& dout, const BwdArgs& a, int max_len, int nz, cudaStream_t st);
-cudaError_t launch_bwd_dq(int dt, const CUtensorMap& q, const CUtensorMap& dout, const CUtensorMap& k,
+cudaError_t launch_bwd_dq(int dt, int d, const CUtensorMap& q, const CUtensorMap& dout, const CUtensorMap& k,
                           const CUtensorMap& v, const BwdArgs& a, int max_len, int nz, cudaStream_t st);
 cudaError_t launch_dq_convert(int dt, const float* acc, void* dq, long long n, float scale, cudaStream_t st);
 

@@ -237,7 +237,8 @@ ATTN_API size_t attn_bwd_deterministic_workspace_size(int B, int Hq, int Hkv, in
  * sums dS K over the KV tiles in increasing order inside one CTA. Every output
  * element has one writer and one summation order, so repeated calls with the
  * same inputs return identical bits. Costs three more GEMMs per tile pair
- * than attn_bwd (S and dP are computed twice). d must be 128.
+ * than attn_bwd (S and dP are computed twice). d must be 64 or 128
+ * (ATTN_ERR_HEADDIM for 256).
  */
 ATTN_API attn_status attn_bwd_deterministic(const void* q, const void* k, const void* v, const void* o,
                                             const float* lse, const void* dout,

@@ -99,11 +99,12 @@ def test_argument_checks_before_any_device_work(lib):
     assert lib.attn_fwd_window(None, P(16), P(16), P(16), P(16), 1, 2, 1, 8, 64, 0.1, 4, 0, 0, None) == 1
     assert lib.attn_bwd_window(*args, P(16), ws, 1, 2, 1, 8, 128, 0.1, -5, 0, 0, None) == 3
     assert lib.attn_bwd_window(*args, P(16), ws - 1, 1, 2, 1, 8, 128, 0.1, 3, 0, 0, None) == 7
-    # deterministic backward: its own (D-only) workspace, d = 128, window bounds
+    # deterministic backward: its own (D-only) workspace, d = 64 or 128, window bounds
     wd = binding.attn_bwd_deterministic_workspace_size(1, 2, 1, 8, 128)
     assert wd == 256
     assert lib.attn_bwd_deterministic(*args, P(16), wd - 1, 1, 2, 1, 8, 128, 0.1, -1, -1, 0, None) == 7
-    assert lib.attn_bwd_deterministic(*args, P(16), wd, 1, 2, 1, 8, 64, 0.1, -1, -1, 0, None) == 4
+    assert lib.attn_bwd_deterministic(*args, P(16), wd, 1, 2, 1, 8, 256, 0.1, -1, -1, 0, None) == 4
+    assert lib.attn_bwd_deterministic(*args, P(16), wd, 1, 2, 1, 8, 96, 0.1, -1, -1, 0, None) == 4
     assert lib.attn_bwd_deterministic(*args, P(16), wd, 1, 2, 1, 8, 128, 0.1, -3, 0, 0, None) == 3
 
 

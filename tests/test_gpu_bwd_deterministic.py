@@ -57,13 +57,14 @@ def run_fused(qd, kd, vd, dod, o, lse, window):
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("window", [(-1, -1), (-1, 0), (100, 7)])
 @pytest.mark.parametrize("n", [1, 64, 200, 640, 1000])
-def test_parity_and_repeats(dtype, window, n):
-    q, k, v, do = inputs.normal(400 + n, [(2, 4, n, 128), (2, 2, n, 128), (2, 2, n, 128), (2, 4, n, 128)],
+@pytest.mark.parametrize("d", [64, 128])
+def test_parity_and_repeats(dtype, window, n, d):
+    q, k, v, do = inputs.normal(400 + n + d, [(2, 4, n, d), (2, 2, n, d), (2, 2, n, d), (2, 4, n, d)],
                                 dtype=dtype)
     qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
     o, lse = forward(qd, kd, vd, window)
     a = run_det(qd, kd, vd, dod, o, lse, window)
-    ref = A.backward(q, k, v, do, 128 ** -0.5, False, window)
+    ref = A.backward(q, k, v, do, d ** -0.5, False, window)
     for name, g, r in zip(("dQ", "dK", "dV"), a, ref):
         assert rel_rms(g.cpu(), r) <= 1e-2, (name, rel_rms(g.cpu(), r))
     b = run_det(qd, kd, vd, dod, o, lse, window)

@@ -75,7 +75,8 @@ def test_forward(dtype, window):
 
 
 @pytest.mark.parametrize("kind,d", [("fused", 128), ("window", 128), ("deterministic", 128), ("noalloc", 128),
-                                    ("fused", 64), ("window", 64), ("noalloc", 64), ("fused", 256), ("window", 256)])
+                                    ("fused", 64), ("window", 64), ("deterministic", 64), ("noalloc", 64),
+                                    ("fused", 256), ("window", 256)])
 def test_backward(kind, d):
     q, k, v, do = dense_inputs(701, d=d)
     B, Hq, N, d = q.shape
