@@ -364,6 +364,54 @@ attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8,
   return from_cuda(launch_fwd(kE4M3, d, tq, tk, tv, a, N, Hq, B, static_cast<cudaStream_t>(stream)));
 }
 
+attn_status attn_fwd_fp8_varlen(const void* q8, const void* k8, const void* v8,
+                                const float* sq, const float* sk, const float* sv,
+                                void* o, float* lse, const int* cu_seqlens, const int* cu_blocks,
+                                int nseq, int T, int max_seqlen, int num_blocks,
+                                int Hq, int Hkv, int d, float scale, int causal, void* stream) {
+  if (!q8 || !k8 || !v8 || !sq || !sk || !sv || !o || !lse || !cu_seqlens || !cu_blocks) return ATTN_ERR_NULL;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(sq) || !aligned16(sk) ||
+      !aligned16(sv) || !aligned16(o) || !aligned16(lse) || !aligned16(cu_seqlens) || !aligned16(cu_blocks))
+    return ATTN_ERR_ALIGN;
+  if (nseq < 1 || nseq > 65535 || T < 1 || max_seqlen < 1 || max_seqlen > T || num_blocks < nseq ||
+      num_blocks > T)
+    return ATTN_ERR_SHAPE;
+  attn_status s = check_heads(Hq, Hkv, d);
+  if (s != ATTN_OK) return s;
+  int* status;
+  if ((s = device_context(&status)) != ATTN_OK) return s;
+  CUtensorMap tq, tk, tv;
+  const int kv_rows = fwd_e4m3_kv_rows(d);
+  if (!operand_map(&tq, q8, kE4M3, d, true, 1, Hq, T, 128) ||
+      !operand_map(&tk, k8, kE4M3, d, true, 1, Hkv, T, kv_rows) ||
+      !operand_map(&tv, v8, kE4M3, d, true, 1, Hkv, T, kv_rows))
+    return ATTN_ERR_CUDA;
+  FwdArgs a{};
+  a.o = o;
+  a.lse = lse;
+  a.o_sn = static_cast<long long>(Hq) * d;
+  a.o_sh = d;
+  a.o_sb = 0;
+  a.l_sh = T;
+  a.l_sb = 0;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.group = Hq / Hkv;
+  a.N = 0;
+  a.cu_seqlens = cu_seqlens;
+  a.scale_log2 = scale * kLog2e;
+  a.causal = causal ? 1 : 0;
+  a.win_left = -1;
+  a.win_right = causal ? 0 : -1;
+  a.sq = sq;
+  a.sk = sk;
+  a.sv = sv;
+  a.nblk = num_blocks;
+  a.cu_blocks = cu_blocks;
+  a.status = status;
+  return from_cuda(launch_fwd(kE4M3, d, tq, tk, tv, a, max_seqlen, Hq, nseq, static_cast<cudaStream_t>(stream)));
+}
+
 int attn_fwd_fp8_kv_tile(int d) { return fwd_e4m3_kv_rows(d); }
 
 attn_status attn_get_device_status(void* stream) {
@@ -408,6 +456,28 @@ extern "C" attn_status attn_quantize_fp8(const void* x, attn_dtype in_dtype, voi
                                          int B, int H, int N, int d, const int8_t* hadamard_signs,
                                          void* stream) {
   return quantize(x, in_dtype, x8, scales, B, H, N, d, nullptr, nullptr, hadamard_signs, stream);
+}
+
+extern "C" attn_status attn_quantize_fp8_varlen(const void* x, attn_dtype in_dtype, void* x8, float* scales,
+                                                const int* cu_seqlens, const int* cu_blocks, int nseq, int T,
+                                                int max_seqlen, int num_blocks, int H, int d,
+                                                const int8_t* hadamard_signs, void* stream) {
+  if (!x || !x8 || !scales || !cu_seqlens || !cu_blocks) return ATTN_ERR_NULL;
+  if (!aligned16(x) || !aligned16(x8) || !aligned16(scales) || !aligned16(cu_seqlens) || !aligned16(cu_blocks) ||
+      (hadamard_signs && !aligned16(hadamard_signs)))
+    return ATTN_ERR_ALIGN;
+  if (nseq < 1 || nseq > 65535 || T < 1 || max_seqlen < 1 || max_seqlen > T || num_blocks < nseq ||
+      num_blocks > T || H < 1 || H > 65535)
+    return ATTN_ERR_SHAPE;
+  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_HEADDIM;
+  if (in_dtype != ATTN_BF16 && in_dtype != ATTN_FP16) return ATTN_ERR_DTYPE;
+  int* status;
+  attn_status s = device_context(&status);
+  if (s != ATTN_OK) return s;
+  const float inv_sqrt_d = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+  return from_cuda(launch_quant_fp8_varlen(x, in_dtype, static_cast<uint8_t*>(x8), scales, cu_seqlens, cu_blocks,
+                                           nseq, max_seqlen, num_blocks, H, d, hadamard_signs, inv_sqrt_d,
+                                           static_cast<cudaStream_t>(stream)));
 }
 
 extern "C" attn_status attn_quantize_fp8_rope(const void* x, attn_dtype in_dtype, void* x8, float* scales,

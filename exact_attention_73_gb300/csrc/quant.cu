@@ -8,8 +8,8 @@
 // One CTA per (128-row block, head, batch). Without rotation and RoPE a
 // lighter instance keeps the inputs packed (quant_plain_kernel). Otherwise a
 // lane holds EPL consecutive
-// elements of a row (d / EPL lanes per row): EPL = 32 for the plain and
-// rotation instances (8 warps of 16 rows, 16-byte loads), EPL = d / 32 for
+// elements of a row (d / EPL lanes per row): EPL = 32 for the rotation
+// instance (8 warps of 16 rows, 16-byte loads), EPL = d / 32 for
 // the RoPE instance (a warp per row, 16 warps of 8 rows). The fast
 // Walsh-Hadamard transform runs in FP32 in radix-2 stages of stride 1, 2, 4,
 // ...: strides below EPL inside a lane, larger ones across the lanes of a row
@@ -77,9 +77,45 @@ __device__ __forceinline__ float to_f32(uint32_t bits16) {
   else return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16)));
 }
 
-// Layout per instance. The plain and rotation instances: a lane holds 32
-// consecutive elements of a row (d/32 lanes per row), so five Hadamard stages
-// run in registers, with 16-byte loads; 8 warps of 16 rows. The RoPE
+// Where a CTA's 128-row block lives. Dense [B, H, N, d]: grid (blocks, H,
+// B), block blk of (b, h) has factor index (b * H + h) * blocks + blk.
+// Packed [T, H, d] (cu_seqlens non-null): grid (blocks of the longest
+// sequence, H, sequences); each sequence is blocked from its own first row,
+// and block blk of sequence z has factor index h * nb + cu_blocks[z] + blk
+// (nb blocks per head in all).
+struct QuantGeom {
+  int H, N;
+  const int* cu_seqlens;
+  const int* cu_blocks;
+  int nb;
+};
+struct QuantBlock {
+  long long row0;   // element offset of row 0 of this (sequence or batch, head)
+  long long rs;     // elements from one row to the next
+  long long si;     // factor index of this block
+  int L;            // rows of this (sequence or batch, head)
+};
+template <int D>
+__device__ __forceinline__ QuantBlock quant_block(const QuantGeom& g, int blk, int h, int z) {
+  QuantBlock q;
+  if (g.cu_seqlens != nullptr) {
+    const int seq0 = g.cu_seqlens[z];
+    q.L = g.cu_seqlens[z + 1] - seq0;
+    q.row0 = (static_cast<long long>(seq0) * g.H + h) * D;
+    q.rs = static_cast<long long>(g.H) * D;
+    q.si = static_cast<long long>(h) * g.nb + g.cu_blocks[z] + blk;
+  } else {
+    q.L = g.N;
+    q.row0 = (static_cast<long long>(z) * g.H + h) * g.N * D;
+    q.rs = D;
+    q.si = (static_cast<long long>(z) * g.H + h) * gridDim.x + blk;
+  }
+  return q;
+}
+
+// Layout per instance. The rotation instance: a lane holds 32 consecutive
+// elements of a row (d/32 lanes per row), so five Hadamard stages run in
+// registers, with 16-byte loads; 8 warps of 16 rows. The RoPE
 // instance: a warp holds one row at a time (d/32 elements per lane); 16 warps
 // of 8 rows, which keeps more cos/sin table loads in flight (measured faster
 // for it than the 32-per-lane layout).
@@ -121,7 +157,7 @@ __device__ __forceinline__ void load_row_part(const T* src, float* v) {
 
 template <typename T, int D, bool kRope>
 __global__ void __launch_bounds__(quant_threads<D, kRope>()) quant_kernel(const T* __restrict__ x, uint8_t* __restrict__ x8,
-                                                             float* __restrict__ scales, int H, int N,
+                                                             float* __restrict__ scales, const QuantGeom geo,
                                                              const int8_t* __restrict__ signs, float inv_sqrt_d,
                                                              const float* __restrict__ rope_cos,
                                                              const float* __restrict__ rope_sin) {
@@ -135,8 +171,10 @@ __global__ void __launch_bounds__(quant_threads<D, kRope>()) quant_kernel(const 
   __shared__ float red[NW];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int lr = lane / R, li = lane % R;
-  const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const long long head_off = (static_cast<long long>(b) * H + h) * N;
+  const int blk = blockIdx.x;
+  const QuantBlock qb = quant_block<D>(geo, blk, blockIdx.y, blockIdx.z);
+  if (blk * 128 >= qb.L) return;   // a packed sequence shorter than the longest
+  const int N = qb.L;
   const int row0 = blk * 128 + warp * RPW;
   float v[NPASS][EPL];
   float amax = 0.f;
@@ -153,7 +191,7 @@ __global__ void __launch_bounds__(quant_threads<D, kRope>()) quant_kernel(const 
       const int row = row0 + p * RP + lr;
 #pragma unroll
       for (int q = 0; q < NRAW; ++q)
-        raw[p][q] = row < N ? reinterpret_cast<const uint4*>(x + (head_off + row) * D + li * EPL)[q]
+        raw[p][q] = row < N ? reinterpret_cast<const uint4*>(x + qb.row0 + row * qb.rs + li * EPL)[q]
                             : make_uint4(0, 0, 0, 0);
     }
   }
@@ -172,7 +210,7 @@ __global__ void __launch_bounds__(quant_threads<D, kRope>()) quant_kernel(const 
         }
       }
     } else if (valid) {
-      load_row_part<T, EPL>(x + (head_off + row) * D + li * EPL, v[p]);
+      load_row_part<T, EPL>(x + qb.row0 + row * qb.rs + li * EPL, v[p]);
     } else {
 #pragma unroll
       for (int e = 0; e < EPL; ++e) v[p][e] = 0.f;
@@ -227,7 +265,7 @@ __global__ void __launch_bounds__(quant_threads<D, kRope>()) quant_kernel(const 
 #pragma unroll
   for (int w = 1; w < NW; ++w) amax = fmaxf(amax, red[w]);
   const int e = e4m3_scale_exponent(amax);
-  if (threadIdx.x == 0) scales[(static_cast<long long>(b) * H + h) * gridDim.x + blk] = ldexpf(1.f, -e);
+  if (threadIdx.x == 0) scales[qb.si] = ldexpf(1.f, -e);
   // x * 2^e in one multiply when 2^e is a normal float (exact either way:
   // a power-of-two scaling), else in two steps
   const int e1 = e / 2, e2 = e - e1;
@@ -244,7 +282,7 @@ __global__ void __launch_bounds__(quant_threads<D, kRope>()) quant_kernel(const 
   for (int p = 0; p < NPASS; ++p) {
     const int row = row0 + p * RP + lr;
     if (row >= N) continue;
-    uint8_t* dst = x8 + (head_off + row) * D + li * EPL;
+    uint8_t* dst = x8 + qb.row0 + row * qb.rs + li * EPL;
     if constexpr (EPL == 2) {
       uint16_t pq;
       asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pq) : "f"(v[p][1] * f1), "f"(v[p][0] * f1));
@@ -275,21 +313,24 @@ __global__ void __launch_bounds__(quant_threads<D, kRope>()) quant_kernel(const 
 // the same values), the same power-of-two factor, each element scaled once.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) quant_plain_kernel(const T* __restrict__ x, uint8_t* __restrict__ x8,
-                                                          float* __restrict__ scales, int H, int N) {
+                                                          float* __restrict__ scales, const QuantGeom geo) {
   constexpr int VPR = D / 8;                 // 16-byte vectors per row
   constexpr int NV = 128 * VPR / 256;        // vectors per thread
   __shared__ float red[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const long long base = ((static_cast<long long>(b) * H + h) * N + static_cast<long long>(blk) * 128) * D;
-  const int rows = min(128, N - blk * 128);
+  const int blk = blockIdx.x;
+  const QuantBlock qb = quant_block<D>(geo, blk, blockIdx.y, blockIdx.z);
+  if (blk * 128 >= qb.L) return;   // a packed sequence shorter than the longest
+  const long long base = qb.row0 + static_cast<long long>(blk) * 128 * qb.rs;
+  const int rows = min(128, qb.L - blk * 128);
+  // element offset of vector vi: row vi / VPR of the block, 8 elements from
+  // column 8 * (vi % VPR); consecutive threads on consecutive vectors
+  auto voff = [&](int vi) { return base + (vi / VPR) * qb.rs + (vi % VPR) * 8; };
   uint4 w[NV];
-  // vector i of this thread: row (i * 256 + threadIdx.x) / VPR, consecutive
-  // threads on consecutive vectors (coalesced)
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     const int vi = i * 256 + static_cast<int>(threadIdx.x);
-    w[i] = vi / VPR < rows ? reinterpret_cast<const uint4*>(x + base)[vi] : make_uint4(0, 0, 0, 0);
+    w[i] = vi / VPR < rows ? *reinterpret_cast<const uint4*>(x + voff(vi)) : make_uint4(0, 0, 0, 0);
   }
   float amax = 0.f;
 #pragma unroll
@@ -307,13 +348,12 @@ __global__ void __launch_bounds__(256) quant_plain_kernel(const T* __restrict__ 
 #pragma unroll
   for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
   const int e = e4m3_scale_exponent(amax);
-  if (threadIdx.x == 0) scales[(static_cast<long long>(b) * H + h) * gridDim.x + blk] = ldexpf(1.f, -e);
+  if (threadIdx.x == 0) scales[qb.si] = ldexpf(1.f, -e);
   // x * 2^e in one multiply when 2^e is a normal float (exact either way:
   // a power-of-two scaling), else in two steps
   const int e1 = e / 2, e2 = e - e1;
   const bool one = e >= -126 && e <= 127;
   const float f = one ? ldexpf(1.f, e) : ldexpf(1.f, e1), f2 = one ? 1.f : ldexpf(1.f, e2);
-  uint2* dst = reinterpret_cast<uint2*>(x8 + base);
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     const int vi = i * 256 + static_cast<int>(threadIdx.x);
@@ -329,31 +369,42 @@ __global__ void __launch_bounds__(256) quant_plain_kernel(const T* __restrict__ 
 #pragma unroll
       for (int u = 0; u < 8; ++u) y[u] *= f2;
     }
-    dst[vi] = make_uint2(pack_e4m3x4(y[0], y[1], y[2], y[3]), pack_e4m3x4(y[4], y[5], y[6], y[7]));
+    *reinterpret_cast<uint2*>(x8 + voff(vi)) =
+        make_uint2(pack_e4m3x4(y[0], y[1], y[2], y[3]), pack_e4m3x4(y[4], y[5], y[6], y[7]));
   }
 }
 
 template <typename T, bool kRope>
-cudaError_t launch_typed(const void* x, uint8_t* x8, float* scales, int B, int H, int N, int d, const int8_t* signs,
-                         float inv_sqrt_d, const float* rc, const float* rs, cudaStream_t st) {
-  const dim3 grid((N + 127) / 128, H, B);
+cudaError_t launch_typed(const void* x, uint8_t* x8, float* scales, dim3 grid, const QuantGeom& geo, int d,
+                         const int8_t* signs, float inv_sqrt_d, const float* rc, const float* rs, cudaStream_t st) {
   const T* xt = static_cast<const T*>(x);
   if (!kRope && signs == nullptr) {
     switch (d) {
-      case 64: quant_plain_kernel<T, 64><<<grid, 256, 0, st>>>(xt, x8, scales, H, N); break;
-      case 128: quant_plain_kernel<T, 128><<<grid, 256, 0, st>>>(xt, x8, scales, H, N); break;
-      case 256: quant_plain_kernel<T, 256><<<grid, 256, 0, st>>>(xt, x8, scales, H, N); break;
+      case 64: quant_plain_kernel<T, 64><<<grid, 256, 0, st>>>(xt, x8, scales, geo); break;
+      case 128: quant_plain_kernel<T, 128><<<grid, 256, 0, st>>>(xt, x8, scales, geo); break;
+      case 256: quant_plain_kernel<T, 256><<<grid, 256, 0, st>>>(xt, x8, scales, geo); break;
       default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
   }
   switch (d) {
-    case 64: quant_kernel<T, 64, kRope><<<grid, quant_threads<64, kRope>(), 0, st>>>(xt, x8, scales, H, N, signs, inv_sqrt_d, rc, rs); break;
-    case 128: quant_kernel<T, 128, kRope><<<grid, quant_threads<128, kRope>(), 0, st>>>(xt, x8, scales, H, N, signs, inv_sqrt_d, rc, rs); break;
-    case 256: quant_kernel<T, 256, kRope><<<grid, quant_threads<256, kRope>(), 0, st>>>(xt, x8, scales, H, N, signs, inv_sqrt_d, rc, rs); break;
+    case 64: quant_kernel<T, 64, kRope><<<grid, quant_threads<64, kRope>(), 0, st>>>(xt, x8, scales, geo, signs, inv_sqrt_d, rc, rs); break;
+    case 128: quant_kernel<T, 128, kRope><<<grid, quant_threads<128, kRope>(), 0, st>>>(xt, x8, scales, geo, signs, inv_sqrt_d, rc, rs); break;
+    case 256: quant_kernel<T, 256, kRope><<<grid, quant_threads<256, kRope>(), 0, st>>>(xt, x8, scales, geo, signs, inv_sqrt_d, rc, rs); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_geo(const void* x, int in_dt, uint8_t* x8, float* scales, dim3 grid, const QuantGeom& geo, int d,
+                       const int8_t* signs, float inv_sqrt_d, const float* rope_cos, const float* rope_sin,
+                       cudaStream_t st) {
+  const bool rope = rope_cos != nullptr;
+  if (in_dt == 0)
+    return rope ? launch_typed<__nv_bfloat16, true>(x, x8, scales, grid, geo, d, signs, inv_sqrt_d, rope_cos, rope_sin, st)
+                : launch_typed<__nv_bfloat16, false>(x, x8, scales, grid, geo, d, signs, inv_sqrt_d, nullptr, nullptr, st);
+  return rope ? launch_typed<__half, true>(x, x8, scales, grid, geo, d, signs, inv_sqrt_d, rope_cos, rope_sin, st)
+              : launch_typed<__half, false>(x, x8, scales, grid, geo, d, signs, inv_sqrt_d, nullptr, nullptr, st);
 }
 
 }  // namespace
@@ -361,12 +412,17 @@ cudaError_t launch_typed(const void* x, uint8_t* x8, float* scales, int B, int H
 cudaError_t launch_quant_fp8(const void* x, int in_dt, uint8_t* x8, float* scales, int B, int H, int N, int d,
                              const int8_t* signs, float inv_sqrt_d, const float* rope_cos, const float* rope_sin,
                              cudaStream_t st) {
-  const bool rope = rope_cos != nullptr;
-  if (in_dt == 0)
-    return rope ? launch_typed<__nv_bfloat16, true>(x, x8, scales, B, H, N, d, signs, inv_sqrt_d, rope_cos, rope_sin, st)
-                : launch_typed<__nv_bfloat16, false>(x, x8, scales, B, H, N, d, signs, inv_sqrt_d, nullptr, nullptr, st);
-  return rope ? launch_typed<__half, true>(x, x8, scales, B, H, N, d, signs, inv_sqrt_d, rope_cos, rope_sin, st)
-              : launch_typed<__half, false>(x, x8, scales, B, H, N, d, signs, inv_sqrt_d, nullptr, nullptr, st);
+  const QuantGeom geo{H, N, nullptr, nullptr, 0};
+  return launch_geo(x, in_dt, x8, scales, dim3((N + 127) / 128, H, B), geo, d, signs, inv_sqrt_d, rope_cos, rope_sin,
+                    st);
+}
+
+cudaError_t launch_quant_fp8_varlen(const void* x, int in_dt, uint8_t* x8, float* scales, const int* cu_seqlens,
+                                    const int* cu_blocks, int nseq, int max_len, int num_blocks, int H, int d,
+                                    const int8_t* signs, float inv_sqrt_d, cudaStream_t st) {
+  const QuantGeom geo{H, 0, cu_seqlens, cu_blocks, num_blocks};
+  return launch_geo(x, in_dt, x8, scales, dim3((max_len + 127) / 128, H, nseq), geo, d, signs, inv_sqrt_d, nullptr,
+                    nullptr, st);
 }
 
 }  // namespace attn

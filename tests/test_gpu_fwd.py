@@ -489,3 +489,80 @@ def test_persistent_walk_matches_one_head_launches(n, fp8):
             one = lambda x: x[b:b + 1, h:h + 1]
             o_ref, lse_ref = A.forward(one(q), one(k), one(v), d ** -0.5, False)
             check_o_lse(one(o), one(lse), o_ref, lse_ref, f"n{n} b{b} h{h}")
+
+
+# Packed FP8: each sequence is blocked from its own first row. Lengths with
+# short, exact-multiple and ragged sequences.
+PACKED_LENS = [1, 127, 128, 300, 700, 5]
+
+
+def packed_quantize_gpu(x, cu, cb, lens, signs=None):
+    T, H, d = x.shape
+    nb = int(cb[-1])
+    x8 = torch.empty((T, H, d), dtype=torch.uint8, device="cuda")
+    sc = torch.full((H, nb), float("nan"), dtype=torch.float32, device="cuda")
+    L.attn_quantize_fp8_varlen(x.cuda(), x8, sc, cu.cuda(), cb.cuda(), max(lens), nb,
+                               None if signs is None else signs.cuda())
+    torch.cuda.synchronize()
+    return x8, sc
+
+
+@pytest.mark.parametrize("rotate", [False, True])
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_packed_quantizer_bit_exact(rotate, d, dtype):
+    """attn_quantize_fp8_varlen against the oracle's block quantisation of
+    each sequence on its own: codes and factors bit for bit."""
+    cu = inputs.cu_seqlens(PACKED_LENS)
+    cb = L.varlen_blocks(PACKED_LENS)
+    T = int(cu[-1])
+    (x,) = inputs.normal(21 + d, [(T, 3, d)], dtype=dtype)
+    signs = inputs.random_signs(4, d) if rotate else None
+    x8, sc = packed_quantize_gpu(x, cu, cb, PACKED_LENS, signs)
+    x8, sc = x8.cpu().numpy(), sc.cpu().numpy()
+    for s_ in range(len(PACKED_LENS)):
+        a, e = int(cu[s_]), int(cu[s_ + 1])
+        codes, fac = F.quantize_blocks(x[a:e].transpose(0, 1)[None], None if signs is None else signs.numpy())
+        assert np.array_equal(x8[a:e].transpose(1, 0, 2), codes[0]), s_
+        assert np.array_equal(sc[:, int(cb[s_]):int(cb[s_ + 1])], fac[0]), s_
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_packed_fp8_forward(causal, d):
+    """attn_fwd_fp8_varlen on packed sequences (GQA 4:2; Q and K rotated):
+    each sequence's O and LSE equal bit for bit those of attn_fwd_fp8 on that
+    sequence alone with the same codes and factors, and match the oracle's
+    FP8 emulation of the sequence (its own block quantisation) within the
+    emulation tolerances."""
+    cu = inputs.cu_seqlens(PACKED_LENS)
+    cb = L.varlen_blocks(PACKED_LENS)
+    T = int(cu[-1])
+    nb = int(cb[-1])
+    q, k, v = inputs.outliers(23 + d, [(T, 4, d), (T, 2, d), (T, 2, d)])
+    signs = inputs.random_signs(4, d)
+    q8, sq = packed_quantize_gpu(q, cu, cb, PACKED_LENS, signs)
+    k8, sk = packed_quantize_gpu(k, cu, cb, PACKED_LENS, signs)
+    v8, sv = packed_quantize_gpu(v, cu, cb, PACKED_LENS)
+    o = torch.full((T, 4, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((4, T), float("nan"), device="cuda")
+    L.attn_fwd_fp8_varlen(q8, k8, v8, sq, sk, sv, o, lse, cu.cuda(), cb.cuda(), max(PACKED_LENS), nb, causal=causal)
+    torch.cuda.synchronize()
+    assert L.attn_get_device_status() == 0
+    for s_, n in enumerate(PACKED_LENS):
+        a, e = int(cu[s_]), int(cu[s_ + 1])
+        b0, b1 = int(cb[s_]), int(cb[s_ + 1])
+        dense = lambda x: x[a:e].transpose(0, 1).contiguous()[None]
+        fac = lambda f: f[:, b0:b1].contiguous()[None]
+        o1 = torch.empty((1, 4, n, d), dtype=torch.bfloat16, device="cuda")
+        lse1 = torch.empty((1, 4, n), device="cuda")
+        L.attn_fwd_fp8(dense(q8), dense(k8), dense(v8), fac(sq), fac(sk), fac(sv), o1, lse1, causal=causal)
+        torch.cuda.synchronize()
+        assert torch.equal(dense(o), o1), s_
+        assert torch.equal(lse[:, a:e][None], lse1), s_
+        gpu = tuple(x.cpu().numpy() for x in (dense(q8), dense(k8), dense(v8), fac(sq), fac(sk), fac(sv)))
+        codes = oracle_fp8_inputs(dense(q).cpu(), dense(k).cpu(), dense(v).cpu(), signs, gpu=gpu)
+        o_ref, lse_ref = F.attention_fp8(*codes, d ** -0.5, causal, tau=F.STALE_MAX_TAU,
+                                         kv_tile=L.attn_fwd_fp8_kv_tile(d))
+        check_fp8_vs_emulation(o1.cpu().double().numpy(), o_ref)
+        assert np.abs(lse1.cpu().double().numpy() - lse_ref).max() <= 1e-3, s_
