@@ -60,8 +60,8 @@ _SIGS = {
     "attn_decode_fp8_workspace_size": ([_I, _I, _I, _I], _Z),
     "attn_decode_fp8": ([_P] * 10 + [_Z, _I, _I, _I, _I, _I, _F, _I, _P], _I),
     "attn_bwd_deterministic": ([_P] * 9 + [_P, _Z, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P], _I),
-    "attn_quantize_fp8_varlen": ([_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
-    "attn_fwd_fp8_varlen": ([_P] * 10 + [_I, _I, _I, _I, _I, _I, _I, _F, _I, _P], _I),
+    "attn_quantize_fp8_varlen": ([_P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
+    "attn_fwd_fp8_varlen": ([_P] * 9 + [_I, _I, _I, _I, _I, _I, _F, _I, _P], _I),
 }
 
 
@@ -195,48 +195,36 @@ def attn_fwd_varlen(q, k, v, o, lse, cu_seqlens, max_seqlen, scale=None, causal=
                                   int(bool(causal)), _dtype(q), _stream(stream)), "attn_fwd_varlen")
 
 
-def varlen_blocks(lengths):
-    """cu_blocks for packed FP8 (int32 [nseq+1], host tensor): sequence z's
-    128-row blocks start at cu_blocks[z]; the last entry is num_blocks."""
-    nb = [0]
-    for n in lengths:
-        nb.append(nb[-1] + (int(n) + 127) // 128)
-    return torch.tensor(nb, dtype=torch.int32)
-
-
-def attn_quantize_fp8_varlen(x, x8, scales, cu_seqlens, cu_blocks, max_seqlen, num_blocks, hadamard_signs=None,
-                             stream=None):
-    """x [T,H,d] bf16/fp16 -> x8 uint8 codes (same shape), scales [H, num_blocks] fp32; each sequence is
-    blocked from its own first row (cu_blocks from varlen_blocks, on the device)."""
+def attn_quantize_fp8_varlen(x, x8, scales, cu_seqlens, max_seqlen, hadamard_signs=None, stream=None):
+    """x [T,H,d] bf16/fp16 -> x8 uint8 codes (same shape), scales [nseq, H, ceil(max_seqlen/128)] fp32;
+    each sequence is blocked from its own first row."""
     T, H, d = _dims(x, "x", 3)
     nseq = cu_seqlens.numel() - 1
     _check(load().attn_quantize_fp8_varlen(_ptr(x, "x"), _dtype(x), _ptr(x8, "x8", x.numel(), torch.uint8),
-                                           _ptr(scales, "scales", H * int(num_blocks), torch.float32),
-                                           _ptr(cu_seqlens, "cu_seqlens", dtype=torch.int32),
-                                           _ptr(cu_blocks, "cu_blocks", nseq + 1, torch.int32), nseq, T,
-                                           int(max_seqlen), int(num_blocks), H, d,
+                                           _ptr(scales, "scales", nseq * H * _nb(int(max_seqlen)), torch.float32),
+                                           _ptr(cu_seqlens, "cu_seqlens", dtype=torch.int32), nseq, T,
+                                           int(max_seqlen), H, d,
                                            _ptr(hadamard_signs, "hadamard_signs", d, torch.int8), _stream(stream)),
            "attn_quantize_fp8_varlen")
 
 
-def attn_fwd_fp8_varlen(q8, k8, v8, sq, sk, sv, o, lse, cu_seqlens, cu_blocks, max_seqlen, num_blocks, scale=None,
-                        causal=False, stream=None):
-    """Packed FP8 forward: q8 [T,Hq,d], k8/v8 [T,Hkv,d] codes, sq [Hq,num_blocks], sk/sv [Hkv,num_blocks];
-    o [T,Hq,d] bf16, lse [Hq,T] fp32."""
+def attn_fwd_fp8_varlen(q8, k8, v8, sq, sk, sv, o, lse, cu_seqlens, max_seqlen, scale=None, causal=False,
+                        stream=None):
+    """Packed FP8 forward: q8 [T,Hq,d], k8/v8 [T,Hkv,d] codes, sq [nseq,Hq,nb], sk/sv [nseq,Hkv,nb]
+    (nb = ceil(max_seqlen/128)); o [T,Hq,d] bf16, lse [Hq,T] fp32."""
     T, Hq, d = _dims(q8, "q8", 3)
     Hkv = _dims(k8, "k8", 3)[1]
     kv = (T, Hkv, d)
     u8, f32 = torch.uint8, torch.float32
     nseq = cu_seqlens.numel() - 1
-    nb = int(num_blocks)
+    nb = _nb(int(max_seqlen))
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     _check(load().attn_fwd_fp8_varlen(_ptr(q8, "q8", dtype=u8), _ptr(k8, "k8", dtype=u8, shape=kv),
-                                      _ptr(v8, "v8", dtype=u8, shape=kv), _ptr(sq, "sq", Hq * nb, f32),
-                                      _ptr(sk, "sk", Hkv * nb, f32), _ptr(sv, "sv", Hkv * nb, f32),
+                                      _ptr(v8, "v8", dtype=u8, shape=kv), _ptr(sq, "sq", nseq * Hq * nb, f32),
+                                      _ptr(sk, "sk", nseq * Hkv * nb, f32), _ptr(sv, "sv", nseq * Hkv * nb, f32),
                                       _ptr(o, "o", q8.numel(), torch.bfloat16), _ptr(lse, "lse", Hq * T, f32),
-                                      _ptr(cu_seqlens, "cu_seqlens", dtype=torch.int32),
-                                      _ptr(cu_blocks, "cu_blocks", nseq + 1, torch.int32), nseq, T,
-                                      int(max_seqlen), nb, Hq, Hkv, d, scale, int(bool(causal)), _stream(stream)),
+                                      _ptr(cu_seqlens, "cu_seqlens", dtype=torch.int32), nseq, T,
+                                      int(max_seqlen), Hq, Hkv, d, scale, int(bool(causal)), _stream(stream)),
            "attn_fwd_fp8_varlen")
 
 

@@ -366,16 +366,13 @@ attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8,
 
 attn_status attn_fwd_fp8_varlen(const void* q8, const void* k8, const void* v8,
                                 const float* sq, const float* sk, const float* sv,
-                                void* o, float* lse, const int* cu_seqlens, const int* cu_blocks,
-                                int nseq, int T, int max_seqlen, int num_blocks,
+                                void* o, float* lse, const int* cu_seqlens, int nseq, int T, int max_seqlen,
                                 int Hq, int Hkv, int d, float scale, int causal, void* stream) {
-  if (!q8 || !k8 || !v8 || !sq || !sk || !sv || !o || !lse || !cu_seqlens || !cu_blocks) return ATTN_ERR_NULL;
+  if (!q8 || !k8 || !v8 || !sq || !sk || !sv || !o || !lse || !cu_seqlens) return ATTN_ERR_NULL;
   if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(sq) || !aligned16(sk) ||
-      !aligned16(sv) || !aligned16(o) || !aligned16(lse) || !aligned16(cu_seqlens) || !aligned16(cu_blocks))
+      !aligned16(sv) || !aligned16(o) || !aligned16(lse) || !aligned16(cu_seqlens))
     return ATTN_ERR_ALIGN;
-  if (nseq < 1 || nseq > 65535 || T < 1 || max_seqlen < 1 || max_seqlen > T || num_blocks < nseq ||
-      num_blocks > T)
-    return ATTN_ERR_SHAPE;
+  if (nseq < 1 || nseq > 65535 || T < 1 || max_seqlen < 1 || max_seqlen > T) return ATTN_ERR_SHAPE;
   attn_status s = check_heads(Hq, Hkv, d);
   if (s != ATTN_OK) return s;
   int* status;
@@ -406,8 +403,7 @@ attn_status attn_fwd_fp8_varlen(const void* q8, const void* k8, const void* v8,
   a.sq = sq;
   a.sk = sk;
   a.sv = sv;
-  a.nblk = num_blocks;
-  a.cu_blocks = cu_blocks;
+  a.nblk = (max_seqlen + 127) / 128;
   a.status = status;
   return from_cuda(launch_fwd(kE4M3, d, tq, tk, tv, a, max_seqlen, Hq, nseq, static_cast<cudaStream_t>(stream)));
 }
@@ -459,15 +455,13 @@ extern "C" attn_status attn_quantize_fp8(const void* x, attn_dtype in_dtype, voi
 }
 
 extern "C" attn_status attn_quantize_fp8_varlen(const void* x, attn_dtype in_dtype, void* x8, float* scales,
-                                                const int* cu_seqlens, const int* cu_blocks, int nseq, int T,
-                                                int max_seqlen, int num_blocks, int H, int d,
-                                                const int8_t* hadamard_signs, void* stream) {
-  if (!x || !x8 || !scales || !cu_seqlens || !cu_blocks) return ATTN_ERR_NULL;
-  if (!aligned16(x) || !aligned16(x8) || !aligned16(scales) || !aligned16(cu_seqlens) || !aligned16(cu_blocks) ||
+                                                const int* cu_seqlens, int nseq, int T, int max_seqlen, int H,
+                                                int d, const int8_t* hadamard_signs, void* stream) {
+  if (!x || !x8 || !scales || !cu_seqlens) return ATTN_ERR_NULL;
+  if (!aligned16(x) || !aligned16(x8) || !aligned16(scales) || !aligned16(cu_seqlens) ||
       (hadamard_signs && !aligned16(hadamard_signs)))
     return ATTN_ERR_ALIGN;
-  if (nseq < 1 || nseq > 65535 || T < 1 || max_seqlen < 1 || max_seqlen > T || num_blocks < nseq ||
-      num_blocks > T || H < 1 || H > 65535)
+  if (nseq < 1 || nseq > 65535 || T < 1 || max_seqlen < 1 || max_seqlen > T || H < 1 || H > 65535)
     return ATTN_ERR_SHAPE;
   if (d != 64 && d != 128 && d != 256) return ATTN_ERR_HEADDIM;
   if (in_dtype != ATTN_BF16 && in_dtype != ATTN_FP16) return ATTN_ERR_DTYPE;
@@ -475,8 +469,8 @@ extern "C" attn_status attn_quantize_fp8_varlen(const void* x, attn_dtype in_dty
   attn_status s = device_context(&status);
   if (s != ATTN_OK) return s;
   const float inv_sqrt_d = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
-  return from_cuda(launch_quant_fp8_varlen(x, in_dtype, static_cast<uint8_t*>(x8), scales, cu_seqlens, cu_blocks,
-                                           nseq, max_seqlen, num_blocks, H, d, hadamard_signs, inv_sqrt_d,
+  return from_cuda(launch_quant_fp8_varlen(x, in_dtype, static_cast<uint8_t*>(x8), scales, cu_seqlens, nseq,
+                                           max_seqlen, H, d, hadamard_signs, inv_sqrt_d,
                                            static_cast<cudaStream_t>(stream)));
 }
 

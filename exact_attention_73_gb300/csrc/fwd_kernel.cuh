@@ -51,8 +51,7 @@ struct FwdArgs {
   const float* sq;              // FP8 dequantisation factors per 128-row block
   const float* sk;
   const float* sv;
-  int nblk;                     // blocks per (batch, head) in sq/sk/sv; packed: per head, all sequences
-  const int* cu_blocks;         // packed FP8: first block of each sequence in sq/sk/sv
+  int nblk;                     // blocks per (batch or packed sequence, head) in sq/sk/sv
   // decode over a KV cache (decode_kernel): items of (split, KV head, batch)
   const int* seqlens;           // valid cache length per sequence (null: N)
   int tiles_per_split;          // KV tiles per split
@@ -139,7 +138,8 @@ __device__ __forceinline__ int kv_index_v(int qt, int j, int nkv) {
 
 // One unit of work: QT query tiles of one (batch or sequence, query head).
 struct FwdUnit {
-  int h, hkv, b, z, seq0, L, nqt, qt0, kv0, nkv;   // z: batch or packed sequence
+  int h, hkv, b, seq0, L, nqt, qt0, kv0, nkv;
+  int fb;   // FP8 factors: batch, or packed sequence (factors [sequences][heads][blocks])
 };
 
 // The k-th unit of this CTA as a linear index over ux * uy * uz units (x
@@ -167,7 +167,6 @@ __device__ __forceinline__ bool fwd_unit(const FwdArgs& a, int lin, FwdUnit& w) 
     bz = lin / a.ux / a.uy;
   }
   w.h = by;
-  w.z = bz;
   if (a.cu_seqlens != nullptr) {
     w.b = 0;
     w.seq0 = a.cu_seqlens[bz];
@@ -189,6 +188,7 @@ __device__ __forceinline__ bool fwd_unit(const FwdArgs& a, int lin, FwdUnit& w) 
   w.kv0 = klo >> 7;
   w.nkv = ((khi + 127) >> 7) - w.kv0;
   w.hkv = w.h / a.group;
+  w.fb = bz;
   return true;
 }
 
@@ -459,16 +459,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       float q_fac = 1.f;
       long long vs_base = 0;
       if constexpr (C::kFp8) {
-        // factors of 128-row blocks: per (batch, head), or per head over the
-        // packed sequences, each blocked from its own first row
-        const bool pk = a.cu_seqlens != nullptr;
-        const long long blk0 = pk ? a.cu_blocks[w.z] : 0;
-        const long long qf = pk ? static_cast<long long>(w.h) * a.nblk + blk0
-                                : (static_cast<long long>(w.b) * a.Hq + w.h) * a.nblk;
-        const long long kf = pk ? static_cast<long long>(w.hkv) * a.nblk + blk0
-                                : (static_cast<long long>(w.b) * a.Hkv + w.hkv) * a.nblk;
-        q_fac = a.sq[qf + min(qtile, w.nqt - 1)];
-        vs_base = kf + kv0;
+        q_fac = a.sq[(static_cast<long long>(w.fb) * a.Hq + w.h) * a.nblk + min(qtile, w.nqt - 1)];
+        vs_base = (static_cast<long long>(w.fb) * a.Hkv + w.hkv) * a.nblk + kv0;
       }
       // FP8: the K and V block factors are fetched one KV step ahead, so their
       // global-load latency overlaps the wait for the next score tile.

@@ -43,9 +43,9 @@ cudaError_t launch_quant_fp8(const void* x, int in_dt, uint8_t* x8, float* scale
                              const int8_t* signs, float inv_sqrt_d, const float* rope_cos, const float* rope_sin,
                              cudaStream_t st);
 // The same over packed [T, H, d] sequences, each blocked from its own first
-// row; factors [H][num_blocks], sequence z's blocks from cu_blocks[z].
+// row; factors [nseq][H][ceil(max_len / 128)].
 cudaError_t launch_quant_fp8_varlen(const void* x, int in_dt, uint8_t* x8, float* scales, const int* cu_seqlens,
-                                    const int* cu_blocks, int nseq, int max_len, int num_blocks, int H, int d,
-                                    const int8_t* signs, float inv_sqrt_d, cudaStream_t st);
+                                    int nseq, int max_len, int H, int d, const int8_t* signs, float inv_sqrt_d,
+                                    cudaStream_t st);
 
 }  // namespace attn

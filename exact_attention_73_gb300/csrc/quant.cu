@@ -78,16 +78,13 @@ __device__ __forceinline__ float to_f32(uint32_t bits16) {
 }
 
 // Where a CTA's 128-row block lives. Dense [B, H, N, d]: grid (blocks, H,
-// B), block blk of (b, h) has factor index (b * H + h) * blocks + blk.
-// Packed [T, H, d] (cu_seqlens non-null): grid (blocks of the longest
-// sequence, H, sequences); each sequence is blocked from its own first row,
-// and block blk of sequence z has factor index h * nb + cu_blocks[z] + blk
-// (nb blocks per head in all).
+// B). Packed [T, H, d] (cu_seqlens non-null): grid (blocks of the longest
+// sequence, H, sequences), each sequence blocked from its own first row.
+// Either way block blk of (batch or sequence z, head h) has factor index
+// (z * H + h) * gridDim.x + blk.
 struct QuantGeom {
   int H, N;
   const int* cu_seqlens;
-  const int* cu_blocks;
-  int nb;
 };
 struct QuantBlock {
   long long row0;   // element offset of row 0 of this (sequence or batch, head)
@@ -95,21 +92,21 @@ struct QuantBlock {
   long long si;     // factor index of this block
   int L;            // rows of this (sequence or batch, head)
 };
-template <int D>
+// kLayout: 0 dense, 1 packed, 2 decided by g.cu_seqlens at run time
+template <int D, int kLayout = 2>
 __device__ __forceinline__ QuantBlock quant_block(const QuantGeom& g, int blk, int h, int z) {
   QuantBlock q;
-  if (g.cu_seqlens != nullptr) {
+  if (kLayout == 1 || (kLayout == 2 && g.cu_seqlens != nullptr)) {
     const int seq0 = g.cu_seqlens[z];
     q.L = g.cu_seqlens[z + 1] - seq0;
     q.row0 = (static_cast<long long>(seq0) * g.H + h) * D;
     q.rs = static_cast<long long>(g.H) * D;
-    q.si = static_cast<long long>(h) * g.nb + g.cu_blocks[z] + blk;
   } else {
     q.L = g.N;
     q.row0 = (static_cast<long long>(z) * g.H + h) * g.N * D;
     q.rs = D;
-    q.si = (static_cast<long long>(z) * g.H + h) * gridDim.x + blk;
   }
+  q.si = (static_cast<long long>(z) * g.H + h) * gridDim.x + blk;
   return q;
 }
 
@@ -311,27 +308,38 @@ __global__ void __launch_bounds__(quant_threads<D, kRope>()) quant_kernel(const 
 // elements per row part (one 16-byte load), 256 threads per 128-row block.
 // The codes and factors equal those of the float layout: the same amax (of
 // the same values), the same power-of-two factor, each element scaled once.
-template <typename T, int D>
-__global__ void __launch_bounds__(256) quant_plain_kernel(const T* __restrict__ x, uint8_t* __restrict__ x8,
+// CTAs per SM the plain instance is built for (its whole block's loads in
+// flight per CTA; more CTAs per SM keep more bytes in flight)
+template <int D>
+__host__ __device__ constexpr int quant_plain_ctas() { return D == 64 ? 5 : (D == 128 ? 3 : 1); }
+
+template <typename T, int D, bool kPacked>
+__global__ void __launch_bounds__(256, quant_plain_ctas<D>()) quant_plain_kernel(const T* __restrict__ x, uint8_t* __restrict__ x8,
                                                           float* __restrict__ scales, const QuantGeom geo) {
   constexpr int VPR = D / 8;                 // 16-byte vectors per row
   constexpr int NV = 128 * VPR / 256;        // vectors per thread
   __shared__ float red[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int blk = blockIdx.x;
-  const QuantBlock qb = quant_block<D>(geo, blk, blockIdx.y, blockIdx.z);
+  const QuantBlock qb = quant_block<D, kPacked ? 1 : 0>(geo, blk, blockIdx.y, blockIdx.z);
   if (blk * 128 >= qb.L) return;   // a packed sequence shorter than the longest
-  const long long base = qb.row0 + static_cast<long long>(blk) * 128 * qb.rs;
   const int rows = min(128, qb.L - blk * 128);
-  // element offset of vector vi: row vi / VPR of the block, 8 elements from
-  // column 8 * (vi % VPR); consecutive threads on consecutive vectors
-  auto voff = [&](int vi) { return base + (vi / VPR) * qb.rs + (vi % VPR) * 8; };
+  // vector i of this thread: row i * RSTEP + r0 of the block, 8 elements from
+  // column 8 * (threadIdx.x % VPR) (consecutive threads on consecutive
+  // vectors of a row). Dense rows are D elements apart, so the block is one
+  // contiguous run of vectors; packed rows are H * D apart.
+  constexpr int RSTEP = 256 / VPR;
+  const int r0 = static_cast<int>(threadIdx.x) / VPR;
+  auto voff = [&](int i) -> long long {
+    if constexpr (kPacked)
+      return qb.row0 + (static_cast<long long>(blk) * 128 + i * RSTEP + r0) * qb.rs + (threadIdx.x % VPR) * 8;
+    else
+      return qb.row0 + static_cast<long long>(blk) * 128 * D + (static_cast<long long>(i) * 256 + threadIdx.x) * 8;
+  };
   uint4 w[NV];
 #pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int vi = i * 256 + static_cast<int>(threadIdx.x);
-    w[i] = vi / VPR < rows ? *reinterpret_cast<const uint4*>(x + voff(vi)) : make_uint4(0, 0, 0, 0);
-  }
+  for (int i = 0; i < NV; ++i)
+    w[i] = i * RSTEP + r0 < rows ? *reinterpret_cast<const uint4*>(x + voff(i)) : make_uint4(0, 0, 0, 0);
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
@@ -356,8 +364,7 @@ __global__ void __launch_bounds__(256) quant_plain_kernel(const T* __restrict__ 
   const float f = one ? ldexpf(1.f, e) : ldexpf(1.f, e1), f2 = one ? 1.f : ldexpf(1.f, e2);
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
-    const int vi = i * 256 + static_cast<int>(threadIdx.x);
-    if (vi / VPR >= rows) continue;
+    if (i * RSTEP + r0 >= rows) continue;
     const uint32_t wv[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
     float y[8];
 #pragma unroll
@@ -369,7 +376,7 @@ __global__ void __launch_bounds__(256) quant_plain_kernel(const T* __restrict__ 
 #pragma unroll
       for (int u = 0; u < 8; ++u) y[u] *= f2;
     }
-    *reinterpret_cast<uint2*>(x8 + voff(vi)) =
+    *reinterpret_cast<uint2*>(x8 + voff(i)) =
         make_uint2(pack_e4m3x4(y[0], y[1], y[2], y[3]), pack_e4m3x4(y[4], y[5], y[6], y[7]));
   }
 }
@@ -379,10 +386,20 @@ cudaError_t launch_typed(const void* x, uint8_t* x8, float* scales, dim3 grid, c
                          const int8_t* signs, float inv_sqrt_d, const float* rc, const float* rs, cudaStream_t st) {
   const T* xt = static_cast<const T*>(x);
   if (!kRope && signs == nullptr) {
+    const bool pk = geo.cu_seqlens != nullptr;
     switch (d) {
-      case 64: quant_plain_kernel<T, 64><<<grid, 256, 0, st>>>(xt, x8, scales, geo); break;
-      case 128: quant_plain_kernel<T, 128><<<grid, 256, 0, st>>>(xt, x8, scales, geo); break;
-      case 256: quant_plain_kernel<T, 256><<<grid, 256, 0, st>>>(xt, x8, scales, geo); break;
+      case 64:
+        if (pk) quant_plain_kernel<T, 64, true><<<grid, 256, 0, st>>>(xt, x8, scales, geo);
+        else quant_plain_kernel<T, 64, false><<<grid, 256, 0, st>>>(xt, x8, scales, geo);
+        break;
+      case 128:
+        if (pk) quant_plain_kernel<T, 128, true><<<grid, 256, 0, st>>>(xt, x8, scales, geo);
+        else quant_plain_kernel<T, 128, false><<<grid, 256, 0, st>>>(xt, x8, scales, geo);
+        break;
+      case 256:
+        if (pk) quant_plain_kernel<T, 256, true><<<grid, 256, 0, st>>>(xt, x8, scales, geo);
+        else quant_plain_kernel<T, 256, false><<<grid, 256, 0, st>>>(xt, x8, scales, geo);
+        break;
       default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
@@ -412,15 +429,15 @@ cudaError_t launch_geo(const void* x, int in_dt, uint8_t* x8, float* scales, dim
 cudaError_t launch_quant_fp8(const void* x, int in_dt, uint8_t* x8, float* scales, int B, int H, int N, int d,
                              const int8_t* signs, float inv_sqrt_d, const float* rope_cos, const float* rope_sin,
                              cudaStream_t st) {
-  const QuantGeom geo{H, N, nullptr, nullptr, 0};
+  const QuantGeom geo{H, N, nullptr};
   return launch_geo(x, in_dt, x8, scales, dim3((N + 127) / 128, H, B), geo, d, signs, inv_sqrt_d, rope_cos, rope_sin,
                     st);
 }
 
 cudaError_t launch_quant_fp8_varlen(const void* x, int in_dt, uint8_t* x8, float* scales, const int* cu_seqlens,
-                                    const int* cu_blocks, int nseq, int max_len, int num_blocks, int H, int d,
-                                    const int8_t* signs, float inv_sqrt_d, cudaStream_t st) {
-  const QuantGeom geo{H, 0, cu_seqlens, cu_blocks, num_blocks};
+                                    int nseq, int max_len, int H, int d, const int8_t* signs, float inv_sqrt_d,
+                                    cudaStream_t st) {
+  const QuantGeom geo{H, 0, cu_seqlens};
   return launch_geo(x, in_dt, x8, scales, dim3((max_len + 127) / 128, H, nseq), geo, d, signs, inv_sqrt_d, nullptr,
                     nullptr, st);
 }

@@ -159,32 +159,30 @@ ATTN_API attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8
 
 /*
  * Block quantisation of packed sequences: x [T,H,d] (THD, as attn_fwd_varlen)
- * -> x8 [T,H,d] E4M3 codes and scales [H][num_blocks] float32. Each sequence
- * is blocked from its own first row (its last block may be short), with the
- * rule of attn_quantize_fp8 per block; sequence z's blocks take the factor
- * slots cu_blocks[z] .. cu_blocks[z+1]-1 of each head. cu_seqlens and
- * cu_blocks: int32 [nseq+1] on the device, cu_blocks[0] = 0 and
- * cu_blocks[z+1] = cu_blocks[z] + ceil(len_z / 128); num_blocks =
- * cu_blocks[nseq] (host value); max_seqlen as attn_fwd_varlen. Optional
- * sign + Hadamard rotation as attn_quantize_fp8 (no RoPE variant).
+ * -> x8 [T,H,d] E4M3 codes and scales [nseq, H, ceil(max_seqlen/128)]
+ * float32. Each sequence is blocked from its own first row (its last block
+ * may be short), with the rule of attn_quantize_fp8 per block; block i of
+ * sequence z, head h takes slot [z, h, i]; slots past a sequence's last
+ * block are not written. cu_seqlens int32 [nseq+1] on the device and
+ * max_seqlen as attn_fwd_varlen. Optional sign + Hadamard rotation as
+ * attn_quantize_fp8 (no RoPE variant).
  */
 ATTN_API attn_status attn_quantize_fp8_varlen(const void* x, attn_dtype in_dtype, void* x8, float* scales,
-                                              const int* cu_seqlens, const int* cu_blocks, int nseq, int T,
-                                              int max_seqlen, int num_blocks, int H, int d,
-                                              const int8_t* hadamard_signs, void* stream);
+                                              const int* cu_seqlens, int nseq, int T, int max_seqlen, int H,
+                                              int d, const int8_t* hadamard_signs, void* stream);
 
 /*
  * FP8 forward over packed sequences: q8 [T,Hq,d], k8/v8 [T,Hkv,d] E4M3
- * codes and sq [Hq][num_blocks], sk/sv [Hkv][num_blocks] factors from
- * attn_quantize_fp8_varlen (same cu_seqlens, cu_blocks, num_blocks);
+ * codes and sq [nseq,Hq,ceil(max_seqlen/128)], sk/sv [nseq,Hkv,...]
+ * factors from attn_quantize_fp8_varlen (same cu_seqlens and max_seqlen);
  * o [T,Hq,d] BF16, lse [Hq,T] float32. Arithmetic as attn_fwd_fp8 within
  * each sequence (every KV tile is one block of its sequence).
  */
 ATTN_API attn_status attn_fwd_fp8_varlen(const void* q8, const void* k8, const void* v8,
                                          const float* sq, const float* sk, const float* sv,
-                                         void* o, float* lse, const int* cu_seqlens, const int* cu_blocks,
-                                         int nseq, int T, int max_seqlen, int num_blocks,
-                                         int Hq, int Hkv, int d, float scale, int causal, void* stream);
+                                         void* o, float* lse, const int* cu_seqlens, int nseq, int T,
+                                         int max_seqlen, int Hq, int Hkv, int d, float scale, int causal,
+                                         void* stream);
 
 /*
  * Keys per KV tile of attn_fwd_fp8 for head dimension d (128 for d = 64,

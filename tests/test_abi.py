@@ -79,20 +79,18 @@ def test_argument_checks_before_any_device_work(lib):
     assert lib.attn_fwd_fp8(*f8, P(16), P(16), P(16), P(16), P(16), 1, 2, 1, 0, 128, 0.1, 0, None) == 3
     assert lib.attn_fwd_fp8(*f8, P(16), P(16), P(16), P(16), P(16), 1, 2, 1, 8, 96, 0.1, 0, None) == 4
     assert lib.attn_fwd_fp8(*f8, P(16), P(16), P(16), P(16), P(16), 1, 3, 2, 8, 128, 0.1, 0, None) == 5
-    # packed FP8: cu_blocks required and aligned, num_blocks within [nseq, T], head dim
-    assert lib.attn_quantize_fp8_varlen(P(16), 0, P(16), P(16), P(16), None, 2, 10, 5, 2, 1, 64, None, None) == 1
-    assert lib.attn_quantize_fp8_varlen(P(16), 0, P(16), P(16), P(16), P(24), 2, 10, 5, 2, 1, 64, None, None) == 2
-    assert lib.attn_quantize_fp8_varlen(P(16), 0, P(16), P(16), P(16), P(16), 2, 10, 5, 1, 1, 64, None, None) == 3
-    assert lib.attn_quantize_fp8_varlen(P(16), 0, P(16), P(16), P(16), P(16), 2, 10, 5, 11, 1, 64, None, None) == 3
-    assert lib.attn_quantize_fp8_varlen(P(16), 0, P(16), P(16), P(16), P(16), 2, 10, 5, 2, 1, 32, None, None) == 4
-    assert lib.attn_quantize_fp8_varlen(P(16), 2, P(16), P(16), P(16), P(16), 2, 10, 5, 2, 1, 64, None, None) == 6
+    # packed FP8: cu_seqlens required and aligned, nseq / T / max_seqlen, head dim, dtype, GQA
+    assert lib.attn_quantize_fp8_varlen(P(16), 0, P(16), P(16), None, 2, 10, 5, 1, 64, None, None) == 1
+    assert lib.attn_quantize_fp8_varlen(P(16), 0, P(16), P(16), P(24), 2, 10, 5, 1, 64, None, None) == 2
+    assert lib.attn_quantize_fp8_varlen(P(16), 0, P(16), P(16), P(16), 2, 10, 11, 1, 64, None, None) == 3
+    assert lib.attn_quantize_fp8_varlen(P(16), 0, P(16), P(16), P(16), 0, 10, 5, 1, 64, None, None) == 3
+    assert lib.attn_quantize_fp8_varlen(P(16), 0, P(16), P(16), P(16), 2, 10, 5, 1, 32, None, None) == 4
+    assert lib.attn_quantize_fp8_varlen(P(16), 2, P(16), P(16), P(16), 2, 10, 5, 1, 64, None, None) == 6
     v8 = [P(16)] * 8
-    assert lib.attn_fwd_fp8_varlen(*v8, P(16), None, 2, 10, 5, 2, 2, 1, 128, 0.1, 0, None) == 1
-    assert lib.attn_fwd_fp8_varlen(*v8, P(16), P(16), 2, 10, 11, 2, 2, 1, 128, 0.1, 0, None) == 3
-    assert lib.attn_fwd_fp8_varlen(*v8, P(16), P(16), 2, 10, 5, 1, 2, 1, 128, 0.1, 0, None) == 3
-    assert lib.attn_fwd_fp8_varlen(*v8, P(16), P(16), 2, 10, 5, 2, 2, 1, 96, 0.1, 0, None) == 4
-    assert lib.attn_fwd_fp8_varlen(*v8, P(16), P(16), 2, 10, 5, 2, 3, 2, 128, 0.1, 0, None) == 5
-    assert [int(x) for x in binding.varlen_blocks([1, 128, 129, 300])] == [0, 1, 2, 4, 7]
+    assert lib.attn_fwd_fp8_varlen(*v8, None, 2, 10, 5, 2, 1, 128, 0.1, 0, None) == 1
+    assert lib.attn_fwd_fp8_varlen(*v8, P(16), 2, 10, 11, 2, 1, 128, 0.1, 0, None) == 3
+    assert lib.attn_fwd_fp8_varlen(*v8, P(16), 2, 10, 5, 2, 1, 96, 0.1, 0, None) == 4
+    assert lib.attn_fwd_fp8_varlen(*v8, P(16), 2, 10, 5, 3, 2, 128, 0.1, 0, None) == 5
     # varlen backward: cu_seqlens, sequence counts and the workspace are checked
     wv = binding.attn_bwd_varlen_workspace_size(10, 2, 1, 128)
     vargs = [P(16)] * 9

@@ -496,13 +496,12 @@ def test_persistent_walk_matches_one_head_launches(n, fp8):
 PACKED_LENS = [1, 127, 128, 300, 700, 5]
 
 
-def packed_quantize_gpu(x, cu, cb, lens, signs=None):
+def packed_quantize_gpu(x, cu, lens, signs=None):
     T, H, d = x.shape
-    nb = int(cb[-1])
+    nb = (max(lens) + 127) // 128
     x8 = torch.empty((T, H, d), dtype=torch.uint8, device="cuda")
-    sc = torch.full((H, nb), float("nan"), dtype=torch.float32, device="cuda")
-    L.attn_quantize_fp8_varlen(x.cuda(), x8, sc, cu.cuda(), cb.cuda(), max(lens), nb,
-                               None if signs is None else signs.cuda())
+    sc = torch.full((len(lens), H, nb), float("nan"), dtype=torch.float32, device="cuda")
+    L.attn_quantize_fp8_varlen(x.cuda(), x8, sc, cu.cuda(), max(lens), None if signs is None else signs.cuda())
     torch.cuda.synchronize()
     return x8, sc
 
@@ -512,19 +511,21 @@ def packed_quantize_gpu(x, cu, cb, lens, signs=None):
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 def test_packed_quantizer_bit_exact(rotate, d, dtype):
     """attn_quantize_fp8_varlen against the oracle's block quantisation of
-    each sequence on its own: codes and factors bit for bit."""
+    each sequence on its own: codes and factors bit for bit; slots past a
+    sequence's last block stay untouched."""
     cu = inputs.cu_seqlens(PACKED_LENS)
-    cb = L.varlen_blocks(PACKED_LENS)
     T = int(cu[-1])
     (x,) = inputs.normal(21 + d, [(T, 3, d)], dtype=dtype)
     signs = inputs.random_signs(4, d) if rotate else None
-    x8, sc = packed_quantize_gpu(x, cu, cb, PACKED_LENS, signs)
+    x8, sc = packed_quantize_gpu(x, cu, PACKED_LENS, signs)
     x8, sc = x8.cpu().numpy(), sc.cpu().numpy()
-    for s_ in range(len(PACKED_LENS)):
+    for s_, n in enumerate(PACKED_LENS):
         a, e = int(cu[s_]), int(cu[s_ + 1])
+        nb_s = (n + 127) // 128
         codes, fac = F.quantize_blocks(x[a:e].transpose(0, 1)[None], None if signs is None else signs.numpy())
         assert np.array_equal(x8[a:e].transpose(1, 0, 2), codes[0]), s_
-        assert np.array_equal(sc[:, int(cb[s_]):int(cb[s_ + 1])], fac[0]), s_
+        assert np.array_equal(sc[s_, :, :nb_s], fac[0]), s_
+        assert np.isnan(sc[s_, :, nb_s:]).all(), s_
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -536,24 +537,22 @@ def test_packed_fp8_forward(causal, d):
     FP8 emulation of the sequence (its own block quantisation) within the
     emulation tolerances."""
     cu = inputs.cu_seqlens(PACKED_LENS)
-    cb = L.varlen_blocks(PACKED_LENS)
     T = int(cu[-1])
-    nb = int(cb[-1])
     q, k, v = inputs.outliers(23 + d, [(T, 4, d), (T, 2, d), (T, 2, d)])
     signs = inputs.random_signs(4, d)
-    q8, sq = packed_quantize_gpu(q, cu, cb, PACKED_LENS, signs)
-    k8, sk = packed_quantize_gpu(k, cu, cb, PACKED_LENS, signs)
-    v8, sv = packed_quantize_gpu(v, cu, cb, PACKED_LENS)
+    q8, sq = packed_quantize_gpu(q, cu, PACKED_LENS, signs)
+    k8, sk = packed_quantize_gpu(k, cu, PACKED_LENS, signs)
+    v8, sv = packed_quantize_gpu(v, cu, PACKED_LENS)
     o = torch.full((T, 4, d), float("nan"), dtype=torch.bfloat16, device="cuda")
     lse = torch.full((4, T), float("nan"), device="cuda")
-    L.attn_fwd_fp8_varlen(q8, k8, v8, sq, sk, sv, o, lse, cu.cuda(), cb.cuda(), max(PACKED_LENS), nb, causal=causal)
+    L.attn_fwd_fp8_varlen(q8, k8, v8, sq, sk, sv, o, lse, cu.cuda(), max(PACKED_LENS), causal=causal)
     torch.cuda.synchronize()
     assert L.attn_get_device_status() == 0
     for s_, n in enumerate(PACKED_LENS):
         a, e = int(cu[s_]), int(cu[s_ + 1])
-        b0, b1 = int(cb[s_]), int(cb[s_ + 1])
+        nb_s = (n + 127) // 128
         dense = lambda x: x[a:e].transpose(0, 1).contiguous()[None]
-        fac = lambda f: f[:, b0:b1].contiguous()[None]
+        fac = lambda f: f[s_, :, :nb_s].contiguous()[None]
         o1 = torch.empty((1, 4, n, d), dtype=torch.bfloat16, device="cuda")
         lse1 = torch.empty((1, 4, n), device="cuda")
         L.attn_fwd_fp8(dense(q8), dense(k8), dense(v8), fac(sq), fac(sk), fac(sv), o1, lse1, causal=causal)
