@@ -5,7 +5,9 @@ KV heads (GQA groups 1..4), sequence length 1..700, head dim 64/128/256,
 dtype, causal, a random key window, and packed sequences; each case runs the
 forward and the backward through the public API (dense, window or varlen
 entry point) and compares O, LSE, dQ, dK and dV with the oracle at the
-tolerances of the dedicated tests.
+tolerances of the dedicated tests. A second sweep does the same for the
+FP8 quantiser and forward on dense shapes (codes bit-exact, O against the
+oracle's FP8 emulation).
 """
 import math
 
@@ -106,3 +108,50 @@ def test_random_case(seed):
         ref = A.backward(q, k, v, do, scale, *args)
     for name, g_, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
         assert rel_rms(g_, r) <= 1e-2, (name, rel_rms(g_, r), tag)
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_fp8_case(seed):
+    """FP8 forward (GPU quantiser, Q and K rotated half of the time) on
+    random dense shapes: codes and factors bit-exact against the oracle's
+    quantisation, O within the tolerances of the stale-max emulation, LSE
+    within 1e-3."""
+    from oracle import fp8 as F
+    rng = np.random.default_rng(2000 + seed)
+    hkv = int(rng.integers(1, 4))
+    hq = hkv * int(rng.choice([1, 2, 4]))
+    d = int(rng.choice([64, 128, 256]))
+    n = int(rng.integers(1, 600))
+    b = int(rng.integers(1, 3))
+    causal = bool(rng.integers(0, 2))
+    rotate = bool(rng.integers(0, 2))
+    tag = dict(hq=hq, hkv=hkv, d=d, n=n, b=b, causal=causal, rotate=rotate)
+    q, k, v = inputs.outliers(seed, [(b, hq, n, d), (b, hkv, n, d), (b, hkv, n, d)])
+    signs = inputs.random_signs(4, d) if rotate else None
+    nb = (n + 127) // 128
+
+    def quant(x, s):
+        x8 = torch.empty(x.shape, dtype=torch.uint8, device="cuda")
+        sc = torch.empty(x.shape[:2] + (nb,), dtype=torch.float32, device="cuda")
+        L.attn_quantize_fp8(x.cuda(), x8, sc, None if s is None else s.cuda())
+        return x8, sc
+
+    (q8, sq), (k8, sk), (v8, sv) = quant(q, signs), quant(k, signs), quant(v, None)
+    o = torch.full((b, hq, n, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((b, hq, n), float("nan"), device="cuda")
+    L.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, o, lse, causal=causal)
+    torch.cuda.synchronize()
+    assert L.attn_get_device_status() == 0
+    s_np = None if signs is None else signs.numpy()
+    ref = (F.quantize_blocks(q, s_np), F.quantize_blocks(k, s_np), F.quantize_blocks(v))
+    for (c_ref, f_ref), (c_gpu, f_gpu) in zip(ref, ((q8, sq), (k8, sk), (v8, sv))):
+        assert np.array_equal(c_gpu.cpu().numpy(), c_ref), tag
+        assert np.array_equal(f_gpu.cpu().numpy(), f_ref), tag
+    codes = (ref[0][0], ref[1][0], ref[2][0], ref[0][1], ref[1][1], ref[2][1])
+    o_ref, lse_ref = F.attention_fp8(*codes, d ** -0.5, causal, tau=F.STALE_MAX_TAU,
+                                     kv_tile=L.attn_fwd_fp8_kv_tile(d))
+    err = np.abs(o.cpu().double().numpy() - o_ref)
+    assert math.sqrt((err ** 2).mean()) <= 2e-3, tag
+    assert np.quantile(err, 0.999) <= 1e-2, tag
+    assert err.max() <= 1e-1, tag
+    assert np.abs(lse.cpu().double().numpy() - lse_ref).max() <= 1e-3, tag
