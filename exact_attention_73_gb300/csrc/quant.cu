@@ -311,7 +311,7 @@ __global__ void __launch_bounds__(quant_threads<D, kRope>()) quant_kernel(const 
 // CTAs per SM the plain instance is built for (its whole block's loads in
 // flight per CTA; more CTAs per SM keep more bytes in flight)
 template <int D>
-__host__ __device__ constexpr int quant_plain_ctas() { return D == 64 ? 5 : (D == 128 ? 3 : 1); }
+__host__ __device__ constexpr int quant_plain_ctas() { return D == 64 ? 4 : (D == 128 ? 3 : 1); }
 
 template <typename T, int D, bool kPacked>
 __global__ void __launch_bounds__(256, quant_plain_ctas<D>()) quant_plain_kernel(const T* __restrict__ x, uint8_t* __restrict__ x8,
