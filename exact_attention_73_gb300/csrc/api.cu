@@ -133,7 +133,7 @@ CUtensorMapDataType tma_type(int dt) {
 
 attn_status from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return ATTN_OK;
-  if (e == cudaErrorInvalidValue) return ATTN_ERR_LAUNCH;
+  if (e == cudaErrorInvalidValue || e == cudaErrorLaunchOutOfResources) return ATTN_ERR_LAUNCH;
   return ATTN_ERR_CUDA;
 }
 

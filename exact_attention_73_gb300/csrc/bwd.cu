@@ -108,6 +108,7 @@ cudaError_t launch_main(const CUtensorMap& k, const CUtensorMap& v, const CUtens
     } else {
       cudaError_t r = smem_attr_once<bwd_kernel<DT, D, kDQ, false>>(C::SMEM_BYTES);
       if (r != cudaSuccess) return r;
+      if ((r = reg_pool_once<bwd_kernel<DT, D, kDQ, false>>(C::NTHREADS, C::kRegsSplit)) != cudaSuccess) return r;
       bwd_kernel<DT, D, kDQ, false><<<grid, C::NTHREADS, C::SMEM_BYTES, st>>>(k, v, q, d, dq, g);
       return cudaGetLastError();
     }

@@ -29,7 +29,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 attn_status from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return ATTN_OK;
-  if (e == cudaErrorInvalidValue) return ATTN_ERR_LAUNCH;
+  if (e == cudaErrorInvalidValue || e == cudaErrorLaunchOutOfResources) return ATTN_ERR_LAUNCH;
   return ATTN_ERR_CUDA;
 }
 

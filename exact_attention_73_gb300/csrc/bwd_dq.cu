@@ -13,6 +13,7 @@ cudaError_t launch(const CUtensorMap& q, const CUtensorMap& dout, const CUtensor
   auto kern = bwd_dq_kernel<DT, D>;
   cudaError_t e = smem_attr_once<bwd_dq_kernel<DT, D>>(C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  if ((e = reg_pool_once<bwd_dq_kernel<DT, D>>(C::NTHREADS, C::kRegsSplit)) != cudaSuccess) return e;
   const dim3 grid((max_len + 127) / 128, a.Hq, nz);
   kern<<<grid, C::NTHREADS, C::SMEM_BYTES, st>>>(q, dout, k, v, a);
   return cudaGetLastError();

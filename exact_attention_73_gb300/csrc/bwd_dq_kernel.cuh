@@ -50,6 +50,7 @@ struct DqCfg {
   // rest to the two compute warpgroups (each thread holds 64 S and 64 dP)
   static constexpr uint32_t kRegsCtl = 88, kRegsMath = 208;
   static_assert(128 * kRegsCtl + 256 * kRegsMath <= NTHREADS * 168, "register split");
+  static constexpr int kRegsSplit = (128 * kRegsCtl + 256 * kRegsMath + NTHREADS - 1) / NTHREADS;   // per thread
   static constexpr uint32_t FMT = DT == kBF16 ? 1u : 0u;
   static constexpr uint32_t IDESC_SP = instr_desc(128, 128, FMT, FMT, 0, 0);   // A, B K-major
   static constexpr uint32_t IDESC_DQ = instr_desc(128, D, FMT, FMT, 0, 1);     // B (K) MN-major

@@ -119,6 +119,7 @@ struct BwdCfg {
   // independent exp2 chains, can keep all of them in flight.
   static constexpr uint32_t kRegsCtl = 88, kRegsDrain = 88, kRegsMath = 168;
   static_assert(128 * (kRegsCtl + kRegsDrain + 2 * kRegsMath) <= NTHREADS * 128, "register split");
+  static constexpr int kRegsSplit = 128 * (kRegsCtl + kRegsDrain + 2 * kRegsMath) / NTHREADS;   // per thread
   static constexpr uint32_t FMT = DT == kBF16 ? 1u : 0u;
   static constexpr uint32_t IDESC_SP = instr_desc(128, BR, FMT, FMT, 0, 0);
   static constexpr uint32_t IDESC_KV = instr_desc(128, DH, FMT, FMT, 0, 1);

@@ -12,6 +12,7 @@ cudaError_t launch_bwd_split(const CUtensorMap& k, const CUtensorMap& v, const C
   using C = BwdCfg<DT, D>;
   cudaError_t e = smem_attr_once<bwd_kernel<DT, D, kDQ, true>>(C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  if ((e = reg_pool_once<bwd_kernel<DT, D, kDQ, true>>(C::NTHREADS, C::kRegsSplit)) != cudaSuccess) return e;
   if (a.nsplit == 1) {
     bwd_kernel<DT, D, kDQ, true><<<grid, C::NTHREADS, C::SMEM_BYTES, st>>>(k, v, q, d, dq, a);
     return cudaGetLastError();

@@ -137,5 +137,5 @@ extern "C" attn_status attn_decode_fp8(const void* q8, const float* sq, const vo
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) return ATTN_OK;
-  return e == cudaErrorInvalidValue ? ATTN_ERR_LAUNCH : ATTN_ERR_CUDA;
+  return e == cudaErrorInvalidValue || e == cudaErrorLaunchOutOfResources ? ATTN_ERR_LAUNCH : ATTN_ERR_CUDA;
 }

@@ -24,6 +24,10 @@ cudaError_t launch_fwd_grid(const CUtensorMap& q, const CUtensorMap& k, const CU
   auto kern = fwd_kernel<DT, D, QT, kPersist>;
   cudaError_t e = smem_attr_once<fwd_kernel<DT, D, QT, kPersist>>(C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  if constexpr (QT >= 2) {   // the role split must fit the registers of the launch
+    constexpr int kSplit = (128 * C::kRegsCtl + 128 * QT * C::kRegsSoft + C::NTHREADS - 1) / C::NTHREADS;
+    if ((e = reg_pool_once<fwd_kernel<DT, D, QT, kPersist>>(C::NTHREADS, kSplit)) != cudaSuccess) return e;
+  }
   long long grid = units;
   if (kPersist) {
     int dev = 0, sms = 0;

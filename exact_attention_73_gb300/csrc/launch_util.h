@@ -21,4 +21,22 @@ cudaError_t smem_attr_once(int bytes) {
   return e;
 }
 
+// Checks once that kernel Kern is built with at least `regs` registers per
+// thread for blocks of `threads`: a register split by role (setmaxnreg)
+// hands out the registers the block was launched with, and a split larger
+// than that would never be granted.
+template <auto Kern>
+cudaError_t reg_pool_once(int threads, int regs) {
+  static std::atomic<int> state{0};   // 0 unknown, 1 enough, 2 too few
+  int s = state.load(std::memory_order_acquire);
+  if (s == 0) {
+    cudaFuncAttributes fa{};
+    const cudaError_t e = cudaFuncGetAttributes(&fa, Kern);
+    if (e != cudaSuccess) return e;
+    s = fa.numRegs >= regs && fa.maxThreadsPerBlock >= threads ? 1 : 2;
+    state.store(s, std::memory_order_release);
+  }
+  return s == 1 ? cudaSuccess : cudaErrorLaunchOutOfResources;
+}
+
 }  // namespace attn

@@ -67,7 +67,7 @@ typedef enum {
   ATTN_ERR_GQA = 5,        /* Hq is not a positive multiple of Hkv */
   ATTN_ERR_DTYPE = 6,      /* dtype not accepted by this entry point */
   ATTN_ERR_WORKSPACE = 7,  /* workspace NULL or smaller than the size query */
-  ATTN_ERR_LAUNCH = 8,     /* kernel resources (shared memory) not granted */
+  ATTN_ERR_LAUNCH = 8,     /* kernel resources (shared memory, registers) not granted */
   ATTN_ERR_TIMEOUT = 9,    /* a device-side wait ran out (see status query) */
   ATTN_ERR_CUDA = 10,      /* CUDA runtime/driver error */
   ATTN_ERR_NODEVICE = 11   /* no sm_103 device is current */
