@@ -657,15 +657,21 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       for (int part = 0; part < C::DQ_PARTS; ++part) {
         if (threadIdx.x == 256) bulk_wait_read_all();   // previous reduce-add has read the buffer
         named_bar_sync(1, 128);
-        if (dim < C::DH) {                              // D = 64: lanes 64..127 are not dQ
+        if (quarter * 32 < C::DH) {                     // D = 64: lanes 64..127 are not dQ
+          // row q of the staging tile holds dQ of query q; lane l's value of
+          // query q goes to word 32 * quarter + l of that row: four queries
+          // per stmatrix, lane l addressing query +l/8, words +4(l%8) .. +3
+          const uint32_t row = smem_u32(sDQ) + ((lane >> 3) * C::DH + quarter * 32 + 4 * (lane & 7)) * 4;
           if constexpr (C::DQ_PARTS == 2) {
+            const uint32_t(&x)[32] = part == 0 ? x0 : x1;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) sDQ[e * C::DH + dim] = __uint_as_float(part == 0 ? x0[e] : x1[e]);
+            for (int g = 0; g < 8; ++g)
+              stmatrix_x4(row + 16 * g * C::DH, x[4 * g], x[4 * g + 1], x[4 * g + 2], x[4 * g + 3]);
           } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              sDQ[e * C::DH + dim] = __uint_as_float(x0[e]);
-              sDQ[(e + 32) * C::DH + dim] = __uint_as_float(x1[e]);
+            for (int g = 0; g < 8; ++g) {
+              stmatrix_x4(row + 16 * g * C::DH, x0[4 * g], x0[4 * g + 1], x0[4 * g + 2], x0[4 * g + 3]);
+              stmatrix_x4(row + 16 * (g + 8) * C::DH, x1[4 * g], x1[4 * g + 1], x1[4 * g + 2], x1[4 * g + 3]);
             }
           }
         }

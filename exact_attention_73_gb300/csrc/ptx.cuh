@@ -251,6 +251,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
+// Four 8 x 8 matrices of 16-bit pairs from the warp's registers to shared
+// memory (stmatrix .x4, not transposed): register m of lane l lands in
+// matrix m, row l / 4, 32-bit word l % 4 of the row; lane l gives the
+// address of row l % 8 of matrix l / 8 (16-byte aligned). With 32-bit data
+// this writes, per matrix, one row of 32 words whose word w comes from lane w.
+__device__ __forceinline__ void stmatrix_x4(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};"
+               ::"r"(addr), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
