@@ -412,19 +412,25 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         }
         mma_commit(&sp_full[it & 1]);
       };
-      // dQ^T first, so the drain warps can read it while dV and dK run and
-      // the next S^T/dP^T never waits for an empty tensor pipe
+      // With several Q/dO stages dQ^T goes first, so the drain warps can read
+      // it while dV and dK run and the next S^T/dP^T never waits for an empty
+      // tensor pipe. With one stage the next tile's loads wait for the stage:
+      // dV and dK (its last readers) go first and release it, and dQ^T runs
+      // while the loads are in flight.
       auto issue_grads = [&](int it) {
         const uint32_t xb = tbase + 128u * (it & 1);
         const uint32_t so = (it % C::NQ) * C::Q_B;
-        if constexpr (kDQ) {
+        auto issue_dq = [&]() {
+          if constexpr (kDQ) {
 #pragma unroll
-          for (int kk = 0; kk < C::BC / 16; ++kk) {   // dQ^T = K^T dS^T, both MN-major
-            mma_ss<false>(xb + C::COL_DQ, dadd(dK_mn, kk * 2048), dadd(dDS0_mn, kk * 2048),
-                          C::IDESC_DQ, kk > 0);
+            for (int kk = 0; kk < C::BC / 16; ++kk) {   // dQ^T = K^T dS^T, both MN-major
+              mma_ss<false>(xb + C::COL_DQ, dadd(dK_mn, kk * 2048), dadd(dDS0_mn, kk * 2048),
+                            C::IDESC_DQ, kk > 0);
+            }
+            mma_commit(dq_full);
           }
-          mma_commit(dq_full);
-        }
+        };
+        if constexpr (C::NQ > 1) issue_dq();
 #pragma unroll
         for (int kk = 0; kk < C::BR / 16; ++kk) {   // dV += P^T dO_i
           mma_ts<false>(tbase + C::COL_DV, xb + C::col_p(kk), dadd(ddO0_mn, so + kk * 2048), C::IDESC_KV,
@@ -436,6 +442,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
                         (it > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&q_empty[it % C::NQ]);
+        if constexpr (C::NQ == 1) issue_dq();
       };
       bool ok = mbar_wait(kv_full, 0, a.status);
       if constexpr (C::NQ == 1) {
