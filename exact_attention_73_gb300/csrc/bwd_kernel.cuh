@@ -502,6 +502,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float2 sl2v = make_float2(a.scale_log2, a.scale_log2);
     bool ok = true;
+    bool dq_ok = true;   // the wait for the previous tile's dQ^T ended in time
     for (int it = 0; it < niter; ++it) {
       const uint32_t xb = tbase + lane_off + 128u * (it & 1);
       uint8_t* ds_row = sDS + r * 128;
@@ -521,9 +522,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         }
       }
       if (got) got = __all_sync(0xffffffffu, mbar_wait(&sp_full[it & 1], (it >> 1) & 1, a.status));
-      // the single dS^T tile in shared memory is read by dQ^T of the previous
-      // tile; it must be complete before this tile's dS^T is stored
-      if (kDQ && got && it > 0) got = __all_sync(0xffffffffu, mbar_wait(dq_full, (it - 1) & 1, a.status));
+      got = got && dq_ok;   // a wait that ran out in the previous tile ends both groups here
       uint32_t sv[32], dp[32];
       if (got) {
         tc_fence_after();
@@ -581,10 +580,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       tmem_st16(xb + C::col_p(2 * half), pp);
       tmem_st16(xb + C::col_ds(2 * half), dd);
       // dS^T row r, queries 32*half .. +31: 16-byte chunks 4*half .. +3 of a
-      // 128-byte row, 128-byte swizzle (chunk ^= row % 8). The tile is free:
-      // dQ^T of the previous tile (its only reader) completed before the
-      // barrier above.
+      // 128-byte row, 128-byte swizzle (chunk ^= row % 8). The single dS^T
+      // tile is read by dQ^T of the previous tile, which must be complete
+      // first; waiting only here lets this tile's exponentials overlap it.
       if constexpr (kDQ) {
+        if (it > 0) dq_ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (it - 1) & 1, a.status));
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           const int chunk = (4 * half + c4) ^ (r & 7);
