@@ -87,6 +87,13 @@ int tail_split_units(const BwdArgs& a, long long units, int per_head, int sms) {
   return 2 * r <= sms ? static_cast<int>(r) : 0;
 }
 
+// Short unmasked rows run persistent: one CTA per SM walks the units, so a
+// unit's dV/dK write-out overlaps the next unit's first products and the
+// CTA set-up is paid once. That pays while a unit holds few query tiles
+// (5-6 % at N = 512); from about N = 1024 on the unit's own walk hides it
+// and the walk's extra state costs as much as it saves.
+constexpr int kBwdPersistMaxRows = 768;
+
 template <int DT, int D, bool kDQ>
 cudaError_t launch_main(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q, const CUtensorMap& d,
                         const CUtensorMap& dq, const BwdArgs& a, int max_len, int nz, cudaStream_t st) {
@@ -101,6 +108,17 @@ cudaError_t launch_main(const CUtensorMap& k, const CUtensorMap& v, const CUtens
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if constexpr (kDQ && D <= 128) {
+    if (a.cu_seqlens == nullptr && a.win_left < 0 && a.win_right < 0 && max_len <= kBwdPersistMaxRows &&
+        units > sms && units <= INT32_MAX) {
+      BwdArgs g = a;
+      g.tiles_x = tiles_x;
+      g.unit0 = 0;
+      g.nsplit = 1;
+      g.units = static_cast<int>(units);
+      return launch_bwd_persist<DT, D>(k, v, q, d, dq, g, sms, st);
+    }
+  }
   const int tail = units <= INT32_MAX ? tail_split_units(a, units, (a.N + C::BR - 1) / C::BR, sms) : 0;
   auto whole = [&](dim3 grid, const BwdArgs& g) -> cudaError_t {
     if constexpr (kSplitAll) {

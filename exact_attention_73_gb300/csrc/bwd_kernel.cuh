@@ -84,6 +84,9 @@ struct BwdArgs {
   // nsplit (nsplit = 2 only in the kSplit instance, launched in clusters of
   // two).
   int tiles_x, unit0, nsplit;
+  // persistent instance: the grid walks units blockIdx.x, + gridDim.x, ...
+  // below `units` (tiles_x * Hkv * batch), in the linear order above
+  int units;
 };
 
 template <int DT, int D>
@@ -104,8 +107,9 @@ struct BwdCfg {
   static constexpr int DQ_ROWS = D == 64 ? BR : BR / 2;   // rows of dQ per reduce-add
   static constexpr int DQ_PARTS = BR / DQ_ROWS;            // reduce-adds per tile
   static constexpr int DQ_STAGE_B = DQ_ROWS * DH * 4;      // FP32 staging for one reduce-add
-  // kv_full, q_full[NQ], q_empty[NQ], sp_full[2], ds_ready[2][2], dq_full, dq_empty, done
-  static constexpr int NBARS = 1 + 2 * NQ + 2 + 4 + 3;
+  // kv_full, q_full[NQ], q_empty[NQ], sp_full[2], ds_ready[2][2], dq_full, dq_empty, done,
+  // kv_empty, acc_empty
+  static constexpr int NBARS = 1 + 2 * NQ + 2 + 4 + 5;
   static constexpr int SMEM_BYTES =
       2 * KV_B + DS_B + NQ * (2 * Q_B) + DQ_STAGE_B + NQ * LD_B + NBARS * 8 + 16;   // base is 1024-aligned
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeded");
@@ -176,12 +180,13 @@ __device__ __forceinline__ void split_add(uint32_t (&v)[32], const float* part1,
 // kDQ = false: dK and dV only (the deterministic backward computes dQ in a
 // separate query-stationary kernel); the dQ^T product, its drain and the
 // reduce-adds are left out.
-template <int DT, int D, bool kDQ = true, bool kSplit = false>
+template <int DT, int D, bool kDQ = true, bool kSplit = false, bool kPersist = false>
 __global__ void __launch_bounds__(512, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
            const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
            const __grid_constant__ CUtensorMap tmdQ, const BwdArgs a) {
   using C = BwdCfg<DT, D>;
+  static_assert(!kPersist || (!kSplit && C::DSPLIT == 1), "persistent walk: whole units, one CTA per key tile");
   // The layout uses all the shared memory it asks for, with no room to align
   // the base by hand: a base that is not 1024-byte aligned (needed by the
   // swizzled tiles) is reported and the CTA leaves before touching it.
@@ -217,8 +222,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
   uint64_t* ds_ready = sp_full + 2;
   uint64_t* dq_full = ds_ready + 4;
   uint64_t* dq_empty = dq_full + 1;
-  uint64_t* done = dq_empty + 1;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* done = dq_empty + 1;                    // one phase per unit
+  uint64_t* kv_empty = done + 1;                    // persistent: the unit's products have read K, V
+  uint64_t* acc_empty = kv_empty + 1;               // persistent: dV, dK read out of tensor memory
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -238,35 +245,75 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     // with causal masking key tile 0 has the most work: heavy tiles start first
     heavy_first_order<16>(bx, by, bz);
   }
-  const int hkv = by;
   const bool packed = a.cu_seqlens != nullptr;
-  int b, seq0, L;
-  if (packed) {
-    b = 0;
-    seq0 = a.cu_seqlens[bz];
-    L = a.cu_seqlens[bz + 1] - seq0;
-  } else {
-    b = bz;
-    seq0 = 0;
-    L = a.N;
-  }
-  const int j = bx / C::DSPLIT;             // key tile
-  const int dh = bx % C::DSPLIT;            // which DH head dims of dK, dV, dQ this CTA owns
+  // The unit: KV head, batch (or packed sequence), key tile j, head-dim part
+  // dh; query tiles i0 .. i0 + per_head - 1 of each query head of the group
+  int hkv, b, seq0, L, j, dh, i0, per_head, it_base, niter, rot;
+  auto set_unit = [&](int ux, int uy, int uz) {
+    hkv = uy;
+    if (packed) {
+      b = 0;
+      seq0 = a.cu_seqlens[uz];
+      L = a.cu_seqlens[uz + 1] - seq0;
+    } else {
+      b = uz;
+      seq0 = 0;
+      L = a.N;
+    }
+    j = ux / C::DSPLIT;             // key tile
+    dh = ux % C::DSPLIT;            // which DH head dims of dK, dV, dQ this CTA owns
+    // query tiles holding a query that sees a key of this tile
+    const int klast = min(j * C::BC + C::BC, L) - 1;
+    const int qlo = a.win_right < 0 ? 0 : max(0, j * C::BC - a.win_right);
+    const int qhi = a.win_left < 0 ? L - 1 : min(L - 1, klast + a.win_left);
+    i0 = qlo / C::BR;
+    per_head = qhi / C::BR + 1 - i0;
+    // this CTA's part of the walk over (query head, query tile): iterations
+    // it_base .. it_base + niter - 1 of the group * per_head
+    it_base = wp * (a.group * per_head) / nsplit;
+    niter = (wp + 1) * (a.group * per_head) / nsplit - it_base;
+    // Each key tile starts its walk at a different query tile, so the CTAs
+    // of one head neither load the same Q/dO tile nor add into the same dQ
+    // rows at the same moment.
+    rot = j % per_head;
+  };
+  set_unit(bx, by, bz);
   if (j * C::BC >= L) return;
-  // query tiles holding a query that sees a key of this tile
-  const int klast = min(j * C::BC + C::BC, L) - 1;
-  const int qlo = a.win_right < 0 ? 0 : max(0, j * C::BC - a.win_right);
-  const int qhi = a.win_left < 0 ? L - 1 : min(L - 1, klast + a.win_left);
-  const int i0 = qlo / C::BR;
-  const int per_head = qhi / C::BR + 1 - i0;
-  // this CTA's part of the walk over (query head, query tile): iterations
-  // it_base .. it_base + niter - 1 of the group * per_head
-  const int it_base = wp * (a.group * per_head) / nsplit;
-  const int niter = (wp + 1) * (a.group * per_head) / nsplit - it_base;
-  // Query tile and head of local iteration it. Each key tile starts its walk
-  // at a different query tile, so the CTAs of one head neither load the same
-  // Q/dO tile nor add into the same dQ rows at the same moment.
-  const int rot = j % per_head;
+  // Persistent walk: unit k >= 1 of this CTA; false past the last unit. Every
+  // role walks the same units, and the barrier phases run on across them
+  // (counted in tiles g of the whole walk, or in units k).
+  // The walk runs over dense rows without masks, so every unit has the same
+  // query tiles (i0 = 0, per_head, niter) and only the key tile, KV head and
+  // batch change.
+  auto more_units = [&](int k) -> bool {
+    return kPersist && static_cast<long long>(blockIdx.x) + static_cast<long long>(k) * gridDim.x < a.units;
+  };
+  // offset of key row `row` of unit k in dK and dV (dense layout), from the
+  // unit index alone, so that the unit's coordinates need not stay live
+  // through its tiles
+  auto persist_key_off = [&](int k, int row) -> long long {
+    const int ui = static_cast<int>(blockIdx.x + static_cast<unsigned>(k) * gridDim.x);
+    const int uj = ui % a.tiles_x, uh = ui / a.tiles_x % a.Hkv, ub = ui / a.tiles_x / a.Hkv;
+    return static_cast<long long>(ub) * a.k_sb + static_cast<long long>(uh) * a.k_sh +
+           static_cast<long long>(uj * C::BC + row) * a.k_sn;
+  };
+  auto persist_key_row = [&](int k, int row) {
+    return static_cast<int>(blockIdx.x + static_cast<unsigned>(k) * gridDim.x) % a.tiles_x * C::BC + row;
+  };
+  auto next_unit = [&](int k) -> bool {
+    if constexpr (!kPersist) {
+      return false;
+    } else {
+      if (!more_units(k)) return false;
+      const int ui = static_cast<int>(blockIdx.x + static_cast<unsigned>(k) * gridDim.x);
+      j = ui % a.tiles_x;
+      hkv = ui / a.tiles_x % a.Hkv;
+      b = ui / a.tiles_x / a.Hkv;
+      rot = j % per_head;
+      return true;
+    }
+  };
+  // Query tile and head of local iteration it
   auto q_tile = [&](int it) {
     const int r = (it_base + it) % per_head + rot;
     return i0 + (r >= per_head ? r - per_head : r);
@@ -294,6 +341,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 128);
     mbar_init(done, 1);
+    mbar_init(kv_empty, 1);
+    mbar_init(acc_empty, 384);   // the two P^T/dS^T groups (dV) and the drain warps (dK)
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -315,6 +364,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
   regs_dec<C::kRegsCtl>();
   if (warp == 0) {
     // ------------------------------------------------------------ loads
+    int gt = 0;   // tiles of the earlier units
+    for (int k = 0;; ++k) {
+    if (k > 0) {
+      if (!next_unit(k)) break;
+      // the previous unit's K and V are read until its last products complete
+      if (!__all_sync(0xffffffffu, mbar_wait(kv_empty, (k - 1) & 1, a.status))) break;
+    }
     const int krow = seq0 + j * C::BC;
     if (lane == 0) {
       mbar_arrive_expect_tx(kv_full, 2 * C::KV_B);
@@ -328,8 +384,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         }
       }
     }
+    bool ok = true;
     for (int it = 0; it < niter; ++it) {
-      const int st = it % C::NQ;
+      const int g = gt + it;
+      const int st = g % C::NQ;
       const int h = q_head(it);
       const int q0 = q_tile(it) * C::BR;
       // LSE and D of this tile are fetched before waiting for the stage (they
@@ -343,7 +401,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         nl[u] = in ? -a.lse[lrow + q] * kLog2e : -INFINITY;    // -LSE in log2 units
         nd[u] = in ? -a.dvec[lrow + q] : 0.f;                  // -D
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(&q_empty[st], ((it / C::NQ) & 1) ^ 1, a.status))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&q_empty[st], ((g / C::NQ) & 1) ^ 1, a.status))) {
+        ok = false;
+        break;
+      }
       if (lane == 0) {
         mbar_arrive_expect_tx(&q_full[st], 2 * C::Q_B);
         for (int c = 0; c < C::NBOX; ++c) {
@@ -368,6 +429,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       if (lane == 0) mbar_arrive(&q_full[st]);
       __syncwarp();
     }
+    if (!ok || !kPersist) break;
+    gt += niter;
+    }
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA
     // Order: SdP(0); per iteration it: SdP(it+1) into the other buffer, then
@@ -388,16 +452,16 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       const uint64_t ddO0_mn = smem_desc(smem_u32(sdO) + dh_off, C::Q_BOX_B, 1024, kSwizzle128);
       const uint64_t dDS0_mn = smem_desc(smem_u32(sDS), C::DS_B, 1024, kSwizzle128);
       auto dadd = [](uint64_t d, uint32_t bytes) { return d + (bytes >> 4); };
-      auto ds_wait = [&](int it) {   // P^T and dS^T of tile it are in tensor memory
+      auto ds_wait = [&](int g) {   // P^T and dS^T of tile g are in tensor memory
         if constexpr (C::kOwnCols)
-          return mbar_wait(&ds_ready[(it & 1) * 2], (it >> 1) & 1, a.status) &&
-                 mbar_wait(&ds_ready[(it & 1) * 2 + 1], (it >> 1) & 1, a.status);
+          return mbar_wait(&ds_ready[(g & 1) * 2], (g >> 1) & 1, a.status) &&
+                 mbar_wait(&ds_ready[(g & 1) * 2 + 1], (g >> 1) & 1, a.status);
         else
-          return mbar_wait(&ds_ready[0], it & 1, a.status);
+          return mbar_wait(&ds_ready[0], g & 1, a.status);
       };
-      auto issue_sdp = [&](int it) {   // S^T = K Q^T and dP^T = V dO^T into buffer it % 2
-        const uint32_t so = (it % C::NQ) * C::Q_B;
-        const uint32_t xb = tbase + 128u * (it & 1);
+      auto issue_sdp = [&](int g) {   // S^T = K Q^T and dP^T = V dO^T into buffer g % 2
+        const uint32_t so = (g % C::NQ) * C::Q_B;
+        const uint32_t xb = tbase + 128u * (g & 1);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t offk = (kk / 4) * C::KV_BOX_B + (kk % 4) * 32;
@@ -410,16 +474,17 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
           const uint32_t offq = so + (kk / 4) * C::Q_BOX_B + (kk % 4) * 32;
           mma_ss<false>(xb + C::COL_DP, dadd(dV_kmaj, offk), dadd(ddO0_kmaj, offq), C::IDESC_SP, kk > 0);
         }
-        mma_commit(&sp_full[it & 1]);
+        mma_commit(&sp_full[g & 1]);
       };
       // With several Q/dO stages dQ^T goes first, so the drain warps can read
       // it while dV and dK run and the next S^T/dP^T never waits for an empty
       // tensor pipe. With one stage the next tile's loads wait for the stage:
       // dV and dK (its last readers) go first and release it, and dQ^T runs
       // while the loads are in flight.
-      auto issue_grads = [&](int it) {
-        const uint32_t xb = tbase + 128u * (it & 1);
-        const uint32_t so = (it % C::NQ) * C::Q_B;
+      // g: tile of the walk, it: tile of unit k (it = 0 starts dV and dK)
+      auto issue_grads = [&](int g, int it, int k) {
+        const uint32_t xb = tbase + 128u * (g & 1);
+        const uint32_t so = (g % C::NQ) * C::Q_B;
         auto issue_dq = [&]() {
           if constexpr (kDQ) {
 #pragma unroll
@@ -431,6 +496,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
           }
         };
         if constexpr (C::NQ > 1) issue_dq();
+        // a persistent walk's next unit starts dV and dK once the previous
+        // unit's have been read out of tensor memory
+        if (kPersist && it == 0 && k > 0 && !mbar_wait(acc_empty, (k - 1) & 1, a.status)) return false;
 #pragma unroll
         for (int kk = 0; kk < C::BR / 16; ++kk) {   // dV += P^T dO_i
           mma_ts<false>(tbase + C::COL_DV, xb + C::col_p(kk), dadd(ddO0_mn, so + kk * 2048), C::IDESC_KV,
@@ -441,47 +509,59 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
           mma_ts<false>(tbase + C::COL_DK, xb + C::col_ds(kk), dadd(dQ0_mn, so + kk * 2048), C::IDESC_KV,
                         (it > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&q_empty[it % C::NQ]);
+        mma_commit(&q_empty[g % C::NQ]);
         if constexpr (C::NQ == 1) issue_dq();
+        return true;
       };
-      bool ok = mbar_wait(kv_full, 0, a.status);
+      int gt = 0;   // tiles of the earlier units
+      for (int k = 0;; ++k) {
+      if (k > 0 && !more_units(k)) break;
+      bool ok = mbar_wait(kv_full, k & 1, a.status);
       if constexpr (C::NQ == 1) {
-        // one Q/dO stage: tile it's products, then tile it+1's
+        // one Q/dO stage: tile g's products, then tile g+1's
         for (int it = 0; it < niter && ok; ++it) {
-          if (!(ok = mbar_wait(&q_full[0], it & 1, a.status))) break;
-          // buffer it%2 was last used by it-2, whose dQ^T was drained before it-1's
-          if (kDQ && it > 0 && !(ok = mbar_wait(dq_empty, (it - 1) & 1, a.status))) break;
+          const int g = gt + it;
+          if (!(ok = mbar_wait(&q_full[0], g & 1, a.status))) break;
+          // buffer g%2 was last used by g-2, whose dQ^T was drained before g-1's
+          if (kDQ && g > 0 && !(ok = mbar_wait(dq_empty, (g - 1) & 1, a.status))) break;
           tc_fence_after();
-          issue_sdp(it);
-          if (!(ok = ds_wait(it))) break;
+          issue_sdp(g);
+          if (!(ok = ds_wait(g))) break;
           tc_fence_after();
-          issue_grads(it);
+          ok = issue_grads(g, it, k);
         }
       } else {
-        ok = ok && mbar_wait(&q_full[0], 0, a.status);
+        ok = ok && mbar_wait(&q_full[gt % C::NQ], (gt / C::NQ) & 1, a.status);
         if (ok) {
           tc_fence_after();
-          issue_sdp(0);
+          issue_sdp(gt);
         }
         for (int it = 0; it < niter && ok; ++it) {
+          const int g = gt + it;
           if (it + 1 < niter) {
-            // buffer (it+1)%2 was last used by it-1: its dQ^T halves must be drained
-            const int sn = (it + 1) % C::NQ;
-            if (!(ok = mbar_wait(&q_full[sn], ((it + 1) / C::NQ) & 1, a.status))) break;
-            if (kDQ && !(ok = mbar_wait(dq_empty, (it & 1) ^ 1, a.status))) break;
+            // buffer (g+1)%2 was last used by g-1: its dQ^T halves must be drained
+            const int sn = (g + 1) % C::NQ;
+            if (!(ok = mbar_wait(&q_full[sn], ((g + 1) / C::NQ) & 1, a.status))) break;
+            if (kDQ && !(ok = mbar_wait(dq_empty, (g & 1) ^ 1, a.status))) break;
             tc_fence_after();
-            issue_sdp(it + 1);
+            issue_sdp(g + 1);
           }
-          if (!(ok = ds_wait(it))) break;
-          // The drain warps wait on dq_full by parity. On the last tile there is
-          // no S^T/dP^T issue (and no dq_empty wait) above, so wait here for the
-          // drain of it-1: dq_full then never runs two phases ahead of them.
-          if (kDQ && it + 1 >= niter && it > 0 && !(ok = mbar_wait(dq_empty, (it & 1) ^ 1, a.status))) break;
+          if (!(ok = ds_wait(g))) break;
+          // The drain warps wait on dq_full by parity. On a unit's last tile
+          // there is no S^T/dP^T issue (and no dq_empty wait) above, so wait
+          // here for the drain of g-1: dq_full then never runs two phases
+          // ahead of them, and the next unit's first S^T/dP^T finds buffer
+          // (g+1)%2 drained.
+          if (kDQ && it + 1 >= niter && g > 0 && !(ok = mbar_wait(dq_empty, (g & 1) ^ 1, a.status))) break;
           tc_fence_after();
-          issue_grads(it);
+          ok = issue_grads(g, it, k);
         }
       }
       mma_commit(done);
+      if (!ok || !kPersist) break;
+      mma_commit(kv_empty);
+      gt += niter;
+      }
     }
     __syncwarp();
   }
@@ -497,21 +577,25 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     const int half = warp >= 12 ? 1 : 0;            // queries 32*half .. +31 of each tile
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;              // key row of the tile
-    const int kloc = j * C::BC + r;                 // key position in the sequence
-    const bool kvalid = kloc < L;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float2 sl2v = make_float2(a.scale_log2, a.scale_log2);
     bool ok = true;
     bool dq_ok = true;   // the wait for the previous tile's dQ^T ended in time
+    int gt = 0;          // tiles of the earlier units
+    for (int k = 0;; ++k) {
+    if (k > 0 && !next_unit(k)) break;
+    const int kloc = j * C::BC + r;                 // key position in the sequence
+    const bool kvalid = kloc < L;
     for (int it = 0; it < niter; ++it) {
-      const uint32_t xb = tbase + lane_off + 128u * (it & 1);
+      const int g = gt + it;
+      const uint32_t xb = tbase + lane_off + 128u * (g & 1);
       uint8_t* ds_row = sDS + r * 128;
-      const int st = it % C::NQ;
+      const int st = g % C::NQ;
       // LSE and D of this stage (written by the load warp before it arrived
       // on q_full[st]) go to registers first: these shared-memory reads then
       // overlap the wait for S^T/dP^T instead of heading every exp2 chain
       // while the tensor core's operand reads keep shared memory busy.
-      bool got = __all_sync(0xffffffffu, mbar_wait(&q_full[st], (it / C::NQ) & 1, a.status));
+      bool got = __all_sync(0xffffffffu, mbar_wait(&q_full[st], (g / C::NQ) & 1, a.status));
       float4 l4r[8], d4r[8];
       if (got) {
         const float* nlse = sLD + st * 2 * C::BR + 32 * half;     // -LSE * log2(e)
@@ -521,7 +605,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
           d4r[e4] = *reinterpret_cast<const float4*>(nlse + C::BR + 4 * e4);   // -D
         }
       }
-      if (got) got = __all_sync(0xffffffffu, mbar_wait(&sp_full[it & 1], (it >> 1) & 1, a.status));
+      if (got) got = __all_sync(0xffffffffu, mbar_wait(&sp_full[g & 1], (g >> 1) & 1, a.status));
       got = got && dq_ok;   // a wait that ran out in the previous tile ends both groups here
       uint32_t sv[32], dp[32];
       if (got) {
@@ -539,8 +623,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       if (!ok) break;
       const int q0 = q_tile(it) * C::BR + 32 * half;
       // this key against queries q0 .. q0 + 31: outside the sequence or the window?
-      const bool edge = !kvalid || (a.win_right >= 0 && kloc > q0 + a.win_right) ||
-                        (a.win_left >= 0 && kloc < q0 + 31 - a.win_left);
+      const bool edge = kPersist ? !kvalid
+                                 : !kvalid || (a.win_right >= 0 && kloc > q0 + a.win_right) ||
+                                       (a.win_left >= 0 && kloc < q0 + 31 - a.win_left);
       uint32_t pp[16], dd[16];
 #pragma unroll
       for (int e4 = 0; e4 < 8; ++e4) {
@@ -584,7 +669,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       // tile is read by dQ^T of the previous tile, which must be complete
       // first; waiting only here lets this tile's exponentials overlap it.
       if constexpr (kDQ) {
-        if (it > 0) dq_ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (it - 1) & 1, a.status));
+        if (g > 0) dq_ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (g - 1) & 1, a.status));
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           const int chunk = (4 * half + c4) ^ (r & 7);
@@ -595,9 +680,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       tmem_wait_st();
       if constexpr (kDQ) fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(C::kOwnCols ? &ds_ready[(it & 1) * 2 + half] : &ds_ready[0]);
+      mbar_arrive(C::kOwnCols ? &ds_ready[(g & 1) * 2 + half] : &ds_ready[0]);
     }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(done, 0, a.status));
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(done, k & 1, a.status));
     tc_fence_after();
     // dV rows, this CTA's columns, DH/2 per group. With a split walk part 1
     // hands its dV to part 0 (between the two cluster barriers, once both
@@ -612,8 +697,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       add = reinterpret_cast<const float*>(smem);
     }
     if (ok && wp == 0) {
-      const long long off = static_cast<long long>(b) * a.k_sb + static_cast<long long>(hkv) * a.k_sh +
-                            static_cast<long long>(seq0 + kloc) * a.k_sn;
+      const long long off = kPersist ? persist_key_off(k, r)
+                                     : static_cast<long long>(b) * a.k_sb + static_cast<long long>(hkv) * a.k_sh +
+                                           static_cast<long long>(seq0 + kloc) * a.k_sn;
 #pragma unroll 1
       for (int c = half * (C::DH / 64); c < (half + 1) * (C::DH / 64); ++c) {
         uint32_t v[32];
@@ -633,6 +719,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         }
       }
     }
+    if constexpr (kPersist) {   // dV is read out: the next unit may start it
+      tc_fence_before();
+      mbar_arrive(acc_empty);
+    }
+    if (!ok || !kPersist) break;
+    gt += niter;
+    }
   } else {
     regs_dec<C::kRegsDrain>();
     // ---------------------------------------------------- dQ^T drain
@@ -640,15 +733,19 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     const int dim = quarter * 32 + lane;            // head-dim index = tensor-memory lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     bool ok = true;
+    int gt = 0;   // tiles of the earlier units
+    for (int k = 0;; ++k) {
+    if (k > 0 && !next_unit(k)) break;
     for (int it = 0; it < (kDQ ? niter : 0); ++it) {
+      const int g = gt + it;
       // one decision for all four drain warps, so none is left alone at the
       // named barriers below
-      ok = named_bar_and(1, 128, __all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, a.status)));
+      ok = named_bar_and(1, 128, __all_sync(0xffffffffu, mbar_wait(dq_full, g & 1, a.status)));
       if (!ok) break;
       tc_fence_after();
       uint32_t x0[32], x1[32];
-      tmem_ld32(tbase + lane_off + 128u * (it & 1) + C::COL_DQ, x0);
-      tmem_ld32(tbase + lane_off + 128u * (it & 1) + C::COL_DQ + 32, x1);
+      tmem_ld32(tbase + lane_off + 128u * (g & 1) + C::COL_DQ, x0);
+      tmem_ld32(tbase + lane_off + 128u * (g & 1) + C::COL_DQ + 32, x1);
       tmem_wait_ld();
       reg_fence(x0);
       reg_fence(x1);
@@ -692,8 +789,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         }
       }
     }
-    if (threadIdx.x == 256) bulk_wait_all();
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(done, 0, a.status));
+    if (!kPersist && threadIdx.x == 256) bulk_wait_all();
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(done, k & 1, a.status));
     tc_fence_after();
     // dK rows (here the lane indexes keys), times scale; a split walk's part 1
     // hands its dK to part 0 as for dV
@@ -705,9 +802,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       add = reinterpret_cast<const float*>(smem) + C::BC * C::DH;
     }
     if (ok && wp == 0) {
-      const int kloc = j * C::BC + dim;
-      const long long off = static_cast<long long>(b) * a.k_sb + static_cast<long long>(hkv) * a.k_sh +
-                            static_cast<long long>(seq0 + kloc) * a.k_sn;
+      const int kloc = kPersist ? persist_key_row(k, dim) : j * C::BC + dim;
+      const long long off = kPersist ? persist_key_off(k, dim)
+                                     : static_cast<long long>(b) * a.k_sb + static_cast<long long>(hkv) * a.k_sh +
+                                           static_cast<long long>(seq0 + kloc) * a.k_sn;
 #pragma unroll 1
       for (int c = 0; c < C::DH / 32; ++c) {
         uint32_t v[32];
@@ -728,6 +826,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         }
       }
     }
+    if constexpr (kPersist) {   // dK is read out: the next unit may start it
+      tc_fence_before();
+      mbar_arrive(acc_empty);
+    }
+    if (!ok || !kPersist) break;
+    gt += niter;
+    }
+    if (kPersist && threadIdx.x == 256) bulk_wait_all();
   }
   // the split grid completes only after the grid it depends on, so work
   // queued after it (the dQ conversion) sees both grids' results
@@ -746,5 +852,12 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
 template <int DT, int D, bool kDQ>
 cudaError_t launch_bwd_split(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q, const CUtensorMap& d,
                              const CUtensorMap& dq, const BwdArgs& a, int n, dim3 grid, cudaStream_t st);
+
+// Launch of the persistent instance (bwd_persist.cu; D = 64, 128, with dQ):
+// `grid` CTAs walk units blockIdx.x, + grid, ... below a.units.
+template <int DT, int D>
+cudaError_t launch_bwd_persist(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
+                               const CUtensorMap& d, const CUtensorMap& dq, const BwdArgs& a, int grid,
+                               cudaStream_t st);
 
 }  // namespace attn

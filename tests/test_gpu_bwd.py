@@ -124,12 +124,12 @@ def test_varlen_config_backward_sampled():
             assert rel_rms(got, r) <= 1e-2, (name, int(s), rel_rms(got, r))
 
 
-def _tail_case(sms, d, split):
-    """Heads H of a (B=1, H, N=1024) non-causal problem whose backward runs
+def _tail_case(sms, d, split, n):
+    """Heads H of a (B=1, H, N=n) non-causal problem whose backward runs
     as whole waves plus a split last wave (split=True: more units than SMs,
     the remainder at most half the SMs) or as one unsplit launch (split=False:
     the remainder above half the SMs)."""
-    per_head_units = 8 * (2 if d == 256 else 1)
+    per_head_units = (n + 127) // 128 * (2 if d == 256 else 1)
     for h in range(1, 4 * sms):
         units = per_head_units * h
         r = units % sms
@@ -146,8 +146,10 @@ def test_last_wave_split_gqa_and_deterministic():
     dQ from the query-stationary kernel): against the oracle, and the
     deterministic result bit-identical across calls."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    hkv = next(h for h in range(1, 4 * sms) if 8 * h > sms and 0 < (8 * h) % sms <= sms // 2)
+    # rows longer than the persistent walk takes
     B, N, d = 1, 1024, 128
+    tiles = (N + 127) // 128
+    hkv = next(h for h in range(1, 4 * sms) if tiles * h > sms and 0 < (tiles * h) % sms <= sms // 2)
     q, k, v, do = inputs.normal(77, [(B, 4 * hkv, N, d), (B, hkv, N, d), (B, hkv, N, d), (B, 4 * hkv, N, d)])
     groups = [0, hkv // 2, hkv - 1]   # KV heads checked against the oracle, each with its 4 query heads
 
@@ -188,8 +190,10 @@ def test_last_wave_split(split, d):
     distributed shared memory). Both launch plans against the oracle, and the
     split one twice: its dK and dV are bit-identical across calls."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    H = _tail_case(sms, d, split)
-    q, k, v, do = inputs.normal(31 + d, [(1, H, 1024, d)] * 4)
+    # rows longer than the persistent walk takes (test_persistent_walk)
+    n = 1024
+    H = _tail_case(sms, d, split, n)
+    q, k, v, do = inputs.normal(31 + d, [(1, H, n, d)] * 4)
     got = run_dense(q, k, v, do, False)
     ref = A.backward(q, k, v, do, d ** -0.5, False)
     for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
@@ -197,3 +201,27 @@ def test_last_wave_split(split, d):
     if split:
         again = run_dense(q, k, v, do, False)
         assert torch.equal(got[1], again[1]) and torch.equal(got[2], again[2])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("shape", [(8, 8, 4, 700), (16, 16, 8, 200), (40, 8, 8, 64), (48, 4, 2, 130)])
+def test_persistent_walk(shape, d, dtype):
+    """Short unmasked rows with more units than SMs: one CTA per SM walks
+    several units (key tile, KV head, batch), the barrier phases running on
+    across them and each unit's dV/dK read out while the next one starts.
+    Ragged rows, GQA, units of one query tile (N = 64: a unit's walk is one
+    tile per query head) and more than two units per CTA, against the
+    oracle."""
+    B, Hq, Hkv, n = shape
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert (n + 127) // 128 * Hkv * B > sms
+    q, k, v, do = inputs.normal(400 + n + d, [(B, Hq, n, d), (B, Hkv, n, d), (B, Hkv, n, d), (B, Hq, n, d)],
+                                dtype=dtype)
+    got = run_dense(q, k, v, do, False)
+    ref = A.backward(q, k, v, do, d ** -0.5, False)
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        assert rel_rms(g, r) <= 1e-2, (name, rel_rms(g, r))
+    # dK and dV come from one unit each, summed in a fixed order
+    again = run_dense(q, k, v, do, False)
+    assert torch.equal(got[1], again[1]) and torch.equal(got[2], again[2])
