@@ -10,11 +10,14 @@ constexpr int kFwdPersistMaxRows = 2048;
 // Two-tile instances over short rows run persistent: one CTA per SM walks
 // the units, so one unit's epilogue overlaps the next unit's loads and S
 // products; there a unit holds few KV steps and its set-up and epilogue
-// weigh. Over long rows (and with masks, where the hardware's dispatch
-// order balances unequal units better than a fixed deal) each CTA takes one
-// unit.
+// weigh. The same holds for a window bounded on both sides whose span is
+// short, however long the rows. Over long rows, and with causal masking
+// (units of unequal work, which the hardware's dispatch in heavy-first
+// order balances better than a fixed deal), each CTA takes one unit.
 inline bool fwd_persistent(int qt, const FwdArgs& a, int rows) {
-  return qt == 2 && a.win_left < 0 && a.win_right < 0 && rows <= kFwdPersistMaxRows;
+  if (qt != 2 || a.causal) return false;
+  if (a.win_left < 0 && a.win_right < 0) return rows <= kFwdPersistMaxRows;
+  return a.win_left >= 0 && a.win_right >= 0 && a.win_left + a.win_right + 256 <= kFwdPersistMaxRows;
 }
 
 template <int DT, int D, int QT, bool kPersist>

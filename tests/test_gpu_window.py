@@ -107,6 +107,23 @@ def test_backward_window(window, n, d):
         assert rel_rms(g, r) <= 1e-2, (name, window, rel_rms(g, r))
 
 
+@pytest.mark.parametrize("window", [(200, 300), (0, 0), (1000, 700)])
+def test_forward_window_persistent_walk(window):
+    """A window bounded on both sides with a short span runs the persistent
+    forward walk (one CTA per SM taking several units); B=4, H=16, N=2000
+    is 512 units of two query tiles. Against the oracle on four heads."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B, H, n, d = 4, 16, 2000, 128
+    assert (n + 255) // 256 * H * B > sms
+    q, k, v = inputs.normal(71, [(B, H, n, d)] * 3)
+    o, lse = run_fwd(q, k, v, window)
+    o, lse = o.cpu(), lse.cpu()
+    for b, h in ((0, 0), (1, 5), (2, 11), (3, 15)):
+        sel = lambda x: x[b:b + 1, h:h + 1]
+        o_ref, lse_ref = A.forward(sel(q), sel(k), sel(v), d ** -0.5, False, window)
+        check_o_lse(sel(o), sel(lse), o_ref, lse_ref, f"b{b} h{h} w{window}")
+
+
 @pytest.mark.slow
 def test_window_config_sampled():
     """B=1, H=16, N=16384, d=128, window (1024, 0): sampled rows of three heads
