@@ -279,12 +279,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
   };
   set_unit(bx, by, bz);
   if (j * C::BC >= L) return;
-  // Persistent walk: unit k >= 1 of this CTA; false past the last unit. Every
-  // role walks the same units, and the barrier phases run on across them
-  // (counted in tiles g of the whole walk, or in units k).
-  // The walk runs over dense rows without masks, so every unit has the same
-  // query tiles (i0 = 0, per_head, niter) and only the key tile, KV head and
-  // batch change.
+  // Persistent walk (dense rows without masks): unit k of this CTA is
+  // blockIdx.x + k * gridDim.x while below a.units. Every unit has the same
+  // query tiles (i0 = 0, per_head, niter); only the key tile, KV head and
+  // batch change. Every role walks the same units, and the barrier phases
+  // run on across them (counted in tiles g of the whole walk, or in units k).
   auto more_units = [&](int k) -> bool {
     return kPersist && static_cast<long long>(blockIdx.x) + static_cast<long long>(k) * gridDim.x < a.units;
   };
