@@ -89,7 +89,11 @@ struct BwdArgs {
   int units;
 };
 
-template <int DT, int D>
+// kP: the persistent walk's layout. At d = 64 it holds two K/V buffers, so
+// the next unit's K and V load while the current unit runs; at d = 128 a
+// second buffer would take the room of two of the four Q/dO stages, which
+// measured far slower than what it hides (22 % at N = 512).
+template <int DT, int D, bool kP = false>
 struct BwdCfg {
   static_assert(D == 64 || D == 128 || D == 256, "backward kernel is written for head dim 64, 128 or 256");
   static constexpr int DSPLIT = D == 256 ? 2 : 1;   // CTAs per key tile (each owns DH dims of dK, dV, dQ)
@@ -102,16 +106,17 @@ struct BwdCfg {
   static constexpr int Q_B = BR * D * 2;            // Q_i or dO_i tile
   static constexpr int Q_BOX_B = BR * 128;
   static constexpr int DS_B = BC * BR * 2;          // dS^T tile [128 keys][64 queries]
+  static constexpr int NKV = kP && D == 64 ? 2 : 1;   // K/V buffers
   static constexpr int NQ = D == 64 ? 6 : (D == 128 ? 4 : 1);   // stages of the Q/dO ring
   static constexpr int LD_B = 2 * BR * 4;           // LSE*log2e and D for one tile
   static constexpr int DQ_ROWS = D == 64 ? BR : BR / 2;   // rows of dQ per reduce-add
   static constexpr int DQ_PARTS = BR / DQ_ROWS;            // reduce-adds per tile
   static constexpr int DQ_STAGE_B = DQ_ROWS * DH * 4;      // FP32 staging for one reduce-add
-  // kv_full, q_full[NQ], q_empty[NQ], sp_full[2], ds_ready[2][2], dq_full, dq_empty, done,
-  // kv_empty, acc_empty
-  static constexpr int NBARS = 1 + 2 * NQ + 2 + 4 + 5;
+  // kv_full[NKV], q_full[NQ], q_empty[NQ], sp_full[2], ds_ready[2][2], dq_full, dq_empty, done,
+  // kv_empty[NKV], acc_empty
+  static constexpr int NBARS = 2 * NKV + 2 * NQ + 2 + 4 + 4;
   static constexpr int SMEM_BYTES =
-      2 * KV_B + DS_B + NQ * (2 * Q_B) + DQ_STAGE_B + NQ * LD_B + NBARS * 8 + 16;   // base is 1024-aligned
+      NKV * 2 * KV_B + DS_B + NQ * (2 * Q_B) + DQ_STAGE_B + NQ * LD_B + NBARS * 8 + 16;   // base is 1024-aligned
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeded");
   // a split walk's hand-over of dV and dK ([2][BC][DH] FP32 from offset 0)
   // stays below the barriers
@@ -185,7 +190,7 @@ __global__ void __launch_bounds__(512, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
            const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
            const __grid_constant__ CUtensorMap tmdQ, const BwdArgs a) {
-  using C = BwdCfg<DT, D>;
+  using C = BwdCfg<DT, D, kPersist>;
   static_assert(!kPersist || (!kSplit && C::DSPLIT == 1), "persistent walk: whole units, one CTA per key tile");
   // The layout uses all the shared memory it asks for, with no room to align
   // the base by hand: a base that is not 1024-byte aligned (needed by the
@@ -203,16 +208,16 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     return;
   }
   uint8_t* smem = bwd_smem;
-  uint8_t* sK = smem;
+  uint8_t* sK = smem;                               // K/V buffer kb: sK + kb * 2 * KV_B, V after K
   uint8_t* sV = sK + C::KV_B;
-  uint8_t* sDS = sV + C::KV_B;                      // [DS_B], 128-byte swizzle
+  uint8_t* sDS = sK + C::NKV * 2 * C::KV_B;         // [DS_B], 128-byte swizzle
   uint8_t* sQ = sDS + C::DS_B;                      // [NQ][Q_B]
   uint8_t* sdO = sQ + C::NQ * C::Q_B;               // [NQ][Q_B]
   float* sDQ = reinterpret_cast<float*>(sdO + C::NQ * C::Q_B);   // [DQ_ROWS][D] FP32
   float* sLD = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(sDQ) + C::DQ_STAGE_B);   // [NQ][2*BR]
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sLD) + C::NQ * C::LD_B);
-  uint64_t* kv_full = bars;
-  uint64_t* q_full = bars + 1;
+  uint64_t* kv_full = bars;                         // [NKV]
+  uint64_t* q_full = bars + C::NKV;
   uint64_t* q_empty = q_full + C::NQ;
   uint64_t* sp_full = q_empty + C::NQ;             // [2], one per score buffer
   // P^T/dS^T ready. With independent groups (kOwnCols) one barrier per score
@@ -223,8 +228,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
   uint64_t* dq_full = ds_ready + 4;
   uint64_t* dq_empty = dq_full + 1;
   uint64_t* done = dq_empty + 1;                    // one phase per unit
-  uint64_t* kv_empty = done + 1;                    // persistent: the unit's products have read K, V
-  uint64_t* acc_empty = kv_empty + 1;               // persistent: dV, dK read out of tensor memory
+  uint64_t* kv_empty = done + 1;                    // [NKV] persistent: the unit's products have read K, V
+  uint64_t* acc_empty = kv_empty + C::NKV;          // persistent: dV, dK read out of tensor memory
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -325,7 +330,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmdO);
     tma_prefetch_desc(&tmdQ);
-    mbar_init(kv_full, 1);
+    for (int s = 0; s < C::NKV; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
     for (int s = 0; s < C::NQ; ++s) {
       mbar_init(&q_full[s], 2);   // TMA transaction + the LSE/D stores
       mbar_init(&q_empty[s], 1);
@@ -340,7 +348,6 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 128);
     mbar_init(done, 1);
-    mbar_init(kv_empty, 1);
     mbar_init(acc_empty, 384);   // the two P^T/dS^T groups (dV) and the drain warps (dK)
     fence_barrier_init();
   }
@@ -365,21 +372,24 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     // ------------------------------------------------------------ loads
     int gt = 0;   // tiles of the earlier units
     for (int k = 0;; ++k) {
+    const int kb = k % C::NKV;   // K/V buffer of unit k
     if (k > 0) {
       if (!next_unit(k)) break;
-      // the previous unit's K and V are read until its last products complete
-      if (!__all_sync(0xffffffffu, mbar_wait(kv_empty, (k - 1) & 1, a.status))) break;
+      // buffer kb was last read by unit k - NKV, whose last products must complete
+      if (k >= C::NKV && !__all_sync(0xffffffffu, mbar_wait(&kv_empty[kb], (k / C::NKV - 1) & 1, a.status))) break;
     }
     const int krow = seq0 + j * C::BC;
     if (lane == 0) {
-      mbar_arrive_expect_tx(kv_full, 2 * C::KV_B);
+      uint8_t* bK = sK + kb * 2 * C::KV_B;
+      uint8_t* bV = bK + C::KV_B;
+      mbar_arrive_expect_tx(&kv_full[kb], 2 * C::KV_B);
       for (int c = 0; c < C::NBOX; ++c) {
         if (packed) {
-          tma_load_4d(sK + c * C::KV_BOX_B, &tmK, kv_full, c * 64, hkv, krow, 0);
-          tma_load_4d(sV + c * C::KV_BOX_B, &tmV, kv_full, c * 64, hkv, krow, 0);
+          tma_load_4d(bK + c * C::KV_BOX_B, &tmK, &kv_full[kb], c * 64, hkv, krow, 0);
+          tma_load_4d(bV + c * C::KV_BOX_B, &tmV, &kv_full[kb], c * 64, hkv, krow, 0);
         } else {
-          tma_load_4d(sK + c * C::KV_BOX_B, &tmK, kv_full, c * 64, krow, hkv, b);
-          tma_load_4d(sV + c * C::KV_BOX_B, &tmV, kv_full, c * 64, krow, hkv, b);
+          tma_load_4d(bK + c * C::KV_BOX_B, &tmK, &kv_full[kb], c * 64, krow, hkv, b);
+          tma_load_4d(bV + c * C::KV_BOX_B, &tmV, &kv_full[kb], c * 64, krow, hkv, b);
         }
       }
     }
@@ -458,18 +468,19 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         else
           return mbar_wait(&ds_ready[0], g & 1, a.status);
       };
-      auto issue_sdp = [&](int g) {   // S^T = K Q^T and dP^T = V dO^T into buffer g % 2
+      // kvo: byte offset of the unit's K/V buffer
+      auto issue_sdp = [&](int g, uint32_t kvo) {   // S^T = K Q^T and dP^T = V dO^T into buffer g % 2
         const uint32_t so = (g % C::NQ) * C::Q_B;
         const uint32_t xb = tbase + 128u * (g & 1);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t offk = (kk / 4) * C::KV_BOX_B + (kk % 4) * 32;
+          const uint32_t offk = kvo + (kk / 4) * C::KV_BOX_B + (kk % 4) * 32;
           const uint32_t offq = so + (kk / 4) * C::Q_BOX_B + (kk % 4) * 32;
           mma_ss<false>(xb + C::COL_S, dadd(dK_kmaj, offk), dadd(dQ0_kmaj, offq), C::IDESC_SP, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t offk = (kk / 4) * C::KV_BOX_B + (kk % 4) * 32;
+          const uint32_t offk = kvo + (kk / 4) * C::KV_BOX_B + (kk % 4) * 32;
           const uint32_t offq = so + (kk / 4) * C::Q_BOX_B + (kk % 4) * 32;
           mma_ss<false>(xb + C::COL_DP, dadd(dV_kmaj, offk), dadd(ddO0_kmaj, offq), C::IDESC_SP, kk > 0);
         }
@@ -481,14 +492,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       // dV and dK (its last readers) go first and release it, and dQ^T runs
       // while the loads are in flight.
       // g: tile of the walk, it: tile of unit k (it = 0 starts dV and dK)
-      auto issue_grads = [&](int g, int it, int k) {
+      auto issue_grads = [&](int g, int it, int k, uint32_t kvo) {
         const uint32_t xb = tbase + 128u * (g & 1);
         const uint32_t so = (g % C::NQ) * C::Q_B;
         auto issue_dq = [&]() {
           if constexpr (kDQ) {
 #pragma unroll
             for (int kk = 0; kk < C::BC / 16; ++kk) {   // dQ^T = K^T dS^T, both MN-major
-              mma_ss<false>(xb + C::COL_DQ, dadd(dK_mn, kk * 2048), dadd(dDS0_mn, kk * 2048),
+              mma_ss<false>(xb + C::COL_DQ, dadd(dK_mn, kvo + kk * 2048), dadd(dDS0_mn, kk * 2048),
                             C::IDESC_DQ, kk > 0);
             }
             mma_commit(dq_full);
@@ -512,54 +523,95 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         if constexpr (C::NQ == 1) issue_dq();
         return true;
       };
-      int gt = 0;   // tiles of the earlier units
-      for (int k = 0;; ++k) {
-      if (k > 0 && !more_units(k)) break;
-      bool ok = mbar_wait(kv_full, k & 1, a.status);
+      if constexpr (!kPersist) {
+      bool ok = mbar_wait(kv_full, 0, a.status);
       if constexpr (C::NQ == 1) {
-        // one Q/dO stage: tile g's products, then tile g+1's
+        // one Q/dO stage: tile it's products, then tile it+1's
         for (int it = 0; it < niter && ok; ++it) {
-          const int g = gt + it;
-          if (!(ok = mbar_wait(&q_full[0], g & 1, a.status))) break;
-          // buffer g%2 was last used by g-2, whose dQ^T was drained before g-1's
-          if (kDQ && g > 0 && !(ok = mbar_wait(dq_empty, (g - 1) & 1, a.status))) break;
+          if (!(ok = mbar_wait(&q_full[0], it & 1, a.status))) break;
+          // buffer it%2 was last used by it-2, whose dQ^T was drained before it-1's
+          if (kDQ && it > 0 && !(ok = mbar_wait(dq_empty, (it - 1) & 1, a.status))) break;
           tc_fence_after();
-          issue_sdp(g);
-          if (!(ok = ds_wait(g))) break;
+          issue_sdp(it, 0);
+          if (!(ok = ds_wait(it))) break;
           tc_fence_after();
-          ok = issue_grads(g, it, k);
+          issue_grads(it, it, 0, 0);
         }
       } else {
-        ok = ok && mbar_wait(&q_full[gt % C::NQ], (gt / C::NQ) & 1, a.status);
+        ok = ok && mbar_wait(&q_full[0], 0, a.status);
         if (ok) {
           tc_fence_after();
-          issue_sdp(gt);
+          issue_sdp(0, 0);
         }
         for (int it = 0; it < niter && ok; ++it) {
-          const int g = gt + it;
           if (it + 1 < niter) {
-            // buffer (g+1)%2 was last used by g-1: its dQ^T halves must be drained
-            const int sn = (g + 1) % C::NQ;
-            if (!(ok = mbar_wait(&q_full[sn], ((g + 1) / C::NQ) & 1, a.status))) break;
-            if (kDQ && !(ok = mbar_wait(dq_empty, (g & 1) ^ 1, a.status))) break;
+            // buffer (it+1)%2 was last used by it-1: its dQ^T halves must be drained
+            const int sn = (it + 1) % C::NQ;
+            if (!(ok = mbar_wait(&q_full[sn], ((it + 1) / C::NQ) & 1, a.status))) break;
+            if (kDQ && !(ok = mbar_wait(dq_empty, (it & 1) ^ 1, a.status))) break;
             tc_fence_after();
-            issue_sdp(g + 1);
+            issue_sdp(it + 1, 0);
           }
-          if (!(ok = ds_wait(g))) break;
-          // The drain warps wait on dq_full by parity. On a unit's last tile
-          // there is no S^T/dP^T issue (and no dq_empty wait) above, so wait
-          // here for the drain of g-1: dq_full then never runs two phases
-          // ahead of them, and the next unit's first S^T/dP^T finds buffer
-          // (g+1)%2 drained.
-          if (kDQ && it + 1 >= niter && g > 0 && !(ok = mbar_wait(dq_empty, (g & 1) ^ 1, a.status))) break;
+          if (!(ok = ds_wait(it))) break;
+          // The drain warps wait on dq_full by parity. On the last tile there is
+          // no S^T/dP^T issue (and no dq_empty wait) above, so wait here for the
+          // drain of it-1: dq_full then never runs two phases ahead of them.
+          if (kDQ && it + 1 >= niter && it > 0 && !(ok = mbar_wait(dq_empty, (it & 1) ^ 1, a.status))) break;
           tc_fence_after();
-          ok = issue_grads(g, it, k);
+          issue_grads(it, it, 0, 0);
         }
       }
       mma_commit(done);
-      if (!ok || !kPersist) break;
-      mma_commit(kv_empty);
-      gt += niter;
+      } else {
+      // Persistent walk (several Q/dO stages): tiles are counted over the
+      // whole walk (g), so the order within a unit is the one above. With
+      // two K/V buffers, at a unit's last tile the next unit's first
+      // S^T/dP^T (from the other buffer) is issued before the last tile's
+      // gradients, so its softmax overlaps them; with one, the next unit's
+      // K and V load once the last products have read the buffer.
+      static_assert(C::NQ > 1, "persistent walk with several Q/dO stages");
+      constexpr bool kAhead = C::NKV > 1;
+      int gt = 0;             // tiles of the earlier units
+      bool ok = true;
+      bool first_issued = false;   // this unit's first S^T/dP^T went out with the previous unit
+      for (int k = 0; ok; ++k) {
+        if (k > 0 && !more_units(k)) break;
+        const uint32_t kvo = (k % C::NKV) * 2 * C::KV_B;
+        const bool more = kAhead && more_units(k + 1);
+        if (!first_issued) {
+          ok = mbar_wait(&kv_full[k % C::NKV], (k / C::NKV) & 1, a.status) &&
+               mbar_wait(&q_full[gt % C::NQ], (gt / C::NQ) & 1, a.status);
+          if (ok) {
+            tc_fence_after();
+            issue_sdp(gt, kvo);
+          }
+        }
+        first_issued = false;
+        for (int it = 0; it < niter && ok; ++it) {
+          const int g = gt + it;
+          const bool last = it + 1 >= niter;
+          if (!last || more) {
+            // tile g+1: this unit's next, or the next unit's first
+            if (last && !(ok = mbar_wait(&kv_full[(k + 1) % C::NKV], ((k + 1) / C::NKV) & 1, a.status))) break;
+            const int sn = (g + 1) % C::NQ;
+            if (!(ok = mbar_wait(&q_full[sn], ((g + 1) / C::NQ) & 1, a.status))) break;
+            // buffer (g+1)%2 was last used by g-1: its dQ^T halves must be drained
+            if (kDQ && !(ok = mbar_wait(dq_empty, (g & 1) ^ 1, a.status))) break;
+            tc_fence_after();
+            issue_sdp(g + 1, last ? ((k + 1) % C::NKV) * 2 * C::KV_B : kvo);
+            first_issued = last;
+          }
+          if (!(ok = ds_wait(g))) break;
+          // a unit's last tile without the next unit's first products above:
+          // as in the single-unit loop, the drain of g-1 first
+          if (kDQ && last && !more && g > 0 && !(ok = mbar_wait(dq_empty, (g & 1) ^ 1, a.status))) break;
+          tc_fence_after();
+          ok = issue_grads(g, it, k, kvo);
+        }
+        mma_commit(done);
+        mma_commit(&kv_empty[k % C::NKV]);
+        gt += niter;
+      }
       }
     }
     __syncwarp();

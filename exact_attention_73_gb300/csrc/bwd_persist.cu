@@ -10,7 +10,7 @@ template <int DT, int D>
 cudaError_t launch_bwd_persist(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q,
                                const CUtensorMap& d, const CUtensorMap& dq, const BwdArgs& a, int grid,
                                cudaStream_t st) {
-  using C = BwdCfg<DT, D>;
+  using C = BwdCfg<DT, D, true>;
   cudaError_t e = smem_attr_once<bwd_kernel<DT, D, true, false, true>>(C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   if ((e = reg_pool_once<bwd_kernel<DT, D, true, false, true>>(C::NTHREADS, C::kRegsSplit)) != cudaSuccess) return e;
