@@ -109,6 +109,32 @@ def test_backward(kind, d):
     assert torch.equal(dk, dk2) and torch.equal(dv, dv2)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_persistent_walks(d):
+    """The persistent walks (more units than SMs over short rows: the forward
+    without masks and with a short two-sided window, the backward without
+    masks), ragged rows, GQA: margins untouched, every element written."""
+    q, k, v, do = dense_inputs(702, B=24, Hq=8, Hkv=4, N=200, d=d)
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert (N + 127) // 128 * Hkv * B > sms and (N + 255) // 256 * Hq * B > sms
+    for window in ((30, 50), None):   # the backward takes the unmasked forward's O and LSE
+        ob, o = padded(q.shape, q.dtype)
+        lb, lse = padded((B, Hq, N), torch.float32)
+        if window is None:
+            L.attn_fwd(q, k, v, o, lse)
+        else:
+            L.attn_fwd_window(q, k, v, o, lse, window)
+        check({"o": ob, "lse": lb}, {"o": o, "lse": lse})
+    bufs, outs = {}, {}
+    for name, like in (("dq", q), ("dk", k), ("dv", v)):
+        bufs[name], outs[name] = padded(like.shape, like.dtype)
+    bufs["workspace"], ws = padded((L.attn_bwd_workspace_size(B, Hq, Hkv, N, d),), torch.uint8)
+    L.attn_bwd(q, k, v, o, lse, do, outs["dq"], outs["dk"], outs["dv"], ws)
+    check(bufs, outs)
+
+
 def test_varlen_forward_and_backward():
     lens = [1, 127, 300, 5, 129]
     cu = inputs.cu_seqlens(lens).to(DEV)
