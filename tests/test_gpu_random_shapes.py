@@ -155,3 +155,50 @@ def test_random_fp8_case(seed):
     assert np.quantile(err, 0.999) <= 1e-2, tag
     assert err.max() <= 1e-1, tag
     assert np.abs(lse.cpu().double().numpy() - lse_ref).max() <= 1e-3, tag
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_persistent_case(seed):
+    """Random shapes with more units than SMs over short rows, so the
+    persistent walks run (the forward unmasked or with a short two-sided
+    window, the backward unmasked): batch 12..48, GQA groups 1..4, length
+    1..768, head dim 64/128, BF16/FP16. Forward and backward through the
+    public API; two (batch, KV group) slices against the oracle."""
+    rng = np.random.default_rng(3000 + seed)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    d = int(rng.choice([64, 128]))
+    g = int(rng.choice([1, 2, 4]))
+    hkv = int(rng.integers(2, 5))
+    n = int(rng.integers(1, 769))
+    b = max(int(rng.integers(12, 49)), sms // ((n + 127) // 128 * hkv) + 1)
+    window = None if rng.integers(0, 2) else (int(rng.integers(0, 600)), int(rng.integers(0, 600)))
+    dtype = str(rng.choice(["bf16", "fp16"]))
+    hq = hkv * g
+    tag = dict(b=b, hq=hq, hkv=hkv, n=n, d=d, window=window, dtype=dtype)
+    q, k, v, do = inputs.normal(seed, [(b, hq, n, d), (b, hkv, n, d), (b, hkv, n, d), (b, hq, n, d)], dtype=dtype)
+    qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
+    o = torch.full_like(qd, float("nan"))
+    lse = torch.full((b, hq, n), float("nan"), device="cuda")
+    if window is None:
+        L.attn_fwd(qd, kd, vd, o, lse)
+    else:
+        L.attn_fwd_window(qd, kd, vd, o, lse, window)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws = torch.empty((L.attn_bwd_workspace_size(b, hq, hkv, n, d),), dtype=torch.uint8, device="cuda")
+    if window is None:
+        L.attn_bwd(qd, kd, vd, o, lse, dod, dq, dk, dv, ws)
+    else:
+        L.attn_bwd_window(qd, kd, vd, o, lse, dod, dq, dk, dv, ws, window)
+    torch.cuda.synchronize()
+    assert L.attn_get_device_status() == 0
+    o, lse, dq, dk, dv = (x.cpu() for x in (o, lse, dq, dk, dv))
+    args = (False, window)
+    for bi, gi in ((0, 0), (b - 1, hkv - 1)):
+        qs, dos = q[bi:bi + 1, gi * g:(gi + 1) * g], do[bi:bi + 1, gi * g:(gi + 1) * g]
+        ks, vs = k[bi:bi + 1, gi:gi + 1], v[bi:bi + 1, gi:gi + 1]
+        o_ref, lse_ref = A.forward(qs, ks, vs, d ** -0.5, *args)
+        check_fwd(o[bi:bi + 1, gi * g:(gi + 1) * g], lse[bi:bi + 1, gi * g:(gi + 1) * g], o_ref, lse_ref, tag)
+        ref = A.backward(qs, ks, vs, dos, d ** -0.5, *args)
+        got = (dq[bi:bi + 1, gi * g:(gi + 1) * g], dk[bi:bi + 1, gi:gi + 1], dv[bi:bi + 1, gi:gi + 1])
+        for name, g_, r in zip(("dQ", "dK", "dV"), got, ref):
+            assert rel_rms(g_, r) <= 1e-2, (name, rel_rms(g_, r), tag)
