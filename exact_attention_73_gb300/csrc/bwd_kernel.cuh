@@ -372,74 +372,74 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     // ------------------------------------------------------------ loads
     int gt = 0;   // tiles of the earlier units
     for (int k = 0;; ++k) {
-    const int kb = k % C::NKV;   // K/V buffer of unit k
-    if (k > 0) {
-      if (!next_unit(k)) break;
-      // buffer kb was last read by unit k - NKV, whose last products must complete
-      if (k >= C::NKV && !__all_sync(0xffffffffu, mbar_wait(&kv_empty[kb], (k / C::NKV - 1) & 1, a.status))) break;
-    }
-    const int krow = seq0 + j * C::BC;
-    if (lane == 0) {
-      uint8_t* bK = sK + kb * 2 * C::KV_B;
-      uint8_t* bV = bK + C::KV_B;
-      mbar_arrive_expect_tx(&kv_full[kb], 2 * C::KV_B);
-      for (int c = 0; c < C::NBOX; ++c) {
-        if (packed) {
-          tma_load_4d(bK + c * C::KV_BOX_B, &tmK, &kv_full[kb], c * 64, hkv, krow, 0);
-          tma_load_4d(bV + c * C::KV_BOX_B, &tmV, &kv_full[kb], c * 64, hkv, krow, 0);
-        } else {
-          tma_load_4d(bK + c * C::KV_BOX_B, &tmK, &kv_full[kb], c * 64, krow, hkv, b);
-          tma_load_4d(bV + c * C::KV_BOX_B, &tmV, &kv_full[kb], c * 64, krow, hkv, b);
-        }
+      const int kb = k % C::NKV;   // K/V buffer of unit k
+      if (k > 0) {
+        if (!next_unit(k)) break;
+        // buffer kb was last read by unit k - NKV, whose last products must complete
+        if (k >= C::NKV && !__all_sync(0xffffffffu, mbar_wait(&kv_empty[kb], (k / C::NKV - 1) & 1, a.status))) break;
       }
-    }
-    bool ok = true;
-    for (int it = 0; it < niter; ++it) {
-      const int g = gt + it;
-      const int st = g % C::NQ;
-      const int h = q_head(it);
-      const int q0 = q_tile(it) * C::BR;
-      // LSE and D of this tile are fetched before waiting for the stage (they
-      // do not depend on it), so their latency hides behind that wait
-      const long long lrow = static_cast<long long>(b) * a.l_sb + static_cast<long long>(h) * a.l_sh + seq0;
-      float nl[C::BR / 32], nd[C::BR / 32];
-#pragma unroll
-      for (int u = 0; u < C::BR / 32; ++u) {
-        const int q = q0 + lane + 32 * u;
-        const bool in = q < L;
-        nl[u] = in ? -a.lse[lrow + q] * kLog2e : -INFINITY;    // -LSE in log2 units
-        nd[u] = in ? -a.dvec[lrow + q] : 0.f;                  // -D
-      }
-      if (!__all_sync(0xffffffffu, mbar_wait(&q_empty[st], ((g / C::NQ) & 1) ^ 1, a.status))) {
-        ok = false;
-        break;
-      }
+      const int krow = seq0 + j * C::BC;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&q_full[st], 2 * C::Q_B);
+        uint8_t* bK = sK + kb * 2 * C::KV_B;
+        uint8_t* bV = bK + C::KV_B;
+        mbar_arrive_expect_tx(&kv_full[kb], 2 * C::KV_B);
         for (int c = 0; c < C::NBOX; ++c) {
-          uint8_t* dq = sQ + st * C::Q_B + c * C::Q_BOX_B;
-          uint8_t* dd = sdO + st * C::Q_B + c * C::Q_BOX_B;
           if (packed) {
-            tma_load_4d(dq, &tmQ, &q_full[st], c * 64, h, seq0 + q0, 0);
-            tma_load_4d(dd, &tmdO, &q_full[st], c * 64, h, seq0 + q0, 0);
+            tma_load_4d(bK + c * C::KV_BOX_B, &tmK, &kv_full[kb], c * 64, hkv, krow, 0);
+            tma_load_4d(bV + c * C::KV_BOX_B, &tmV, &kv_full[kb], c * 64, hkv, krow, 0);
           } else {
-            tma_load_4d(dq, &tmQ, &q_full[st], c * 64, q0, h, b);
-            tma_load_4d(dd, &tmdO, &q_full[st], c * 64, q0, h, b);
+            tma_load_4d(bK + c * C::KV_BOX_B, &tmK, &kv_full[kb], c * 64, krow, hkv, b);
+            tma_load_4d(bV + c * C::KV_BOX_B, &tmV, &kv_full[kb], c * 64, krow, hkv, b);
           }
         }
       }
-      float* ld = sLD + st * 2 * C::BR;
-#pragma unroll
-      for (int u = 0; u < C::BR / 32; ++u) {
-        ld[lane + 32 * u] = nl[u];
-        ld[C::BR + lane + 32 * u] = nd[u];
+      bool ok = true;
+      for (int it = 0; it < niter; ++it) {
+        const int g = gt + it;
+        const int st = g % C::NQ;
+        const int h = q_head(it);
+        const int q0 = q_tile(it) * C::BR;
+        // LSE and D of this tile are fetched before waiting for the stage (they
+        // do not depend on it), so their latency hides behind that wait
+        const long long lrow = static_cast<long long>(b) * a.l_sb + static_cast<long long>(h) * a.l_sh + seq0;
+        float nl[C::BR / 32], nd[C::BR / 32];
+  #pragma unroll
+        for (int u = 0; u < C::BR / 32; ++u) {
+          const int q = q0 + lane + 32 * u;
+          const bool in = q < L;
+          nl[u] = in ? -a.lse[lrow + q] * kLog2e : -INFINITY;    // -LSE in log2 units
+          nd[u] = in ? -a.dvec[lrow + q] : 0.f;                  // -D
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(&q_empty[st], ((g / C::NQ) & 1) ^ 1, a.status))) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&q_full[st], 2 * C::Q_B);
+          for (int c = 0; c < C::NBOX; ++c) {
+            uint8_t* dq = sQ + st * C::Q_B + c * C::Q_BOX_B;
+            uint8_t* dd = sdO + st * C::Q_B + c * C::Q_BOX_B;
+            if (packed) {
+              tma_load_4d(dq, &tmQ, &q_full[st], c * 64, h, seq0 + q0, 0);
+              tma_load_4d(dd, &tmdO, &q_full[st], c * 64, h, seq0 + q0, 0);
+            } else {
+              tma_load_4d(dq, &tmQ, &q_full[st], c * 64, q0, h, b);
+              tma_load_4d(dd, &tmdO, &q_full[st], c * 64, q0, h, b);
+            }
+          }
+        }
+        float* ld = sLD + st * 2 * C::BR;
+  #pragma unroll
+        for (int u = 0; u < C::BR / 32; ++u) {
+          ld[lane + 32 * u] = nl[u];
+          ld[C::BR + lane + 32 * u] = nd[u];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_full[st]);
+        __syncwarp();
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&q_full[st]);
-      __syncwarp();
-    }
-    if (!ok || !kPersist) break;
-    gt += niter;
+      if (!ok || !kPersist) break;
+      gt += niter;
     }
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA
@@ -524,93 +524,93 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         return true;
       };
       if constexpr (!kPersist) {
-      bool ok = mbar_wait(kv_full, 0, a.status);
-      if constexpr (C::NQ == 1) {
-        // one Q/dO stage: tile it's products, then tile it+1's
-        for (int it = 0; it < niter && ok; ++it) {
-          if (!(ok = mbar_wait(&q_full[0], it & 1, a.status))) break;
-          // buffer it%2 was last used by it-2, whose dQ^T was drained before it-1's
-          if (kDQ && it > 0 && !(ok = mbar_wait(dq_empty, (it - 1) & 1, a.status))) break;
-          tc_fence_after();
-          issue_sdp(it, 0);
-          if (!(ok = ds_wait(it))) break;
-          tc_fence_after();
-          issue_grads(it, it, 0, 0);
-        }
-      } else {
-        ok = ok && mbar_wait(&q_full[0], 0, a.status);
-        if (ok) {
-          tc_fence_after();
-          issue_sdp(0, 0);
-        }
-        for (int it = 0; it < niter && ok; ++it) {
-          if (it + 1 < niter) {
-            // buffer (it+1)%2 was last used by it-1: its dQ^T halves must be drained
-            const int sn = (it + 1) % C::NQ;
-            if (!(ok = mbar_wait(&q_full[sn], ((it + 1) / C::NQ) & 1, a.status))) break;
-            if (kDQ && !(ok = mbar_wait(dq_empty, (it & 1) ^ 1, a.status))) break;
+        bool ok = mbar_wait(kv_full, 0, a.status);
+        if constexpr (C::NQ == 1) {
+          // one Q/dO stage: tile it's products, then tile it+1's
+          for (int it = 0; it < niter && ok; ++it) {
+            if (!(ok = mbar_wait(&q_full[0], it & 1, a.status))) break;
+            // buffer it%2 was last used by it-2, whose dQ^T was drained before it-1's
+            if (kDQ && it > 0 && !(ok = mbar_wait(dq_empty, (it - 1) & 1, a.status))) break;
             tc_fence_after();
-            issue_sdp(it + 1, 0);
+            issue_sdp(it, 0);
+            if (!(ok = ds_wait(it))) break;
+            tc_fence_after();
+            issue_grads(it, it, 0, 0);
           }
-          if (!(ok = ds_wait(it))) break;
-          // The drain warps wait on dq_full by parity. On the last tile there is
-          // no S^T/dP^T issue (and no dq_empty wait) above, so wait here for the
-          // drain of it-1: dq_full then never runs two phases ahead of them.
-          if (kDQ && it + 1 >= niter && it > 0 && !(ok = mbar_wait(dq_empty, (it & 1) ^ 1, a.status))) break;
-          tc_fence_after();
-          issue_grads(it, it, 0, 0);
-        }
-      }
-      mma_commit(done);
-      } else {
-      // Persistent walk (several Q/dO stages): tiles are counted over the
-      // whole walk (g), so the order within a unit is the one above. With
-      // two K/V buffers, at a unit's last tile the next unit's first
-      // S^T/dP^T (from the other buffer) is issued before the last tile's
-      // gradients, so its softmax overlaps them; with one, the next unit's
-      // K and V load once the last products have read the buffer.
-      static_assert(C::NQ > 1, "persistent walk with several Q/dO stages");
-      constexpr bool kAhead = C::NKV > 1;
-      int gt = 0;             // tiles of the earlier units
-      bool ok = true;
-      bool first_issued = false;   // this unit's first S^T/dP^T went out with the previous unit
-      for (int k = 0; ok; ++k) {
-        if (k > 0 && !more_units(k)) break;
-        const uint32_t kvo = (k % C::NKV) * 2 * C::KV_B;
-        const bool more = kAhead && more_units(k + 1);
-        if (!first_issued) {
-          ok = mbar_wait(&kv_full[k % C::NKV], (k / C::NKV) & 1, a.status) &&
-               mbar_wait(&q_full[gt % C::NQ], (gt / C::NQ) & 1, a.status);
+        } else {
+          ok = ok && mbar_wait(&q_full[0], 0, a.status);
           if (ok) {
             tc_fence_after();
-            issue_sdp(gt, kvo);
+            issue_sdp(0, 0);
           }
-        }
-        first_issued = false;
-        for (int it = 0; it < niter && ok; ++it) {
-          const int g = gt + it;
-          const bool last = it + 1 >= niter;
-          if (!last || more) {
-            // tile g+1: this unit's next, or the next unit's first
-            if (last && !(ok = mbar_wait(&kv_full[(k + 1) % C::NKV], ((k + 1) / C::NKV) & 1, a.status))) break;
-            const int sn = (g + 1) % C::NQ;
-            if (!(ok = mbar_wait(&q_full[sn], ((g + 1) / C::NQ) & 1, a.status))) break;
-            // buffer (g+1)%2 was last used by g-1: its dQ^T halves must be drained
-            if (kDQ && !(ok = mbar_wait(dq_empty, (g & 1) ^ 1, a.status))) break;
+          for (int it = 0; it < niter && ok; ++it) {
+            if (it + 1 < niter) {
+              // buffer (it+1)%2 was last used by it-1: its dQ^T halves must be drained
+              const int sn = (it + 1) % C::NQ;
+              if (!(ok = mbar_wait(&q_full[sn], ((it + 1) / C::NQ) & 1, a.status))) break;
+              if (kDQ && !(ok = mbar_wait(dq_empty, (it & 1) ^ 1, a.status))) break;
+              tc_fence_after();
+              issue_sdp(it + 1, 0);
+            }
+            if (!(ok = ds_wait(it))) break;
+            // The drain warps wait on dq_full by parity. On the last tile there is
+            // no S^T/dP^T issue (and no dq_empty wait) above, so wait here for the
+            // drain of it-1: dq_full then never runs two phases ahead of them.
+            if (kDQ && it + 1 >= niter && it > 0 && !(ok = mbar_wait(dq_empty, (it & 1) ^ 1, a.status))) break;
             tc_fence_after();
-            issue_sdp(g + 1, last ? ((k + 1) % C::NKV) * 2 * C::KV_B : kvo);
-            first_issued = last;
+            issue_grads(it, it, 0, 0);
           }
-          if (!(ok = ds_wait(g))) break;
-          // a unit's last tile without the next unit's first products above:
-          // as in the single-unit loop, the drain of g-1 first
-          if (kDQ && last && !more && g > 0 && !(ok = mbar_wait(dq_empty, (g & 1) ^ 1, a.status))) break;
-          tc_fence_after();
-          ok = issue_grads(g, it, k, kvo);
         }
         mma_commit(done);
-        mma_commit(&kv_empty[k % C::NKV]);
-        gt += niter;
+      } else {
+        // Persistent walk (several Q/dO stages): tiles are counted over the
+        // whole walk (g), so the order within a unit is the one above. With
+        // two K/V buffers, at a unit's last tile the next unit's first
+        // S^T/dP^T (from the other buffer) is issued before the last tile's
+        // gradients, so its softmax overlaps them; with one, the next unit's
+        // K and V load once the last products have read the buffer.
+        static_assert(C::NQ > 1, "persistent walk with several Q/dO stages");
+        constexpr bool kAhead = C::NKV > 1;
+        int gt = 0;             // tiles of the earlier units
+        bool ok = true;
+        bool first_issued = false;   // this unit's first S^T/dP^T went out with the previous unit
+        for (int k = 0; ok; ++k) {
+          if (k > 0 && !more_units(k)) break;
+          const uint32_t kvo = (k % C::NKV) * 2 * C::KV_B;
+          const bool more = kAhead && more_units(k + 1);
+          if (!first_issued) {
+            ok = mbar_wait(&kv_full[k % C::NKV], (k / C::NKV) & 1, a.status) &&
+                 mbar_wait(&q_full[gt % C::NQ], (gt / C::NQ) & 1, a.status);
+            if (ok) {
+              tc_fence_after();
+              issue_sdp(gt, kvo);
+            }
+          }
+          first_issued = false;
+          for (int it = 0; it < niter && ok; ++it) {
+            const int g = gt + it;
+            const bool last = it + 1 >= niter;
+            if (!last || more) {
+              // tile g+1: this unit's next, or the next unit's first
+              if (last && !(ok = mbar_wait(&kv_full[(k + 1) % C::NKV], ((k + 1) / C::NKV) & 1, a.status))) break;
+              const int sn = (g + 1) % C::NQ;
+              if (!(ok = mbar_wait(&q_full[sn], ((g + 1) / C::NQ) & 1, a.status))) break;
+              // buffer (g+1)%2 was last used by g-1: its dQ^T halves must be drained
+              if (kDQ && !(ok = mbar_wait(dq_empty, (g & 1) ^ 1, a.status))) break;
+              tc_fence_after();
+              issue_sdp(g + 1, last ? ((k + 1) % C::NKV) * 2 * C::KV_B : kvo);
+              first_issued = last;
+            }
+            if (!(ok = ds_wait(g))) break;
+            // a unit's last tile without the next unit's first products above:
+            // as in the single-unit loop, the drain of g-1 first
+            if (kDQ && last && !more && g > 0 && !(ok = mbar_wait(dq_empty, (g & 1) ^ 1, a.status))) break;
+            tc_fence_after();
+            ok = issue_grads(g, it, k, kvo);
+          }
+          mma_commit(done);
+          mma_commit(&kv_empty[k % C::NKV]);
+          gt += niter;
       }
       }
     }
@@ -634,148 +634,148 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     bool dq_ok = true;   // the wait for the previous tile's dQ^T ended in time
     int gt = 0;          // tiles of the earlier units
     for (int k = 0;; ++k) {
-    if (k > 0 && !next_unit(k)) break;
-    const int kloc = j * C::BC + r;                 // key position in the sequence
-    const bool kvalid = kloc < L;
-    for (int it = 0; it < niter; ++it) {
-      const int g = gt + it;
-      const uint32_t xb = tbase + lane_off + 128u * (g & 1);
-      uint8_t* ds_row = sDS + r * 128;
-      const int st = g % C::NQ;
-      // LSE and D of this stage (written by the load warp before it arrived
-      // on q_full[st]) go to registers first: these shared-memory reads then
-      // overlap the wait for S^T/dP^T instead of heading every exp2 chain
-      // while the tensor core's operand reads keep shared memory busy.
-      bool got = __all_sync(0xffffffffu, mbar_wait(&q_full[st], (g / C::NQ) & 1, a.status));
-      float4 l4r[8], d4r[8];
-      if (got) {
-        const float* nlse = sLD + st * 2 * C::BR + 32 * half;     // -LSE * log2(e)
-#pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          l4r[e4] = *reinterpret_cast<const float4*>(nlse + 4 * e4);
-          d4r[e4] = *reinterpret_cast<const float4*>(nlse + C::BR + 4 * e4);   // -D
-        }
-      }
-      if (got) got = __all_sync(0xffffffffu, mbar_wait(&sp_full[g & 1], (g >> 1) & 1, a.status));
-      got = got && dq_ok;   // a wait that ran out in the previous tile ends both groups here
-      uint32_t sv[32], dp[32];
-      if (got) {
-        tc_fence_after();
-        tmem_ld32(xb + C::COL_S + 32 * half, sv);
-        tmem_ld32(xb + C::COL_DP + 32 * half, dp);
-        tmem_wait_ld();
-        reg_fence(sv);
-        reg_fence(dp);
-      }
-      // D = 128: both groups have their scores in registers before either
-      // overwrites columns the other reads; one decision for both groups
-      if constexpr (!C::kOwnCols) ok = named_bar_and(2, 256, got);
-      else ok = got;
-      if (!ok) break;
-      const int q0 = q_tile(it) * C::BR + 32 * half;
-      // this key against queries q0 .. q0 + 31: outside the sequence or the window?
-      const bool edge = kPersist ? !kvalid
-                                 : !kvalid || (a.win_right >= 0 && kloc > q0 + a.win_right) ||
-                                       (a.win_left >= 0 && kloc < q0 + 31 - a.win_left);
-      uint32_t pp[16], dd[16];
-#pragma unroll
-      for (int e4 = 0; e4 < 8; ++e4) {
-        const float4 l4 = l4r[e4];
-        const float4 d4 = d4r[e4];
-        float2 x01 = ffma2(make_float2(__uint_as_float(sv[4 * e4]), __uint_as_float(sv[4 * e4 + 1])), sl2v,
-                           make_float2(l4.x, l4.y));
-        float2 x23 = ffma2(make_float2(__uint_as_float(sv[4 * e4 + 2]), __uint_as_float(sv[4 * e4 + 3])), sl2v,
-                           make_float2(l4.z, l4.w));
-        float p[4] = {ex2(x01.x), ex2(x01.y), ex2(x23.x), ex2(x23.y)};
-        if (edge) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int q = q0 + 4 * e4 + u;
-            if (!kvalid || (a.win_right >= 0 && kloc > q + a.win_right) || (a.win_left >= 0 && kloc < q - a.win_left))
-              p[u] = 0.f;
+      if (k > 0 && !next_unit(k)) break;
+      const int kloc = j * C::BC + r;                 // key position in the sequence
+      const bool kvalid = kloc < L;
+      for (int it = 0; it < niter; ++it) {
+        const int g = gt + it;
+        const uint32_t xb = tbase + lane_off + 128u * (g & 1);
+        uint8_t* ds_row = sDS + r * 128;
+        const int st = g % C::NQ;
+        // LSE and D of this stage (written by the load warp before it arrived
+        // on q_full[st]) go to registers first: these shared-memory reads then
+        // overlap the wait for S^T/dP^T instead of heading every exp2 chain
+        // while the tensor core's operand reads keep shared memory busy.
+        bool got = __all_sync(0xffffffffu, mbar_wait(&q_full[st], (g / C::NQ) & 1, a.status));
+        float4 l4r[8], d4r[8];
+        if (got) {
+          const float* nlse = sLD + st * 2 * C::BR + 32 * half;     // -LSE * log2(e)
+  #pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            l4r[e4] = *reinterpret_cast<const float4*>(nlse + 4 * e4);
+            d4r[e4] = *reinterpret_cast<const float4*>(nlse + C::BR + 4 * e4);   // -D
           }
         }
-        const float2 t01 = fadd2(make_float2(__uint_as_float(dp[4 * e4]), __uint_as_float(dp[4 * e4 + 1])),
-                                 make_float2(d4.x, d4.y));
-        const float2 t23 = fadd2(make_float2(__uint_as_float(dp[4 * e4 + 2]), __uint_as_float(dp[4 * e4 + 3])),
-                                 make_float2(d4.z, d4.w));
-        const float2 g01 = fmul2(make_float2(p[0], p[1]), t01);
-        const float2 g23 = fmul2(make_float2(p[2], p[3]), t23);
-        if constexpr (DT == kBF16) {
-          pp[2 * e4] = pack_bf16x2(p[0], p[1]);
-          pp[2 * e4 + 1] = pack_bf16x2(p[2], p[3]);
-          dd[2 * e4] = pack_bf16x2(g01.x, g01.y);
-          dd[2 * e4 + 1] = pack_bf16x2(g23.x, g23.y);
-        } else {
-          pp[2 * e4] = pack_f16x2(p[0], p[1]);
-          pp[2 * e4 + 1] = pack_f16x2(p[2], p[3]);
-          dd[2 * e4] = pack_f16x2(g01.x, g01.y);
-          dd[2 * e4 + 1] = pack_f16x2(g23.x, g23.y);
+        if (got) got = __all_sync(0xffffffffu, mbar_wait(&sp_full[g & 1], (g >> 1) & 1, a.status));
+        got = got && dq_ok;   // a wait that ran out in the previous tile ends both groups here
+        uint32_t sv[32], dp[32];
+        if (got) {
+          tc_fence_after();
+          tmem_ld32(xb + C::COL_S + 32 * half, sv);
+          tmem_ld32(xb + C::COL_DP + 32 * half, dp);
+          tmem_wait_ld();
+          reg_fence(sv);
+          reg_fence(dp);
+        }
+        // D = 128: both groups have their scores in registers before either
+        // overwrites columns the other reads; one decision for both groups
+        if constexpr (!C::kOwnCols) ok = named_bar_and(2, 256, got);
+        else ok = got;
+        if (!ok) break;
+        const int q0 = q_tile(it) * C::BR + 32 * half;
+        // this key against queries q0 .. q0 + 31: outside the sequence or the window?
+        const bool edge = kPersist ? !kvalid
+                                   : !kvalid || (a.win_right >= 0 && kloc > q0 + a.win_right) ||
+                                         (a.win_left >= 0 && kloc < q0 + 31 - a.win_left);
+        uint32_t pp[16], dd[16];
+  #pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 l4 = l4r[e4];
+          const float4 d4 = d4r[e4];
+          float2 x01 = ffma2(make_float2(__uint_as_float(sv[4 * e4]), __uint_as_float(sv[4 * e4 + 1])), sl2v,
+                             make_float2(l4.x, l4.y));
+          float2 x23 = ffma2(make_float2(__uint_as_float(sv[4 * e4 + 2]), __uint_as_float(sv[4 * e4 + 3])), sl2v,
+                             make_float2(l4.z, l4.w));
+          float p[4] = {ex2(x01.x), ex2(x01.y), ex2(x23.x), ex2(x23.y)};
+          if (edge) {
+  #pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int q = q0 + 4 * e4 + u;
+              if (!kvalid || (a.win_right >= 0 && kloc > q + a.win_right) || (a.win_left >= 0 && kloc < q - a.win_left))
+                p[u] = 0.f;
+            }
+          }
+          const float2 t01 = fadd2(make_float2(__uint_as_float(dp[4 * e4]), __uint_as_float(dp[4 * e4 + 1])),
+                                   make_float2(d4.x, d4.y));
+          const float2 t23 = fadd2(make_float2(__uint_as_float(dp[4 * e4 + 2]), __uint_as_float(dp[4 * e4 + 3])),
+                                   make_float2(d4.z, d4.w));
+          const float2 g01 = fmul2(make_float2(p[0], p[1]), t01);
+          const float2 g23 = fmul2(make_float2(p[2], p[3]), t23);
+          if constexpr (DT == kBF16) {
+            pp[2 * e4] = pack_bf16x2(p[0], p[1]);
+            pp[2 * e4 + 1] = pack_bf16x2(p[2], p[3]);
+            dd[2 * e4] = pack_bf16x2(g01.x, g01.y);
+            dd[2 * e4 + 1] = pack_bf16x2(g23.x, g23.y);
+          } else {
+            pp[2 * e4] = pack_f16x2(p[0], p[1]);
+            pp[2 * e4 + 1] = pack_f16x2(p[2], p[3]);
+            dd[2 * e4] = pack_f16x2(g01.x, g01.y);
+            dd[2 * e4 + 1] = pack_f16x2(g23.x, g23.y);
+          }
+        }
+        tmem_st16(xb + C::col_p(2 * half), pp);
+        tmem_st16(xb + C::col_ds(2 * half), dd);
+        // dS^T row r, queries 32*half .. +31: 16-byte chunks 4*half .. +3 of a
+        // 128-byte row, 128-byte swizzle (chunk ^= row % 8). The single dS^T
+        // tile is read by dQ^T of the previous tile, which must be complete
+        // first; waiting only here lets this tile's exponentials overlap it.
+        if constexpr (kDQ) {
+          if (g > 0) dq_ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (g - 1) & 1, a.status));
+  #pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const int chunk = (4 * half + c4) ^ (r & 7);
+            *reinterpret_cast<uint4*>(ds_row + chunk * 16) =
+                make_uint4(dd[4 * c4], dd[4 * c4 + 1], dd[4 * c4 + 2], dd[4 * c4 + 3]);
+          }
+        }
+        tmem_wait_st();
+        if constexpr (kDQ) fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(C::kOwnCols ? &ds_ready[(g & 1) * 2 + half] : &ds_ready[0]);
+      }
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(done, k & 1, a.status));
+      tc_fence_after();
+      // dV rows, this CTA's columns, DH/2 per group. With a split walk part 1
+      // hands its dV to part 0 (between the two cluster barriers, once both
+      // parts' products are complete and part 0's shared memory is idle), and
+      // part 0 stores the sum.
+      const float* add = nullptr;
+      if (kSplit && nsplit > 1) {
+        cluster_sync_all();
+        if (ok && wp == 1) split_handover<C>(smem, tbase + lane_off + C::COL_DV, r, half * (C::DH / 64),
+                                             (half + 1) * (C::DH / 64), 0);
+        cluster_sync_all();
+        add = reinterpret_cast<const float*>(smem);
+      }
+      if (ok && wp == 0) {
+        const long long off = kPersist ? persist_key_off(k, r)
+                                       : static_cast<long long>(b) * a.k_sb + static_cast<long long>(hkv) * a.k_sh +
+                                             static_cast<long long>(seq0 + kloc) * a.k_sn;
+  #pragma unroll 1
+        for (int c = half * (C::DH / 64); c < (half + 1) * (C::DH / 64); ++c) {
+          uint32_t v[32];
+          tmem_ld32(tbase + lane_off + C::COL_DV + 32 * c, v);
+          tmem_wait_ld();
+          reg_fence(v);
+          if (kSplit && add) split_add<C>(v, add, r, c);
+          uint32_t pk[16];
+  #pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = (DT == kBF16) ? pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]))
+                                  : pack_f16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+          if (kvalid) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dv) + off + dh * C::DH + 32 * c);
+  #pragma unroll
+            for (int w = 0; w < 4; ++w) dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+          }
         }
       }
-      tmem_st16(xb + C::col_p(2 * half), pp);
-      tmem_st16(xb + C::col_ds(2 * half), dd);
-      // dS^T row r, queries 32*half .. +31: 16-byte chunks 4*half .. +3 of a
-      // 128-byte row, 128-byte swizzle (chunk ^= row % 8). The single dS^T
-      // tile is read by dQ^T of the previous tile, which must be complete
-      // first; waiting only here lets this tile's exponentials overlap it.
-      if constexpr (kDQ) {
-        if (g > 0) dq_ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (g - 1) & 1, a.status));
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          const int chunk = (4 * half + c4) ^ (r & 7);
-          *reinterpret_cast<uint4*>(ds_row + chunk * 16) =
-              make_uint4(dd[4 * c4], dd[4 * c4 + 1], dd[4 * c4 + 2], dd[4 * c4 + 3]);
-        }
+      if constexpr (kPersist) {   // dV is read out: the next unit may start it
+        tc_fence_before();
+        mbar_arrive(acc_empty);
       }
-      tmem_wait_st();
-      if constexpr (kDQ) fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(C::kOwnCols ? &ds_ready[(g & 1) * 2 + half] : &ds_ready[0]);
-    }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(done, k & 1, a.status));
-    tc_fence_after();
-    // dV rows, this CTA's columns, DH/2 per group. With a split walk part 1
-    // hands its dV to part 0 (between the two cluster barriers, once both
-    // parts' products are complete and part 0's shared memory is idle), and
-    // part 0 stores the sum.
-    const float* add = nullptr;
-    if (kSplit && nsplit > 1) {
-      cluster_sync_all();
-      if (ok && wp == 1) split_handover<C>(smem, tbase + lane_off + C::COL_DV, r, half * (C::DH / 64),
-                                           (half + 1) * (C::DH / 64), 0);
-      cluster_sync_all();
-      add = reinterpret_cast<const float*>(smem);
-    }
-    if (ok && wp == 0) {
-      const long long off = kPersist ? persist_key_off(k, r)
-                                     : static_cast<long long>(b) * a.k_sb + static_cast<long long>(hkv) * a.k_sh +
-                                           static_cast<long long>(seq0 + kloc) * a.k_sn;
-#pragma unroll 1
-      for (int c = half * (C::DH / 64); c < (half + 1) * (C::DH / 64); ++c) {
-        uint32_t v[32];
-        tmem_ld32(tbase + lane_off + C::COL_DV + 32 * c, v);
-        tmem_wait_ld();
-        reg_fence(v);
-        if (kSplit && add) split_add<C>(v, add, r, c);
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pk[e] = (DT == kBF16) ? pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]))
-                                : pack_f16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
-        if (kvalid) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dv) + off + dh * C::DH + 32 * c);
-#pragma unroll
-          for (int w = 0; w < 4; ++w) dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
-        }
-      }
-    }
-    if constexpr (kPersist) {   // dV is read out: the next unit may start it
-      tc_fence_before();
-      mbar_arrive(acc_empty);
-    }
-    if (!ok || !kPersist) break;
-    gt += niter;
+      if (!ok || !kPersist) break;
+      gt += niter;
     }
   } else {
     regs_dec<C::kRegsDrain>();
@@ -786,103 +786,103 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     bool ok = true;
     int gt = 0;   // tiles of the earlier units
     for (int k = 0;; ++k) {
-    if (k > 0 && !next_unit(k)) break;
-    for (int it = 0; it < (kDQ ? niter : 0); ++it) {
-      const int g = gt + it;
-      // one decision for all four drain warps, so none is left alone at the
-      // named barriers below
-      ok = named_bar_and(1, 128, __all_sync(0xffffffffu, mbar_wait(dq_full, g & 1, a.status)));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t x0[32], x1[32];
-      tmem_ld32(tbase + lane_off + 128u * (g & 1) + C::COL_DQ, x0);
-      tmem_ld32(tbase + lane_off + 128u * (g & 1) + C::COL_DQ + 32, x1);
-      tmem_wait_ld();
-      reg_fence(x0);
-      reg_fence(x1);
-      tc_fence_before();
-      mbar_arrive(dq_empty);
-      const int h = q_head(it);
-      const int q0 = q_tile(it) * C::BR;
-      // reduce-adds of DQ_ROWS rows through one FP32 staging buffer; rows past
-      // the sequence hold exact zeros (P = 0 there): for the dense layout the
-      // map clips them, for the packed layout they add 0 to the next
-      // sequence's rows
-#pragma unroll
-      for (int part = 0; part < C::DQ_PARTS; ++part) {
-        if (threadIdx.x == 256) bulk_wait_read_all();   // previous reduce-add has read the buffer
-        named_bar_sync(1, 128);
-        if (quarter * 32 < C::DH) {                     // D = 64: lanes 64..127 are not dQ
-          // row q of the staging tile holds dQ of query q; lane l's value of
-          // query q goes to word 32 * quarter + l of that row: four queries
-          // per stmatrix, lane l addressing query +l/8, words +4(l%8) .. +3
-          const uint32_t row = smem_u32(sDQ) + ((lane >> 3) * C::DH + quarter * 32 + 4 * (lane & 7)) * 4;
-          if constexpr (C::DQ_PARTS == 2) {
-            const uint32_t(&x)[32] = part == 0 ? x0 : x1;
-#pragma unroll
-            for (int g = 0; g < 8; ++g)
-              stmatrix_x4(row + 16 * g * C::DH, x[4 * g], x[4 * g + 1], x[4 * g + 2], x[4 * g + 3]);
-          } else {
-#pragma unroll
-            for (int g = 0; g < 8; ++g) {
-              stmatrix_x4(row + 16 * g * C::DH, x0[4 * g], x0[4 * g + 1], x0[4 * g + 2], x0[4 * g + 3]);
-              stmatrix_x4(row + 16 * (g + 8) * C::DH, x1[4 * g], x1[4 * g + 1], x1[4 * g + 2], x1[4 * g + 3]);
+      if (k > 0 && !next_unit(k)) break;
+      for (int it = 0; it < (kDQ ? niter : 0); ++it) {
+        const int g = gt + it;
+        // one decision for all four drain warps, so none is left alone at the
+        // named barriers below
+        ok = named_bar_and(1, 128, __all_sync(0xffffffffu, mbar_wait(dq_full, g & 1, a.status)));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t x0[32], x1[32];
+        tmem_ld32(tbase + lane_off + 128u * (g & 1) + C::COL_DQ, x0);
+        tmem_ld32(tbase + lane_off + 128u * (g & 1) + C::COL_DQ + 32, x1);
+        tmem_wait_ld();
+        reg_fence(x0);
+        reg_fence(x1);
+        tc_fence_before();
+        mbar_arrive(dq_empty);
+        const int h = q_head(it);
+        const int q0 = q_tile(it) * C::BR;
+        // reduce-adds of DQ_ROWS rows through one FP32 staging buffer; rows past
+        // the sequence hold exact zeros (P = 0 there): for the dense layout the
+        // map clips them, for the packed layout they add 0 to the next
+        // sequence's rows
+  #pragma unroll
+        for (int part = 0; part < C::DQ_PARTS; ++part) {
+          if (threadIdx.x == 256) bulk_wait_read_all();   // previous reduce-add has read the buffer
+          named_bar_sync(1, 128);
+          if (quarter * 32 < C::DH) {                     // D = 64: lanes 64..127 are not dQ
+            // row q of the staging tile holds dQ of query q; lane l's value of
+            // query q goes to word 32 * quarter + l of that row: four queries
+            // per stmatrix, lane l addressing query +l/8, words +4(l%8) .. +3
+            const uint32_t row = smem_u32(sDQ) + ((lane >> 3) * C::DH + quarter * 32 + 4 * (lane & 7)) * 4;
+            if constexpr (C::DQ_PARTS == 2) {
+              const uint32_t(&x)[32] = part == 0 ? x0 : x1;
+  #pragma unroll
+              for (int g = 0; g < 8; ++g)
+                stmatrix_x4(row + 16 * g * C::DH, x[4 * g], x[4 * g + 1], x[4 * g + 2], x[4 * g + 3]);
+            } else {
+  #pragma unroll
+              for (int g = 0; g < 8; ++g) {
+                stmatrix_x4(row + 16 * g * C::DH, x0[4 * g], x0[4 * g + 1], x0[4 * g + 2], x0[4 * g + 3]);
+                stmatrix_x4(row + 16 * (g + 8) * C::DH, x1[4 * g], x1[4 * g + 1], x1[4 * g + 2], x1[4 * g + 3]);
+              }
             }
           }
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (threadIdx.x == 256) {
-          const int row = q0 + C::DQ_ROWS * part;
-          if (packed) tma_reduce_add_4d(&tmdQ, sDQ, dh * C::DH, h, seq0 + row, 0);
-          else tma_reduce_add_4d(&tmdQ, sDQ, dh * C::DH, row, h, b);
-          bulk_commit();
-        }
-      }
-    }
-    if (!kPersist && threadIdx.x == 256) bulk_wait_all();
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(done, k & 1, a.status));
-    tc_fence_after();
-    // dK rows (here the lane indexes keys), times scale; a split walk's part 1
-    // hands its dK to part 0 as for dV
-    const float* add = nullptr;
-    if (kSplit && nsplit > 1) {
-      cluster_sync_all();
-      if (ok && wp == 1) split_handover<C>(smem, tbase + lane_off + C::COL_DK, dim, 0, C::DH / 32, C::BC * C::DH);
-      cluster_sync_all();
-      add = reinterpret_cast<const float*>(smem) + C::BC * C::DH;
-    }
-    if (ok && wp == 0) {
-      const int kloc = kPersist ? persist_key_row(k, dim) : j * C::BC + dim;
-      const long long off = kPersist ? persist_key_off(k, dim)
-                                     : static_cast<long long>(b) * a.k_sb + static_cast<long long>(hkv) * a.k_sh +
-                                           static_cast<long long>(seq0 + kloc) * a.k_sn;
-#pragma unroll 1
-      for (int c = 0; c < C::DH / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tbase + lane_off + C::COL_DK + 32 * c, v);
-        tmem_wait_ld();
-        reg_fence(v);
-        if (kSplit && add) split_add<C>(v, add, dim, c);
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float x0 = __uint_as_float(v[2 * e]) * a.scale, x1 = __uint_as_float(v[2 * e + 1]) * a.scale;
-          pk[e] = (DT == kBF16) ? pack_bf16x2(x0, x1) : pack_f16x2(x0, x1);
-        }
-        if (kloc < L) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dk) + off + dh * C::DH + 32 * c);
-#pragma unroll
-          for (int w = 0; w < 4; ++w) dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+          fence_proxy_async_smem();
+          named_bar_sync(1, 128);
+          if (threadIdx.x == 256) {
+            const int row = q0 + C::DQ_ROWS * part;
+            if (packed) tma_reduce_add_4d(&tmdQ, sDQ, dh * C::DH, h, seq0 + row, 0);
+            else tma_reduce_add_4d(&tmdQ, sDQ, dh * C::DH, row, h, b);
+            bulk_commit();
+          }
         }
       }
-    }
-    if constexpr (kPersist) {   // dK is read out: the next unit may start it
-      tc_fence_before();
-      mbar_arrive(acc_empty);
-    }
-    if (!ok || !kPersist) break;
-    gt += niter;
+      if (!kPersist && threadIdx.x == 256) bulk_wait_all();
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(done, k & 1, a.status));
+      tc_fence_after();
+      // dK rows (here the lane indexes keys), times scale; a split walk's part 1
+      // hands its dK to part 0 as for dV
+      const float* add = nullptr;
+      if (kSplit && nsplit > 1) {
+        cluster_sync_all();
+        if (ok && wp == 1) split_handover<C>(smem, tbase + lane_off + C::COL_DK, dim, 0, C::DH / 32, C::BC * C::DH);
+        cluster_sync_all();
+        add = reinterpret_cast<const float*>(smem) + C::BC * C::DH;
+      }
+      if (ok && wp == 0) {
+        const int kloc = kPersist ? persist_key_row(k, dim) : j * C::BC + dim;
+        const long long off = kPersist ? persist_key_off(k, dim)
+                                       : static_cast<long long>(b) * a.k_sb + static_cast<long long>(hkv) * a.k_sh +
+                                             static_cast<long long>(seq0 + kloc) * a.k_sn;
+  #pragma unroll 1
+        for (int c = 0; c < C::DH / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tbase + lane_off + C::COL_DK + 32 * c, v);
+          tmem_wait_ld();
+          reg_fence(v);
+          if (kSplit && add) split_add<C>(v, add, dim, c);
+          uint32_t pk[16];
+  #pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float x0 = __uint_as_float(v[2 * e]) * a.scale, x1 = __uint_as_float(v[2 * e + 1]) * a.scale;
+            pk[e] = (DT == kBF16) ? pack_bf16x2(x0, x1) : pack_f16x2(x0, x1);
+          }
+          if (kloc < L) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dk) + off + dh * C::DH + 32 * c);
+  #pragma unroll
+            for (int w = 0; w < 4; ++w) dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+          }
+        }
+      }
+      if constexpr (kPersist) {   // dK is read out: the next unit may start it
+        tc_fence_before();
+        mbar_arrive(acc_empty);
+      }
+      if (!ok || !kPersist) break;
+      gt += niter;
     }
     if (kPersist && threadIdx.x == 256) bulk_wait_all();
   }
