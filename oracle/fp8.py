@@ -233,7 +233,7 @@ def quantize_tensor(x, signs=None, block=BLOCK):
 
 
 def _fp8_rows(qrows, q_fac, kf, vf, sk, sv, tiles, n, scale, causal=False, rows=None, block=BLOCK, p_shift=4,
-              tau=0.0, kv_tile=None, round_p=True, bound=False):
+              tau=0.0, kv_tile=None, round_p=True, bound=False, window=None):
     """Algorithm 1 in its FP8 form for query rows ``qrows`` [R, d] (decoded,
     with per-row factors q_fac) over the key tiles ``tiles`` (indices of tiles
     of kv_tile keys, in order) of one KV head: kf/vf [N, d] decoded, sk/sv the
@@ -243,8 +243,12 @@ def _fp8_rows(qrows, q_fac, kf, vf, sk, sv, tiles, n, scale, causal=False, rows=
     ``round_p=False`` leaves out the E4M3 rounding of P~ (for pins: the rest
     is then exact). Returns (O [R, d], LSE [R]); with ``bound`` also E [R, d],
     the sum over keys of each rounded entry's half_step times |V|, carried
-    through the same corrections as O: |O - O_unrounded| <= E elementwise."""
+    through the same corrections as O: |O - O_unrounded| <= E elementwise.
+    ``window`` (left, right): key j is visible to row i iff i - left <= j <=
+    i + right, -1 leaving that side open; causal is (-1, 0). Keys outside it
+    get the score -inf, as causal masking does."""
     kv_tile = block if kv_tile is None else kv_tile
+    left, right = window if window is not None else ((-1, 0) if causal else (-1, -1))
     d = qrows.shape[1]
     m = np.full(len(qrows), -np.inf)
     l = np.zeros(len(qrows))
@@ -255,8 +259,10 @@ def _fp8_rows(qrows, q_fac, kf, vf, sk, sv, tiles, n, scale, causal=False, rows=
         cols = np.arange(j * kv_tile, min(n, (j + 1) * kv_tile))
         blk = cols // block
         s = scale * q_fac[:, None] * sk[blk][None, :] * (qrows @ kf[cols].T)
-        if causal:
-            s = np.where(cols[None, :] > rows[:, None], -np.inf, s)
+        if right >= 0:
+            s = np.where(cols[None, :] > rows[:, None] + right, -np.inf, s)
+        if left >= 0:
+            s = np.where(cols[None, :] < rows[:, None] - left, -np.inf, s)
         mx = s.max(axis=1)
         m_new = np.where(mx > m + tau * np.log(2.0), mx, m)   # tau = 0: the running max itself
         m_use = np.where(np.isfinite(m_new), m_new, 0.0)
@@ -280,7 +286,7 @@ def _fp8_rows(qrows, q_fac, kf, vf, sk, sv, tiles, n, scale, causal=False, rows=
 
 
 def attention_fp8(q8, k8, v8, sq, sk, sv, scale, causal=False, block=BLOCK, p_shift=4, tau=0.0, heads=None,
-                  rows=None, kv_tile=None, round_p=True, bound=False):
+                  rows=None, kv_tile=None, round_p=True, bound=False, window=None):
     """FP8 forward following Algorithm 1 tile by tile (Bc = kv_tile keys per
     tile, by default the quantisation block; the stale max and the V exponent
     F move at tile granularity, so the E4M3 rounding of P~ depends on it).
@@ -294,6 +300,7 @@ def attention_fp8(q8, k8, v8, sq, sk, sv, scale, causal=False, block=BLOCK, p_sh
     ``tau`` = 0 is the running max of Algorithm 1; STALE_MAX_TAU the stale-max
     variant. With ``bound`` a third array E (like O) bounds the effect of the
     E4M3 rounding of P~: |O - O(round_p=False)| <= E elementwise.
+    ``window`` (left, right) as in ``_fp8_rows`` (it replaces ``causal``).
     """
     qf, kf, vf = e4m3_decode(q8), e4m3_decode(k8), e4m3_decode(v8)
     sq, sk, sv = (np.asarray(a, dtype=np.float64) for a in (sq, sk, sv))
@@ -309,7 +316,8 @@ def attention_fp8(q8, k8, v8, sq, sk, sv, scale, causal=False, block=BLOCK, p_sh
         kv = h // g
         o[b, h, rows], lse[b, h, rows], e[b, h, rows] = _fp8_rows(
             qf[b, h, rows], sq[b, h, rows // block], kf[b, kv], vf[b, kv], sk[b, kv], sv[b, kv],
-            range((n + kvt - 1) // kvt), n, scale, causal, rows, block, p_shift, tau, kvt, round_p, bound=True)
+            range((n + kvt - 1) // kvt), n, scale, causal, rows, block, p_shift, tau, kvt, round_p, bound=True,
+            window=window)
     return (o, lse, e) if bound else (o, lse)
 
 

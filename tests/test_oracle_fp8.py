@@ -217,6 +217,37 @@ def test_fp8_emulation_without_p_rounding_is_exact_attention(kv_tile, causal):
     np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-10 * np.abs(o_ref).max())
 
 
+@pytest.mark.parametrize("kv_tile", [None, 64])
+@pytest.mark.parametrize("window", [(0, 0), (3, 0), (130, 5), (-1, 40), (64, 64), (300, -1)])
+def test_fp8_emulation_with_window_without_p_rounding_is_exact_attention(window, kv_tile):
+    """The key window in the FP8 emulation: without the E4M3 rounding of P~
+    it must give float64 windowed attention of the dequantised inputs (keys
+    outside the window contribute nothing, rows whose visible keys start or
+    end inside a tile are handled exactly)."""
+    from exact_attention_73_gb300 import inputs
+    n, d = 300, 64
+    q, k, v = _blocky(23, (1, 4, n, d)), _blocky(24, (1, 2, n, d)), _blocky(25, (1, 2, n, d))
+    signs = inputs.random_signs(4, d).numpy()
+    (q8, sq), (k8, sk), (v8, sv) = F.quantize_blocks(q, signs), F.quantize_blocks(k, signs), F.quantize_blocks(v)
+    o, lse = F.attention_fp8(q8, k8, v8, sq, sk, sv, d ** -0.5, kv_tile=kv_tile, round_p=False, window=window)
+    o_ref, l_ref = A.forward(_dequantised(q8, sq), _dequantised(k8, sk), _dequantised(v8, sv), d ** -0.5, False,
+                             window)
+    np.testing.assert_allclose(lse, l_ref, rtol=0, atol=1e-10)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-10 * np.abs(o_ref).max())
+
+
+def test_fp8_emulation_causal_is_the_window_minus1_0():
+    """Causal masking is the window (-1, 0): identical emulation results,
+    with the E4M3 rounding of P~ and the stale max."""
+    n, d = 200, 64
+    q, k, v = _blocky(26, (1, 2, n, d)), _blocky(27, (1, 2, n, d)), _blocky(28, (1, 2, n, d))
+    codes = F.quantize_blocks(q), F.quantize_blocks(k), F.quantize_blocks(v)
+    args = (codes[0][0], codes[1][0], codes[2][0], codes[0][1], codes[1][1], codes[2][1], d ** -0.5)
+    oc, lc = F.attention_fp8(*args, True, tau=F.STALE_MAX_TAU)
+    ow, lw = F.attention_fp8(*args, False, tau=F.STALE_MAX_TAU, window=(-1, 0))
+    assert np.array_equal(oc, ow) and np.array_equal(lc, lw)
+
+
 def test_decode_without_p_rounding_is_exact_attention():
     """The split decode with the E4M3 rounding of P~ left out: float64
     attention of the g query rows over each sequence's valid keys, whatever

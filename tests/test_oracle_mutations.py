@@ -138,8 +138,10 @@ FP8_MUTANTS = {
     "Q factor dropped from the scores": ("s = scale * q_fac[:, None] * sk[blk][None, :] * (qrows @ kf[cols].T)",
                                          "s = scale * sk[blk][None, :] * (qrows @ kf[cols].T)"),
     "each tile takes its first key's block": ("blk = cols // block", "blk = np.full(len(cols), cols[0] // block)"),
-    "causal mask off by one": ("s = np.where(cols[None, :] > rows[:, None], -np.inf, s)",
-                               "s = np.where(cols[None, :] >= rows[:, None], -np.inf, s)"),
+    "causal mask off by one": ("s = np.where(cols[None, :] > rows[:, None] + right, -np.inf, s)",
+                               "s = np.where(cols[None, :] >= rows[:, None] + right, -np.inf, s)"),
+    "window's left bound off by one": ("s = np.where(cols[None, :] < rows[:, None] - left, -np.inf, s)",
+                                       "s = np.where(cols[None, :] <= rows[:, None] - left, -np.inf, s)"),
     "O not rescaled when F grows": ("v_corr = np.exp2(f_run - f_new)", "v_corr = 1.0"),
     "F correction with the wrong sign": ("v_corr = np.exp2(f_run - f_new)", "v_corr = np.exp2(f_new - f_run)"),
     "row max correction with the wrong sign": ("corr = np.exp(m - m_use)", "corr = np.exp(m_use - m)"),
