@@ -28,7 +28,8 @@ EXPORTS = ("attn_status_string", "attn_version", "attn_fwd", "attn_fwd_varlen", 
            "attn_bwd_varlen", "attn_get_device_status", "attn_bwd_noalloc", "attn_selftest_wait_timeout",
            "attn_fwd_window", "attn_bwd_window", "attn_bwd_deterministic_workspace_size",
            "attn_bwd_deterministic", "attn_quantize_fp8_rope", "attn_decode_fp8_workspace_size",
-           "attn_decode_fp8", "attn_fwd_fp8_kv_tile", "attn_quantize_fp8_varlen", "attn_fwd_fp8_varlen")
+           "attn_decode_fp8", "attn_fwd_fp8_kv_tile", "attn_quantize_fp8_varlen", "attn_fwd_fp8_varlen",
+           "attn_fwd_fp8_window")
 
 
 class AttnError(RuntimeError):
@@ -45,6 +46,7 @@ _SIGS = {
     "attn_fwd_varlen": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P], _I),
     "attn_quantize_fp8": ([_P, _I, _P, _P, _I, _I, _I, _I, _P, _P], _I),
     "attn_fwd_fp8": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P], _I),
+    "attn_fwd_fp8_window": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P], _I),
     "attn_fwd_fp8_kv_tile": ([_I], _I),
     "attn_bwd_workspace_size": ([_I, _I, _I, _I, _I], _Z),
     "attn_bwd": ([_P] * 9 + [_P, _Z, _I, _I, _I, _I, _I, _F, _I, _I, _P], _I),
@@ -249,18 +251,34 @@ def attn_quantize_fp8_rope(x, x8, scales, rope_cos, rope_sin, hadamard_signs=Non
            "attn_quantize_fp8_rope")
 
 
-def attn_fwd_fp8(q8, k8, v8, sq, sk, sv, o, lse, scale=None, causal=False, stream=None):
-    """FP8 forward on E4M3 codes (uint8) with block factors; o bf16, lse fp32."""
+def _fp8_ptrs(q8, k8, v8, sq, sk, sv, o, lse):
+    """Checked pointers of a dense FP8 forward and its sizes (B, Hq, Hkv, N, d)."""
     B, Hq, N, d = _dims(q8, "q8", 4)
     Hkv = _dims(k8, "k8", 4)[1]
     kv = (B, Hkv, N, d)
     u8, f32 = torch.uint8, torch.float32
+    ptrs = (_ptr(q8, "q8", dtype=u8), _ptr(k8, "k8", dtype=u8, shape=kv), _ptr(v8, "v8", dtype=u8, shape=kv),
+            _ptr(sq, "sq", B * Hq * _nb(N), f32), _ptr(sk, "sk", B * Hkv * _nb(N), f32),
+            _ptr(sv, "sv", B * Hkv * _nb(N), f32), _ptr(o, "o", q8.numel(), torch.bfloat16),
+            _ptr(lse, "lse", B * Hq * N, f32))
+    return ptrs, (B, Hq, Hkv, N, d)
+
+
+def attn_fwd_fp8(q8, k8, v8, sq, sk, sv, o, lse, scale=None, causal=False, stream=None):
+    """FP8 forward on E4M3 codes (uint8) with block factors; o bf16, lse fp32."""
+    ptrs, dims = _fp8_ptrs(q8, k8, v8, sq, sk, sv, o, lse)
+    d = dims[-1]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
-    _check(load().attn_fwd_fp8(_ptr(q8, "q8", dtype=u8), _ptr(k8, "k8", dtype=u8, shape=kv),
-                               _ptr(v8, "v8", dtype=u8, shape=kv), _ptr(sq, "sq", B * Hq * _nb(N), f32),
-                               _ptr(sk, "sk", B * Hkv * _nb(N), f32), _ptr(sv, "sv", B * Hkv * _nb(N), f32),
-                               _ptr(o, "o", q8.numel(), torch.bfloat16), _ptr(lse, "lse", B * Hq * N, f32),
-                               B, Hq, Hkv, N, d, scale, int(bool(causal)), _stream(stream)), "attn_fwd_fp8")
+    _check(load().attn_fwd_fp8(*ptrs, *dims, scale, int(bool(causal)), _stream(stream)), "attn_fwd_fp8")
+
+
+def attn_fwd_fp8_window(q8, k8, v8, sq, sk, sv, o, lse, window, scale=None, stream=None):
+    """FP8 forward with a key window (left, right), as attn_fwd_window."""
+    ptrs, dims = _fp8_ptrs(q8, k8, v8, sq, sk, sv, o, lse)
+    d = dims[-1]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    left, right = (int(w) for w in window)
+    _check(load().attn_fwd_fp8_window(*ptrs, *dims, scale, left, right, _stream(stream)), "attn_fwd_fp8_window")
 
 
 def attn_fwd_fp8_kv_tile(d):

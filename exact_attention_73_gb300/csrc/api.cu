@@ -319,16 +319,18 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
   return from_cuda(launch_fwd(dtype, d, tq, tk, tv, a, max_seqlen, Hq, nseq, static_cast<cudaStream_t>(stream)));
 }
 
-attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8,
-                         const float* sq, const float* sk, const float* sv,
-                         void* o, float* lse,
-                         int B, int Hq, int Hkv, int N, int d, float scale, int causal,
-                         void* stream) {
+}  // extern "C"
+
+namespace {
+// Dense FP8 forward with a key window (left, right); -1 means no bound.
+attn_status fwd_fp8_dense(const void* q8, const void* k8, const void* v8, const float* sq, const float* sk,
+                          const float* sv, void* o, float* lse, int B, int Hq, int Hkv, int N, int d, float scale,
+                          int win_left, int win_right, void* stream) {
   if (!q8 || !k8 || !v8 || !sq || !sk || !sv || !o || !lse) return ATTN_ERR_NULL;
   if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(sq) || !aligned16(sk) ||
       !aligned16(sv) || !aligned16(o) || !aligned16(lse))
     return ATTN_ERR_ALIGN;
-  if (B < 1 || B > 65535 || N < 1) return ATTN_ERR_SHAPE;
+  if (B < 1 || B > 65535 || N < 1 || win_left < -1 || win_right < -1) return ATTN_ERR_SHAPE;
   attn_status s = check_heads(Hq, Hkv, d);
   if (s != ATTN_OK) return s;
   int* status;
@@ -353,15 +355,35 @@ attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8,
   a.N = N;
   a.cu_seqlens = nullptr;
   a.scale_log2 = scale * kLog2e;
-  a.causal = causal ? 1 : 0;
-  a.win_left = -1;
-  a.win_right = causal ? 0 : -1;
+  a.win_left = win_left;
+  a.win_right = win_right;
+  a.causal = (win_left < 0 && win_right == 0) ? 1 : 0;
   a.sq = sq;
   a.sk = sk;
   a.sv = sv;
   a.nblk = (N + 127) / 128;
   a.status = status;
   return from_cuda(launch_fwd(kE4M3, d, tq, tk, tv, a, N, Hq, B, static_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+extern "C" {
+
+attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8,
+                         const float* sq, const float* sk, const float* sv,
+                         void* o, float* lse,
+                         int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                         void* stream) {
+  return fwd_fp8_dense(q8, k8, v8, sq, sk, sv, o, lse, B, Hq, Hkv, N, d, scale, -1, causal ? 0 : -1, stream);
+}
+
+attn_status attn_fwd_fp8_window(const void* q8, const void* k8, const void* v8,
+                                const float* sq, const float* sk, const float* sv,
+                                void* o, float* lse,
+                                int B, int Hq, int Hkv, int N, int d, float scale, int window_left,
+                                int window_right, void* stream) {
+  return fwd_fp8_dense(q8, k8, v8, sq, sk, sv, o, lse, B, Hq, Hkv, N, d, scale, window_left, window_right,
+                       stream);
 }
 
 attn_status attn_fwd_fp8_varlen(const void* q8, const void* k8, const void* v8,

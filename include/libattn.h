@@ -158,6 +158,20 @@ ATTN_API attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8
                          void* stream);
 
 /*
+ * FP8 forward with a key window (guijiagi.com, practical notes: sliding-window
+ * attention): as attn_fwd_fp8 (same operands, factors, layouts and
+ * arithmetic), with key j visible to query i iff
+ * i - window_left <= j <= i + window_right; -1 leaves that side unbounded,
+ * so (-1, 0) is attn_fwd_fp8 with causal = 1 and (-1, -1) without masking.
+ * Every row sees at least its own key. ATTN_ERR_SHAPE for a bound below -1.
+ */
+ATTN_API attn_status attn_fwd_fp8_window(const void* q8, const void* k8, const void* v8,
+                                         const float* sq, const float* sk, const float* sv,
+                                         void* o, float* lse,
+                                         int B, int Hq, int Hkv, int N, int d, float scale, int window_left,
+                                         int window_right, void* stream);
+
+/*
  * Block quantisation of packed sequences: x [T,H,d] (THD, as attn_fwd_varlen)
  * -> x8 [T,H,d] E4M3 codes and scales [nseq, H, ceil(max_seqlen/128)]
  * float32. Each sequence is blocked from its own first row (its last block

@@ -79,6 +79,12 @@ def test_argument_checks_before_any_device_work(lib):
     assert lib.attn_fwd_fp8(*f8, P(16), P(16), P(16), P(16), P(16), 1, 2, 1, 0, 128, 0.1, 0, None) == 3
     assert lib.attn_fwd_fp8(*f8, P(16), P(16), P(16), P(16), P(16), 1, 2, 1, 8, 96, 0.1, 0, None) == 4
     assert lib.attn_fwd_fp8(*f8, P(16), P(16), P(16), P(16), P(16), 1, 3, 2, 8, 128, 0.1, 0, None) == 5
+    # FP8 with a key window: bounds below -1 refused, the rest as attn_fwd_fp8
+    assert lib.attn_fwd_fp8_window(*f8, P(16), P(16), P(16), P(16), P(16), 1, 2, 1, 8, 128, 0.1, -2, 0, None) == 3
+    assert lib.attn_fwd_fp8_window(*f8, P(16), P(16), P(16), P(16), P(16), 1, 2, 1, 8, 128, 0.1, 4, -3, None) == 3
+    assert lib.attn_fwd_fp8_window(*f8, None, P(16), P(16), P(16), P(16), 1, 2, 1, 8, 128, 0.1, 4, 4, None) == 1
+    assert lib.attn_fwd_fp8_window(*f8, P(16), P(16), P(16), P(16), P(16), 1, 2, 1, 8, 96, 0.1, 4, 4, None) == 4
+    assert lib.attn_fwd_fp8_window(*f8, P(16), P(16), P(16), P(16), P(16), 1, 3, 2, 8, 128, 0.1, 4, 4, None) == 5
     # packed FP8: cu_seqlens required and aligned, nseq / T / max_seqlen, head dim, dtype, GQA
     assert lib.attn_quantize_fp8_varlen(P(16), 0, P(16), P(16), None, 2, 10, 5, 1, 64, None, None) == 1
     assert lib.attn_quantize_fp8_varlen(P(16), 0, P(16), P(16), P(24), 2, 10, 5, 1, 64, None, None) == 2

@@ -204,6 +204,17 @@ def test_fp8_forward(d, causal):
     assert torch.equal(o, o2) and torch.equal(lse, l2)
 
 
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("window", [(30, 50), (200, 0)])
+def test_fp8_forward_window(d, window):
+    B, Hq, Hkv, N = 1, 4, 2, 300
+    (q8, sq), (k8, sk), (v8, sv) = _fp8_operands(705, [(B, Hq, N, d), (B, Hkv, N, d), (B, Hkv, N, d)])
+    ob, o = padded((B, Hq, N, d), torch.bfloat16)
+    lb, lse = padded((B, Hq, N), torch.float32)
+    L.attn_fwd_fp8_window(q8, k8, v8, sq, sk, sv, o, lse, window)
+    check({"o": ob, "lse": lb}, {"o": o, "lse": lse})
+
+
 @pytest.mark.parametrize("splits", [1, 3])
 def test_fp8_decode(splits):
     B, Hq, Hkv, Nmax, d = 3, 16, 4, 500, 128

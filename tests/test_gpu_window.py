@@ -145,3 +145,67 @@ def test_window_config_sampled():
     ref = A.backward(qs, ks, vs, do, 128 ** -0.5, False, window)
     for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
         assert rel_rms(g, r) <= 1e-2, (name, rel_rms(g, r))
+
+
+def _fp8_window_case(seed, b, hq, hkv, n, d, rotate):
+    """Seeded outlier inputs quantised on the GPU and by the oracle (codes and
+    factors checked bit for bit); returns the GPU codes and the oracle's."""
+    from oracle import fp8 as F
+    q, k, v = inputs.outliers(seed, [(b, hq, n, d), (b, hkv, n, d), (b, hkv, n, d)])
+    signs = inputs.random_signs(4, d) if rotate else None
+    nb = (n + 127) // 128
+
+    def quant(x, s):
+        x8 = torch.empty(x.shape, dtype=torch.uint8, device="cuda")
+        sc = torch.empty(x.shape[:2] + (nb,), dtype=torch.float32, device="cuda")
+        L.attn_quantize_fp8(x.cuda(), x8, sc, None if s is None else s.cuda())
+        return x8, sc
+
+    gpu = (quant(q, signs), quant(k, signs), quant(v, None))
+    s_np = None if signs is None else signs.numpy()
+    ref = (F.quantize_blocks(q, s_np), F.quantize_blocks(k, s_np), F.quantize_blocks(v))
+    for (c_ref, f_ref), (c_gpu, f_gpu) in zip(ref, gpu):
+        assert np.array_equal(c_gpu.cpu().numpy(), c_ref)
+        assert np.array_equal(f_gpu.cpu().numpy(), f_ref)
+    return gpu, ref
+
+
+@pytest.mark.parametrize("window", [(0, 0), (127, 0), (130, 5), (-1, 40), (64, 64), (300, -1)])
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("n", [200, 700])
+def test_fp8_forward_window(window, d, n):
+    """attn_fwd_fp8_window against the oracle's FP8 emulation with the same
+    window, stale-max rule and KV tile (the tolerances of the dense FP8
+    tests: RMS 2e-3, 99.9th percentile 1e-2, max 1e-1; LSE 1e-3)."""
+    from oracle import fp8 as F
+    b, hq, hkv = 1, 4, 2
+    (q8g, k8g, v8g), ref = _fp8_window_case(40 + d + n, b, hq, hkv, n, d, rotate=(d != 256))
+    o = torch.full((b, hq, n, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((b, hq, n), float("nan"), device="cuda")
+    L.attn_fwd_fp8_window(q8g[0], k8g[0], v8g[0], q8g[1], k8g[1], v8g[1], o, lse, window)
+    torch.cuda.synchronize()
+    assert L.attn_get_device_status() == 0
+    codes = (ref[0][0], ref[1][0], ref[2][0], ref[0][1], ref[1][1], ref[2][1])
+    o_ref, lse_ref = F.attention_fp8(*codes, d ** -0.5, tau=F.STALE_MAX_TAU, kv_tile=L.attn_fwd_fp8_kv_tile(d),
+                                     window=window)
+    err = np.abs(o.cpu().double().numpy() - o_ref)
+    tag = f"d{d} n{n} w{window}"
+    assert math.sqrt((err ** 2).mean()) <= 2e-3, tag
+    assert np.quantile(err, 0.999) <= 1e-2, tag
+    assert err.max() <= 1e-1, tag
+    assert np.abs(lse.cpu().double().numpy() - lse_ref).max() <= 1e-3, tag
+
+
+def test_fp8_window_special_cases_are_the_dense_entry_point():
+    """The window (-1, 0) is attn_fwd_fp8 with causal masking and (-1, -1)
+    attn_fwd_fp8 without: the same kernel with the same bounds, bit for bit."""
+    b, hq, hkv, n, d = 2, 4, 2, 333, 128
+    (q8g, k8g, v8g), _ = _fp8_window_case(55, b, hq, hkv, n, d, rotate=True)
+    args = (q8g[0], k8g[0], v8g[0], q8g[1], k8g[1], v8g[1])
+    for window, causal in (((-1, 0), True), ((-1, -1), False)):
+        o1 = torch.empty((b, hq, n, d), dtype=torch.bfloat16, device="cuda")
+        o2, l1, l2 = torch.empty_like(o1), torch.empty((b, hq, n), device="cuda"), torch.empty((b, hq, n), device="cuda")
+        L.attn_fwd_fp8_window(*args, o1, l1, window)
+        L.attn_fwd_fp8(*args, o2, l2, causal=causal)
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o2) and torch.equal(l1, l2), window
