@@ -89,9 +89,10 @@ int tail_split_units(const BwdArgs& a, long long units, int per_head, int sms) {
 
 // Short unmasked rows run persistent: one CTA per SM walks the units, so a
 // unit's dV/dK write-out overlaps the next unit's first products and the
-// CTA set-up is paid once. That pays while a unit holds few query tiles
-// (5-6 % at N = 512); from about N = 1024 on the unit's own walk hides it
-// and the walk's extra state costs as much as it saves.
+// CTA set-up is paid once (at d = 64 also the next unit's K/V load, from a
+// second buffer). That pays while a unit holds few query tiles (N = 512:
+// 6 % at d = 128, 13 % at d = 64); from about N = 1024 on the unit's own
+// walk hides it and the walk's extra state costs as much as it saves.
 constexpr int kBwdPersistMaxRows = 768;
 
 template <int DT, int D, bool kDQ>
