@@ -88,7 +88,16 @@ def test_fp8_calls_of_the_tests_pass(lib):
     L.attn_fwd_fp8(z(B, Hq, N, d, dtype=U8), z(B, Hkv, N, d, dtype=U8), z(B, Hkv, N, d, dtype=U8),
                    z(B, Hq, nb, dtype=F32), z(B, Hkv, nb, dtype=F32), z(B, Hkv, nb, dtype=F32), z(B, Hq, N, d),
                    z(B, Hq, N, dtype=F32), causal=True, stream=STREAM)
-    assert lib.calls == ["attn_quantize_fp8"] * 2 + ["attn_quantize_fp8_rope", "attn_quantize_fp8", "attn_fwd_fp8"]
+    L.attn_fwd_fp8_window(z(B, Hq, N, d, dtype=U8), z(B, Hkv, N, d, dtype=U8), z(B, Hkv, N, d, dtype=U8),
+                          z(B, Hq, nb, dtype=F32), z(B, Hkv, nb, dtype=F32), z(B, Hkv, nb, dtype=F32),
+                          z(B, Hq, N, d), z(B, Hq, N, dtype=F32), (130, 5), stream=STREAM)
+    assert lib.calls == ["attn_quantize_fp8"] * 2 + ["attn_quantize_fp8_rope", "attn_quantize_fp8", "attn_fwd_fp8",
+                         "attn_fwd_fp8_window"]
+    # the window call refuses what the plain one refuses: a short factor array
+    with pytest.raises(ValueError):
+        L.attn_fwd_fp8_window(z(B, Hq, N, d, dtype=U8), z(B, Hkv, N, d, dtype=U8), z(B, Hkv, N, d, dtype=U8),
+                              z(B, Hq, nb - 1, dtype=F32), z(B, Hkv, nb, dtype=F32), z(B, Hkv, nb, dtype=F32),
+                              z(B, Hq, N, d), z(B, Hq, N, dtype=F32), (130, 5), stream=STREAM)
 
 
 @pytest.mark.parametrize("with_lengths", [False, True])
