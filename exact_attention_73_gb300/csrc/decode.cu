@@ -3,6 +3,7 @@
 // merges the splits of every (batch, query head) by their log-sum-exp
 // weights: LSE = log sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s.
 // The decode step reads the whole cache once: it is HBM-bound.
+#include <climits>
 #include <cmath>
 #include <cstdint>
 
@@ -86,6 +87,8 @@ extern "C" attn_status attn_decode_fp8(const void* q8, const float* sq, const vo
   const int g = Hq / Hkv;
   const int ntiles = (Nmax + 127) / 128;
   if (g > 128 || num_splits < 1 || num_splits > ntiles) return ATTN_ERR_SHAPE;
+  // one combine CTA per (sequence, query head): the row count is an int
+  if (static_cast<long long>(B) * Hq > INT_MAX) return ATTN_ERR_SHAPE;
   if (ws_bytes < attn_decode_fp8_workspace_size(B, Hq, d, num_splits)) return ATTN_ERR_WORKSPACE;
   int* status;
   attn_status s = device_context(&status);

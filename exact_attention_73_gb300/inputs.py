@@ -18,6 +18,11 @@ Recipes
 * Variable-length packing: sequence lengths drawn uniformly from [lo, hi] with
   ``integers(lo, hi + 1, n)``; ``cu_seqlens`` is their exclusive prefix sum.
 * Random signs for the incoherent-processing rotation: +-1 drawn from the seed.
+* Device-drawn N(0,1) for tensors too large to draw on the host in a test's
+  time (past 2^31 elements): torch's seeded CUDA generator, drawn in the
+  input dtype in the order of ``shapes``. Its values depend on torch's
+  generator, not on this seed alone, so both sides of a comparison take the
+  same drawn tensors (the oracle receives host copies of what it checks).
 """
 from __future__ import annotations
 
@@ -71,3 +76,10 @@ def random_signs(seed: int, d: int):
     """A vector of d random signs (+1/-1) as int8."""
     s = np.random.default_rng(seed).integers(0, 2, d)
     return torch.from_numpy((2 * s - 1).astype(np.int8))
+
+
+def normal_device(seed: int, shapes, dtype: str = "bf16", device: str = "cuda"):
+    """Draw one tensor per entry of ``shapes`` from N(0,1) on ``device``."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    return [torch.randn(tuple(shp), generator=gen, dtype=_TORCH_DTYPES[dtype], device=device) for shp in shapes]

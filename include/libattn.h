@@ -226,7 +226,8 @@ ATTN_API size_t attn_decode_fp8_workspace_size(int B, int Hq, int d, int num_spl
  * num_splits) tiles (1 <= num_splits <= ceil(Nmax/128)); each run of each
  * (sequence, KV group) is one CTA computing the FP8 forward for the group's
  * g = Hq / Hkv query heads (g <= 128) from a fresh state, and a second kernel
- * combines the runs by their log-sum-exp weights. Runs past a sequence's
+ * combines the runs by their log-sum-exp weights (B * Hq <= 2^31 - 1, else
+ * ATTN_ERR_SHAPE). Runs past a sequence's
  * length contribute nothing. workspace: attn_decode_fp8_workspace_size bytes.
  */
 ATTN_API attn_status attn_decode_fp8(const void* q8, const float* sq, const void* k8, const void* v8,
@@ -244,9 +245,10 @@ ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d);
  * [B,Hq,N,d], dk/dv [B,Hkv,N,d] of `dtype` (dk/dv sum over the query heads
  * of each group). P is recomputed from lse. workspace: device memory of at
  * least attn_bwd_workspace_size bytes, contents need not be initialised.
- * lse is treated as a non-differentiable output. Head dim d must be 128
- * (other values return ATTN_ERR_HEADDIM). Kernels: D = rowsum(dO o O) with
- * the FP32 dQ accumulator cleared, the main kernel, the dQ conversion.
+ * lse is treated as a non-differentiable output. Head dim d is 64, 128 or
+ * 256 (other values return ATTN_ERR_HEADDIM; at 256 two CTAs share a key tile,
+ * each owning half of the head dims). Kernels: D = rowsum(dO o O) with the
+ * FP32 dQ accumulator cleared, the main kernel, the dQ conversion.
  */
 ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
                      const float* lse, const void* dout,

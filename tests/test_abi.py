@@ -65,6 +65,9 @@ def test_argument_checks_before_any_device_work(lib):
     assert lib.attn_decode_fp8(*dargs, wdec, 2, 8, 3, 300, 128, 0.1, 3, None) == 5
     assert lib.attn_decode_fp8(*dargs, wdec, 2, 8, 2, 300, 96, 0.1, 3, None) == 4
     assert lib.attn_decode_fp8(*dargs, wdec, 1, 256, 1, 300, 128, 0.1, 1, None) == 3        # g > 128
+    # B * Hq past 2^31 - 1 (one combine CTA per row), refused before the workspace is sized
+    assert lib.attn_decode_fp8(*dargs, wdec, 65535, 32769, 32769, 128, 128, 0.1, 1, None) == 3
+    assert lib.attn_decode_fp8(*dargs, wdec, 65535, 32768, 256, 128, 64, 0.1, 1, None) == 7   # fits: workspace next
     # fused RoPE producer: the tables are required and aligned
     assert lib.attn_quantize_fp8_rope(P(16), 0, P(16), P(16), 1, 1, 8, 64, None, P(16), None, None) == 1
     assert lib.attn_quantize_fp8_rope(P(16), 0, P(16), P(16), 1, 1, 8, 64, P(16), P(20), None, None) == 2
