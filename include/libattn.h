@@ -35,6 +35,15 @@
  *   - Arguments are checked before anything is launched; a failed check
  *     returns an error code and launches nothing. A CUDA error raised by a
  *     launch is returned as ATTN_ERR_CUDA.
+ *   - CUDA graphs: the first call on a device probes it, and the first
+ *     launch of each kernel instance raises its shared-memory limit; after
+ *     that a call only encodes tensor maps on the host (passed by value in
+ *     the kernel parameters) and enqueues kernels on `stream`, so it can be
+ *     captured into a graph and replayed. Make one direct call with the same
+ *     shapes and flags before capturing. A replay keeps the captured
+ *     pointers, sizes and flags and reads the buffers' current contents
+ *     (cu_seqlens and decode seqlens included). attn_get_device_status
+ *     synchronises and cannot be captured.
  */
 #ifndef LIBATTN_H
 #define LIBATTN_H
