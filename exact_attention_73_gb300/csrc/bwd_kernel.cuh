@@ -106,6 +106,11 @@ struct BwdCfg {
   static constexpr int Q_B = BR * D * 2;            // Q_i or dO_i tile
   static constexpr int Q_BOX_B = BR * 128;
   static constexpr int DS_B = BC * BR * 2;          // dS^T tile [128 keys][64 queries]
+  // dS^T tiles in shared memory (the B operand of dQ^T). Head dim 64 has the
+  // room for two, one per score buffer: tile g's dS^T then overwrites tile
+  // g-2's, whose dQ^T was complete before tile g's S^T/dP^T were issued, so
+  // the P^T/dS^T warps never wait for a product.
+  static constexpr int NDS = D == 64 ? 2 : 1;
   static constexpr int NKV = kP && D == 64 ? 2 : 1;   // K/V buffers
   static constexpr int NQ = D == 64 ? 6 : (D == 128 ? 4 : 1);   // stages of the Q/dO ring
   static constexpr int LD_B = 2 * BR * 4;           // LSE*log2e and D for one tile
@@ -116,11 +121,11 @@ struct BwdCfg {
   // kv_empty[NKV], acc_empty
   static constexpr int NBARS = 2 * NKV + 2 * NQ + 2 + 4 + 4;
   static constexpr int SMEM_BYTES =
-      NKV * 2 * KV_B + DS_B + NQ * (2 * Q_B) + DQ_STAGE_B + NQ * LD_B + NBARS * 8 + 16;   // base is 1024-aligned
+      NKV * 2 * KV_B + NDS * DS_B + NQ * (2 * Q_B) + DQ_STAGE_B + NQ * LD_B + NBARS * 8 + 16;   // base is 1024-aligned
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeded");
   // a split walk's hand-over of dV and dK ([2][BC][DH] FP32 from offset 0)
   // stays below the barriers
-  static_assert(2 * BC * DH * 4 <= 2 * KV_B + DS_B + NQ * (2 * Q_B) + DQ_STAGE_B + NQ * LD_B, "hand-over area");
+  static_assert(2 * BC * DH * 4 <= 2 * KV_B + NDS * DS_B + NQ * (2 * Q_B) + DQ_STAGE_B + NQ * LD_B, "hand-over area");
   static constexpr int NTHREADS = 512;
   // Registers: the launch gives 128 per thread (the whole register file);
   // the load/MMA warpgroup and the dQ drain warpgroup return part of theirs
@@ -210,8 +215,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
   uint8_t* smem = bwd_smem;
   uint8_t* sK = smem;                               // K/V buffer kb: sK + kb * 2 * KV_B, V after K
   uint8_t* sV = sK + C::KV_B;
-  uint8_t* sDS = sK + C::NKV * 2 * C::KV_B;         // [DS_B], 128-byte swizzle
-  uint8_t* sQ = sDS + C::DS_B;                      // [NQ][Q_B]
+  uint8_t* sDS = sK + C::NKV * 2 * C::KV_B;         // [NDS][DS_B], 128-byte swizzle
+  uint8_t* sQ = sDS + C::NDS * C::DS_B;             // [NQ][Q_B]
   uint8_t* sdO = sQ + C::NQ * C::Q_B;               // [NQ][Q_B]
   float* sDQ = reinterpret_cast<float*>(sdO + C::NQ * C::Q_B);   // [DQ_ROWS][D] FP32
   float* sLD = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(sDQ) + C::DQ_STAGE_B);   // [NQ][2*BR]
@@ -499,8 +504,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
           if constexpr (kDQ) {
 #pragma unroll
             for (int kk = 0; kk < C::BC / 16; ++kk) {   // dQ^T = K^T dS^T, both MN-major
-              mma_ss<false>(xb + C::COL_DQ, dadd(dK_mn, kvo + kk * 2048), dadd(dDS0_mn, kk * 2048),
-                            C::IDESC_DQ, kk > 0);
+              mma_ss<false>(xb + C::COL_DQ, dadd(dK_mn, kvo + kk * 2048),
+                            dadd(dDS0_mn, (C::NDS > 1 ? (g & 1) * C::DS_B : 0) + kk * 2048), C::IDESC_DQ, kk > 0);
             }
             mma_commit(dq_full);
           }
@@ -640,7 +645,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
       for (int it = 0; it < niter; ++it) {
         const int g = gt + it;
         const uint32_t xb = tbase + lane_off + 128u * (g & 1);
-        uint8_t* ds_row = sDS + r * 128;
+        uint8_t* ds_row = sDS + (C::NDS > 1 ? (g & 1) * C::DS_B : 0) + r * 128;
         const int st = g % C::NQ;
         // LSE and D of this stage (written by the load warp before it arrived
         // on q_full[st]) go to registers first: these shared-memory reads then
@@ -716,11 +721,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
         tmem_st16(xb + C::col_p(2 * half), pp);
         tmem_st16(xb + C::col_ds(2 * half), dd);
         // dS^T row r, queries 32*half .. +31: 16-byte chunks 4*half .. +3 of a
-        // 128-byte row, 128-byte swizzle (chunk ^= row % 8). The single dS^T
+        // 128-byte row, 128-byte swizzle (chunk ^= row % 8). A single dS^T
         // tile is read by dQ^T of the previous tile, which must be complete
         // first; waiting only here lets this tile's exponentials overlap it.
+        // With two, this tile's buffer was last read by dQ^T of tile g-2,
+        // drained before S^T/dP^T of this tile were issued.
         if constexpr (kDQ) {
-          if (g > 0) dq_ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (g - 1) & 1, a.status));
+          if (C::NDS == 1 && g > 0) dq_ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (g - 1) & 1, a.status));
   #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
             const int chunk = (4 * half + c4) ^ (r & 7);
