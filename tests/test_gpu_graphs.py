@@ -37,6 +37,16 @@ def rel_rms(x, ref):
     return float(np.linalg.norm(x - ref) / max(np.linalg.norm(ref), 1e-3 * np.sqrt(ref.size)))
 
 
+def poison(outputs):
+    """NaN into floating outputs and zeros into code tensors before each call, so that the
+    comparison sees only what that call wrote."""
+    for t in outputs.values():
+        if t.is_floating_point():
+            t.fill_(float("nan"))
+        else:
+            t.zero_()
+
+
 def replay_and_compare(step, fill, outputs, loose=()):
     """Capture step() once, then for two new fillings of the inputs compare the
     replayed outputs with a direct call. Returns the last replay's outputs."""
@@ -49,14 +59,12 @@ def replay_and_compare(step, fill, outputs, loose=()):
     got = None
     for it in (1, 2):
         fill(it)
-        for t in outputs.values():
-            t.fill_(float("nan")) if t.is_floating_point() else t.fill_(0)
+        poison(outputs)
         g.replay()
         torch.cuda.synchronize()
         assert L.attn_get_device_status() == 0
         got = {k: t.clone() for k, t in outputs.items()}
-        for t in outputs.values():
-            t.fill_(float("nan")) if t.is_floating_point() else t.fill_(0)
+        poison(outputs)
         step()
         torch.cuda.synchronize()
         for name, t in outputs.items():
