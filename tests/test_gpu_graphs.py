@@ -115,6 +115,30 @@ def test_training_step_replays(B, Hq, Hkv, N, d, causal):
     assert rel_rms(one(got["dq"]).double().numpy(), dq_ref) <= 1e-2
 
 
+def test_noalloc_backward_replays():
+    # the library-owned workspace: its address is looked up by the first
+    # (direct) call, after which the call captures like the others
+    B, Hq, Hkv, N, d = 1, 4, 2, 1000, 128
+    q = torch.empty((B, Hq, N, d), dtype=torch.bfloat16, device="cuda")
+    do = torch.empty_like(q)
+    k = torch.empty((B, Hkv, N, d), dtype=torch.bfloat16, device="cuda")
+    v = torch.empty_like(k)
+    o, lse = torch.empty_like(q), torch.empty((B, Hq, N), device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def step():
+        L.attn_fwd(q, k, v, o, lse, causal=True)
+        L.attn_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, causal=True)
+
+    got = replay_and_compare(step, fill_from([q, k, v, do], 650), {"o": o, "lse": lse, "dq": dq, "dk": dk,
+                                                                   "dv": dv}, loose=("dq",))
+    # KV head 0 and the query heads 0 and 1 that read it, against the oracle
+    full = A.backward(q[:, :2].cpu(), k[:, :1].cpu(), v[:, :1].cpu(), do[:, :2].cpu(), d ** -0.5, True)
+    assert rel_rms(got["dk"][:, :1].double().cpu().numpy(), full[1]) <= 1e-2
+    assert rel_rms(got["dv"][:, :1].double().cpu().numpy(), full[2]) <= 1e-2
+    assert rel_rms(got["dq"][:, 1:2].double().cpu().numpy(), full[0][:, 1:2]) <= 1e-2
+
+
 def test_fp8_step_replays():
     B, H, N, d = 2, 4, 1000, 128
     x = [torch.empty((B, H, N, d), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
