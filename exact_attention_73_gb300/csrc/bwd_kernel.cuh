@@ -252,8 +252,12 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     by = static_cast<int>(blockIdx.x) / a.tiles_x % a.Hkv;
     bz = static_cast<int>(blockIdx.x) / a.tiles_x / a.Hkv;
   } else if (a.causal) {
-    // with causal masking key tile 0 has the most work: heavy tiles start first
-    heavy_first_order<16>(bx, by, bz);
+    // with causal masking key tile 0 has the most work: heavy tiles start
+    // first. Packed sequences run in blocks of 64 key tiles per (sequence,
+    // KV head): fewer pairs at a time, so more of each pair's Q, dO and dQ
+    // lines stay in L2 (a long sequence's are tens of MB).
+    if (a.cu_seqlens != nullptr) heavy_first_order<64>(bx, by, bz);
+    else heavy_first_order<16>(bx, by, bz);
   }
   const bool packed = a.cu_seqlens != nullptr;
   // The unit: KV head, batch (or packed sequence), key tile j, head-dim part
