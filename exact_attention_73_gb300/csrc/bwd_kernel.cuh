@@ -256,8 +256,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUte
     // first. Packed sequences run in blocks of 64 key tiles per (sequence,
     // KV head): fewer pairs at a time, so more of each pair's Q, dO and dQ
     // lines stay in L2 (a long sequence's are tens of MB).
-    if (a.cu_seqlens != nullptr) heavy_first_order<64>(bx, by, bz);
-    else heavy_first_order<16>(bx, by, bz);
+    heavy_first_order(a.cu_seqlens != nullptr ? 64 : 16, bx, by, bz);
   }
   const bool packed = a.cu_seqlens != nullptr;
   // The unit: KV head, batch (or packed sequence), key tile j, head-dim part

@@ -160,7 +160,7 @@ __device__ __forceinline__ bool fwd_unit(const FwdArgs& a, int lin, FwdUnit& w) 
   if (a.causal) {
     // the last query tiles have the most work: those of every (head, batch)
     // come first
-    heavy_first_map<8>(lin, a.ux, a.uy, a.uz, bx, by, bz);
+    heavy_first_map(8, lin, a.ux, a.uy, a.uz, bx, by, bz);
   } else {
     bx = lin % a.ux;
     by = (lin / a.ux) % a.uy;

@@ -373,9 +373,10 @@ __device__ __forceinline__ int warp_any(int pred) { return __any_sync(0xffffffff
 // tail. This maps the linear index to (x, y, z) in blocks of JB consecutive x
 // of one (y, z) pair, block by block from the heaviest x: every pair's heavy
 // CTAs start in the first waves, and the CTAs running together still share a
-// pair's data in L2 (JB of them per pair).
-template <int JB>
-__device__ __forceinline__ void heavy_first_map(int lin, int nx, int ny, int nz, int& x, int& y, int& z) {
+// pair's data in L2 (JB of them per pair). JB is an argument rather than a
+// template parameter so that a kernel choosing it at run time keeps one copy
+// of its dispatch code.
+__device__ __forceinline__ void heavy_first_map(int JB, int lin, int nx, int ny, int nz, int& x, int& y, int& z) {
   const int groups = ny * nz;
   const int blk = lin / (JB * groups);
   const int width = min(JB, nx - blk * JB);       // the last block may be narrower
@@ -386,11 +387,10 @@ __device__ __forceinline__ void heavy_first_map(int lin, int nx, int ny, int nz,
   z = g / ny;
 }
 // the same over this CTA's place in a 3-D grid
-template <int JB>
-__device__ __forceinline__ void heavy_first_order(int& x, int& y, int& z) {
+__device__ __forceinline__ void heavy_first_order(int JB, int& x, int& y, int& z) {
   const int nx = static_cast<int>(gridDim.x), ny = static_cast<int>(gridDim.y);
   const int lin = static_cast<int>(blockIdx.x) + nx * (static_cast<int>(blockIdx.y) + ny * static_cast<int>(blockIdx.z));
-  heavy_first_map<JB>(lin, nx, ny, static_cast<int>(gridDim.z), x, y, z);
+  heavy_first_map(JB, lin, nx, ny, static_cast<int>(gridDim.z), x, y, z);
 }
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
